@@ -1,0 +1,203 @@
+"""Oracle for the decode-step paged-KV attention path (TEST INFRASTRUCTURE ONLY).
+
+A plain fp64 CPU implementation (``pkv_oracle.c``) of what the path computes,
+written from the Zero TVM documentation ("KV cache", "Decode loop", "How it
+works", "Port to Phi-4-mini or Qwen3").  Only the tests, the smoke check and
+the bench's CPU baseline load it; the product library never does, and the two
+share no code.  Every function here is a thin ctypes marshaller around the C
+definitions; the arithmetic lives in ``pkv_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB = os.environ.get("PKV_ORACLE_LIB") or os.path.join(_HERE, "liboracle.so")
+
+ERRORS = {1: "invalid argument", 3: "out of range", 5: "duplicate position in one sequence"}
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"oracle rejected the input: {ERRORS.get(code, code)}")
+        self.code = code
+
+
+def build_command(source=None, target=None):
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+            source or os.path.join(_HERE, "pkv_oracle.c"), "-o", target or LIB, "-lm"]
+
+
+def build() -> None:
+    subprocess.run(build_command(), check=True)
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int), ("num_qo_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("max_position", ctypes.c_int), ("rope_theta", ctypes.c_double)]
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: run oracle.build()")
+        lib = ctypes.CDLL(LIB)
+        P = ctypes.c_void_p
+        i, d = ctypes.c_int, ctypes.c_double
+        lib.orc_f16_to_f64.restype = d
+        lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.orc_f64_to_f16.restype = ctypes.c_uint16
+        lib.orc_f64_to_f16.argtypes = [d]
+        lib.orc_f16_decode_array.argtypes = [P, P, ctypes.c_int64]
+        lib.orc_f16_encode_array.argtypes = [P, P, ctypes.c_int64]
+        lib.orc_rope.argtypes = [P, P, i, ctypes.c_int64, d]
+        lib.orc_append.restype = i
+        lib.orc_append.argtypes = [P, P, P, P, i, P, P, i, P, P, P, P]
+        lib.orc_attention.restype = i
+        lib.orc_attention.argtypes = [P, P, P, i, P, P, P, d, P, P]
+        lib.orc_split_attention.restype = i
+        lib.orc_split_attention.argtypes = [P, P, P, i, P, P, P, i, i, i, d, P, P]
+        lib.orc_combine.restype = i
+        lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P]
+        lib.orc_init.restype = None
+        lib.orc_init()
+        _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+@dataclass
+class Geometry:
+    num_pages: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    max_position: int
+    rope_theta: float
+
+    def c(self) -> Geom:
+        return Geom(self.num_pages, self.num_qo_heads, self.num_kv_heads, self.head_dim,
+                    self.max_position, self.rope_theta)
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    b, pb = _c(bits, np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    _L().orc_f16_decode_array(pb, out.ctypes.data, b.size)
+    return out
+
+
+def f64_to_f16(x) -> np.ndarray:
+    a, pa = _c(x, np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _L().orc_f16_encode_array(pa, out.ctypes.data, a.size)
+    return out
+
+
+def rope(x, pos: int, theta: float) -> np.ndarray:
+    a, pa = _c(x, np.float64)
+    out = np.empty_like(a)
+    _L().orc_rope(pa, out.ctypes.data, a.size, int(pos), float(theta))
+    return out
+
+
+def append(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, page_indices, pool):
+    """RoPE + KV append.  ``pool`` (uint16 [pages, 2, Hkv, 16, d]) is updated in place.
+
+    Returns q_out (uint16 [T, Hq, d])."""
+    q, pq = _c(q, np.uint16)
+    k, pk = _c(k, np.uint16)
+    v, pv = _c(v, np.uint16)
+    pm, ppm = _c(pos_map, np.int32)
+    ai, pai = _c(append_indptr, np.int32)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    assert pool.dtype == np.uint16 and pool.flags["C_CONTIGUOUS"]
+    T = pm.size
+    q_out = np.empty((T, geom.num_qo_heads, geom.head_dim), dtype=np.uint16)
+    g = geom.c()
+    rc = _L().orc_append(ctypes.byref(g), pq, pk, pv, T, ppm, pai, ai.size - 1, ppi, ppx,
+                         pool.ctypes.data, q_out.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return q_out
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)
+
+
+def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len, sm_scale=None):
+    """Unsplit decode attention: returns out (float64 [B, Hq, d]) and lse (float64 [B, Hq])."""
+    sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
+    pool, pp = _c(pool, np.uint16)
+    q, pq = _c(q_rope, np.uint16)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    lp, plp = _c(last_page_len, np.int32)
+    B = pi.size - 1
+    out = np.empty((B, geom.num_qo_heads, geom.head_dim), dtype=np.float64)
+    lse = np.empty((B, geom.num_qo_heads), dtype=np.float64)
+    g = geom.c()
+    rc = _L().orc_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, float(sm_scale),
+                            out.ctypes.data, lse.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return out, lse
+
+
+def split_attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len,
+                    num_splits: int = 0, chunk_pages: int = 0, num_out_splits: int | None = None,
+                    sm_scale=None):
+    """Split-K partials: (partial_o float64 [B, Hq, S, d], partial_lse float64 [B, Hq, S])."""
+    sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
+    pool, pp = _c(pool, np.uint16)
+    q, pq = _c(q_rope, np.uint16)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    lp, plp = _c(last_page_len, np.int32)
+    B = pi.size - 1
+    if num_out_splits is None:
+        if chunk_pages > 0:
+            n = np.diff(pi)
+            num_out_splits = max(1, int(-(-n.max() // chunk_pages)) if n.size else 1)
+        else:
+            num_out_splits = num_splits
+    S = num_out_splits
+    po = np.empty((B, geom.num_qo_heads, S, geom.head_dim), dtype=np.float64)
+    pl = np.empty((B, geom.num_qo_heads, S), dtype=np.float64)
+    g = geom.c()
+    rc = _L().orc_split_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, int(num_splits),
+                                  int(chunk_pages), S, float(sm_scale), po.ctypes.data, pl.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return po, pl
+
+
+def combine(partial_o, partial_lse):
+    """LSE merge: returns (out float64 [B, Hq, d], out fp16 bits uint16, lse float64 [B, Hq])."""
+    po, ppo = _c(partial_o, np.float64)
+    pl, ppl = _c(partial_lse, np.float64)
+    B, Hq, S, d = po.shape
+    out = np.empty((B, Hq, d), dtype=np.float64)
+    out16 = np.empty((B, Hq, d), dtype=np.uint16)
+    lse = np.empty((B, Hq), dtype=np.float64)
+    rc = _L().orc_combine(ppo, ppl, B, Hq, S, d, out.ctypes.data, out16.ctypes.data, lse.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return out, out16, lse

@@ -1,0 +1,359 @@
+/*
+ * ORACLE for the decode-step paged-KV attention path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline / reference arm load this library; the product path (the CUDA
+ * library and its Python binding) never does, and it shares no code with it.
+ *
+ * Plain, slow, obviously correct: fp64 arithmetic from fp16 inputs, one loop
+ * per definition, OpenMP only across independent (sequence, head) pairs.
+ *
+ * What it follows (page title, section):
+ *  - Zero TVM Documentation, "KV cache": fixed pages of 16 slots, a page table
+ *    mapping logical positions to physical pages, K rotated by RoPE before the
+ *    cache write (a page is valid only at the positions it was written at).
+ *  - Zero TVM Documentation, "Decode loop": per-step position map, page range
+ *    per sequence, sequence length = position + 1 (the new token attends to
+ *    itself); QKV + RoPE + KV-append in one dispatch, which also writes the
+ *    rotated query (binding order q_out, k_out, v_out, qkv, posMap, "Debugging
+ *    tips").
+ *  - Zero TVM Documentation, "How it works": split-K attention over KV chunks
+ *    followed by a combine dispatch per layer.
+ *  - Zero TVM Documentation, "Port to Phi-4-mini or Qwen3": when KV heads are
+ *    fewer than query heads, KV heads are repeated (query head h reads KV head
+ *    h / (Hq/Hkv)).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *  - RoPE is the rotate-half form over the whole head: element i pairs with
+ *    i + d/2, inverse frequency theta^(-2i/d), angle = position * frequency.
+ *  - Pool layout per layer: [page][K=0,V=1][kv_head][slot][dim], fp16.
+ *  - softmax scale 1/sqrt(d); split chunks are page-aligned and contiguous;
+ *    a chunk with no token gives o = 0 and lse = -inf (natural log); the
+ *    combine of all-empty chunks gives out = 0 and lse = -inf.
+ *  - fp16 results are rounded to nearest, ties to even.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_PAGE 16
+
+enum { ORC_OK = 0, ORC_INVALID = 1, ORC_OUT_OF_RANGE = 3, ORC_DUPLICATE = 5 };
+
+typedef struct {
+  int num_pages;
+  int num_qo_heads;
+  int num_kv_heads;
+  int head_dim;
+  int max_position;
+  double rope_theta;
+} orc_geom;
+
+/* ------------------------------------------------------------------------------------------ */
+/* IEEE 754 binary16 <-> binary64, written from the format's definition.                       */
+
+double orc_f16_to_f64(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int m = h & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24); /* zero or subnormal: m * 2^-24 */
+  } else if (e == 31) {
+    v = m ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(1024 + m), e - 25); /* (1 + m/1024) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round to nearest binary16, ties to even. */
+uint16_t orc_f64_to_f16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  if (isnan(x)) return 0x7e00;
+  double a = fabs(x);
+  if (isinf(a)) return sign | 0x7c00;
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);    /* a = f * 2^e2, f in [0.5, 1) */
+  int E = e2 - 1;   /* floor(log2 a) */
+  if (E < -14) E = -14; /* subnormal range shares the quantum 2^-24 */
+  double quantum = ldexp(1.0, E - 10);
+  double n = nearbyint(a / quantum); /* exact division; nearbyint rounds ties to even */
+  double r = n * quantum;
+  if (r >= 65536.0) return sign | 0x7c00; /* overflow */
+  if (r < ldexp(1.0, -14)) return sign | (uint16_t)(r / ldexp(1.0, -24)); /* subnormal */
+  int er;
+  frexp(r, &er);
+  int Er = er - 1;
+  uint16_t mant = (uint16_t)(r / ldexp(1.0, Er - 10) - 1024.0);
+  return sign | (uint16_t)((Er + 15) << 10) | mant;
+}
+
+static double g_f16_table[65536];
+static int g_table_ready = 0;
+
+/* Fill the decode cache (a table of orc_f16_to_f64 for every bit pattern). */
+void orc_init(void) {
+  if (g_table_ready) return;
+  for (int i = 0; i < 65536; ++i) g_f16_table[i] = orc_f16_to_f64((uint16_t)i);
+  g_table_ready = 1;
+}
+
+static inline double dec(uint16_t h) { return g_f16_table[h]; }
+
+void orc_f16_decode_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_f64(in[i]);
+}
+
+void orc_f16_encode_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_f16(in[i]);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* RoPE (rotate-half), fp64.                                                                   */
+
+void orc_rope(const double* x, double* y, int d, int64_t pos, double theta) {
+  int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
+    double phi = (double)pos * inv_freq;
+    double c = cos(phi), s = sin(phi);
+    double a = x[i], b = x[i + half];
+    y[i] = a * c - b * s;
+    y[i + half] = b * c + a * s;
+  }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Append: rotate q and k at their positions, write k and v into the page slots.               */
+
+static int64_t pool_row(const orc_geom* g, int64_t page, int kv, int head, int slot) {
+  /* element offset of pool[page][kv][head][slot][0] */
+  return (((page * 2 + kv) * g->num_kv_heads + head) * (int64_t)ORC_PAGE + slot) * g->head_dim;
+}
+
+static int cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const uint16_t* v, int T,
+               const int32_t* pos_map, const int32_t* append_indptr, int B,
+               const int32_t* page_indptr, const int32_t* page_indices, uint16_t* pool,
+               uint16_t* q_out) {
+  orc_init();
+  const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads;
+  if (d <= 0 || d % 2 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T < 0 || B < 0) return ORC_INVALID;
+  if (append_indptr[0] != 0 || append_indptr[B] != T || page_indptr[0] != 0) return ORC_INVALID;
+  for (int s = 0; s < B; ++s)
+    if (append_indptr[s + 1] < append_indptr[s] || page_indptr[s + 1] < page_indptr[s]) return ORC_INVALID;
+
+  /* validate every token before writing anything */
+  for (int s = 0; s < B; ++s) {
+    int t0 = append_indptr[s], t1 = append_indptr[s + 1];
+    int n_pages = page_indptr[s + 1] - page_indptr[s];
+    for (int t = t0; t < t1; ++t) {
+      int p = pos_map[t];
+      if (p < 0 || p >= g->max_position) return ORC_OUT_OF_RANGE;
+      if (p / ORC_PAGE >= n_pages) return ORC_OUT_OF_RANGE;
+      int page = page_indices[page_indptr[s] + p / ORC_PAGE];
+      if (page < 0 || page >= g->num_pages) return ORC_OUT_OF_RANGE;
+    }
+    if (t1 - t0 > 1) {
+      int32_t* sorted = (int32_t*)malloc(sizeof(int32_t) * (size_t)(t1 - t0));
+      memcpy(sorted, pos_map + t0, sizeof(int32_t) * (size_t)(t1 - t0));
+      qsort(sorted, (size_t)(t1 - t0), sizeof(int32_t), cmp_i32);
+      int dup = 0;
+      for (int i = 1; i < t1 - t0; ++i) dup |= (sorted[i] == sorted[i - 1]);
+      free(sorted);
+      if (dup) return ORC_DUPLICATE;
+    }
+  }
+
+  double* x = (double*)malloc(sizeof(double) * (size_t)d);
+  double* y = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int s = 0; s < B; ++s) {
+    for (int t = append_indptr[s]; t < append_indptr[s + 1]; ++t) {
+      int p = pos_map[t];
+      int64_t page = page_indices[page_indptr[s] + p / ORC_PAGE];
+      int slot = p % ORC_PAGE;
+      for (int h = 0; h < Hq; ++h) {
+        const uint16_t* src = q + ((int64_t)t * Hq + h) * d;
+        for (int i = 0; i < d; ++i) x[i] = dec(src[i]);
+        orc_rope(x, y, d, p, g->rope_theta);
+        for (int i = 0; i < d; ++i) q_out[((int64_t)t * Hq + h) * d + i] = orc_f64_to_f16(y[i]);
+      }
+      for (int h = 0; h < Hkv; ++h) {
+        const uint16_t* ks = k + ((int64_t)t * Hkv + h) * d;
+        const uint16_t* vs = v + ((int64_t)t * Hkv + h) * d;
+        for (int i = 0; i < d; ++i) x[i] = dec(ks[i]);
+        orc_rope(x, y, d, p, g->rope_theta);
+        uint16_t* kd = pool + pool_row(g, page, 0, h, slot);
+        uint16_t* vd = pool + pool_row(g, page, 1, h, slot);
+        for (int i = 0; i < d; ++i) kd[i] = orc_f64_to_f16(y[i]);
+        memcpy(vd, vs, sizeof(uint16_t) * (size_t)d);
+      }
+    }
+  }
+  free(x);
+  free(y);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Attention of one query head over logical tokens [t0, t1) of sequence s.                     */
+
+static int seq_len_of(const int32_t* page_indptr, const int32_t* last_page_len, int s, int* len) {
+  int n = page_indptr[s + 1] - page_indptr[s];
+  if (n < 0) return ORC_INVALID;
+  if (n == 0) {
+    *len = 0;
+    return ORC_OK;
+  }
+  int last = last_page_len[s];
+  if (last < 1 || last > ORC_PAGE) return ORC_OUT_OF_RANGE;
+  *len = (n - 1) * ORC_PAGE + last;
+  return ORC_OK;
+}
+
+/* o[d] = sum_t softmax(score)_t V_t, lse = ln sum_t exp(score_t); empty range: o = 0, lse = -inf */
+static int attend(const orc_geom* g, const uint16_t* pool, const double* q, int s, int kv_head,
+                  int t0, int t1, const int32_t* page_indptr, const int32_t* page_indices,
+                  double sm_scale, double* o, double* lse) {
+  const int d = g->head_dim;
+  for (int i = 0; i < d; ++i) o[i] = 0.0;
+  if (t1 <= t0) {
+    *lse = -INFINITY;
+    return ORC_OK;
+  }
+  double* score = (double*)malloc(sizeof(double) * (size_t)(t1 - t0));
+  double m = -INFINITY;
+  for (int t = t0; t < t1; ++t) {
+    int page = page_indices[page_indptr[s] + t / ORC_PAGE];
+    if (page < 0 || page >= g->num_pages) {
+      free(score);
+      return ORC_OUT_OF_RANGE;
+    }
+    const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);
+    double dot = 0.0;
+    for (int i = 0; i < d; ++i) dot += q[i] * dec(K[i]);
+    score[t - t0] = sm_scale * dot;
+    if (score[t - t0] > m) m = score[t - t0];
+  }
+  double l = 0.0;
+  for (int t = t0; t < t1; ++t) {
+    int page = page_indices[page_indptr[s] + t / ORC_PAGE];
+    const uint16_t* V = pool + pool_row(g, page, 1, kv_head, t % ORC_PAGE);
+    double w = exp(score[t - t0] - m);
+    l += w;
+    for (int i = 0; i < d; ++i) o[i] += w * dec(V[i]);
+  }
+  for (int i = 0; i < d; ++i) o[i] /= l;
+  *lse = m + log(l);
+  free(score);
+  return ORC_OK;
+}
+
+/* Full (unsplit) decode attention.  q_rope: [B][Hq][d] fp16 bits; out: [B][Hq][d]; lse: [B][Hq]. */
+int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
+                  const int32_t* page_indptr, const int32_t* page_indices,
+                  const int32_t* last_page_len, double sm_scale, double* out, double* lse) {
+  orc_init();
+  const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads;
+  if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0) return ORC_INVALID;
+  const int G = Hq / Hkv;
+  int rc = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
+    int s = (int)(sh / Hq), h = (int)(sh % Hq);
+    int len;
+    int r = seq_len_of(page_indptr, last_page_len, s, &len);
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) q[i] = dec(q_rope[sh * d + i]);
+    if (r == ORC_OK)
+      r = attend(g, pool, q, s, h / G, 0, len, page_indptr, page_indices, sm_scale, out + sh * d, lse + sh);
+    free(q);
+    if (r != ORC_OK) {
+#pragma omp critical
+      rc = r;
+    }
+  }
+  return rc;
+}
+
+/* Split-K partial attention.  Chunk size in pages: chunk_pages if > 0 (uniform), otherwise
+ * ceil(n_s / num_splits) for sequence s.  Chunk j covers pages [j*c, min((j+1)*c, n_s)).
+ * partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S] with S = num_out_splits. */
+int orc_split_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
+                        const int32_t* page_indptr, const int32_t* page_indices,
+                        const int32_t* last_page_len, int num_splits, int chunk_pages,
+                        int num_out_splits, double sm_scale, double* partial_o, double* partial_lse) {
+  orc_init();
+  const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads, S = num_out_splits;
+  if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0 || S <= 0) return ORC_INVALID;
+  if (chunk_pages <= 0 && num_splits <= 0) return ORC_INVALID;
+  const int G = Hq / Hkv;
+  for (int s = 0; s < B; ++s) {
+    int n = page_indptr[s + 1] - page_indptr[s];
+    int c = chunk_pages > 0 ? chunk_pages : (n + num_splits - 1) / num_splits;
+    int chunks = (c > 0) ? (n + c - 1) / c : 0;
+    if (chunks > S) return ORC_INVALID;
+  }
+  int rc = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
+    int s = (int)(sh / Hq), h = (int)(sh % Hq);
+    int len;
+    int r = seq_len_of(page_indptr, last_page_len, s, &len);
+    int n = page_indptr[s + 1] - page_indptr[s];
+    int c = chunk_pages > 0 ? chunk_pages : (n + num_splits - 1) / num_splits;
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) q[i] = dec(q_rope[sh * d + i]);
+    for (int j = 0; j < S && r == ORC_OK; ++j) {
+      int64_t t0 = (int64_t)j * c * ORC_PAGE, t1 = (int64_t)(j + 1) * c * ORC_PAGE;
+      if (t1 > len) t1 = len;
+      if (t0 > len) t0 = len;
+      r = attend(g, pool, q, s, h / G, (int)t0, (int)t1, page_indptr, page_indices, sm_scale,
+                 partial_o + (sh * S + j) * d, partial_lse + sh * S + j);
+    }
+    free(q);
+    if (r != ORC_OK) {
+#pragma omp critical
+      rc = r;
+    }
+  }
+  return rc;
+}
+
+/* Log-sum-exp merge of the partials: out = sum_j w_j o_j / sum_j w_j with w_j = exp(lse_j - M),
+ * M = max_j lse_j, lse = M + ln sum_j w_j.  out_f16 (nullable) gets out rounded to fp16. */
+int orc_combine(const double* partial_o, const double* partial_lse, int B, int Hq, int S, int d,
+                double* out, uint16_t* out_f16, double* lse) {
+  if (B < 0 || Hq <= 0 || S <= 0 || d <= 0) return ORC_INVALID;
+  for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
+    const double* L = partial_lse + sh * S;
+    double M = -INFINITY;
+    for (int j = 0; j < S; ++j)
+      if (L[j] > M) M = L[j];
+    double* o = out + sh * d;
+    for (int i = 0; i < d; ++i) o[i] = 0.0;
+    if (M == -INFINITY) {
+      lse[sh] = -INFINITY;
+    } else {
+      double W = 0.0;
+      for (int j = 0; j < S; ++j) {
+        if (L[j] == -INFINITY) continue;
+        double w = exp(L[j] - M);
+        W += w;
+        for (int i = 0; i < d; ++i) o[i] += w * partial_o[(sh * S + j) * d + i];
+      }
+      for (int i = 0; i < d; ++i) o[i] /= W;
+      lse[sh] = M + log(W);
+    }
+    if (out_f16)
+      for (int i = 0; i < d; ++i) out_f16[sh * d + i] = orc_f64_to_f16(o[i]);
+  }
+  return ORC_OK;
+}

@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in a copy of the oracle (CPU only) and check that the pins catch each.
+
+Each mutant is compiled from an edited copy of ``oracle/pkv_oracle.c`` into a temporary
+library; the pin suite then runs against it in a subprocess and must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
+
+MUTANTS = [
+    ("rope sign", "    y[i] = a * c - b * s;", "    y[i] = a * c + b * s;"),
+    ("rope frequency exponent", "pow(theta, -2.0 * (double)i / (double)d)", "pow(theta, -1.0 * (double)i / (double)d)"),
+    ("rope pairing", "double a = x[i], b = x[i + half];", "double a = x[i], b = x[d - 1 - i];"),
+    ("gqa head mapping", "s, h / G, 0, len,", "s, h % Hkv, 0, len,"),
+    ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
+    ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
+     "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
+    ("softmax scale dropped", "score[t - t0] = sm_scale * dot;", "score[t - t0] = dot;"),
+    ("combine lse", "lse[sh] = M + log(W);", "lse[sh] = log(W);"),
+    ("fp16 rounding truncates", "double n = nearbyint(a / quantum);", "double n = floor(a / quantum);"),
+    ("append page lookup", "      int64_t page = page_indices[page_indptr[s] + p / ORC_PAGE];",
+     "      int64_t page = page_indices[page_indptr[s] + p % ORC_PAGE];"),
+    ("empty chunk lse", "    *lse = -INFINITY;\n    return ORC_OK;\n  }\n  double* score",
+     "    *lse = 0.0;\n    return ORC_OK;\n  }\n  double* score"),
+    ("split partition floors", "int c = chunk_pages > 0 ? chunk_pages : (n + num_splits - 1) / num_splits;\n    double* q",
+     "int c = chunk_pages > 0 ? chunk_pages : n / num_splits + (n % num_splits > 1);\n    double* q"),
+    ("v not copied", "memcpy(vd, vs, sizeof(uint16_t) * (size_t)d);", "memcpy(vd, ks, sizeof(uint16_t) * (size_t)d);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for '{name}' must be unique"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(oracle.build_command(str(mutant), str(lib)), check=True)
+    env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"the pins did not catch the planted mistake '{name}'"
