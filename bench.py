@@ -1,0 +1,431 @@
+"""Benchmark of the decode-step paged-KV attention path (append -> split-K decode -> combine).
+
+Default workload: the Phi-3-mini-shaped single-stream decode (32 layers, 32 heads of 96, batch 1,
+context 4096, 16-slot pages, identity page table).  One step runs the whole path for every layer;
+the step is captured once as a CUDA graph with programmatic dependent launch and replayed.
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
+Multi-GPU runs (torchrun) are independent replicas: the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from pkv_inputs import workloads as W  # noqa: E402
+
+METRIC = "decode-attention KV GB/s & % of GB300 HBM roofline; attention µs/step/layer"
+DEFAULT_CONFIG = 2
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_phi3_b1_ctx4096.md")
+DECODE_SOURCE = os.path.join(ROOT, "paged_kv_decode_pkv_gb300", "csrc", "decode_partial.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        src = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
+        m_hash = re.search(r"decode_partial\.cu sha256:\s*([0-9a-f]{64})", text)
+        m_val = re.search(r"dram bytes per launch:\s*([0-9]+)", text)
+        if m_hash and m_val and m_hash.group(1) == src:
+            return int(m_val.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (test infrastructure: the oracle is never on the product path)
+
+
+def oracle_sample(step: W.Step, seconds: float, max_layers: int):
+    """Time the oracle (append + attention) layer by layer on the host cores until `seconds` of
+    oracle work or `max_layers` layers; returns (GB/s, threads, description)."""
+    import oracle
+
+    from tests import harness as H
+
+    # bound the sample to one sequence when a layer is large, so a few layers fit in the budget
+    seqs = list(range(step.batch))
+    if step.kv_bytes() > 256e6:
+        seqs = [int(np.argmax(step.seq_len))]
+    sub = W.substep(step, seqs) if len(seqs) < step.batch else step
+    done_bytes, done_time, layers = 0, 0.0, 0
+    for layer in range(max_layers):
+        pool = W.host_pool_pages(sub, layer, np.arange(sub.num_pages))
+        q, k, v = W.new_qkv(step, layer, rows=W.token_rows(step, seqs))
+        g = H.geometry(sub)
+        t0 = time.perf_counter()
+        q_out = oracle.append(g, q, k, v, sub.pos_map, sub.append_indptr, sub.page_indptr, sub.page_indices, pool)
+        oracle.attention(g, pool, q_out[H.query_rows(sub)], sub.page_indptr, sub.page_indices, sub.last_page_len)
+        done_time += time.perf_counter() - t0
+        done_bytes += sub.kv_bytes()
+        layers += 1
+        if done_time >= seconds:
+            break
+    what = (f"{layers} layer(s) x {len(seqs)} of {step.batch} sequence(s) of {step.cfg.name}: fp64 append + "
+            f"unsplit attention, {done_bytes / 1e9:.3f} GB of KV")
+    return done_bytes / done_time / 1e9, oracle.threads(), what
+
+
+def reference_sample(step: W.Step, budget_bytes: float = 2e9):
+    """The bounded sample the oracle arm times per step: the whole step when its KV fits the
+    budget, else one layer, else the longest sequence of one layer."""
+    cfg = step.cfg
+    if step.kv_bytes() * cfg.layers <= budget_bytes:
+        return list(range(cfg.layers)), list(range(step.batch))
+    if step.kv_bytes() <= budget_bytes:
+        return [0], list(range(step.batch))
+    return [0], [int(np.argmax(step.seq_len))]
+
+
+def run_reference(args):
+    """The oracle arm: fp64 CPU oracle on the host cores, same metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    from tests import harness as H
+
+    cfg = W.CONFIGS[args.config]
+    step = W.make_step(cfg)
+    layers, seqs = reference_sample(step)
+    sub = W.substep(step, seqs) if len(seqs) < step.batch else step
+    g = H.geometry(sub)
+    rows = W.token_rows(step, seqs)
+    inputs = [(W.host_pool_pages(sub, l, np.arange(sub.num_pages)), *W.new_qkv(step, l, rows=rows)) for l in layers]
+    times = []
+    for i in range(args.warmup + args.steps):
+        pools = [x[0].copy() for x in inputs]
+        t0 = time.perf_counter()
+        for pool, (_, q, k, v) in zip(pools, inputs):
+            q_out = oracle.append(g, q, k, v, sub.pos_map, sub.append_indptr, sub.page_indptr, sub.page_indices,
+                                  pool)
+            oracle.attention(g, pool, q_out[H.query_rows(sub)], sub.page_indptr, sub.page_indices,
+                             sub.last_page_len)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    sample_bytes = sub.kv_bytes() * len(layers)
+    value = sample_bytes / t / 1e9
+    sample = (f"each step: {len(layers)} of {cfg.layers} layer(s) x {len(seqs)} of {step.batch} sequence(s) of "
+              f"{cfg.name} ({sample_bytes / 1e6:.1f} MB KV): fp64 append + unsplit attention")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------------------------
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    cfg = W.CONFIGS[args.config]
+    step = W.make_step(cfg)
+    layers = list(range(cfg.layers))
+    pools = [W.device_pool(step, l) for l in layers]
+    cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+                      pools=pools, options=pkv.OPT_PDL)
+    B, T = step.batch, step.num_tokens
+    total_pages = int(step.page_indptr[-1])
+    S, chunk = cache.plan_decode(B, step.max_pages_per_seq, total_pages)
+
+    def h(a):
+        return torch.from_numpy(np.ascontiguousarray(a))
+
+    tab_host = {k: h(getattr(step, k)).pin_memory() for k in
+                ("pos_map", "append_indptr", "page_indptr", "page_indices", "last_page_len")}
+    tabs = {k: v.to(dev) for k, v in tab_host.items()}
+    use_q_indptr = int(step.new_tokens.max()) > 1
+    qkv_host = []
+    for l in layers:
+        q, k, v = W.new_qkv(step, l)
+        qkv_host.append(tuple(h(x).view(torch.float16).pin_memory() for x in (q, k, v)))
+    qkv = [tuple(x.to(dev) for x in t) for t in qkv_host]
+    q_out = [torch.empty((T, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
+    po = torch.empty((B, cfg.hq, S, cfg.head_dim), dtype=torch.float32, device=dev)
+    pl = torch.empty((B, cfg.hq, S), dtype=torch.float32, device=dev)
+    outs = [torch.empty((B, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
+    lses = [torch.empty((B, cfg.hq), dtype=torch.float32, device=dev) for _ in layers]
+    out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    lse_host = [torch.empty_like(x, device="cpu").pin_memory() for x in lses]
+
+    def layer_chain(l, events=None):
+        q, k, v = qkv[l]
+        cache.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                          tabs["page_indices"], q_out=q_out[l])
+        if events is not None:
+            events[0].record()
+        cache.decode_attention(l, q_out[l], tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
+                               step.max_pages_per_seq, q_indptr=tabs["append_indptr"] if use_q_indptr else None,
+                               total_pages=total_pages, partial_o=po, partial_lse=pl)
+        if events is not None:
+            events[1].record()
+        cache.combine(po, pl, out=outs[l], lse=lses[l])
+        if events is not None:
+            events[2].record()
+
+    def step_fn():
+        for l in layers:
+            layer_chain(l)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step_fn()
+    torch.cuda.synchronize()
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status {pkv.status_string(code)} flags {flags:#x}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_fn()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world > 1:
+            t = torch.tensor([x], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    # ---- timed region: K graph replays ----------------------------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record()
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record()
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after the timed region: {pkv.status_string(code)} flags {flags:#x}")
+    kv_step = step.kv_bytes() * cfg.layers
+    value = world * kv_step / (step_ms * 1e-3) / 1e9
+
+    # ---- per-kernel durations: events around decode and combine on the launching stream -----------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps * cfg.layers)]
+    with torch.cuda.stream(stream):
+        for l in layers:
+            layer_chain(l)
+        i = 0
+        for _ in range(args.steps):
+            for l in layers:
+                layer_chain(l, ev[i])
+                i += 1
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    kv_layer = step.kv_bytes()
+    achieved = kv_layer / (dec_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = ncu_traffic()
+
+    # ---- end to end through the API with host buffers ------------------------------------------
+    h2d = sum(t.numel() * t.element_size() for t in tab_host.values()) + \
+        sum(x.numel() * x.element_size() for t in qkv_host for x in t)
+    d2h = sum(o.numel() * o.element_size() for o in out_host) + sum(x.numel() * x.element_size() for x in lse_host)
+
+    def e2e_step():
+        for k_, v_ in tab_host.items():
+            tabs[k_].copy_(v_, non_blocking=True)
+        for l in layers:
+            for dst, src in zip(qkv[l], qkv_host[l]):
+                dst.copy_(src, non_blocking=True)
+            layer_chain(l)
+            out_host[l].copy_(outs[l], non_blocking=True)
+            lse_host[l].copy_(lses[l], non_blocking=True)
+
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_step()
+    torch.cuda.synchronize()
+
+    def timed_e2e(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+                stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                fn()
+                stream.synchronize()  # the step's result is on the host
+        barrier()
+        return max_over_ranks((time.perf_counter() - t0) / args.steps)
+
+    e2e_s = timed_e2e(e2e_graph.replay)
+    e2e_eager_s = timed_e2e(e2e_step)
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after the e2e region: {pkv.status_string(code)} flags {flags:#x}")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 data, f32 accumulate", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "batch": B, "q_heads": cfg.hq,
+                   "kv_heads": cfg.hkv, "head_dim": cfg.head_dim, "page_size": 16,
+                   "context_tokens": int(step.seq_len.sum()), "kv_bytes_per_step": kv_step,
+                   "splits": S, "chunk_pages": chunk,
+                   "l2": f"inputs larger than L2: {kv_step / 1e9:.2f} GB of KV per step",
+                   "launch": "CUDA graph of the step, programmatic dependent launch",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm_roofline_frac_step": value / world / peak,
+        "attention_us_per_step_per_layer": (dec_ms + comb_ms) * 1e3,
+        "step_us_per_layer": step_ms * 1e3 / cfg.layers,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "decode_kernel",
+                     "algorithmic_bytes_per_launch": kv_layer, "avg_launch_us": dec_ms * 1e3,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "e2e": {"value": world * kv_step / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "mode": "CUDA graph of the API calls",
+                "eager_value": world * kv_step / e2e_eager_s / 1e9, "eager_ms_per_step": e2e_eager_s * 1e3},
+        "gpu_launches": args.steps * cfg.layers * 3,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, threads, what = oracle_sample(step, args.cpu_seconds, cfg.layers)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": what}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

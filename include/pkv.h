@@ -1,0 +1,239 @@
+/*
+ * pkv.h - C ABI of the GB300 paged-KV decode attention library (libpkv.so).
+ *
+ * The library implements, for one transformer layer at a time, the decode-step
+ * attention path over a paged KV cache:
+ *
+ *   1. pkv_append_rope       rotate the new tokens' q and k with RoPE and write
+ *                            k and v into 16-slot pages of the cache;
+ *   2. pkv_decode_attention  split-K partial attention of every query head over
+ *                            its sequence's pages;
+ *   3. pkv_combine           log-sum-exp merge of the partials.
+ *
+ * Sources: Zero TVM Documentation ("KV cache", "Decode loop", "How it works",
+ * "Port to Phi-4-mini or Qwen3"); the MLC model artifact manifest page (the
+ * create_kv_cache role "takes only its size arguments"; decode_tokens takes a
+ * [batch_size, 1] batch); everything-webgpu AI.md (fail fast, typed errors).
+ *
+ * Conventions that hold for every entry point:
+ *  - Ownership: the caller allocates and frees every device buffer (pools, the
+ *    RoPE table, the status word, q/k/v, page tables, partials, outputs).  A
+ *    pkv_cache handle owns host memory only; pkv_destroy frees nothing else.
+ *  - Device: a cache is bound to the CUDA device that was current when it was
+ *    created; call the other entry points with that device current.
+ *  - Asynchrony: calls enqueue kernels on the given stream and return; results
+ *    are stream-ordered.  Only pkv_create_cache and pkv_check_status block.
+ *  - Errors found on the host (null pointers, bad sizes, unsupported shapes)
+ *    return a status before anything is enqueued and nothing is written.
+ *    Errors that only the device can see (an index out of range in a page table
+ *    or position map) make the kernel skip the offending read or write and set
+ *    bits in the cache's status word; pkv_check_status reports them.  No
+ *    kernel traps, asserts or aborts.
+ *  - int32 index arrays are device arrays of the stated length.
+ *  - fp16 means IEEE binary16; results are rounded to nearest even.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Slots per KV page (Zero TVM Documentation, "KV cache": fixed pages of 16 slots). */
+#define PKV_PAGE_SIZE 16
+
+typedef struct CUstream_st* pkv_stream_t; /* a cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent sizes */
+  PKV_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels are built for */
+  PKV_ERR_OUT_OF_RANGE = 3, /* device saw an index out of range (see pkv_check_status) */
+  PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  PKV_ERR_TIMEOUT = 5       /* a device-side wait gave up (reported by pkv_check_status) */
+} pkv_status;
+
+/* Bits of the device status word (pkv_check_status returns them in *flags). */
+#define PKV_FLAG_BAD_PAGE 0x1     /* a page-table entry outside [0, num_pages) */
+#define PKV_FLAG_BAD_POSITION 0x2 /* a position < 0, >= max_position, or past the sequence's pages */
+#define PKV_FLAG_BAD_SEQUENCE 0x4 /* last_page_len outside [1, 16], more pages than declared, bad token or query range */
+#define PKV_FLAG_TIMEOUT 0x8      /* a bounded wait on a shared-memory barrier expired */
+
+/* Cache option bits (pkv_cache_desc.options). */
+#define PKV_OPT_PDL 0x1 /* launch with programmatic dependent launch: each kernel may start while
+                           the previous kernel in the stream finishes.  Kernels wait for it before
+                           reading q, k, v, the pool and the partials, but read their int32 page
+                           tables (page_indptr, append_indptr, last_page_len, q_indptr) earlier:
+                           do not produce those arrays in the kernel launched right before. */
+
+typedef struct pkv_cache pkv_cache; /* opaque, host-only */
+
+/*
+ * Geometry and caller-owned device storage of a paged KV cache.
+ *
+ * Pool layout, one pool per layer (a reading of Zero TVM Documentation, "KV
+ * cache": one buffer of pages per layer; the page-internal order is ours):
+ *     fp16 pool[num_pages][2][num_kv_heads][16][head_dim]
+ * index 0 of the second dimension holds K (rotated), index 1 holds V, so the
+ * K (or V) of one page and one KV head is a contiguous 16*head_dim*2-byte run.
+ */
+typedef struct {
+  int num_layers;        /* >= 1 */
+  int num_pages;         /* pages in each layer's pool, >= 1 */
+  int page_size;         /* must be PKV_PAGE_SIZE */
+  int num_qo_heads;      /* Hq >= 1 */
+  int num_kv_heads;      /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 */
+  int head_dim;          /* 64, 96 or 128 */
+  int max_position;      /* appended positions must lie in [0, max_position) */
+  double rope_theta;     /* RoPE base (e.g. 1e4, 1e6) */
+  void* const* layer_pools; /* host array [num_layers] of device pointers, each 256-byte aligned,
+                               pkv_pool_bytes(num_pages, num_kv_heads, head_dim) bytes */
+  float* rope_table;     /* device buffer of pkv_rope_table_bytes(max_position, head_dim) bytes,
+                            filled by pkv_create_cache; must outlive the cache */
+  int* status_word;      /* device int32, zeroed by pkv_create_cache; must outlive the cache */
+  int options;           /* PKV_OPT_* bits */
+} pkv_cache_desc;
+
+/* Bytes of one layer's pool. */
+size_t pkv_pool_bytes(int num_pages, int num_kv_heads, int head_dim);
+
+/* Bytes of the RoPE table: max_position * (head_dim / 2) (cos, sin) pairs of fp32, computed on
+ * the host in fp64 as cos/sin(p * theta^(-2i/head_dim)) and rounded once to fp32. */
+size_t pkv_rope_table_bytes(int max_position, int head_dim);
+
+/*
+ * Create a cache handle over caller-owned storage (the create_kv_cache role of the MLC model
+ * artifact manifest page: the constructor takes sizes only; here also the storage).
+ * Blocks: fills desc->rope_table and zeroes desc->status_word with synchronous copies, and
+ * builds one TMA descriptor per layer pool.  The pools' contents are not touched.
+ * Returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED for bad descriptors, PKV_ERR_CUDA if a
+ * CUDA call fails; *out is set only on PKV_OK.
+ */
+pkv_status pkv_create_cache(const pkv_cache_desc* desc, pkv_cache** out);
+
+/* Free the handle (host memory only).  NULL is ignored. */
+void pkv_destroy(pkv_cache* cache);
+
+/*
+ * RoPE + KV append for one layer (Zero TVM Documentation, "Decode loop": the QKV dispatch
+ * rotates q and k at posMap and scatters k and v into page slots; "KV cache": K is rotated
+ * before the cache write).
+ *
+ *   q       fp16 [num_tokens][Hq][head_dim]   raw queries of the new tokens
+ *   k, v    fp16 [num_tokens][Hkv][head_dim]  raw keys and values of the new tokens
+ *   pos_map int32 [num_tokens]                position of each new token in its sequence
+ *   append_indptr int32 [batch+1]             tokens of sequence s are append_indptr[s] ..
+ *                                             append_indptr[s+1]-1 (non-decreasing, [0] = 0,
+ *                                             [batch] = num_tokens)
+ *   page_indptr   int32 [batch+1]             pages of sequence s are page_indices[page_indptr[s]
+ *   page_indices  int32 [page_indptr[batch]]  .. page_indptr[s+1]-1], logical page order
+ *   q_out   fp16 [num_tokens][Hq][head_dim]   rotated queries (may not alias q)
+ *
+ * Token t of sequence s at position p = pos_map[t] goes to page
+ * page_indices[page_indptr[s] + p / 16], slot p % 16:
+ *   pool[page][0][g][slot][:] = RoPE(k[t][g][:], p)   for every KV head g
+ *   pool[page][1][g][slot][:] = v[t][g][:]            (bit copy)
+ *   q_out[t][h][:]            = RoPE(q[t][h][:], p)   for every query head h
+ * RoPE is the rotate-half form: element i pairs with i + head_dim/2.  Rotations are computed
+ * in fp32 from the fp64-derived table; results are rounded to fp16.
+ * Positions must be distinct within a sequence (duplicates: the last write wins, unspecified).
+ * Device-detected: positions out of range (PKV_FLAG_BAD_POSITION), page ids out of range
+ * (PKV_FLAG_BAD_PAGE), token ranges outside [0, num_tokens) (PKV_FLAG_BAD_SEQUENCE);
+ * the affected token is skipped.  num_tokens == 0 or batch == 0 is a no-op.
+ */
+pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const void* k, const void* v,
+                           const int32_t* pos_map, const int32_t* append_indptr, int num_tokens,
+                           int batch, const int32_t* page_indptr, const int32_t* page_indices,
+                           void* q_out, pkv_stream_t stream);
+
+/*
+ * Split plan (host only, no device access).  Returns in *splits the number of partial slots per
+ * (sequence, query head) that pkv_decode_attention will produce for these arguments, and in
+ * *chunk_pages the uniform chunk size in pages (0 when num_splits > 0 selects per-sequence
+ * chunks of ceil(n_s / num_splits) pages).
+ *   num_splits > 0            per-sequence chunks: c_s = ceil(n_s / num_splits), splits = num_splits
+ *   chunk_pages > 0           uniform chunks of chunk_pages pages, splits = ceil(max_pages / c)
+ *   both 0                    the planner picks a uniform chunk size from the batch, the KV heads,
+ *                             max_pages_per_seq, total_pages (0 = unknown, taken as
+ *                             batch * max_pages_per_seq) and the device's SM count, so that the
+ *                             work items fill the resident warps; the split count never exceeds
+ *                             max_splits.
+ * (Zero TVM Documentation, "How it works": split-K over KV chunks with a fixed ?splitk=N; the
+ * choice from length and SM count is this library's.)
+ */
+pkv_status pkv_plan_decode(const pkv_cache* cache, int batch, int max_pages_per_seq, int total_pages,
+                           int num_splits, int chunk_pages, int max_splits, int* splits,
+                           int* chunk_pages_out);
+
+/* Bytes of partial_o for (batch, Hq, splits, head_dim): batch*Hq*splits*head_dim*4.
+ * partial_lse takes batch*Hq*splits*4 bytes. */
+size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim);
+
+/*
+ * Split-K partial attention for one layer (Zero TVM Documentation, "How it works": attention
+ * split over KV chunks; "Port to Phi-4-mini or Qwen3": KV heads repeated for grouped queries).
+ *
+ *   q_rope  fp16 [rows][Hq][head_dim]  rotated queries (e.g. q_out of pkv_append_rope)
+ *   q_indptr int32 [batch+1] or NULL   NULL: sequence s uses row s; otherwise row
+ *                                      q_indptr[s+1]-1 (the last appended token of s)
+ *   page_indptr, page_indices          as for pkv_append_rope (after the append)
+ *   last_page_len int32 [batch]        valid slots of each sequence's last page, in [1, 16];
+ *                                      sequence length = 16 * (n_s - 1) + last_page_len[s]
+ *                                      (n_s = 0 means an empty sequence)
+ *   max_pages_per_seq                  an upper bound of every n_s
+ *   total_pages                        page_indptr[batch] if known on the host, else 0
+ *   num_splits, chunk_pages, max_splits  split selection, see pkv_plan_decode
+ *   sm_scale                           score scale; 0 selects 1/sqrt(head_dim)
+ *   partial_o   fp32 [batch][Hq][S][head_dim]  S = *splits_used (capacity max_splits)
+ *   partial_lse fp32 [batch][Hq][S]            natural-log LSE of each chunk
+ *   splits_used (host, nullable)       receives S
+ *
+ * Query head h reads KV head h / (Hq / Hkv).  Chunk j of sequence s covers its pages
+ * [j*c, min((j+1)*c, n_s)); for each (s, h, j) with at least one token:
+ *   partial_lse = ln sum_t exp(sm_scale * q.K_t),  partial_o = sum_t softmax_t * V_t
+ * in fp32 from fp16 data.  Chunks with no token get partial_lse = -inf and partial_o is not
+ * written.  Device-detected: page ids out of range (the page is masked out), n_s above
+ * max_pages_per_seq, bad last_page_len or q_indptr rows (the sequence is reported empty).
+ */
+pkv_status pkv_decode_attention(const pkv_cache* cache, int layer, const void* q_rope,
+                                const int32_t* q_indptr, const int32_t* page_indptr,
+                                const int32_t* page_indices, const int32_t* last_page_len, int batch,
+                                int max_pages_per_seq, int total_pages, int num_splits,
+                                int chunk_pages, int max_splits, float sm_scale, float* partial_o,
+                                float* partial_lse, int* splits_used, pkv_stream_t stream);
+
+/*
+ * Log-sum-exp combine (Zero TVM Documentation, "How it works": one combine dispatch per layer
+ * after split-K attention).  For each (s, h): M = max_j lse_j, w_j = exp(lse_j - M),
+ *   out[s][h][:] = fp16( sum_j w_j o_j / sum_j w_j ),   lse_out[s][h] = M + ln sum_j w_j.
+ * Splits with lse_j = -inf are skipped (their o_j is not read); if every split is -inf,
+ * out = 0 and lse_out = -inf.  out: fp16 [batch][Hq][head_dim]; lse_out: fp32 [batch][Hq]
+ * or NULL.  num_splits >= 1; head_dim in {64, 96, 128}.
+ * The cache supplies the launch options (PKV_OPT_PDL); it may be NULL for plain launches.
+ */
+pkv_status pkv_combine(const pkv_cache* cache, const float* partial_o, const float* partial_lse,
+                       int batch, int num_qo_heads, int num_splits, int head_dim, void* out,
+                       float* lse_out, pkv_stream_t stream);
+
+/*
+ * Synchronise `stream`, read and clear the cache's status word.  Returns PKV_OK when no bit was
+ * set, PKV_ERR_TIMEOUT when PKV_FLAG_TIMEOUT was set, PKV_ERR_OUT_OF_RANGE for any other bit,
+ * PKV_ERR_CUDA if a CUDA call failed.  flags (nullable) receives the raw bits.
+ */
+pkv_status pkv_check_status(pkv_cache* cache, pkv_stream_t stream, int* flags);
+
+/* Static description of a status code. */
+const char* pkv_status_string(pkv_status status);
+
+/* Number of streaming multiprocessors of the cache's device and the resident warps the decode
+ * kernel uses per SM (what the planner fills). */
+pkv_status pkv_device_info(const pkv_cache* cache, int* num_sms, int* decode_warps_per_sm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -70,6 +70,8 @@ def _L():
         lib.orc_split_attention.argtypes = [P, P, P, i, P, P, P, i, i, i, d, P, P]
         lib.orc_combine.restype = i
         lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P]
+        lib.orc_threads.restype = i
+        lib.orc_threads.argtypes = []
         lib.orc_init.restype = None
         lib.orc_init()
         _lib = lib
@@ -93,6 +95,11 @@ class Geometry:
     def c(self) -> Geom:
         return Geom(self.num_pages, self.num_qo_heads, self.num_kv_heads, self.head_dim,
                     self.max_position, self.rope_theta)
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_L().orc_threads())
 
 
 def f16_to_f64(bits) -> np.ndarray:

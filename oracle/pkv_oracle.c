@@ -33,6 +33,7 @@
  *  - fp16 results are rounded to nearest, ties to even.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -90,6 +91,9 @@ uint16_t orc_f64_to_f16(double x) {
   uint16_t mant = (uint16_t)(r / ldexp(1.0, Er - 10) - 1024.0);
   return sign | (uint16_t)((Er + 15) << 10) | mant;
 }
+
+/* Threads the OpenMP loops below use (reported with CPU timings). */
+int orc_threads(void) { return omp_get_max_threads(); }
 
 static double g_f16_table[65536];
 static int g_table_ready = 0;

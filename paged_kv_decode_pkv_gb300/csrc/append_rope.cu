@@ -1,0 +1,163 @@
+// RoPE + KV append: rotate the new tokens' q and k at their positions and scatter k and v into
+// their page slots (Zero TVM Documentation, "Decode loop": the QKV dispatch applies RoPE and
+// writes the KV cache; "KV cache": K is rotated before the cache write).
+//
+// One CTA handles kTokensPerCta consecutive tokens.  Every thread moves 16-byte vectors: a RoPE
+// unit is 8 consecutive elements i..i+7 of one head together with their rotation partners
+// i+d/2..i+d/2+7 (rotate-half form), a V unit is 8 consecutive elements.  The cos/sin values come
+// from the fp64-derived fp32 table built at cache creation; the rotation is evaluated in fp32
+// with fused multiply-adds and rounded once to fp16.  V is a bit copy.
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTokensPerCta = 4;
+constexpr int kIndptrSmemCap = 8192;  // sequences whose append_indptr fits the shared copy
+
+struct TokenSlot {
+  long long k_off;  // element offset of pool[page][0][0][slot][0]; -1 = skip the token
+  int pos;
+};
+
+__device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const float2* cs, uint4& out_lo,
+                                      uint4& out_hi) {
+  const __half2* a = reinterpret_cast<const __half2*>(&lo);
+  const __half2* b = reinterpret_cast<const __half2*>(&hi);
+  __half2* ya = reinterpret_cast<__half2*>(&out_lo);
+  __half2* yb = reinterpret_cast<__half2*>(&out_hi);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 xa = __half22float2(a[e]);
+    const float2 xb = __half22float2(b[e]);
+    const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];  // (cos, sin) of elements 2e and 2e+1
+    // x'_i = x_i cos - x_{i+d/2} sin ;  x'_{i+d/2} = x_{i+d/2} cos + x_i sin
+    const float lo0 = __fmaf_rn(xa.x, c0.x, -__fmul_rn(xb.x, c0.y));
+    const float lo1 = __fmaf_rn(xa.y, c1.x, -__fmul_rn(xb.y, c1.y));
+    const float hi0 = __fmaf_rn(xb.x, c0.x, __fmul_rn(xa.x, c0.y));
+    const float hi1 = __fmaf_rn(xb.y, c1.x, __fmul_rn(xa.y, c1.y));
+    ya[e] = __floats2half2_rn(lo0, lo1);
+    yb[e] = __floats2half2_rn(hi0, hi1);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
+  __shared__ int s_indptr[kIndptrSmemCap + 1];
+  __shared__ TokenSlot s_tok[kTokensPerCta];
+  pdl_launch_dependents();
+
+  const int t0 = blockIdx.x * kTokensPerCta;
+  const bool indptr_in_smem = p.batch <= kIndptrSmemCap;
+  if (indptr_in_smem) {
+    for (int i = threadIdx.x; i <= p.batch; i += kThreads) s_indptr[i] = p.append_indptr[i];
+  }
+  __syncthreads();
+  const int* indptr = indptr_in_smem ? s_indptr : p.append_indptr;
+
+  if (threadIdx.x < kTokensPerCta) {
+    const int t = t0 + threadIdx.x;
+    TokenSlot ts{-1, 0};
+    if (t < p.num_tokens) {
+      // sequence of token t: the last s with indptr[s] <= t
+      int lo = 0, hi = p.batch;  // invariant: indptr[lo] <= t < indptr[hi] when t is in range
+      if (indptr[0] <= t && t < indptr[p.batch]) {
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (indptr[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int s = lo;
+        const int pos = p.pos_map[t];
+        const int first = p.page_indptr[s];
+        const int n_pages = p.page_indptr[s + 1] - first;
+        if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
+          atomicOr(p.status, kFlagBadPosition);
+        } else {
+          const int page = p.page_indices[first + (pos >> 4)];
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.status, kFlagBadPage);
+          } else {
+            ts.k_off = ((long long)page * 2 * p.hkv * kPageSize + (pos & 15)) * D;
+            ts.pos = pos;
+          }
+        }
+      } else {
+        atomicOr(p.status, kFlagBadSequence);
+      }
+    }
+    s_tok[threadIdx.x] = ts;
+  }
+  __syncthreads();
+  pdl_wait();  // q, k, v and the pool may be produced or read by the preceding kernel
+
+  constexpr int kRopeUnits = D / 16;  // 8-element blocks in the first half of a head
+  constexpr int kVUnits = D / 8;
+  const int q_units = p.hq * kRopeUnits;
+  const int k_units = p.hkv * kRopeUnits;
+  const int v_units = p.hkv * kVUnits;
+  const int per_token = q_units + k_units + v_units;
+  const long long head_stride = (long long)kPageSize * D;  // pool elements between heads
+
+  for (int idx = threadIdx.x; idx < kTokensPerCta * per_token; idx += kThreads) {
+    const int tk = idx / per_token;
+    const int u = idx - tk * per_token;
+    const int t = t0 + tk;
+    const TokenSlot ts = s_tok[tk];
+    if (ts.k_off < 0) continue;
+    if (u < q_units + k_units) {
+      const bool is_q = u < q_units;
+      const int uu = is_q ? u : u - q_units;
+      const int h = uu / kRopeUnits;
+      const int i0 = (uu - h * kRopeUnits) * 8;
+      const __half* src = is_q ? p.q + ((long long)t * p.hq + h) * D : p.k + ((long long)t * p.hkv + h) * D;
+      const uint4 lo = *reinterpret_cast<const uint4*>(src + i0);
+      const uint4 hi = *reinterpret_cast<const uint4*>(src + i0 + D / 2);
+      float2 cs[8];
+      const float4* tab = reinterpret_cast<const float4*>(p.rope + (long long)ts.pos * (D / 2) + i0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 f = tab[e];
+        cs[2 * e] = make_float2(f.x, f.y);
+        cs[2 * e + 1] = make_float2(f.z, f.w);
+      }
+      uint4 ylo, yhi;
+      rope8(lo, hi, cs, ylo, yhi);
+      __half* dst = is_q ? p.q_out + ((long long)t * p.hq + h) * D : p.pool + ts.k_off + h * head_stride;
+      *reinterpret_cast<uint4*>(dst + i0) = ylo;
+      *reinterpret_cast<uint4*>(dst + i0 + D / 2) = yhi;
+    } else {
+      const int uu = u - q_units - k_units;
+      const int h = uu / kVUnits;
+      const int i0 = (uu - h * kVUnits) * 8;
+      const uint4 val = *reinterpret_cast<const uint4*>(p.v + ((long long)t * p.hkv + h) * D + i0);
+      __half* dst = p.pool + ts.k_off + (long long)p.hkv * head_stride + h * head_stride;  // V block
+      *reinterpret_cast<uint4*>(dst + i0) = val;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) {
+  if (p.num_tokens <= 0 || p.batch <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.num_tokens + kTokensPerCta - 1) / kTokensPerCta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (p.head_dim) {
+    case 64: return cudaLaunchKernelEx(&cfg, append_rope_kernel<64>, p);
+    case 96: return cudaLaunchKernelEx(&cfg, append_rope_kernel<96>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, append_rope_kernel<128>, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

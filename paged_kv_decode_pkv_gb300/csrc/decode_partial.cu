@@ -1,0 +1,641 @@
+// Split-K partial attention over paged KV (Zero TVM Documentation, "How it works": attention
+// split over KV chunks, then a combine; "KV cache": 16-slot pages behind a page table; "Port to
+// Phi-4-mini or Qwen3": query head h reads KV head h / (Hq / Hkv)).
+//
+// Work decomposition.  A work item is (sequence s, chunk j, KV head g): the pages
+// [j*c, min((j+1)*c, n_s)) of s for one KV head and all G = Hq/Hkv query heads that read it, so
+// every KV page is fetched once per KV head.  Items are enumerated sequence-major through a
+// prefix sum of items per sequence that each CTA builds in shared memory from page_indptr.  The
+// grid is persistent (one CTA per SM); every warp owns items gw, gw + W, gw + 2W, ... (W = warps
+// in the grid) and works alone: no CTA-wide barrier after the prologue.
+//
+// Memory pipeline.  Each warp has a private ring of `nstage` shared-memory stages.  Lane 0 is the
+// producer: for each page it issues one TMA tensor copy per box of the page's K and V blocks
+// (fp16 [2][16][head_dim] of one KV head, a 4-D tensor map over the pool), plus a bulk copy of
+// the item's G query rows for the first page of an item, all completing on the stage's mbarrier.
+// The same warp consumes stages in order and refills each stage right after it is consumed, so
+// nstage pages per warp are in flight.  Per-stage metadata (sequence, chunk, head, valid slots,
+// first/last flags) travels through shared memory with the barrier's release/acquire order.
+//
+// Compute.  G = 1 runs on CUDA cores: a half-warp covers one 16-slot row pair, each lane owns
+// head_dim/16 dimensions; q.k partials of 8 rows are reduced with a transposing butterfly (one
+// shuffle per row), the online softmax runs in the log2 domain, and P.V reuses the lane's
+// dimensions.  G >= 2 runs q.K^T and P.V on tensor cores with mma.sync m16n8k16 (fp16 in, fp32
+// accumulate): the G query heads are rows of A (padded to 16), the 16 slots of a page are two
+// n-blocks, and the score accumulators are re-used directly as the A operand of P.V.  K/V boxes
+// use the 128-byte (64-byte for head_dim 96) TMA swizzle so the ldmatrix row reads are free of
+// bank conflicts.
+//
+// Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
+// bounded time for its own copies in flight and returns.
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+constexpr int kMetaValid = 0x1f;
+constexpr int kMetaFirst = 1 << 5;
+constexpr int kMetaLast = 1 << 6;
+constexpr int kMetaLastChunk = 1 << 7;
+constexpr int kMetaEmpty = 1 << 8;
+
+struct __align__(16) StageMeta {
+  int s, j, g, flags;
+};
+
+constexpr int kSmemBudget = 232448;  // 227 KB, the per-block opt-in maximum
+
+struct Layout {
+  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, total;
+};
+
+__host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch) {
+  Layout L;
+  const int n = warps * nstage;
+  L.stage_bytes = 64 * head_dim;  // K and V of one page for one KV head
+  L.qslot_bytes = (group * head_dim * 2 + 127) & ~127;
+  L.q_off = n * L.stage_bytes;
+  L.bar_off = L.q_off + n * L.qslot_bytes;
+  L.meta_off = L.bar_off + n * 8;
+  L.meta_off = (L.meta_off + 15) & ~15;
+  L.prefix_off = L.meta_off + n * 16;
+  L.total = L.prefix_off + (batch + 1) * 4 + 1024;  // + slack to align the base to 1024
+  return L;
+}
+
+// Chunks of a sequence with n pages; c receives the chunk size.  Returns 0 for an invalid n.
+__device__ __forceinline__ int seq_chunks(const DecodeParams& p, int n, int& c) {
+  if (n < 0 || n > p.max_pages) return 0;
+  if (n == 0) {
+    c = 1;
+    return 1;
+  }
+  c = p.chunk_pages > 0 ? p.chunk_pages : (n + p.splits - 1) / p.splits;
+  const int nch = (n + c - 1) / c;
+  return nch <= p.splits ? nch : 0;
+}
+
+// ------------------------------------------------------------------------------------------------
+// CUDA-core compute for one query head per KV head.
+
+template <int D>
+struct GroupOne {
+  static constexpr int DPL = D / 16;  // dimensions per lane
+  float q[DPL], o[DPL], m, l;
+  int lane, half, li;
+
+  __device__ void init(int lane_) {
+    lane = lane_;
+    half = lane >> 4;
+    li = lane & 15;
+  }
+
+  __device__ static void load_row(const unsigned char* row, int li, float (&x)[DPL]) {
+    if constexpr (D == 128) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + li * 16);
+      const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+    } else if constexpr (D == 96) {
+      const unsigned char* b = row + li * 12;
+#pragma unroll
+      for (int e = 0; e < 3; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(b + 4 * e));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(row + li * 8);
+      const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 f = __half22float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+    }
+  }
+
+  __device__ void begin(const unsigned char* qslot, float scale_log2) {
+    float x[DPL];
+    load_row(qslot, li, x);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      q[e] = x[e] * scale_log2;
+      o[e] = 0.f;
+    }
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  __device__ void page(const unsigned char* stage, int nvalid) {
+    const unsigned char* Kb = stage;
+    const unsigned char* Vb = stage + kPageSize * D * 2;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float x[DPL];
+      load_row(Kb + (2 * i + half) * D * 2, li, x);
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) a = fmaf(q[e], x[e], a);
+      acc[i] = a;
+    }
+    // Transposing butterfly over the 16 lanes of each half: after the xor-8/4/2 steps lane li
+    // holds row pair-sum for row index (li >> 1), the xor-1 step completes the sum.
+    const bool b3 = li & 8, b2 = li & 4, b1 = li & 2;
+    float t4[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float send = b3 ? acc[a] : acc[a + 4];
+      const float keep = b3 ? acc[a + 4] : acc[a];
+      t4[a] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
+    float t2[2];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const float send = b2 ? t4[a] : t4[a + 2];
+      const float keep = b2 ? t4[a + 2] : t4[a];
+      t2[a] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    float t1 = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(kFull, b1 ? t2[0] : t2[1], 2);
+    float sc = t1 + __shfl_xor_sync(kFull, t1, 1);
+    const int row = 2 * ((li >> 1) & 7) + half;
+    sc = (row < nvalid) ? sc : -INFINITY;
+
+    float mx = sc;
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const float alpha = exp2f(m - m_new);
+    const float pr = exp2f(sc - m_new);
+    l = l * alpha + ((li & 1) ? 0.f : pr);
+    m = m_new;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] *= alpha;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float pi = __shfl_sync(kFull, pr, (lane & 16) | (2 * i));
+      if (2 * i + half < nvalid) {
+        float x[DPL];
+        load_row(Vb + (2 * i + half) * D * 2, li, x);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = fmaf(pi, x[e], o[e]);
+      }
+    }
+  }
+
+  // Writes the item's partial; returns false when nothing was accumulated.
+  __device__ bool finish(float* po, float* pl, long long row_base, int S, int j) {
+    float lt = l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFull, lt, off);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], 16);
+    if (!(lt > 0.f)) return false;
+    const float inv = 1.f / lt;
+    if (half == 0) {
+      float* dst = po + (row_base * S + j) * D + li * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) dst[e] = o[e] * inv;
+    }
+    if (lane == 0) pl[row_base * S + j] = (m + log2f(lt)) * kLn2;
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core compute for a group of G in [2, 8] query heads per KV head.
+
+template <int D>
+struct GroupMma {
+  static constexpr int E = (D == 96) ? 32 : 64;  // TMA box extent along head_dim
+  static constexpr int REGION = 64 * E;          // bytes of one box: [2][16][E] fp16
+  static constexpr int SWZ = (E == 64) ? 7 : 3;  // 128-byte or 64-byte swizzle
+  static constexpr int KS = D / 16;              // k-steps of q.K^T
+  static constexpr int NB = D / 8;               // n-blocks of P.V
+  uint32_t qa[KS][2];
+  float acc[NB][4];
+  float m, l;
+  int lane, h, group;
+
+  __device__ void init(int lane_, int group_) {
+    lane = lane_;
+    h = lane >> 2;
+    group = group_;
+  }
+
+  // Shared-memory address of the 16-byte chunk holding (kv, slot t, dims dim..dim+7).
+  __device__ static uint32_t chunk_addr(uint32_t stage, int kv, int t, int dim) {
+    const int u = dim / E;
+    const uint32_t off = (uint32_t)((kv * kPageSize + t) * (E * 2) + (dim % E) * 2);
+    return stage + u * REGION + (off ^ (((off >> 7) & SWZ) << 4));
+  }
+
+  __device__ void begin(const unsigned char* qslot) {
+    const int c = 2 * (lane & 3);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (h < group) {
+        const __half* qr = reinterpret_cast<const __half*>(qslot) + h * D + ks * 16 + c;
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qr);
+        qa[ks][1] = *reinterpret_cast<const uint32_t*>(qr + 8);
+      } else {
+        qa[ks][0] = 0u;
+        qa[ks][1] = 0u;
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  __device__ void page(unsigned char* stage_ptr, int nvalid, float scale_log2) {
+    const uint32_t stage = smem_u32(stage_ptr);
+    if (nvalid < kPageSize) {
+      // Slots past the sequence end may hold anything (even NaN): zero their V rows so that
+      // P = 0 times V stays 0 inside the tensor-core product.
+      constexpr int kChunksPerRow = D / 8;
+      const int n = (kPageSize - nvalid) * kChunksPerRow;
+      for (int i = lane; i < n; i += 32) {
+        const int t = nvalid + i / kChunksPerRow;
+        const int dim = (i % kChunksPerRow) * 8;
+        const uint32_t a = chunk_addr(stage, 1, t, dim);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+      }
+      __syncwarp();
+    }
+    // scores S^T[h][t] = q_h . K_t : rows = query heads, columns = slots (two n-blocks)
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, r = lane & 7;
+      const int t = (mi >> 1) * 8 + r;
+      const int dsub = (mi & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(chunk_addr(stage, 0, t, ks * 16 + dsub), b0, b1, b2, b3);
+        mma_16816(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+        mma_16816(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+      }
+    }
+    const int c = 2 * (lane & 3);
+    float s[4] = {sc[0][0] * scale_log2, sc[0][1] * scale_log2, sc[1][0] * scale_log2, sc[1][1] * scale_log2};
+    s[0] = (c < nvalid) ? s[0] : -INFINITY;
+    s[1] = (c + 1 < nvalid) ? s[1] : -INFINITY;
+    s[2] = (c + 8 < nvalid) ? s[2] : -INFINITY;
+    s[3] = (c + 9 < nvalid) ? s[3] : -INFINITY;
+    float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const float alpha = exp2f(m - m_new);
+    m = m_new;
+    const __half2 p01 = __floats2half2_rn(exp2f(s[0] - m_new), exp2f(s[1] - m_new));
+    const __half2 p23 = __floats2half2_rn(exp2f(s[2] - m_new), exp2f(s[3] - m_new));
+    const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+    l = l * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      acc[nb][0] *= alpha;
+      acc[nb][1] *= alpha;
+    }
+    const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
+    const uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
+    {
+      const int mi = lane >> 3, r = lane & 7;
+      const int t = (mi & 1) * 8 + r;
+      const int dsub = (mi >> 1) * 8;
+#pragma unroll
+      for (int mm = 0; mm < D / 16; ++mm) {
+        uint32_t v0, v1, v2, v3;
+        ldmatrix_x4_trans(chunk_addr(stage, 1, t, mm * 16 + dsub), v0, v1, v2, v3);
+        mma_16816(acc[2 * mm], pa0, 0u, pa2, 0u, v0, v1);
+        mma_16816(acc[2 * mm + 1], pa0, 0u, pa2, 0u, v2, v3);
+      }
+    }
+  }
+
+  __device__ bool finish(float* po, float* pl, long long head_row0, int S, int j) {
+    float lt = l;
+    lt += __shfl_xor_sync(kFull, lt, 1);
+    lt += __shfl_xor_sync(kFull, lt, 2);
+    const bool any = __shfl_sync(kFull, lt, 0) > 0.f;  // every head row saw the same tokens
+    if (!any) return false;
+    if (h < group) {
+      const float inv = 1.f / lt;
+      const long long row = head_row0 + h;
+      float* dst = po + (row * S + j) * D + 2 * (lane & 3);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        *reinterpret_cast<float2*>(dst + nb * 8) = make_float2(acc[nb][0] * inv, acc[nb][1] * inv);
+      if ((lane & 3) == 0) pl[row * S + j] = (m + log2f(lt)) * kLn2;
+    }
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ int find_sequence(const int* prefix, int batch, int w) {
+  int lo = 0, hi = batch;  // prefix[lo] <= w < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= w) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int D, bool MMA>
+__global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
+  StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
+  int* prefix = reinterpret_cast<int*>(base + L.prefix_off);
+  __shared__ int warp_sums[32];
+
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) prefetch_tensormap(&map);
+  for (int i = tid; i < p.warps * p.nstage; i += blockDim.x) mbar_init(&bars[i], 1);
+  fence_mbarrier_init();
+
+  // Items per sequence and their exclusive prefix sum (block-wide scan).
+  {
+    const int per = (p.batch + blockDim.x - 1) / blockDim.x;
+    const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
+    int local = 0;
+    for (int s = s0; s < s1; ++s) {
+      int c;
+      const int nch = seq_chunks(p, p.page_indptr[s + 1] - p.page_indptr[s], c);
+      local += p.hkv * (nch > 0 ? nch : 1);
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int warp_base = 0;
+    for (int w = 0; w < warp; ++w) warp_base += warp_sums[w];
+    int run = warp_base + incl - local;
+    for (int s = s0; s < s1; ++s) {
+      prefix[s] = run;
+      int c;
+      const int nch = seq_chunks(p, p.page_indptr[s + 1] - p.page_indptr[s], c);
+      run += p.hkv * (nch > 0 ? nch : 1);
+    }
+    if (tid == blockDim.x - 1) prefix[p.batch] = run;
+  }
+  __syncthreads();
+  pdl_wait();  // q_rope and the pool pages come from the preceding kernel
+  if (warp >= p.warps) return;
+
+  const int total = prefix[p.batch];
+  const int W = gridDim.x * p.warps;
+  const int nst = p.nstage;
+  uint64_t* bar = bars + warp * nst;
+  StageMeta* meta = metas + warp * nst;
+  unsigned char* stages = base + (size_t)warp * nst * L.stage_bytes;
+  unsigned char* qslots = base + L.q_off + (size_t)warp * nst * L.qslot_bytes;
+  const uint32_t q_bytes = (uint32_t)(p.group * D * 2);
+  const uint32_t page_bytes = (uint32_t)(64 * D);
+  const uint64_t policy = l2_policy_evict_first();
+
+  // producer state (lane-uniform)
+  int w_next = blockIdx.x * p.warps + warp;
+  bool have = false;
+  int it_s = 0, it_j = 0, it_g = 0, it_first = 0, it_n = 0, it_last = 16, it_qrow = 0;
+  int p0 = 0, p1 = 0, pnext = 0, win_base = -1, window = 0;
+  bool it_lastchunk = false;
+  int issued = 0, consumed = 0;
+
+  auto produce = [&]() -> bool {
+    if (!have) {
+      if (w_next >= total) return false;
+      const int w = w_next;
+      w_next += W;
+      const int s = find_sequence(prefix, p.batch, w);
+      const int r = w - prefix[s];
+      it_s = s;
+      it_j = r / p.hkv;
+      it_g = r - it_j * p.hkv;
+      it_first = p.page_indptr[s];
+      it_n = p.page_indptr[s + 1] - it_first;
+      it_last = p.last_page_len[s];
+      int c = 1;
+      const int nch = seq_chunks(p, it_n, c);
+      bool ok = nch > 0;
+      it_qrow = s;
+      if (it_n > 0) {  // an empty sequence reads neither its query nor its last-page length
+        ok = ok && it_last >= 1 && it_last <= kPageSize;
+        if (p.q_indptr != nullptr) {
+          const int q0 = p.q_indptr[s], q1 = p.q_indptr[s + 1];
+          ok = ok && q1 > q0;
+          it_qrow = q1 - 1;
+        }
+      }
+      if (!ok && lane == 0) atomicOr(p.status, kFlagBadSequence);
+      if (!ok || it_n == 0) {
+        p0 = p1 = 0;
+        it_lastchunk = true;
+      } else {
+        p0 = it_j * c;
+        p1 = min(p0 + c, it_n);
+        it_lastchunk = (it_j == nch - 1);
+      }
+      pnext = p0;
+      win_base = -1;
+      have = true;
+    }
+    const int k = issued % nst;
+    StageMeta mt;
+    mt.s = it_s;
+    mt.j = it_j;
+    mt.g = it_g;
+    if (p1 == p0) {
+      mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | kMetaLastChunk;
+      if (lane == 0) {
+        meta[k] = mt;
+        mbar_arrive(&bar[k]);
+      }
+      have = false;
+    } else {
+      const bool first = pnext == p0, lastp = pnext + 1 == p1;
+      if (win_base < 0 || pnext - win_base >= 32) {
+        win_base = pnext;
+        const int idx = pnext + lane;
+        window = idx < p1 ? p.page_indices[it_first + idx] : 0;
+      }
+      const int pid = __shfl_sync(kFull, window, pnext - win_base);
+      const bool page_ok = pid >= 0 && pid < p.num_pages;
+      const int nvalid = page_ok ? ((pnext == it_n - 1) ? it_last : kPageSize) : 0;
+      mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (it_lastchunk ? kMetaLastChunk : 0);
+      if (lane == 0) {
+        if (!page_ok) atomicOr(p.status, kFlagBadPage);
+        meta[k] = mt;
+        const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes : 0u);
+        if (bytes) {
+          mbar_arrive_expect_tx(&bar[k], bytes);
+        } else {
+          mbar_arrive(&bar[k]);
+        }
+        if (first) {
+          const __half* qsrc = p.q + ((long long)it_qrow * p.hq + (long long)it_g * p.group) * D;
+          bulk_load(qslots + k * L.qslot_bytes, qsrc, q_bytes, &bar[k]);
+        }
+        if (page_ok) {
+          unsigned char* dst = stages + (size_t)k * L.stage_bytes;
+          if constexpr (MMA) {
+            constexpr int E = GroupMma<D>::E;
+#pragma unroll
+            for (int u = 0; u < D / E; ++u)
+              tma_load_4d(dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, it_g, 2 * pid, policy);
+          } else {
+            tma_load_4d(dst, &map, &bar[k], 0, 0, it_g, 2 * pid, policy);
+          }
+        }
+      }
+      ++pnext;
+      if (lastp) have = false;
+    }
+    ++issued;
+    return true;
+  };
+
+  using Compute = typename std::conditional<MMA, GroupMma<D>, GroupOne<D>>::type;
+  Compute cmp;
+  if constexpr (MMA) {
+    cmp.init(lane, p.group);
+  } else {
+    cmp.init(lane);
+  }
+
+  for (int i = 0; i < nst; ++i)
+    if (!produce()) break;
+
+  while (consumed < issued) {
+    const int k = consumed % nst;
+    const uint32_t parity = (uint32_t)((consumed / nst) & 1);
+    if (!mbar_wait_bounded(&bar[k], parity, kWaitLimitNs)) {
+      if (lane == 0) atomicOr(p.status, kFlagTimeout);
+      for (int c = consumed + 1; c < issued; ++c)
+        mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs / 16);
+      return;
+    }
+    const StageMeta mt = meta[k];
+    const long long head_row0 = (long long)mt.s * p.hq + (long long)mt.g * p.group;
+    if (!(mt.flags & kMetaEmpty)) {
+      if (mt.flags & kMetaFirst) {
+        if constexpr (MMA) {
+          cmp.begin(qslots + k * L.qslot_bytes);
+        } else {
+          cmp.begin(qslots + k * L.qslot_bytes, p.scale_log2);
+        }
+      }
+      const int nvalid = mt.flags & kMetaValid;
+      if (nvalid > 0) {
+        if constexpr (MMA) {
+          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid, p.scale_log2);
+        } else {
+          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid);
+        }
+      }
+    }
+    if (mt.flags & kMetaLast) {
+      bool wrote = false;
+      if (!(mt.flags & kMetaEmpty)) wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
+      // -inf for this chunk when nothing was accumulated, and for every chunk after the last one
+      const int j0 = wrote ? mt.j + 1 : mt.j;
+      const int j1 = (mt.flags & kMetaLastChunk) ? p.splits : mt.j + 1;
+      const int cnt = j1 - j0;
+      for (int i = lane; i < p.group * cnt && cnt > 0; i += 32) {
+        const int hh = i / cnt, jj = j0 + i % cnt;
+        p.partial_lse[(head_row0 + hh) * p.splits + jj] = -INFINITY;
+      }
+    }
+    ++consumed;
+    fence_proxy_async_smem();  // this lane's reads/writes of the stage before the TMA refill
+    __syncwarp();
+    produce();
+  }
+}
+
+template <int D, bool MMA>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&decode_kernel<D, MMA>);
+}
+
+void* select_kernel(int head_dim, bool mma) {
+  switch (head_dim) {
+    case 64: return mma ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
+    case 96: return mma ? kernel_ptr<96, true>() : kernel_ptr<96, false>();
+    case 128: return mma ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+DecodeConfig decode_config(int group, int head_dim, int batch) {
+  DecodeConfig c;
+  c.mma = group >= 2;
+  c.warps = c.mma ? 6 : 8;
+  const Layout one = make_layout(c.warps, 1, head_dim, group, batch);
+  const int per_stage = c.warps * (one.stage_bytes + one.qslot_bytes + 8 + 16);
+  const int fixed = (batch + 1) * 4 + 1024 + 64;
+  int nstage = (kSmemBudget - fixed) / per_stage;
+  if (nstage > 8) nstage = 8;
+  c.nstage = nstage;
+  c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch).total : 0;
+  if (c.mma) {
+    c.box_inner = head_dim == 96 ? 32 : 64;
+    c.swizzle_bytes = head_dim == 96 ? 64 : 128;
+  } else {
+    c.box_inner = head_dim;
+    c.swizzle_bytes = 0;
+  }
+  return c;
+}
+
+cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
+  void* k = select_kernel(head_dim, cfg.mma);
+  if (k == nullptr) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
+                          int grid, cudaStream_t stream, bool pdl) {
+  void* k = select_kernel(head_dim, cfg.mma);
+  if (k == nullptr || cfg.smem_bytes == 0) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(cfg.warps * 32);
+  lc.dynamicSmemBytes = cfg.smem_bytes;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  void* args[] = {const_cast<CUtensorMap*>(&map), const_cast<DecodeParams*>(&p)};
+  return cudaLaunchKernelExC(&lc, k, args);
+}
+
+}  // namespace pkv

@@ -1,0 +1,331 @@
+// Host side of libpkv.so: argument validation, the split planner, the RoPE table, TMA
+// descriptors and kernel launches.  Every entry point of include/pkv.h is defined here.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+struct pkv_cache {
+  pkv_cache_desc desc;
+  std::vector<void*> pools;
+  std::vector<CUtensorMap> maps;  // one per layer pool
+  int device = 0;
+  int num_sms = 0;
+  int group = 1;
+  bool pdl = false;
+};
+
+namespace {
+
+using pkv::DecodeConfig;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
+
+pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Split selection shared by pkv_plan_decode and pkv_decode_attention.
+pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits, int chunk_pages,
+                int max_splits, int* splits, int* chunk) {
+  if (batch < 0 || max_pages < 0 || total_pages < 0 || num_splits < 0 || chunk_pages < 0 || max_splits < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (num_splits > 0 && chunk_pages > 0) return PKV_ERR_INVALID_ARG;
+  if (num_splits > 0) {
+    if (num_splits > max_splits) return PKV_ERR_INVALID_ARG;
+    *splits = num_splits;
+    *chunk = 0;
+    return PKV_OK;
+  }
+  if (chunk_pages > 0) {
+    const int s = max_pages > 0 ? (max_pages + chunk_pages - 1) / chunk_pages : 1;
+    if (s > max_splits) return PKV_ERR_INVALID_ARG;
+    *splits = s;
+    *chunk = chunk_pages;
+    return PKV_OK;
+  }
+  // Automatic: chunk size so that the items fill the resident warps once (uniform lengths) or
+  // about four times (ragged lengths, where small items balance the long ones).
+  const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, batch > 0 ? batch : 1);
+  const long long warps = (long long)c->num_sms * cfg.warps;
+  const long long uniform_pages = (long long)batch * max_pages;
+  const long long pages = total_pages > 0 ? total_pages : uniform_pages;
+  const bool ragged = total_pages > 0 && 10 * (long long)total_pages < 9 * uniform_pages;
+  const long long units = pages * c->desc.num_kv_heads;
+  const long long target = ragged ? 4 * warps : warps;
+  long long cp = target > 0 ? (units + target - 1) / target : 1;
+  if (cp < 1) cp = 1;
+  if (max_pages > 0 && cp > max_pages) cp = max_pages;
+  int s = max_pages > 0 ? (int)((max_pages + cp - 1) / cp) : 1;
+  if (s > max_splits) {
+    cp = (max_pages + max_splits - 1) / max_splits;
+    s = (int)((max_pages + cp - 1) / cp);
+  }
+  *splits = s;
+  *chunk = (int)cp;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_pool_bytes(int num_pages, int num_kv_heads, int head_dim) {
+  if (num_pages <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return (size_t)num_pages * 2 * num_kv_heads * PKV_PAGE_SIZE * head_dim * 2;
+}
+
+size_t pkv_rope_table_bytes(int max_position, int head_dim) {
+  if (max_position <= 0 || head_dim <= 0 || head_dim % 2) return 0;
+  return (size_t)max_position * (head_dim / 2) * 2 * sizeof(float);
+}
+
+size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim) {
+  if (batch < 0 || num_qo_heads <= 0 || splits <= 0 || head_dim <= 0) return 0;
+  return (size_t)batch * num_qo_heads * splits * head_dim * sizeof(float);
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_OUT_OF_RANGE: return "index out of range (device)";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
+  if (d == nullptr || out == nullptr) return PKV_ERR_INVALID_ARG;
+  if (d->num_layers < 1 || d->num_pages < 1 || d->num_qo_heads < 1 || d->num_kv_heads < 1 ||
+      d->max_position < 1 || !(d->rope_theta > 0.0) || d->layer_pools == nullptr || d->rope_table == nullptr ||
+      d->status_word == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (d->page_size != PKV_PAGE_SIZE || !head_dim_ok(d->head_dim)) return PKV_ERR_UNSUPPORTED;
+  if (d->num_qo_heads % d->num_kv_heads) return PKV_ERR_INVALID_ARG;
+  const int group = d->num_qo_heads / d->num_kv_heads;
+  if (group > pkv::kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if ((long long)d->num_pages * 2 > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(d->rope_table, 16)) return PKV_ERR_INVALID_ARG;
+  for (int l = 0; l < d->num_layers; ++l)
+    if (d->layer_pools[l] == nullptr || !aligned(d->layer_pools[l], 256)) return PKV_ERR_INVALID_ARG;
+  if (d->options & ~PKV_OPT_PDL) return PKV_ERR_INVALID_ARG;
+
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) return PKV_ERR_CUDA;
+
+  pkv_cache* c = new (std::nothrow) pkv_cache();
+  if (c == nullptr) return PKV_ERR_CUDA;
+  c->desc = *d;
+  c->pools.assign(d->layer_pools, d->layer_pools + d->num_layers);
+  c->desc.layer_pools = nullptr;
+  c->group = group;
+  c->pdl = (d->options & PKV_OPT_PDL) != 0;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return PKV_ERR_CUDA;
+  }
+
+  // RoPE table: cos/sin(p * theta^(-2i/d)) in fp64, rounded once to fp32, interleaved (cos, sin).
+  const int D = d->head_dim, half = D / 2;
+  std::vector<double> inv_freq(half);
+  for (int i = 0; i < half; ++i) inv_freq[i] = std::pow(d->rope_theta, -2.0 * i / D);
+  std::vector<float> table((size_t)d->max_position * half * 2);
+  for (int p = 0; p < d->max_position; ++p) {
+    for (int i = 0; i < half; ++i) {
+      const double phi = (double)p * inv_freq[i];
+      table[((size_t)p * half + i) * 2] = (float)std::cos(phi);
+      table[((size_t)p * half + i) * 2 + 1] = (float)std::sin(phi);
+    }
+  }
+  if (cudaMemcpy(d->rope_table, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemset(d->status_word, 0, sizeof(int)) != cudaSuccess) {
+    delete c;
+    return PKV_ERR_CUDA;
+  }
+
+  // One 4-D tensor map per pool: dims (head_dim, slot, kv_head, page*2 + kv).
+  const DecodeConfig cfg = pkv::decode_config(group, D, 1);
+  if (pkv::decode_prepare(cfg, D) != cudaSuccess) {
+    delete c;
+    return PKV_ERR_CUDA;
+  }
+  c->maps.resize(d->num_layers);
+  for (int l = 0; l < d->num_layers; ++l) {
+    const cuuint64_t gdim[4] = {(cuuint64_t)D, (cuuint64_t)PKV_PAGE_SIZE, (cuuint64_t)d->num_kv_heads,
+                                (cuuint64_t)d->num_pages * 2};
+    const cuuint64_t gstride[3] = {(cuuint64_t)D * 2, (cuuint64_t)PKV_PAGE_SIZE * D * 2,
+                                   (cuuint64_t)d->num_kv_heads * PKV_PAGE_SIZE * D * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)cfg.box_inner, (cuuint32_t)PKV_PAGE_SIZE, 1, 2};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle swz = cfg.swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : cfg.swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                             : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUresult r = encode(&c->maps[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      delete c;
+      return PKV_ERR_CUDA;
+    }
+  }
+  *out = c;
+  return PKV_OK;
+}
+
+void pkv_destroy(pkv_cache* c) { delete c; }
+
+pkv_status pkv_device_info(const pkv_cache* c, int* num_sms, int* decode_warps_per_sm) {
+  if (c == nullptr) return PKV_ERR_INVALID_ARG;
+  if (num_sms) *num_sms = c->num_sms;
+  if (decode_warps_per_sm) *decode_warps_per_sm = pkv::decode_config(c->group, c->desc.head_dim, 1).warps;
+  return PKV_OK;
+}
+
+pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k, const void* v,
+                           const int32_t* pos_map, const int32_t* append_indptr, int num_tokens, int batch,
+                           const int32_t* page_indptr, const int32_t* page_indices, void* q_out,
+                           pkv_stream_t stream) {
+  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers || num_tokens < 0 || batch < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0 || batch == 0) return PKV_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || pos_map == nullptr || append_indptr == nullptr ||
+      page_indptr == nullptr || page_indices == nullptr || q_out == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) || q_out == q)
+    return PKV_ERR_INVALID_ARG;
+  pkv::AppendParams p;
+  p.q = static_cast<const __half*>(q);
+  p.k = static_cast<const __half*>(k);
+  p.v = static_cast<const __half*>(v);
+  p.pos_map = pos_map;
+  p.append_indptr = append_indptr;
+  p.page_indptr = page_indptr;
+  p.page_indices = page_indices;
+  p.q_out = static_cast<__half*>(q_out);
+  p.pool = static_cast<__half*>(c->pools[layer]);
+  p.rope = reinterpret_cast<const float2*>(c->desc.rope_table);
+  p.status = c->desc.status_word;
+  p.num_tokens = num_tokens;
+  p.batch = batch;
+  p.hq = c->desc.num_qo_heads;
+  p.hkv = c->desc.num_kv_heads;
+  p.head_dim = c->desc.head_dim;
+  p.max_position = c->desc.max_position;
+  p.num_pages = c->desc.num_pages;
+  return cuda_status(pkv::launch_append(p, stream, c->pdl));
+}
+
+pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,
+                           int chunk_pages, int max_splits, int* splits, int* chunk_out) {
+  if (c == nullptr || splits == nullptr || chunk_out == nullptr) return PKV_ERR_INVALID_ARG;
+  return plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, splits, chunk_out);
+}
+
+pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
+                                const int32_t* page_indptr, const int32_t* page_indices,
+                                const int32_t* last_page_len, int batch, int max_pages, int total_pages,
+                                int num_splits, int chunk_pages, int max_splits, float sm_scale, float* partial_o,
+                                float* partial_lse, int* splits_used, pkv_stream_t stream) {
+  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return PKV_ERR_INVALID_ARG;
+  int S = 0, chunk = 0;
+  const pkv_status ps = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
+  if (ps != PKV_OK) return ps;
+  if (splits_used) *splits_used = S;
+  if (batch == 0) return PKV_OK;
+  if (batch > pkv::kMaxDecodeBatch) return PKV_ERR_UNSUPPORTED;
+  if (q_rope == nullptr || page_indptr == nullptr || page_indices == nullptr || last_page_len == nullptr ||
+      partial_o == nullptr || partial_lse == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q_rope, 16) || !aligned(partial_o, 8) || !aligned(partial_lse, 4)) return PKV_ERR_INVALID_ARG;
+  if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return PKV_ERR_INVALID_ARG;
+  const long long items = (long long)batch * c->desc.num_kv_heads * S;
+  if (items > 0x3fffffffLL) return PKV_ERR_UNSUPPORTED;
+
+  const int D = c->desc.head_dim;
+  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch);
+  if (cfg.nstage < 2) return PKV_ERR_UNSUPPORTED;
+  pkv::DecodeParams p;
+  p.q = static_cast<const __half*>(q_rope);
+  p.q_indptr = q_indptr;
+  p.page_indptr = page_indptr;
+  p.page_indices = page_indices;
+  p.last_page_len = last_page_len;
+  p.partial_o = partial_o;
+  p.partial_lse = partial_lse;
+  p.status = c->desc.status_word;
+  p.batch = batch;
+  p.hq = c->desc.num_qo_heads;
+  p.hkv = c->desc.num_kv_heads;
+  p.group = c->group;
+  p.num_pages = c->desc.num_pages;
+  p.splits = S;
+  p.chunk_pages = chunk;
+  p.max_pages = max_pages;
+  const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.nstage = cfg.nstage;
+  p.warps = cfg.warps;
+  long long grid = (items + cfg.warps - 1) / cfg.warps;
+  if (grid > c->num_sms) grid = c->num_sms;
+  if (grid < 1) grid = 1;
+  return cuda_status(pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
+}
+
+pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* partial_lse, int batch,
+                       int num_qo_heads, int num_splits, int head_dim, void* out, float* lse_out,
+                       pkv_stream_t stream) {
+  if (batch < 0 || num_qo_heads < 1 || num_splits < 1) return PKV_ERR_INVALID_ARG;
+  if (!head_dim_ok(head_dim)) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (partial_o == nullptr || partial_lse == nullptr || out == nullptr) return PKV_ERR_INVALID_ARG;
+  if (!aligned(partial_o, 16) || !aligned(out, 16)) return PKV_ERR_INVALID_ARG;
+  pkv::CombineParams p;
+  p.partial_o = partial_o;
+  p.partial_lse = partial_lse;
+  p.out = static_cast<__half*>(out);
+  p.lse = lse_out;
+  p.batch = batch;
+  p.hq = num_qo_heads;
+  p.splits = num_splits;
+  p.head_dim = head_dim;
+  return cuda_status(pkv::launch_combine(p, stream, c != nullptr && c->pdl));
+}
+
+pkv_status pkv_check_status(pkv_cache* c, pkv_stream_t stream, int* flags) {
+  if (c == nullptr) return PKV_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemcpy(&v, c->desc.status_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  if (v != 0 && cudaMemset(c->desc.status_word, 0, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (flags) *flags = v;
+  if (v == 0) return PKV_OK;
+  return (v & PKV_FLAG_TIMEOUT) ? PKV_ERR_TIMEOUT : PKV_ERR_OUT_OF_RANGE;
+}
+
+}  // extern "C"

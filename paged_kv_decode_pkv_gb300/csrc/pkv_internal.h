@@ -1,0 +1,81 @@
+// Internal interface between the host library (pkv_host.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kPageSize = 16;
+constexpr int kMaxGroup = 8;        // Hq / Hkv handled by the kernels
+constexpr int kMaxDecodeBatch = 4096;  // sequences per decode call (per-CTA shared-memory prefix)
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s
+
+// Device status word bits (mirrors PKV_FLAG_* of include/pkv.h).
+constexpr int kFlagBadPage = 0x1;
+constexpr int kFlagBadPosition = 0x2;
+constexpr int kFlagBadSequence = 0x4;
+constexpr int kFlagTimeout = 0x8;
+
+struct AppendParams {
+  const __half* q;
+  const __half* k;
+  const __half* v;
+  const int* pos_map;
+  const int* append_indptr;
+  const int* page_indptr;
+  const int* page_indices;
+  __half* q_out;
+  __half* pool;
+  const float2* rope;  // [max_position][head_dim / 2] (cos, sin)
+  int* status;
+  int num_tokens, batch, hq, hkv, head_dim, max_position, num_pages;
+};
+
+struct DecodeParams {
+  const __half* q;
+  const int* q_indptr;  // nullable
+  const int* page_indptr;
+  const int* page_indices;
+  const int* last_page_len;
+  float* partial_o;
+  float* partial_lse;
+  int* status;
+  int batch, hq, hkv, group, num_pages;
+  int splits;       // S: partial slots per (sequence, head)
+  int chunk_pages;  // > 0: uniform chunks of this many pages; 0: ceil(n_s / splits) per sequence
+  int max_pages;    // declared bound of n_s
+  float scale_log2; // sm_scale * log2(e)
+  int nstage;       // ring depth per warp
+  int warps;        // consumer warps per CTA
+};
+
+struct CombineParams {
+  const float* partial_o;
+  const float* partial_lse;
+  __half* out;
+  float* lse;
+  int batch, hq, splits, head_dim;
+};
+
+// Decode launch geometry for a (group, head_dim) pair and a batch size.
+struct DecodeConfig {
+  bool mma;             // tensor-core path (group >= 2)
+  int warps;            // warps per CTA
+  int nstage;           // per-warp ring depth
+  size_t smem_bytes;    // dynamic shared memory
+  int box_inner;        // TMA box extent along head_dim (elements)
+  int swizzle_bytes;    // 0 (none), 64 or 128
+};
+
+DecodeConfig decode_config(int group, int head_dim, int batch);
+cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim);  // function attributes
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
+                          int grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+
+}  // namespace pkv
