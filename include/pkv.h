@@ -228,6 +228,10 @@ pkv_status pkv_check_status(pkv_cache* cache, pkv_stream_t stream, int* flags);
 /* Static description of a status code. */
 const char* pkv_status_string(pkv_status status);
 
+/* Description of the last failure on the calling thread (the CUDA call and its error string, or
+ * the rejected argument); empty before any failure.  Valid until the thread's next failing call. */
+const char* pkv_last_error(void);
+
 /* Number of streaming multiprocessors of the cache's device and the resident warps the decode
  * kernel uses per SM (what the planner fills). */
 pkv_status pkv_device_info(const pkv_cache* cache, int* num_sms, int* decode_warps_per_sm);

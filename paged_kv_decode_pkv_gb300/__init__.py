@@ -25,8 +25,8 @@ OPT_PDL = 0x1
 
 
 class PkvError(RuntimeError):
-    def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {status_string(code)} ({code})")
+    def __init__(self, code: int, what: str, detail: str = ""):
+        super().__init__(f"{what}: {status_string(code)} ({code})" + (f" - {detail}" if detail else ""))
         self.code = code
 
 
@@ -58,6 +58,8 @@ def lib():
         L.pkv_partial_bytes.argtypes = [i, i, i, i]
         L.pkv_status_string.restype = ctypes.c_char_p
         L.pkv_status_string.argtypes = [i]
+        L.pkv_last_error.restype = ctypes.c_char_p
+        L.pkv_last_error.argtypes = []
         L.pkv_create_cache.restype = i
         L.pkv_create_cache.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(P)]
         L.pkv_destroy.restype = None
@@ -85,7 +87,7 @@ def status_string(code: int) -> str:
 
 def _check(code: int, what: str) -> None:
     if code != OK:
-        raise PkvError(code, what)
+        raise PkvError(code, what, lib().pkv_last_error().decode())
 
 
 def _ptr(t):

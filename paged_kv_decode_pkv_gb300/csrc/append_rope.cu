@@ -47,6 +47,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
   __shared__ int s_indptr[kIndptrSmemCap + 1];
   __shared__ TokenSlot s_tok[kTokensPerCta];
+  __shared__ float2 s_cs[kTokensPerCta][D / 2];  // (cos, sin) rows of the CTA's tokens
   pdl_launch_dependents();
 
   const int t0 = blockIdx.x * kTokensPerCta;
@@ -90,6 +91,13 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
     s_tok[threadIdx.x] = ts;
   }
   __syncthreads();
+  // The RoPE table is written once at cache creation, so its rows can be staged before the wait.
+  for (int i = threadIdx.x; i < kTokensPerCta * (D / 2); i += kThreads) {
+    const int tk = i / (D / 2), e = i - tk * (D / 2);
+    const TokenSlot ts = s_tok[tk];
+    if (ts.k_off >= 0) s_cs[tk][e] = p.rope[(long long)ts.pos * (D / 2) + e];
+  }
+  __syncthreads();
   pdl_wait();  // q, k, v and the pool may be produced or read by the preceding kernel
 
   constexpr int kRopeUnits = D / 16;  // 8-element blocks in the first half of a head
@@ -114,16 +122,8 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
       const __half* src = is_q ? p.q + ((long long)t * p.hq + h) * D : p.k + ((long long)t * p.hkv + h) * D;
       const uint4 lo = *reinterpret_cast<const uint4*>(src + i0);
       const uint4 hi = *reinterpret_cast<const uint4*>(src + i0 + D / 2);
-      float2 cs[8];
-      const float4* tab = reinterpret_cast<const float4*>(p.rope + (long long)ts.pos * (D / 2) + i0);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 f = tab[e];
-        cs[2 * e] = make_float2(f.x, f.y);
-        cs[2 * e + 1] = make_float2(f.z, f.w);
-      }
       uint4 ylo, yhi;
-      rope8(lo, hi, cs, ylo, yhi);
+      rope8(lo, hi, &s_cs[tk][i0], ylo, yhi);
       __half* dst = is_q ? p.q_out + ((long long)t * p.hq + h) * D : p.pool + ts.k_off + h * head_stride;
       *reinterpret_cast<uint4*>(dst + i0) = ylo;
       *reinterpret_cast<uint4*>(dst + i0 + D / 2) = yhi;
@@ -139,6 +139,17 @@ __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
 }
 
 }  // namespace
+
+cudaError_t append_prepare() {
+  const void* k[] = {(const void*)&append_rope_kernel<64>, (const void*)&append_rope_kernel<96>,
+                     (const void*)&append_rope_kernel<128>};
+  for (const void* f : k) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) {
   if (p.num_tokens <= 0 || p.batch <= 0) return cudaSuccess;

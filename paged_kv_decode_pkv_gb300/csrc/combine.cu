@@ -12,6 +12,7 @@ namespace pkv {
 namespace {
 
 constexpr int kWarpsPerCta = 4;
+constexpr int kBatch = 8;  // partial rows in flight per warp
 
 template <int D>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) combine_kernel(CombineParams p) {
@@ -39,15 +40,29 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) combine_kernel(CombineParam
     for (int jb = 0; jb < S; jb += 32) {
       const int j = jb + lane;
       const float lj = j < S ? lse[j] : -INFINITY;
-      const float wl = (lj == -INFINITY) ? 0.f : __expf(lj - M);
+      const float wl = (lj == -INFINITY) ? 0.f : expf(lj - M);
       W += wl;
       const int n = min(32, S - jb);
-      for (int k = 0; k < n; ++k) {
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        if (w == 0.f) continue;  // empty split: its partial_o was never written
-        const float* row = po + (long long)(jb + k) * D;
+      // Rows are read kBatch at a time with independent (predicated) loads so that their
+      // latencies overlap instead of forming one dependent chain per split.
+      for (int k0 = 0; k0 < n; k0 += kBatch) {
+        float w[kBatch];
+        float v[kBatch][kPerLane];
 #pragma unroll
-        for (int e = 0; e < kPerLane; ++e) acc[e] = fmaf(w, row[lane + 32 * e], acc[e]);
+        for (int u = 0; u < kBatch; ++u) {
+          w[u] = __shfl_sync(0xffffffffu, wl, (k0 + u) & 31);
+          if (k0 + u >= n) w[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float* row = po + (long long)(jb + k0 + u) * D;
+#pragma unroll
+          for (int e = 0; e < kPerLane; ++e) v[u][e] = (w[u] != 0.f) ? row[lane + 32 * e] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int e = 0; e < kPerLane; ++e) acc[e] = fmaf(w[u], v[u][e], acc[e]);
       }
     }
 #pragma unroll
@@ -57,10 +72,21 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) combine_kernel(CombineParam
   const float inv = (W > 0.f) ? 1.f / W : 0.f;
 #pragma unroll
   for (int e = 0; e < kPerLane; ++e) out[lane + 32 * e] = __float2half_rn(acc[e] * inv);
-  if (p.lse != nullptr && lane == 0) p.lse[sh] = (W > 0.f) ? M + __logf(W) : -INFINITY;
+  if (p.lse != nullptr && lane == 0) p.lse[sh] = (W > 0.f) ? M + logf(W) : -INFINITY;
 }
 
 }  // namespace
+
+cudaError_t combine_prepare() {
+  const void* k[] = {(const void*)&combine_kernel<64>, (const void*)&combine_kernel<96>,
+                     (const void*)&combine_kernel<128>};
+  for (const void* f : k) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
   const long long pairs = (long long)p.batch * p.hq;

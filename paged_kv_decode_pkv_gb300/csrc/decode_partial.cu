@@ -47,10 +47,12 @@ struct __align__(16) StageMeta {
   int s, j, g, flags;
 };
 
-constexpr int kSmemBudget = 232448;  // 227 KB, the per-block opt-in maximum
+// Dynamic shared memory budget: the 227 KB per-block opt-in maximum less room for the kernel's
+// static shared memory.
+constexpr int kSmemBudget = 232448 - 1024;
 
 struct Layout {
-  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, total;
+  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, indptr_off, total;
 };
 
 __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch) {
@@ -63,7 +65,8 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
   L.meta_off = L.bar_off + n * 8;
   L.meta_off = (L.meta_off + 15) & ~15;
   L.prefix_off = L.meta_off + n * 16;
-  L.total = L.prefix_off + (batch + 1) * 4 + 1024;  // + slack to align the base to 1024
+  L.indptr_off = L.prefix_off + (batch + 1) * 4;
+  L.total = L.indptr_off + (batch + 1) * 4 + 1024;  // + slack to align the base to 1024
   return L;
 }
 
@@ -357,6 +360,58 @@ __device__ __forceinline__ int find_sequence(const int* prefix, int batch, int w
   return lo;
 }
 
+// One work item as the producer sees it (lane-uniform except `window`, which holds the page id
+// of page win_base + lane).
+struct Item {
+  int s, j, g, first, n, nch, p0, p1, pnext, win_base, window, last, q0, q1;
+  bool active;
+};
+
+// Locate item w and start the global loads it needs (last-page length, query row, the first 32
+// page ids).  The loaded values are consumed later by activate(), so the loads overlap other work.
+__device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams& p, const int* prefix,
+                                             const int* indptr, int lane) {
+  const int s = find_sequence(prefix, p.batch, w);
+  const int r = w - prefix[s];
+  it.s = s;
+  it.j = r / p.hkv;
+  it.g = r - it.j * p.hkv;
+  it.first = indptr[s];
+  it.n = indptr[s + 1] - it.first;
+  int c = 1;
+  it.nch = seq_chunks(p, it.n, c);
+  if (it.nch > 0 && it.n > 0) {
+    it.p0 = it.j * c;
+    it.p1 = min(it.p0 + c, it.n);
+  } else {
+    it.p0 = it.p1 = 0;
+  }
+  it.pnext = it.p0;
+  it.win_base = it.p0;
+  const int idx = it.p0 + lane;
+  it.window = idx < it.p1 ? p.page_indices[it.first + idx] : 0;
+  it.last = it.n > 0 ? p.last_page_len[s] : kPageSize;
+  if (p.q_indptr != nullptr && it.n > 0) {
+    it.q0 = p.q_indptr[s];
+    it.q1 = p.q_indptr[s + 1];
+  } else {
+    it.q0 = s;
+    it.q1 = s + 1;
+  }
+  it.active = true;
+}
+
+// Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
+// item per KV head (its chunks are reported as -inf).
+__device__ __forceinline__ void activate_item(Item& it, int* status, int lane) {
+  bool ok = it.nch > 0;
+  if (it.n > 0) ok = ok && it.last >= 1 && it.last <= kPageSize && it.q1 > it.q0;
+  if (!ok) {
+    if (lane == 0) atomicOr(status, kFlagBadSequence);
+    it.p0 = it.p1 = it.pnext = 0;
+  }
+}
+
 template <int D, bool MMA>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -366,6 +421,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
   int* prefix = reinterpret_cast<int*>(base + L.prefix_off);
+  int* indptr = reinterpret_cast<int*>(base + L.indptr_off);
   __shared__ int warp_sums[32];
 
   pdl_launch_dependents();
@@ -374,14 +430,16 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   for (int i = tid; i < p.warps * p.nstage; i += blockDim.x) mbar_init(&bars[i], 1);
   fence_mbarrier_init();
 
-  // Items per sequence and their exclusive prefix sum (block-wide scan).
+  // Page ranges of every sequence, then items per sequence and their exclusive prefix sum.
+  for (int i = tid; i <= p.batch; i += blockDim.x) indptr[i] = p.page_indptr[i];
+  __syncthreads();
   {
     const int per = (p.batch + blockDim.x - 1) / blockDim.x;
     const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
     int local = 0;
     for (int s = s0; s < s1; ++s) {
       int c;
-      const int nch = seq_chunks(p, p.page_indptr[s + 1] - p.page_indptr[s], c);
+      const int nch = seq_chunks(p, indptr[s + 1] - indptr[s], c);
       local += p.hkv * (nch > 0 ? nch : 1);
     }
     int incl = local;
@@ -398,14 +456,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     for (int s = s0; s < s1; ++s) {
       prefix[s] = run;
       int c;
-      const int nch = seq_chunks(p, p.page_indptr[s + 1] - p.page_indptr[s], c);
+      const int nch = seq_chunks(p, indptr[s + 1] - indptr[s], c);
       run += p.hkv * (nch > 0 ? nch : 1);
     }
     if (tid == blockDim.x - 1) prefix[p.batch] = run;
   }
   __syncthreads();
-  pdl_wait();  // q_rope and the pool pages come from the preceding kernel
-  if (warp >= p.warps) return;
 
   const int total = prefix[p.batch];
   const int W = gridDim.x * p.warps;
@@ -418,75 +474,53 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   const uint32_t page_bytes = (uint32_t)(64 * D);
   const uint64_t policy = l2_policy_evict_first();
 
-  // producer state (lane-uniform)
+  // Producer state: the item being issued (cur) and the next one, whose loads are in flight.
   int w_next = blockIdx.x * p.warps + warp;
-  bool have = false;
-  int it_s = 0, it_j = 0, it_g = 0, it_first = 0, it_n = 0, it_last = 16, it_qrow = 0;
-  int p0 = 0, p1 = 0, pnext = 0, win_base = -1, window = 0;
-  bool it_lastchunk = false;
+  Item cur, nxt;
+  cur.active = false;
+  nxt.active = false;
+  if (w_next < total) {
+    prepare_item(nxt, w_next, p, prefix, indptr, lane);  // index loads only: allowed before the wait
+    w_next += W;
+  }
+  pdl_wait();  // q_rope and the pool pages come from the preceding kernel
   int issued = 0, consumed = 0;
 
   auto produce = [&]() -> bool {
-    if (!have) {
-      if (w_next >= total) return false;
-      const int w = w_next;
-      w_next += W;
-      const int s = find_sequence(prefix, p.batch, w);
-      const int r = w - prefix[s];
-      it_s = s;
-      it_j = r / p.hkv;
-      it_g = r - it_j * p.hkv;
-      it_first = p.page_indptr[s];
-      it_n = p.page_indptr[s + 1] - it_first;
-      it_last = p.last_page_len[s];
-      int c = 1;
-      const int nch = seq_chunks(p, it_n, c);
-      bool ok = nch > 0;
-      it_qrow = s;
-      if (it_n > 0) {  // an empty sequence reads neither its query nor its last-page length
-        ok = ok && it_last >= 1 && it_last <= kPageSize;
-        if (p.q_indptr != nullptr) {
-          const int q0 = p.q_indptr[s], q1 = p.q_indptr[s + 1];
-          ok = ok && q1 > q0;
-          it_qrow = q1 - 1;
-        }
+    if (!cur.active) {
+      if (!nxt.active) return false;
+      cur = nxt;
+      activate_item(cur, p.status, lane);
+      nxt.active = false;
+      if (w_next < total) {
+        prepare_item(nxt, w_next, p, prefix, indptr, lane);
+        w_next += W;
       }
-      if (!ok && lane == 0) atomicOr(p.status, kFlagBadSequence);
-      if (!ok || it_n == 0) {
-        p0 = p1 = 0;
-        it_lastchunk = true;
-      } else {
-        p0 = it_j * c;
-        p1 = min(p0 + c, it_n);
-        it_lastchunk = (it_j == nch - 1);
-      }
-      pnext = p0;
-      win_base = -1;
-      have = true;
     }
     const int k = issued % nst;
     StageMeta mt;
-    mt.s = it_s;
-    mt.j = it_j;
-    mt.g = it_g;
-    if (p1 == p0) {
+    mt.s = cur.s;
+    mt.j = cur.j;
+    mt.g = cur.g;
+    if (cur.p1 == cur.p0) {
       mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | kMetaLastChunk;
       if (lane == 0) {
         meta[k] = mt;
         mbar_arrive(&bar[k]);
       }
-      have = false;
+      cur.active = false;
     } else {
-      const bool first = pnext == p0, lastp = pnext + 1 == p1;
-      if (win_base < 0 || pnext - win_base >= 32) {
-        win_base = pnext;
-        const int idx = pnext + lane;
-        window = idx < p1 ? p.page_indices[it_first + idx] : 0;
+      const bool first = cur.pnext == cur.p0, lastp = cur.pnext + 1 == cur.p1;
+      if (cur.pnext - cur.win_base >= 32) {
+        cur.win_base = cur.pnext;
+        const int idx = cur.pnext + lane;
+        cur.window = idx < cur.p1 ? p.page_indices[cur.first + idx] : 0;
       }
-      const int pid = __shfl_sync(kFull, window, pnext - win_base);
+      const int pid = __shfl_sync(kFull, cur.window, cur.pnext - cur.win_base);
       const bool page_ok = pid >= 0 && pid < p.num_pages;
-      const int nvalid = page_ok ? ((pnext == it_n - 1) ? it_last : kPageSize) : 0;
-      mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (it_lastchunk ? kMetaLastChunk : 0);
+      const int nvalid = page_ok ? ((cur.pnext == cur.n - 1) ? cur.last : kPageSize) : 0;
+      const bool lastchunk = cur.j == cur.nch - 1;
+      mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0);
       if (lane == 0) {
         if (!page_ok) atomicOr(p.status, kFlagBadPage);
         meta[k] = mt;
@@ -497,7 +531,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           mbar_arrive(&bar[k]);
         }
         if (first) {
-          const __half* qsrc = p.q + ((long long)it_qrow * p.hq + (long long)it_g * p.group) * D;
+          const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
           bulk_load(qslots + k * L.qslot_bytes, qsrc, q_bytes, &bar[k]);
         }
         if (page_ok) {
@@ -506,14 +540,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
             constexpr int E = GroupMma<D>::E;
 #pragma unroll
             for (int u = 0; u < D / E; ++u)
-              tma_load_4d(dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, it_g, 2 * pid, policy);
+              tma_load_4d(dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, cur.g, 2 * pid, policy);
           } else {
-            tma_load_4d(dst, &map, &bar[k], 0, 0, it_g, 2 * pid, policy);
+            tma_load_4d(dst, &map, &bar[k], 0, 0, cur.g, 2 * pid, policy);
           }
         }
       }
-      ++pnext;
-      if (lastp) have = false;
+      ++cur.pnext;
+      if (lastp) cur.active = false;
     }
     ++issued;
     return true;
@@ -599,7 +633,7 @@ DecodeConfig decode_config(int group, int head_dim, int batch) {
   c.warps = c.mma ? 6 : 8;
   const Layout one = make_layout(c.warps, 1, head_dim, group, batch);
   const int per_stage = c.warps * (one.stage_bytes + one.qslot_bytes + 8 + 16);
-  const int fixed = (batch + 1) * 4 + 1024 + 64;
+  const int fixed = (batch + 1) * 8 + 1024 + 64;
   int nstage = (kSmemBudget - fixed) / per_stage;
   if (nstage > 8) nstage = 8;
   c.nstage = nstage;
@@ -617,7 +651,9 @@ DecodeConfig decode_config(int group, int head_dim, int batch) {
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
   void* k = select_kernel(head_dim, cfg.mma);
   if (k == nullptr) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,

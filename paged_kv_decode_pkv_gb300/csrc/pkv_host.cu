@@ -1,9 +1,12 @@
 // Host side of libpkv.so: argument validation, the split planner, the RoPE table, TMA
 // descriptors and kernel launches.  Every entry point of include/pkv.h is defined here.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "../../include/pkv.h"
@@ -40,11 +43,31 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+thread_local std::string g_last_error;
+
+void set_error(const char* what, const char* detail) {
+  g_last_error = what;
+  if (detail != nullptr) {
+    g_last_error += ": ";
+    g_last_error += detail;
+  }
+}
+
+pkv_status fail(pkv_status s, const char* what, const char* detail = nullptr) {
+  set_error(what, detail);
+  return s;
+}
+
+pkv_status cuda_fail(const char* what, cudaError_t e) {
+  set_error(what, cudaGetErrorString(e));
+  return PKV_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
 
-pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+pkv_status launch_status(const char* what, cudaError_t e) { return e == cudaSuccess ? PKV_OK : cuda_fail(what, e); }
 
 // Split selection shared by pkv_plan_decode and pkv_decode_attention.
 pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits, int chunk_pages,
@@ -73,8 +96,17 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
   const long long pages = total_pages > 0 ? total_pages : uniform_pages;
   const bool ragged = total_pages > 0 && 10 * (long long)total_pages < 9 * uniform_pages;
   const long long units = pages * c->desc.num_kv_heads;
-  const long long target = ragged ? 4 * warps : warps;
-  long long cp = target > 0 ? (units + target - 1) / target : 1;
+  const long long heads = (long long)batch * c->desc.num_kv_heads;
+  const long long per_head = heads > 0 ? warps / heads : 0;  // items each (sequence, KV head) may have
+  long long cp;
+  if (!ragged && per_head >= 1) {
+    // uniform lengths: at most one item per warp, as small as that allows
+    cp = std::max((units + warps - 1) / warps, ((long long)max_pages + per_head - 1) / per_head);
+  } else {
+    // ragged lengths or more (sequence, head) pairs than warps: about four items per warp, so that
+    // small items even out the long ones under the static round-robin assignment
+    cp = (units + 4 * warps - 1) / (4 * warps);
+  }
   if (cp < 1) cp = 1;
   if (max_pages > 0 && cp > max_pages) cp = max_pages;
   int s = max_pages > 0 ? (int)((max_pages + cp - 1) / cp) : 1;
@@ -106,6 +138,8 @@ size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim) 
   return (size_t)batch * num_qo_heads * splits * head_dim * sizeof(float);
 }
 
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
 const char* pkv_status_string(pkv_status s) {
   switch (s) {
     case PKV_OK: return "ok";
@@ -135,19 +169,20 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   if (d->options & ~PKV_OPT_PDL) return PKV_ERR_INVALID_ARG;
 
   EncodeTiledFn encode = encode_tiled_fn();
-  if (encode == nullptr) return PKV_ERR_CUDA;
+  if (encode == nullptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
 
   pkv_cache* c = new (std::nothrow) pkv_cache();
-  if (c == nullptr) return PKV_ERR_CUDA;
+  if (c == nullptr) return fail(PKV_ERR_CUDA, "out of host memory");
   c->desc = *d;
   c->pools.assign(d->layer_pools, d->layer_pools + d->num_layers);
   c->desc.layer_pools = nullptr;
   c->group = group;
   c->pdl = (d->options & PKV_OPT_PDL) != 0;
-  if (cudaGetDevice(&c->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
     delete c;
-    return PKV_ERR_CUDA;
+    return cuda_fail("querying the device", e);
   }
 
   // RoPE table: cos/sin(p * theta^(-2i/d)) in fp64, rounded once to fp32, interleaved (cos, sin).
@@ -162,18 +197,21 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
       table[((size_t)p * half + i) * 2 + 1] = (float)std::sin(phi);
     }
   }
-  if (cudaMemcpy(d->rope_table, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice) !=
-          cudaSuccess ||
-      cudaMemset(d->status_word, 0, sizeof(int)) != cudaSuccess) {
+  e = cudaMemcpy(d->rope_table, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(d->status_word, 0, sizeof(int));
+  if (e != cudaSuccess) {
     delete c;
-    return PKV_ERR_CUDA;
+    return cuda_fail("writing the RoPE table / status word", e);
   }
 
   // One 4-D tensor map per pool: dims (head_dim, slot, kv_head, page*2 + kv).
   const DecodeConfig cfg = pkv::decode_config(group, D, 1);
-  if (pkv::decode_prepare(cfg, D) != cudaSuccess) {
+  e = pkv::decode_prepare(cfg, D);
+  if (e == cudaSuccess) e = pkv::append_prepare();
+  if (e == cudaSuccess) e = pkv::combine_prepare();
+  if (e != cudaSuccess) {
     delete c;
-    return PKV_ERR_CUDA;
+    return cuda_fail("setting kernel attributes", e);
   }
   c->maps.resize(d->num_layers);
   for (int l = 0; l < d->num_layers; ++l) {
@@ -191,7 +229,9 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       delete c;
-      return PKV_ERR_CUDA;
+      char msg[64];
+      snprintf(msg, sizeof(msg), "CUresult %d for layer %d", (int)r, l);
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled", msg);
     }
   }
   *out = c;
@@ -238,7 +278,7 @@ pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k
   p.head_dim = c->desc.head_dim;
   p.max_position = c->desc.max_position;
   p.num_pages = c->desc.num_pages;
-  return cuda_status(pkv::launch_append(p, stream, c->pdl));
+  return launch_status("append_rope launch", pkv::launch_append(p, stream, c->pdl));
 }
 
 pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,
@@ -294,7 +334,7 @@ pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rop
   long long grid = (items + cfg.warps - 1) / cfg.warps;
   if (grid > c->num_sms) grid = c->num_sms;
   if (grid < 1) grid = 1;
-  return cuda_status(pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
+  return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 
 pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* partial_lse, int batch,
@@ -314,15 +354,17 @@ pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* 
   p.hq = num_qo_heads;
   p.splits = num_splits;
   p.head_dim = head_dim;
-  return cuda_status(pkv::launch_combine(p, stream, c != nullptr && c->pdl));
+  return launch_status("combine launch", pkv::launch_combine(p, stream, c != nullptr && c->pdl));
 }
 
 pkv_status pkv_check_status(pkv_cache* c, pkv_stream_t stream, int* flags) {
   if (c == nullptr) return PKV_ERR_INVALID_ARG;
   int v = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
-  if (cudaMemcpy(&v, c->desc.status_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
-  if (v != 0 && cudaMemset(c->desc.status_word, 0, sizeof(int)) != cudaSuccess) return PKV_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail("synchronising the stream", e);
+  e = cudaMemcpy(&v, c->desc.status_word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v != 0) e = cudaMemset(c->desc.status_word, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail("reading the status word", e);
   if (flags) *flags = v;
   if (v == 0) return PKV_OK;
   return (v & PKV_FLAG_TIMEOUT) ? PKV_ERR_TIMEOUT : PKV_ERR_OUT_OF_RANGE;

@@ -76,6 +76,8 @@ cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim);  // function 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl);
+cudaError_t append_prepare();   // function attributes (shared-memory carveout)
+cudaError_t combine_prepare();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 
 }  // namespace pkv

@@ -29,7 +29,7 @@ def _run(step, host_pool, plan=None, layer=0):
 
 
 CASES = {
-    "mha_d96": W.scaled(W.CONFIGS[3], batch=6, pool_pages=1000),
+    "mha_d96": W.scaled(W.CONFIGS[3], batch=6, pool_pages=2000),
     "gqa4_d128": W.scaled(W.CONFIGS[5], batch=10, lengths=("loguniform", 16, 4000), pool_pages=3000,
                           chunk_seqs=2, chunk_tokens=33),
 }
@@ -85,7 +85,10 @@ def test_length_one_returns_v_exactly(hq, hkv, d):
     q, k, v = W.new_qkv(step, 0)
     expect = np.repeat(v, hq // hkv, axis=1)  # query head h reads KV head h / G
     assert np.array_equal(_bits(r["out"]).view(np.uint16), expect)
-    assert np.all(r["lse"].cpu().numpy() == 0.0)
+    # the LSE of a single token is its scaled score
+    gp = _bits(r["pool"]).view(np.uint16)
+    _, lse_ref = H.oracle_attention_on(step, gp, _bits(r["q_out"]).view(np.uint16))
+    H.assert_close_lse(r["lse"].cpu().numpy(), lse_ref)
 
 
 def test_position_zero_rotation_is_identity():
@@ -103,7 +106,7 @@ def test_position_zero_rotation_is_identity():
 def test_empty_sequence_and_zero_query():
     import torch
 
-    cfg = W.scaled(W.CONFIGS[3], batch=4, pool_pages=600)
+    cfg = W.scaled(W.CONFIGS[3], batch=4, pool_pages=1200)
     step = W.make_step(cfg)
     pool = W.host_pool(step, 0)
     # sequence 1 becomes empty: no pages, no appended token
@@ -153,7 +156,7 @@ def test_device_errors_set_status_and_skip():
 
     import paged_kv_decode_pkv_gb300 as pkv
 
-    cfg = W.scaled(W.CONFIGS[3], batch=3, pool_pages=500)
+    cfg = W.scaled(W.CONFIGS[3], batch=3, pool_pages=1000)
     step = W.make_step(cfg)
     pool = W.host_pool(step, 0)
     good = _run(step, pool)

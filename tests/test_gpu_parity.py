@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 SMALL = {
     "tiny": W.CONFIGS[1],
     "phi3_b1_ctx300": W.scaled(W.CONFIGS[2], layers=2, lengths=("fixed", 300), pool_pages=24),
-    "ragged_d96": W.scaled(W.CONFIGS[3], batch=9, pool_pages=1500),
+    "ragged_d96": W.scaled(W.CONFIGS[3], batch=9, pool_pages=3000),
     "gqa2_d128_outliers": W.scaled(W.CONFIGS[4], layers=2, batch=3, lengths=("fixed", 1000), pool_pages=260),
     "gqa4_mixed_chunks": W.scaled(W.CONFIGS[5], batch=12, lengths=("loguniform", 16, 3000), pool_pages=3000,
                                   chunk_seqs=3, chunk_tokens=40),

@@ -99,3 +99,14 @@ def test_substep_regenerates_the_same_pages():
     q, k, v = W.new_qkv(st, 0)
     q2, k2, v2 = W.new_qkv(st, 0, rows=W.token_rows(st, [3, 1]))
     assert np.array_equal(q2, q[W.token_rows(st, [3, 1])]) and np.array_equal(v2, v[W.token_rows(st, [3, 1])])
+
+
+def test_gpu_test_cases_are_constructible():
+    """Every scaled workload the GPU tests use builds on the host (pool large enough, valid tables)."""
+    from tests import test_gpu_invariants as inv
+    from tests import test_gpu_parity as par
+
+    extra = [W.scaled(W.CONFIGS[3], batch=4, pool_pages=1200), W.scaled(W.CONFIGS[3], batch=3, pool_pages=1000)]
+    for cfg in list(par.SMALL.values()) + list(inv.CASES.values()) + extra:
+        st = W.make_step(cfg)
+        assert st.page_indices.size <= st.num_pages
