@@ -260,7 +260,21 @@ def run_ours(args):
     out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
     lse_host = [torch.empty_like(x, device="cpu").pin_memory() for x in lses]
 
+    counters = torch.zeros(B * cfg.hkv, dtype=torch.int32, device=dev)
+
     def layer_chain(l):
+        """append -> split-K decode with the combine merged into the same launch"""
+        q, k, v = qkv[l]
+        cache.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                          tabs["page_indices"], q_out=q_out[l])
+        cache.decode_attention_merged(l, q_out[l], tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
+                                      step.max_pages_per_seq, counters,
+                                      q_indptr=tabs["append_indptr"] if use_q_indptr else None,
+                                      total_pages=total_pages, partial_o=po, partial_lse=pl, out=outs[l],
+                                      lse=lses[l])
+
+    def layer_chain_separate(l):
+        """append -> split-K decode -> combine, three launches"""
         q, k, v = qkv[l]
         cache.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
                           tabs["page_indices"], q_out=q_out[l])
@@ -273,6 +287,10 @@ def run_ours(args):
         for l in layers:
             layer_chain(l)
 
+    def step_fn_separate():
+        for l in layers:
+            layer_chain_separate(l)
+
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         step_fn()
@@ -283,6 +301,9 @@ def run_ours(args):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         step_fn()
+    graph_sep = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_sep, stream=stream):
+        step_fn_separate()
     torch.cuda.synchronize()
 
     def barrier():
@@ -313,6 +334,16 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    # the same step as three launches per layer (append, decode, combine), for reference
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph_sep.replay()
+        ev0.record()
+        for _ in range(args.steps):
+            graph_sep.replay()
+        ev1.record()
+    torch.cuda.synchronize()
+    step_sep_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
     code, flags = cache.check_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after the timed region: {pkv.status_string(code)} flags {flags:#x}")
@@ -331,14 +362,14 @@ def run_ours(args):
         plain.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
                           tabs["page_indices"], q_out=q_out[l])
         events[0].record()
-        plain.decode_attention(l, q_out[l], tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
-                               step.max_pages_per_seq, q_indptr=tabs["append_indptr"] if use_q_indptr else None,
-                               total_pages=total_pages, partial_o=po, partial_lse=pl)
+        plain.decode_attention_merged(l, q_out[l], tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
+                                      step.max_pages_per_seq, counters,
+                                      q_indptr=tabs["append_indptr"] if use_q_indptr else None,
+                                      total_pages=total_pages, partial_o=po, partial_lse=pl, out=outs[l],
+                                      lse=lses[l])
         events[1].record()
-        plain.combine(po, pl, out=outs[l], lse=lses[l])
-        events[2].record()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps * cfg.layers)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps * cfg.layers)]
     sleep_cycles = int(2e9 * max(0.02, 0.002 * cfg.layers))
     with torch.cuda.stream(stream):
         i = 0
@@ -349,7 +380,6 @@ def run_ours(args):
                 i += 1
     torch.cuda.synchronize()
     dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     kv_layer = step.kv_bytes()
     achieved = kv_layer / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -410,16 +440,19 @@ def run_ours(args):
                    "launch": "CUDA graph of the step, programmatic dependent launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_roofline_frac_step": value / world / peak,
-        "attention_us_per_step_per_layer": (dec_ms + comb_ms) * 1e3,
+        "attention_us_per_step_per_layer": dec_ms * 1e3,
         "step_us_per_layer": step_ms * 1e3 / cfg.layers,
+        "step": "per layer: pkv_append_rope + pkv_decode_attention_merged (2 launches)",
+        "separate_kernels": {"value": world * kv_step / (step_sep_ms * 1e-3) / 1e9, "ms_per_step": step_sep_ms,
+                             "step": "per layer: pkv_append_rope + pkv_decode_attention + pkv_combine"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "decode_kernel",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "decode_kernel (merged combine)",
                      "algorithmic_bytes_per_launch": kv_layer, "avg_launch_us": dec_ms * 1e3,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
         "e2e": {"value": world * kv_step / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "mode": "CUDA graph of the API calls",
                 "eager_value": world * kv_step / e2e_eager_s / 1e9, "eager_ms_per_step": e2e_eager_s * 1e3},
-        "gpu_launches": args.steps * cfg.layers * 3,
+        "gpu_launches": args.steps * cfg.layers * 2,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -206,6 +206,26 @@ pkv_status pkv_decode_attention(const pkv_cache* cache, int layer, const void* q
                                 float* partial_lse, int* splits_used, pkv_stream_t stream);
 
 /*
+ * Split-K decode attention and the log-sum-exp combine in one launch: the same chunks as
+ * pkv_decode_attention, but the last chunk of each (sequence, KV head) to finish merges the
+ * chunks' partials exactly as pkv_combine does and writes the result, so no separate combine
+ * kernel runs.  A sequence with a single chunk writes its result directly (the same bits as the
+ * merge of one split).  Arguments as pkv_decode_attention, plus:
+ *   partial_o, partial_lse  workspace of the same shapes (contents undefined on return)
+ *   chunk_counters  int32 [batch * Hkv] device workspace; all zero before the first call and left
+ *                   all zero by every call that completes (re-zero it after PKV_ERR_TIMEOUT)
+ *   out             fp16 [batch][Hq][head_dim] result;  lse_out  fp32 [batch][Hq] or NULL
+ * Calls that share chunk_counters must not overlap on the device.
+ */
+pkv_status pkv_decode_attention_merged(const pkv_cache* cache, int layer, const void* q_rope,
+                                       const int32_t* q_indptr, const int32_t* page_indptr,
+                                       const int32_t* page_indices, const int32_t* last_page_len,
+                                       int batch, int max_pages_per_seq, int total_pages, int num_splits,
+                                       int chunk_pages, int max_splits, float sm_scale, float* partial_o,
+                                       float* partial_lse, int32_t* chunk_counters, void* out,
+                                       float* lse_out, int* splits_used, pkv_stream_t stream);
+
+/*
  * Log-sum-exp combine (Zero TVM Documentation, "How it works": one combine dispatch per layer
  * after split-K attention).  For each (s, h): M = max_j lse_j, w_j = exp(lse_j - M),
  *   out[s][h][:] = fp16( sum_j w_j o_j / sum_j w_j ),   lse_out[s][h] = M + ln sum_j w_j.

@@ -28,6 +28,7 @@
 //
 // Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
 // bounded time for its own copies in flight and returns.
+#include "merge.cuh"
 #include "pkv_internal.h"
 #include "ptx.cuh"
 
@@ -42,6 +43,7 @@ constexpr int kMetaFirst = 1 << 5;
 constexpr int kMetaLast = 1 << 6;
 constexpr int kMetaLastChunk = 1 << 7;
 constexpr int kMetaEmpty = 1 << 8;
+constexpr int kMetaChunkShift = 16;  // bits 16..31: chunks of the item's sequence
 
 struct __align__(16) StageMeta {
   int s, j, g, flags;
@@ -88,7 +90,9 @@ __device__ __forceinline__ int seq_chunks(const DecodeParams& p, int n, int& c) 
 template <int D>
 struct GroupOne {
   static constexpr int DPL = D / 16;  // dimensions per lane
-  float q[DPL], o[DPL], m, l;
+  static constexpr int HPL = DPL / 2; // half2 pairs per lane
+  uint32_t q2[HPL];                   // the lane's query dimensions, fp16 pairs
+  float o[DPL], m, l, scale_log2;
   int lane, half, li;
 
   __device__ void init(int lane_) {
@@ -97,46 +101,45 @@ struct GroupOne {
     li = lane & 15;
   }
 
-  __device__ static void load_row(const unsigned char* row, int li, float (&x)[DPL]) {
+  // The lane's DPL consecutive fp16 values of a row, as half2 pairs.
+  __device__ static void load_row(const unsigned char* row, int li, uint32_t (&x)[HPL]) {
     if constexpr (D == 128) {
       const uint4 v = *reinterpret_cast<const uint4*>(row + li * 16);
-      const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(h[e]);
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-      }
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     } else if constexpr (D == 96) {
-      const unsigned char* b = row + li * 12;
-#pragma unroll
-      for (int e = 0; e < 3; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(b + 4 * e));
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-      }
+      const uint32_t* b = reinterpret_cast<const uint32_t*>(row + li * 12);
+      x[0] = b[0]; x[1] = b[1]; x[2] = b[2];
     } else {
       const uint2 v = *reinterpret_cast<const uint2*>(row + li * 8);
-      const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 f = __half22float2(h[e]);
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-      }
+      x[0] = v.x; x[1] = v.y;
     }
   }
 
-  __device__ void begin(const unsigned char* qslot, float scale_log2) {
-    float x[DPL];
-    load_row(qslot, li, x);
+  // acc + a.lo * b.lo + a.hi * b.hi with fp16 operands and fp32 accumulation (the fp16 products
+  // are exact in fp32, so this equals converting first and using fp32 fused multiply-adds).
+  __device__ static float fma2(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+  }
+
+  // o + p * v for both halves of v (p already an fp16 value held in the low half of pp).
+  __device__ static void fma_pv(uint16_t p16, uint32_t v, float& o0, float& o1) {
+    asm("{\n\t.reg .b16 vl, vh;\n\t"
+        "mov.b32 {vl, vh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, %3, vl, %0;\n\tfma.rn.f32.f16 %1, %3, vh, %1;\n\t}"
+        : "+f"(o0), "+f"(o1) : "r"(v), "h"(p16));
+  }
+
+  __device__ void begin(const unsigned char* qslot, float scale_log2_) {
+    load_row(qslot, li, q2);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      q[e] = x[e] * scale_log2;
-      o[e] = 0.f;
-    }
+    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
     m = -INFINITY;
     l = 0.f;
+    scale_log2 = scale_log2_;
   }
 
   __device__ void page(const unsigned char* stage, int nvalid) {
@@ -145,15 +148,15 @@ struct GroupOne {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float x[DPL];
+      uint32_t x[HPL];
       load_row(Kb + (2 * i + half) * D * 2, li, x);
       float a = 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) a = fmaf(q[e], x[e], a);
+      for (int e = 0; e < HPL; ++e) a = fma2(q2[e], x[e], a);
       acc[i] = a;
     }
     // Transposing butterfly over the 16 lanes of each half: after the xor-8/4/2 steps lane li
-    // holds row pair-sum for row index (li >> 1), the xor-1 step completes the sum.
+    // holds a pair-sum for row index (li >> 1), the xor-1 step completes the sum.
     const bool b3 = li & 8, b2 = li & 4, b1 = li & 2;
     float t4[4];
 #pragma unroll
@@ -170,7 +173,7 @@ struct GroupOne {
       t2[a] = keep + __shfl_xor_sync(kFull, send, 4);
     }
     float t1 = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(kFull, b1 ? t2[0] : t2[1], 2);
-    float sc = t1 + __shfl_xor_sync(kFull, t1, 1);
+    float sc = (t1 + __shfl_xor_sync(kFull, t1, 1)) * scale_log2;
     const int row = 2 * ((li >> 1) & 7) + half;
     sc = (row < nvalid) ? sc : -INFINITY;
 
@@ -181,19 +184,21 @@ struct GroupOne {
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     const float m_new = fmaxf(m, mx);
     const float alpha = exp2f(m - m_new);
-    const float pr = exp2f(sc - m_new);
-    l = l * alpha + ((li & 1) ? 0.f : pr);
+    // probabilities rounded to fp16 for the P.V products; l sums the same rounded values
+    const __half pr16 = __float2half_rn(exp2f(sc - m_new));
+    const uint16_t pbits = __half_as_ushort(pr16);
+    l = l * alpha + ((li & 1) ? 0.f : __half2float(pr16));
     m = m_new;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[e] *= alpha;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float pi = __shfl_sync(kFull, pr, (lane & 16) | (2 * i));
+      const uint16_t pi = (uint16_t)__shfl_sync(kFull, (uint32_t)pbits, (lane & 16) | (2 * i));
       if (2 * i + half < nvalid) {
-        float x[DPL];
+        uint32_t x[HPL];
         load_row(Vb + (2 * i + half) * D * 2, li, x);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = fmaf(pi, x[e], o[e]);
+        for (int e = 0; e < HPL; ++e) fma_pv(pi, x[e], o[2 * e], o[2 * e + 1]);
       }
     }
   }
@@ -214,6 +219,24 @@ struct GroupOne {
     }
     if (lane == 0) pl[row_base * S + j] = (m + log2f(lt)) * kLn2;
     return true;
+  }
+
+  // The item is its sequence's only chunk: write the final output (the merge of one split gives
+  // the same bits, since its weight is exactly 1).
+  __device__ void finish_out(__half* out, float* lse_out, long long row) {
+    float lt = l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFull, lt, off);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], 16);
+    const bool any = lt > 0.f;
+    const float inv = any ? 1.f / lt : 0.f;
+    if (half == 0) {
+      __half* dst = out + row * D + li * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) dst[e] = __float2half_rn(any ? o[e] * inv : 0.f);
+    }
+    if (lse_out != nullptr && lane == 0) lse_out[row] = any ? (m + log2f(lt)) * kLn2 : -INFINITY;
   }
 };
 
@@ -346,6 +369,23 @@ struct GroupMma {
       if ((lane & 3) == 0) pl[row * S + j] = (m + log2f(lt)) * kLn2;
     }
     return true;
+  }
+
+  __device__ void finish_out(__half* out, float* lse_out, long long head_row0) {
+    float lt = l;
+    lt += __shfl_xor_sync(kFull, lt, 1);
+    lt += __shfl_xor_sync(kFull, lt, 2);
+    if (h < group) {
+      const bool any = lt > 0.f;
+      const float inv = any ? 1.f / lt : 0.f;
+      const long long row = head_row0 + h;
+      __half* dst = out + row * D + 2 * (lane & 3);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        *reinterpret_cast<__half2*>(dst + nb * 8) =
+            __floats2half2_rn(any ? acc[nb][0] * inv : 0.f, any ? acc[nb][1] * inv : 0.f);
+      if (lse_out != nullptr && (lane & 3) == 0) lse_out[row] = any ? (m + log2f(lt)) * kLn2 : -INFINITY;
+    }
   }
 };
 
@@ -503,7 +543,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     mt.j = cur.j;
     mt.g = cur.g;
     if (cur.p1 == cur.p0) {
-      mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | kMetaLastChunk;
+      mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | kMetaLastChunk | (1 << kMetaChunkShift);
       if (lane == 0) {
         meta[k] = mt;
         mbar_arrive(&bar[k]);
@@ -520,7 +560,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       const bool page_ok = pid >= 0 && pid < p.num_pages;
       const int nvalid = page_ok ? ((cur.pnext == cur.n - 1) ? cur.last : kPageSize) : 0;
       const bool lastchunk = cur.j == cur.nch - 1;
-      mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0);
+      mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0) |
+                 (cur.nch << kMetaChunkShift);
       if (lane == 0) {
         if (!page_ok) atomicOr(p.status, kFlagBadPage);
         meta[k] = mt;
@@ -592,7 +633,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         }
       }
     }
-    if (mt.flags & kMetaLast) {
+    if ((mt.flags & kMetaLast) && !p.merged) {
       bool wrote = false;
       if (!(mt.flags & kMetaEmpty)) wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
       // -inf for this chunk when nothing was accumulated, and for every chunk after the last one
@@ -602,6 +643,29 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       for (int i = lane; i < p.group * cnt && cnt > 0; i += 32) {
         const int hh = i / cnt, jj = j0 + i % cnt;
         p.partial_lse[(head_row0 + hh) * p.splits + jj] = -INFINITY;
+      }
+    } else if (mt.flags & kMetaLast) {
+      const int nch = (mt.flags >> kMetaChunkShift) & 0xffff;
+      if (mt.flags & kMetaEmpty) {
+        for (int i = lane; i < p.group * D; i += 32) p.out[head_row0 * D + i] = __float2half_rn(0.f);
+        if (p.lse_out != nullptr && lane < p.group) p.lse_out[head_row0 + lane] = -INFINITY;
+      } else if (nch == 1) {
+        cmp.finish_out(p.out, p.lse_out, head_row0);
+      } else {
+        const bool wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
+        if (!wrote && lane < p.group) p.partial_lse[(head_row0 + lane) * p.splits + mt.j] = -INFINITY;
+        // Publish this chunk, then count it; the chunk that completes the count merges them all.
+        __threadfence();
+        __syncwarp();
+        int* counter = p.counters + (long long)mt.s * p.hkv + mt.g;
+        int done = 0;
+        if (lane == 0) done = atomicAdd(counter, 1) + 1;
+        done = __shfl_sync(kFull, done, 0);
+        if (done == nch) {
+          __threadfence();
+          merge_group<D>(p.partial_lse, p.partial_o, head_row0, p.group, p.splits, nch, lane, p.out, p.lse_out);
+          if (lane == 0) *counter = 0;  // ready for the next launch
+        }
       }
     }
     ++consumed;

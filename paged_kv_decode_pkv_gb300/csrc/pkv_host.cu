@@ -287,29 +287,37 @@ pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int tot
   return plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, splits, chunk_out);
 }
 
-pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
-                                const int32_t* page_indptr, const int32_t* page_indices,
-                                const int32_t* last_page_len, int batch, int max_pages, int total_pages,
-                                int num_splits, int chunk_pages, int max_splits, float sm_scale, float* partial_o,
-                                float* partial_lse, int* splits_used, pkv_stream_t stream) {
-  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return PKV_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Shared body of pkv_decode_attention and pkv_decode_attention_merged.
+pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
+                         const int32_t* page_indptr, const int32_t* page_indices, const int32_t* last_page_len,
+                         int batch, int max_pages, int total_pages, int num_splits, int chunk_pages, int max_splits,
+                         float sm_scale, float* partial_o, float* partial_lse, int32_t* counters, void* out,
+                         float* lse_out, bool merged, int* splits_used, cudaStream_t stream) {
+  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return fail(PKV_ERR_INVALID_ARG, "cache or layer");
   int S = 0, chunk = 0;
   const pkv_status ps = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
-  if (ps != PKV_OK) return ps;
+  if (ps != PKV_OK) return fail(ps, "split plan arguments");
   if (splits_used) *splits_used = S;
   if (batch == 0) return PKV_OK;
-  if (batch > pkv::kMaxDecodeBatch) return PKV_ERR_UNSUPPORTED;
+  if (batch > pkv::kMaxDecodeBatch) return fail(PKV_ERR_UNSUPPORTED, "batch above 4096 sequences");
   if (q_rope == nullptr || page_indptr == nullptr || page_indices == nullptr || last_page_len == nullptr ||
       partial_o == nullptr || partial_lse == nullptr)
-    return PKV_ERR_INVALID_ARG;
-  if (!aligned(q_rope, 16) || !aligned(partial_o, 8) || !aligned(partial_lse, 4)) return PKV_ERR_INVALID_ARG;
-  if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return PKV_ERR_INVALID_ARG;
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (merged && (counters == nullptr || out == nullptr)) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q_rope, 16) || !aligned(partial_o, 8) || !aligned(partial_lse, 4) ||
+      (merged && (!aligned(out, 16) || !aligned(counters, 4))))
+    return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale");
   const long long items = (long long)batch * c->desc.num_kv_heads * S;
-  if (items > 0x3fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (items > 0x3fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
   const int D = c->desc.head_dim;
   const DecodeConfig cfg = pkv::decode_config(c->group, D, batch);
-  if (cfg.nstage < 2) return PKV_ERR_UNSUPPORTED;
+  if (cfg.nstage < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this batch");
   pkv::DecodeParams p;
   p.q = static_cast<const __half*>(q_rope);
   p.q_indptr = q_indptr;
@@ -331,10 +339,39 @@ pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rop
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.nstage = cfg.nstage;
   p.warps = cfg.warps;
+  p.merged = merged ? 1 : 0;
+  p.counters = counters;
+  p.out = static_cast<__half*>(out);
+  p.lse_out = lse_out;
   long long grid = (items + cfg.warps - 1) / cfg.warps;
   if (grid > c->num_sms) grid = c->num_sms;
   if (grid < 1) grid = 1;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
+                                const int32_t* page_indptr, const int32_t* page_indices,
+                                const int32_t* last_page_len, int batch, int max_pages, int total_pages,
+                                int num_splits, int chunk_pages, int max_splits, float sm_scale, float* partial_o,
+                                float* partial_lse, int* splits_used, pkv_stream_t stream) {
+  return decode_common(c, layer, q_rope, q_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
+                       total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse, nullptr,
+                       nullptr, nullptr, false, splits_used, stream);
+}
+
+pkv_status pkv_decode_attention_merged(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
+                                       const int32_t* page_indptr, const int32_t* page_indices,
+                                       const int32_t* last_page_len, int batch, int max_pages, int total_pages,
+                                       int num_splits, int chunk_pages, int max_splits, float sm_scale,
+                                       float* partial_o, float* partial_lse, int32_t* chunk_counters, void* out,
+                                       float* lse_out, int* splits_used, pkv_stream_t stream) {
+  return decode_common(c, layer, q_rope, q_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
+                       total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse,
+                       chunk_counters, out, lse_out, true, splits_used, stream);
 }
 
 pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* partial_lse, int batch,

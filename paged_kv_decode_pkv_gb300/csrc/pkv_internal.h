@@ -51,6 +51,12 @@ struct DecodeParams {
   float scale_log2; // sm_scale * log2(e)
   int nstage;       // ring depth per warp
   int warps;        // consumer warps per CTA
+  // Merged mode: the last chunk of each (sequence, KV head) to finish merges the partials and
+  // writes out / lse_out; counters[s * hkv + g] counts finished chunks and is reset to zero.
+  int merged;
+  int* counters;
+  __half* out;
+  float* lse_out;   // nullable
 };
 
 struct CombineParams {

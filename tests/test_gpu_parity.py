@@ -98,6 +98,28 @@ def test_partials_parity_explicit_plans(name, plan):
     H.assert_close_lse(g["lse"], lse)
 
 
+@pytest.mark.parametrize("name", ["tiny", "phi3_b1_ctx300", "ragged_d96", "gqa4_mixed_chunks", "gqa8_d128",
+                                  "gqa2_d96", "mha_d64_long"])
+@pytest.mark.parametrize("plan", [{}, {"num_splits": 3}, {"chunk_pages": 2}])
+def test_merged_decode_is_bit_identical_to_decode_then_combine(name, plan):
+    import torch
+
+    step, host_pool, cache, tabs, g = _gpu_pool_after(SMALL[name], plan=plan)
+    cfg = step.cfg
+    counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")
+    q_out = torch.from_numpy(g["q_out"]).view(torch.float16).cuda()
+    tp = int(step.page_indptr[-1])
+    for _ in range(2):  # the second call checks that the counters were left at zero
+        out, lse = cache.decode_attention_merged(0, q_out, tabs["page_indptr"], tabs["page_indices"],
+                                                 tabs["last_page_len"], step.max_pages_per_seq, counters,
+                                                 q_indptr=tabs["q_indptr"], total_pages=tp, **plan)
+        torch.cuda.synchronize()
+        assert cache.check_status()[0] == 0
+        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), g["out"])
+        assert np.array_equal(lse.cpu().numpy().view(np.uint32), g["lse"].view(np.uint32))
+        assert int(counters.abs().sum()) == 0
+
+
 def test_device_generator_matches_host():
     import torch
 
