@@ -226,6 +226,29 @@ pkv_status pkv_decode_attention_merged(const pkv_cache* cache, int layer, const 
                                        float* lse_out, int* splits_used, pkv_stream_t stream);
 
 /*
+ * pkv_decode_attention_merged without caller workspace, for callers that cannot allocate device
+ * memory on this path: a framework that reserved the whole device for its own allocator up
+ * front, or a serving loop that must not risk an allocation failure or the implicit device
+ * synchronisation an allocation can cause in the middle of a step.  (This entry point has no
+ * counterpart in the source pages; it is a property of this library's memory handling.)
+ *
+ * The caller passes inputs and outputs only (arguments as pkv_decode_attention_merged).  The
+ * chunk counters and partials live in one file-scope device array of 32 MiB that every GPU that
+ * loads the library holds until the process exits; nothing is allocated or freed by the call.
+ * A request whose partials (batch * Hq * splits * (head_dim + 1) * 4 bytes) and counters
+ * (batch * Hkv * 4 bytes) exceed 32 MiB returns PKV_ERR_UNSUPPORTED (see pkv_last_error).
+ * The first call on a device, with that device current, looks up the array's device address
+ * once; make that first call before any stream capture.  Each call clears the counters on its
+ * stream before launching.  All calls share the one array: calls that overlap on the GPU race.
+ */
+pkv_status pkv_decode_attention_noalloc(const pkv_cache* cache, int layer, const void* q_rope,
+                                        const int32_t* q_indptr, const int32_t* page_indptr,
+                                        const int32_t* page_indices, const int32_t* last_page_len,
+                                        int batch, int max_pages_per_seq, int total_pages, int num_splits,
+                                        int chunk_pages, float sm_scale, void* out, float* lse_out,
+                                        int* splits_used, pkv_stream_t stream);
+
+/*
  * Log-sum-exp combine (Zero TVM Documentation, "How it works": one combine dispatch per layer
  * after split-K attention).  For each (s, h): M = max_j lse_j, w_j = exp(lse_j - M),
  *   out[s][h][:] = fp16( sum_j w_j o_j / sum_j w_j ),   lse_out[s][h] = M + ln sum_j w_j.

@@ -76,6 +76,9 @@ def lib():
         L.pkv_decode_attention_merged.restype = i
         L.pkv_decode_attention_merged.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, i, f, P, P, P, P, P,
                                                   ctypes.POINTER(i), P]
+        L.pkv_decode_attention_noalloc.restype = i
+        L.pkv_decode_attention_noalloc.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, f, P, P,
+                                                   ctypes.POINTER(i), P]
         L.pkv_combine.restype = i
         L.pkv_combine.argtypes = [P, P, P, i, i, i, i, P, P, P]
         L.pkv_check_status.restype = i
@@ -249,6 +252,22 @@ class Cache:
             _ptr(last_page_len), B, max_pages_per_seq, total_pages, num_splits, chunk_pages, max(cap, 1),
             float(sm_scale), _ptr(partial_o), _ptr(partial_lse), _ptr(chunk_counters), _ptr(out), _ptr(lse),
             ctypes.byref(used), _stream(stream)), "pkv_decode_attention_merged")
+        return out, lse
+
+    def decode_attention_noalloc(self, layer, q_rope, page_indptr, page_indices, last_page_len,
+                                 max_pages_per_seq, out, lse=None, q_indptr=None, total_pages=0, num_splits=0,
+                                 chunk_pages=0, sm_scale=0.0, stream=None):
+        """pkv_decode_attention_noalloc: the merged decode with the library's own fixed scratch.
+
+        For callers that cannot allocate device memory on this path: ``out`` (fp16 [B,Hq,d]) and
+        ``lse`` (fp32 [B,Hq] or None) are caller tensors, and nothing is allocated here or in the
+        library.  Calls share one scratch array: do not let them overlap on the GPU."""
+        B = int(page_indptr.numel()) - 1
+        used = ctypes.c_int()
+        _check(lib().pkv_decode_attention_noalloc(
+            self.handle, layer, _ptr(q_rope), _ptr(q_indptr), _ptr(page_indptr), _ptr(page_indices),
+            _ptr(last_page_len), B, max_pages_per_seq, total_pages, num_splits, chunk_pages, float(sm_scale),
+            _ptr(out), _ptr(lse), ctypes.byref(used), _stream(stream)), "pkv_decode_attention_noalloc")
         return out, lse
 
     def combine(self, partial_o, partial_lse, out=None, lse=None, stream=None):

@@ -121,6 +121,18 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
 
 }  // namespace
 
+namespace pkv {
+
+void cache_geometry(const pkv_cache* c, int* hq, int* hkv, int* d) {
+  *hq = c->desc.num_qo_heads;
+  *hkv = c->desc.num_kv_heads;
+  *d = c->desc.head_dim;
+}
+
+void set_last_error(const char* what) { ::set_error(what, nullptr); }
+
+}  // namespace pkv
+
 extern "C" {
 
 size_t pkv_pool_bytes(int num_pages, int num_kv_heads, int head_dim) {

@@ -87,3 +87,13 @@ cudaError_t combine_prepare();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 
 }  // namespace pkv
+
+struct pkv_cache;
+
+namespace pkv {
+
+// Host-side helpers for entry points defined outside pkv_host.cu.
+void cache_geometry(const pkv_cache* cache, int* num_qo_heads, int* num_kv_heads, int* head_dim);
+void set_last_error(const char* what);
+
+}  // namespace pkv
