@@ -127,6 +127,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------
+# ranks: one per GPU, each on its own batch of the workload (weak scaling, no collective on the data path)
+
+
+def rank_seed(cfg: W.Config, rank: int) -> int:
+    """Seed of rank r's batch: rank 0 runs the standard workload, the others distinct batches of it."""
+    return W.SEED_BASE + cfg.cid + 7919 * rank
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (a no-op on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
 # CPU oracle timing (test infrastructure: the oracle is never on the product path)
 
 
@@ -231,7 +252,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     cfg = W.CONFIGS[args.config]
-    step = W.make_step(cfg)
+    step = W.make_step(cfg, rank_seed(cfg, rank))
     layers = list(range(cfg.layers))
     pools = [W.device_pool(step, l) for l in layers]
     cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
@@ -311,11 +332,7 @@ def run_ours(args):
             dist.barrier()
 
     def max_over_ranks(x):
-        if world > 1:
-            t = torch.tensor([x], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return x
+        return reduce_max(x, world, dev)
 
     # ---- timed region: K graph replays ----------------------------------------------------------
     with torch.cuda.stream(stream):
