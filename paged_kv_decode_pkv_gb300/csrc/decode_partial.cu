@@ -37,6 +37,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLazyRescale = 8.f;  // raise the running max only when a score exceeds it by 2^8
 
 constexpr int kMetaValid = 0x1f;
 constexpr int kMetaFirst = 1 << 5;
@@ -142,10 +143,8 @@ struct GroupOne {
     scale_log2 = scale_log2_;
   }
 
-  __device__ void page(const unsigned char* stage, int nvalid) {
-    const unsigned char* Kb = stage;
-    const unsigned char* Vb = stage + kPageSize * D * 2;
-    float acc[8];
+  // q.k partial of the lane's 8 rows of one page.
+  __device__ void dots(const unsigned char* Kb, float (&acc)[8]) const {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t x[HPL];
@@ -155,42 +154,74 @@ struct GroupOne {
       for (int e = 0; e < HPL; ++e) a = fma2(q2[e], x[e], a);
       acc[i] = a;
     }
-    // Transposing butterfly over the 16 lanes of each half: after the xor-8/4/2 steps lane li
-    // holds a pair-sum for row index (li >> 1), the xor-1 step completes the sum.
+  }
+
+  // Transposing butterfly over the 16 lanes of each half for NP pages (8*NP row partials per
+  // lane): halving exchanges at xor 8, 4, 2 leave NP values per lane, the row pair-sums of rows
+  // 2*(li>>1)+half of each page; the xor-1 exchange completes them.
+  template <int NP>
+  __device__ void reduce_rows(float (&acc)[8 * NP], float (&sc)[NP]) const {
     const bool b3 = li & 8, b2 = li & 4, b1 = li & 2;
-    float t4[4];
+    constexpr int N = 8 * NP;
+    float t4[N / 2];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const float send = b3 ? acc[a] : acc[a + 4];
-      const float keep = b3 ? acc[a + 4] : acc[a];
+    for (int a = 0; a < N / 2; ++a) {
+      // the kept half alternates in blocks of 4 so each page keeps its own rows
+      const int lo = (a / 4) * 8 + (a % 4), hi = lo + 4;
+      const float send = b3 ? acc[lo] : acc[hi];
+      const float keep = b3 ? acc[hi] : acc[lo];
       t4[a] = keep + __shfl_xor_sync(kFull, send, 8);
     }
-    float t2[2];
+    float t2[N / 4];
 #pragma unroll
-    for (int a = 0; a < 2; ++a) {
-      const float send = b2 ? t4[a] : t4[a + 2];
-      const float keep = b2 ? t4[a + 2] : t4[a];
+    for (int a = 0; a < N / 4; ++a) {
+      const int lo = (a / 2) * 4 + (a % 2), hi = lo + 2;
+      const float send = b2 ? t4[lo] : t4[hi];
+      const float keep = b2 ? t4[hi] : t4[lo];
       t2[a] = keep + __shfl_xor_sync(kFull, send, 4);
     }
-    float t1 = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(kFull, b1 ? t2[0] : t2[1], 2);
-    float sc = (t1 + __shfl_xor_sync(kFull, t1, 1)) * scale_log2;
-    const int row = 2 * ((li >> 1) & 7) + half;
-    sc = (row < nvalid) ? sc : -INFINITY;
-
-    float mx = sc;
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float m_new = fmaxf(m, mx);
-    const float alpha = exp2f(m - m_new);
-    // probabilities rounded to fp16 for the P.V products; l sums the same rounded values
-    const __half pr16 = __float2half_rn(exp2f(sc - m_new));
-    const uint16_t pbits = __half_as_ushort(pr16);
-    l = l * alpha + ((li & 1) ? 0.f : __half2float(pr16));
-    m = m_new;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) o[e] *= alpha;
+    for (int pg = 0; pg < NP; ++pg) {
+      const float t1 = (b1 ? t2[2 * pg + 1] : t2[2 * pg]) +
+                       __shfl_xor_sync(kFull, b1 ? t2[2 * pg] : t2[2 * pg + 1], 2);
+      sc[pg] = (t1 + __shfl_xor_sync(kFull, t1, 1)) * scale_log2;
+    }
+  }
+
+  // Online-softmax update for NP pages' scores (log2 domain).  The running max m is only raised,
+  // with a warp-wide reduction and a rescale of o and l, when some score exceeds it by more than
+  // 2^8; otherwise the page's probabilities exp2(s - m) stay below 256 and the stale max is kept
+  // (the final normalisation by l makes the result independent of m).
+  template <int NP>
+  __device__ void softmax(float (&sc)[NP], uint16_t (&pbits)[NP]) {
+    bool need = false;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) need |= sc[pg] > m + kLazyRescale;
+    if (__any_sync(kFull, need)) {
+      float mx = sc[0];
+#pragma unroll
+      for (int pg = 1; pg < NP; ++pg) mx = fmaxf(mx, sc[pg]);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = exp2f(m - m_new);
+      l *= alpha;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[e] *= alpha;
+      m = m_new;
+    }
+    // probabilities rounded to fp16 for the P.V products; l sums the same rounded values
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const __half pr16 = __float2half_rn(exp2f(sc[pg] - m));
+      pbits[pg] = __half_as_ushort(pr16);
+      l += (li & 1) ? 0.f : __half2float(pr16);
+    }
+  }
+
+  __device__ void pv(const unsigned char* Vb, uint16_t pbits, int nvalid) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint16_t pi = (uint16_t)__shfl_sync(kFull, (uint32_t)pbits, (lane & 16) | (2 * i));
@@ -201,6 +232,39 @@ struct GroupOne {
         for (int e = 0; e < HPL; ++e) fma_pv(pi, x[e], o[2 * e], o[2 * e + 1]);
       }
     }
+  }
+
+  __device__ float mask(float sc, int nvalid) const {
+    const int row = 2 * ((li >> 1) & 7) + half;
+    return (row < nvalid) ? sc : -INFINITY;
+  }
+
+  __device__ void page(const unsigned char* stage, int nvalid) {
+    float acc[8];
+    dots(stage, acc);
+    float sc[1];
+    reduce_rows<1>(acc, sc);
+    sc[0] = mask(sc[0], nvalid);
+    uint16_t pb[1];
+    softmax<1>(sc, pb);
+    pv(stage + kPageSize * D * 2, pb[0], nvalid);
+  }
+
+  // Two consecutive pages of one item at once: independent q.k work for both, one softmax update.
+  __device__ void page2(const unsigned char* sa, int na, const unsigned char* sb, int nb) {
+    float acc[16];
+    float (&a0)[8] = *reinterpret_cast<float(*)[8]>(&acc[0]);
+    float (&a1)[8] = *reinterpret_cast<float(*)[8]>(&acc[8]);
+    dots(sa, a0);
+    dots(sb, a1);
+    float sc[2];
+    reduce_rows<2>(acc, sc);
+    sc[0] = mask(sc[0], na);
+    sc[1] = mask(sc[1], nb);
+    uint16_t pb[2];
+    softmax<2>(sc, pb);
+    pv(sa + kPageSize * D * 2, pb[0], na);
+    pv(sb + kPageSize * D * 2, pb[1], nb);
   }
 
   // Writes the item's partial; returns false when nothing was accumulated.
@@ -325,18 +389,23 @@ struct GroupMma {
     float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float m_new = fmaxf(m, mx);
-    const float alpha = exp2f(m - m_new);
-    m = m_new;
-    const __half2 p01 = __floats2half2_rn(exp2f(s[0] - m_new), exp2f(s[1] - m_new));
-    const __half2 p23 = __floats2half2_rn(exp2f(s[2] - m_new), exp2f(s[3] - m_new));
-    const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
-    l = l * alpha + ((f01.x + f01.y) + (f23.x + f23.y));
+    // Raise the head's running max (and rescale) only when a score exceeds it by more than 2^8;
+    // otherwise the probabilities exp2(s - m) stay below 256 (the final division by l makes
+    // the result independent of m).
+    if (mx > m + kLazyRescale) {
+      const float alpha = exp2f(m - mx);
+      l *= alpha;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      acc[nb][0] *= alpha;
-      acc[nb][1] *= alpha;
+      for (int nb = 0; nb < NB; ++nb) {
+        acc[nb][0] *= alpha;
+        acc[nb][1] *= alpha;
+      }
+      m = mx;
     }
+    const __half2 p01 = __floats2half2_rn(exp2f(s[0] - m), exp2f(s[1] - m));
+    const __half2 p23 = __floats2half2_rn(exp2f(s[2] - m), exp2f(s[3] - m));
+    const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
+    l += (f01.x + f01.y) + (f23.x + f23.y);
     const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
     const uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
     {
@@ -605,35 +674,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   for (int i = 0; i < nst; ++i)
     if (!produce()) break;
 
-  while (consumed < issued) {
-    const int k = consumed % nst;
-    const uint32_t parity = (uint32_t)((consumed / nst) & 1);
-    if (!mbar_wait_bounded(&bar[k], parity, kWaitLimitNs)) {
-      if (lane == 0) atomicOr(p.status, kFlagTimeout);
-      for (int c = consumed + 1; c < issued; ++c)
-        mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs / 16);
-      return;
-    }
-    const StageMeta mt = meta[k];
+  // Finish an item: write its partial (or, merged, its output / its share of the merge).
+  auto finish_item = [&](const StageMeta& mt) {
     const long long head_row0 = (long long)mt.s * p.hq + (long long)mt.g * p.group;
-    if (!(mt.flags & kMetaEmpty)) {
-      if (mt.flags & kMetaFirst) {
-        if constexpr (MMA) {
-          cmp.begin(qslots + k * L.qslot_bytes);
-        } else {
-          cmp.begin(qslots + k * L.qslot_bytes, p.scale_log2);
-        }
-      }
-      const int nvalid = mt.flags & kMetaValid;
-      if (nvalid > 0) {
-        if constexpr (MMA) {
-          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid, p.scale_log2);
-        } else {
-          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid);
-        }
-      }
-    }
-    if ((mt.flags & kMetaLast) && !p.merged) {
+    if (!p.merged) {
       bool wrote = false;
       if (!(mt.flags & kMetaEmpty)) wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
       // -inf for this chunk when nothing was accumulated, and for every chunk after the last one
@@ -644,34 +688,83 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         const int hh = i / cnt, jj = j0 + i % cnt;
         p.partial_lse[(head_row0 + hh) * p.splits + jj] = -INFINITY;
       }
-    } else if (mt.flags & kMetaLast) {
-      const int nch = (mt.flags >> kMetaChunkShift) & 0xffff;
-      if (mt.flags & kMetaEmpty) {
-        for (int i = lane; i < p.group * D; i += 32) p.out[head_row0 * D + i] = __float2half_rn(0.f);
-        if (p.lse_out != nullptr && lane < p.group) p.lse_out[head_row0 + lane] = -INFINITY;
-      } else if (nch == 1) {
-        cmp.finish_out(p.out, p.lse_out, head_row0);
-      } else {
-        const bool wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
-        if (!wrote && lane < p.group) p.partial_lse[(head_row0 + lane) * p.splits + mt.j] = -INFINITY;
-        // Publish this chunk, then count it; the chunk that completes the count merges them all.
+      return;
+    }
+    const int nch = (mt.flags >> kMetaChunkShift) & 0xffff;
+    if (mt.flags & kMetaEmpty) {
+      for (int i = lane; i < p.group * D; i += 32) p.out[head_row0 * D + i] = __float2half_rn(0.f);
+      if (p.lse_out != nullptr && lane < p.group) p.lse_out[head_row0 + lane] = -INFINITY;
+    } else if (nch == 1) {
+      cmp.finish_out(p.out, p.lse_out, head_row0);
+    } else {
+      const bool wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
+      if (!wrote && lane < p.group) p.partial_lse[(head_row0 + lane) * p.splits + mt.j] = -INFINITY;
+      // Publish this chunk, then count it; the chunk that completes the count merges them all.
+      __threadfence();
+      __syncwarp();
+      int* counter = p.counters + (long long)mt.s * p.hkv + mt.g;
+      int done = 0;
+      if (lane == 0) done = atomicAdd(counter, 1) + 1;
+      done = __shfl_sync(kFull, done, 0);
+      if (done == nch) {
         __threadfence();
-        __syncwarp();
-        int* counter = p.counters + (long long)mt.s * p.hkv + mt.g;
-        int done = 0;
-        if (lane == 0) done = atomicAdd(counter, 1) + 1;
-        done = __shfl_sync(kFull, done, 0);
-        if (done == nch) {
-          __threadfence();
-          merge_group<D>(p.partial_lse, p.partial_o, head_row0, p.group, p.splits, nch, lane, p.out, p.lse_out);
-          if (lane == 0) *counter = 0;  // ready for the next launch
-        }
+        merge_group<D>(p.partial_lse, p.partial_o, head_row0, p.group, p.splits, nch, lane, p.out, p.lse_out);
+        if (lane == 0) *counter = 0;  // ready for the next launch
       }
     }
-    ++consumed;
-    fence_proxy_async_smem();  // this lane's reads/writes of the stage before the TMA refill
+  };
+
+  // Bounded wait for stage `c`; on expiry flag a timeout and drain (bounded) the copies in flight.
+  auto wait_stage = [&](int c) -> bool {
+    if (mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs)) return true;
+    if (lane == 0) atomicOr(p.status, kFlagTimeout);
+    for (int d = c + 1; d < issued; ++d) mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kWaitLimitNs / 16);
+    return false;
+  };
+
+  while (consumed < issued) {
+    const int k = consumed % nst;
+    if (!wait_stage(consumed)) return;
+    const StageMeta mt = meta[k];
+    int used = 1;
+    if (!(mt.flags & kMetaEmpty)) {
+      if (mt.flags & kMetaFirst) {
+        if constexpr (MMA) {
+          cmp.begin(qslots + k * L.qslot_bytes);
+        } else {
+          cmp.begin(qslots + k * L.qslot_bytes, p.scale_log2);
+        }
+      }
+      const int nvalid = mt.flags & kMetaValid;
+      if constexpr (!MMA) {
+        // two pages of the same item at once when the next one is already in flight
+        if (!(mt.flags & kMetaLast) && consumed + 1 < issued) {
+          if (!wait_stage(consumed + 1)) return;
+          const int k2 = (consumed + 1) % nst;
+          const StageMeta mt2 = meta[k2];
+          const int nvalid2 = mt2.flags & kMetaValid;
+          unsigned char* s1 = stages + (size_t)k * L.stage_bytes;
+          unsigned char* s2 = stages + (size_t)k2 * L.stage_bytes;
+          if (nvalid > 0 && nvalid2 > 0) {
+            cmp.page2(s1, nvalid, s2, nvalid2);
+          } else {
+            if (nvalid > 0) cmp.page(s1, nvalid);
+            if (nvalid2 > 0) cmp.page(s2, nvalid2);
+          }
+          used = 2;
+          if (mt2.flags & kMetaLast) finish_item(mt2);
+        } else if (nvalid > 0) {
+          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid);
+        }
+      } else {
+        if (nvalid > 0) cmp.page(stages + (size_t)k * L.stage_bytes, nvalid, p.scale_log2);
+      }
+    }
+    if (used == 1 && (mt.flags & kMetaLast)) finish_item(mt);
+    consumed += used;
+    fence_proxy_async_smem();  // this lane's reads/writes of the stages before their TMA refill
     __syncwarp();
-    produce();
+    for (int u = 0; u < used; ++u) produce();
   }
 }
 
