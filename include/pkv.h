@@ -156,11 +156,16 @@ pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const voi
  * chunks of ceil(n_s / num_splits) pages).
  *   num_splits > 0            per-sequence chunks: c_s = ceil(n_s / num_splits), splits = num_splits
  *   chunk_pages > 0           uniform chunks of chunk_pages pages, splits = ceil(max_pages / c)
- *   both 0                    the planner picks a uniform chunk size from the batch, the KV heads,
- *                             max_pages_per_seq, total_pages (0 = unknown, taken as
- *                             batch * max_pages_per_seq) and the device's SM count, so that the
- *                             work items fill the resident warps; the split count never exceeds
- *                             max_splits.
+ *   both 0, total_pages > 0   the balanced partition (*chunk_pages_out = -1): the page units of all
+ *                             (sequence, KV head) pairs, in sequence, head, page order, are cut
+ *                             into W = min(SMs x resident decode warps, U) equal runs, run w being
+ *                             units [floor(w*U/W), floor((w+1)*U/W)) with U = Hkv * total_pages;
+ *                             chunk j of a (sequence, KV head) is its piece in the j-th run that
+ *                             meets it; splits = ceil(max_pages * W / U) + 1.  total_pages must
+ *                             equal page_indptr[batch].
+ *   both 0, total_pages == 0  a uniform chunk size from the batch, the KV heads, max_pages_per_seq
+ *                             and the SM count, so that the work items fill the resident warps.
+ *   The split count never exceeds max_splits (the balanced partition is not used when it would).
  * (Zero TVM Documentation, "How it works": split-K over KV chunks with a fixed ?splitk=N; the
  * choice from length and SM count is this library's.)
  */
@@ -184,7 +189,7 @@ size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim);
  *                                      sequence length = 16 * (n_s - 1) + last_page_len[s]
  *                                      (n_s = 0 means an empty sequence)
  *   max_pages_per_seq                  an upper bound of every n_s
- *   total_pages                        page_indptr[batch] if known on the host, else 0
+ *   total_pages                        page_indptr[batch] if known on the host (then exact), else 0
  *   num_splits, chunk_pages, max_splits  split selection, see pkv_plan_decode
  *   sm_scale                           score scale; 0 selects 1/sqrt(head_dim)
  *   partial_o   fp32 [batch][Hq][S][head_dim]  S = *splits_used (capacity max_splits)
@@ -192,7 +197,8 @@ size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim);
  *   splits_used (host, nullable)       receives S
  *
  * Query head h reads KV head h / (Hq / Hkv).  Chunk j of sequence s covers its pages
- * [j*c, min((j+1)*c, n_s)); for each (s, h, j) with at least one token:
+ * [j*c, min((j+1)*c, n_s)) (or its j-th piece of the balanced partition); for each (s, h, j)
+ * with at least one token:
  *   partial_lse = ln sum_t exp(sm_scale * q.K_t),  partial_o = sum_t softmax_t * V_t
  * in fp32 from fp16 data.  Chunks with no token get partial_lse = -inf and partial_o is not
  * written.  Device-detected: page ids out of range (the page is masked out), n_s above

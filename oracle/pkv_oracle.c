@@ -331,6 +331,62 @@ int orc_split_attention(const orc_geom* g, const uint16_t* pool, const uint16_t*
   return rc;
 }
 
+/* Split-K partial attention with the page-balanced partition: the page units of all
+ * (sequence, KV head) segments, ordered sequence-major, then KV head, then page, are cut into
+ * num_warps contiguous runs, run w being units [floor(w*U/W), floor((w+1)*U/W)) with
+ * U = Hkv * page_indptr[B].  Piece k of a segment is its intersection with the k-th run that
+ * meets it.  partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S]; slots without a piece are
+ * (0, -inf).  Requires num_warps <= U (every run non-empty). */
+int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
+                                 const int32_t* page_indptr, const int32_t* page_indices,
+                                 const int32_t* last_page_len, int num_warps, int num_out_splits,
+                                 double sm_scale, double* partial_o, double* partial_lse) {
+  orc_init();
+  const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads, S = num_out_splits;
+  if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0 || S <= 0 || num_warps <= 0) return ORC_INVALID;
+  const int G = Hq / Hkv;
+  const int64_t U = (int64_t)Hkv * page_indptr[B];
+  const int64_t W = num_warps;
+  if (U > 0 && W > U) return ORC_INVALID;
+  int rc = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
+    int s = (int)(sh / Hq), h = (int)(sh % Hq), kvh = h / G;
+    int len;
+    int r = seq_len_of(page_indptr, last_page_len, s, &len);
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) q[i] = dec(q_rope[sh * d + i]);
+    for (int j = 0; j < S; ++j) {
+      for (int i = 0; i < d; ++i) partial_o[(sh * S + j) * d + i] = 0.0;
+      partial_lse[sh * S + j] = -INFINITY;
+    }
+    const int64_t n = page_indptr[s + 1] - page_indptr[s];
+    const int64_t b = (int64_t)Hkv * page_indptr[s] + (int64_t)kvh * n; /* first unit of the segment */
+    int k = 0;
+    for (int64_t w = 0; w < W && r == ORC_OK && n > 0; ++w) {
+      const int64_t u0 = w * U / W, u1 = (w + 1) * U / W;
+      const int64_t lo = u0 > b ? u0 : b, hi = u1 < b + n ? u1 : b + n;
+      if (hi <= lo) continue;
+      if (k >= S) {
+        r = ORC_INVALID;
+        break;
+      }
+      int64_t t0 = (lo - b) * ORC_PAGE, t1 = (hi - b) * ORC_PAGE;
+      if (t1 > len) t1 = len;
+      if (t0 > len) t0 = len;
+      r = attend(g, pool, q, s, kvh, (int)t0, (int)t1, page_indptr, page_indices, sm_scale,
+                 partial_o + (sh * S + k) * d, partial_lse + sh * S + k);
+      ++k;
+    }
+    free(q);
+    if (r != ORC_OK) {
+#pragma omp critical
+      rc = r;
+    }
+  }
+  return rc;
+}
+
 /* Log-sum-exp merge of the partials: out = sum_j w_j o_j / sum_j w_j with w_j = exp(lse_j - M),
  * M = max_j lse_j, lse = M + ln sum_j w_j.  out_f16 (nullable) gets out rounded to fp16. */
 int orc_combine(const double* partial_o, const double* partial_lse, int B, int Hq, int S, int d,

@@ -474,10 +474,13 @@ __device__ __forceinline__ int find_sequence(const int* prefix, int batch, int w
 struct Item {
   int s, j, g, first, n, nch, p0, p1, pnext, win_base, window, last, q0, q1;
   bool active;
+  bool drop;  // balanced mode: a piece of a sequence with more pieces than partial slots
 };
 
 // Locate item w and start the global loads it needs (last-page length, query row, the first 32
 // page ids).  The loaded values are consumed later by activate(), so the loads overlap other work.
+__device__ __forceinline__ void issue_item_loads(Item& it, const DecodeParams& p, int lane);
+
 __device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams& p, const int* prefix,
                                              const int* indptr, int lane) {
   const int s = find_sequence(prefix, p.batch, w);
@@ -495,6 +498,40 @@ __device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams
   } else {
     it.p0 = it.p1 = 0;
   }
+  it.drop = false;
+  issue_item_loads(it, p, lane);
+}
+
+// First warp of the balanced partition whose run contains unit b.
+__device__ __forceinline__ long long first_run(long long b, long long U, long long W) {
+  return ((b + 1) * W + U - 1) / U - 1;
+}
+
+// Balanced mode: the piece of warp gw that starts at unit u of its run [u, u_end).
+__device__ __forceinline__ void prepare_piece(Item& it, long long u, long long u_end, int gw, const DecodeParams& p,
+                                              const int* prefix, const int* indptr, int lane) {
+  const int s = find_sequence(prefix, p.batch, (int)u);
+  const int n = indptr[s + 1] - indptr[s];
+  const long long r = u - prefix[s];
+  const int g = (int)(r / n);
+  const int page = (int)(r - (long long)g * n);
+  it.s = s;
+  it.g = g;
+  it.first = indptr[s];
+  it.n = n;
+  it.p0 = page;
+  it.p1 = (int)min((long long)n, (long long)page + (u_end - u));
+  const long long b = (long long)prefix[s] + (long long)g * n;  // first unit of the segment
+  const long long wf = first_run(b, p.units, p.part_warps);
+  const long long wl = first_run(b + n - 1, p.units, p.part_warps);
+  it.j = (int)(gw - wf);
+  it.nch = (int)(wl - wf + 1);
+  it.drop = false;
+  issue_item_loads(it, p, lane);
+}
+
+__device__ __forceinline__ void issue_item_loads(Item& it, const DecodeParams& p, int lane) {
+  const int s = it.s;
   it.pnext = it.p0;
   it.win_base = it.p0;
   const int idx = it.p0 + lane;
@@ -512,11 +549,19 @@ __device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams
 
 // Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
 // item per KV head (its chunks are reported as -inf).
-__device__ __forceinline__ void activate_item(Item& it, int* status, int lane) {
+__device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, int lane) {
   bool ok = it.nch > 0;
   if (it.n > 0) ok = ok && it.last >= 1 && it.last <= kPageSize && it.q1 > it.q0;
+  if (p.balanced && it.nch > p.splits) {
+    // more pieces than partial slots (more pages than declared): the first piece reports the
+    // sequence empty, the others are dropped
+    ok = false;
+    it.drop = it.j != 0;
+    it.j = 0;
+    it.nch = 1;
+  }
   if (!ok) {
-    if (lane == 0) atomicOr(status, kFlagBadSequence);
+    if (lane == 0) atomicOr(p.status, kFlagBadSequence);
     it.p0 = it.p1 = it.pnext = 0;
   }
 }
@@ -539,10 +584,13 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   for (int i = tid; i < p.warps * p.nstage; i += blockDim.x) mbar_init(&bars[i], 1);
   fence_mbarrier_init();
 
-  // Page ranges of every sequence, then items per sequence and their exclusive prefix sum.
+  // Page ranges of every sequence, then items per sequence and their exclusive prefix sum (chunk
+  // mode) or the first page unit of every sequence (balanced mode).
   for (int i = tid; i <= p.batch; i += blockDim.x) indptr[i] = p.page_indptr[i];
   __syncthreads();
-  {
+  if (p.balanced) {
+    for (int i = tid; i <= p.batch; i += blockDim.x) prefix[i] = p.hkv * indptr[i];
+  } else {
     const int per = (p.batch + blockDim.x - 1) / blockDim.x;
     const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
     int local = 0;
@@ -584,27 +632,44 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   const uint64_t policy = l2_policy_evict_first();
 
   // Producer state: the item being issued (cur) and the next one, whose loads are in flight.
-  int w_next = blockIdx.x * p.warps + warp;
+  const int gw = blockIdx.x * p.warps + warp;
+  int w_next = gw;
+  long long u_next = 0, u_end = 0;  // balanced mode: the rest of this warp's run of page units
+  if (p.balanced && gw < p.part_warps) {
+    u_next = (long long)gw * p.units / p.part_warps;
+    u_end = (long long)(gw + 1) * p.units / p.part_warps;
+  }
+  auto prepare_next = [&](Item& it) -> bool {
+    if (p.balanced) {
+      if (u_next >= u_end) return false;
+      prepare_piece(it, u_next, u_end, gw, p, prefix, indptr, lane);
+      u_next += it.p1 - it.p0;
+      return true;
+    }
+    if (w_next >= total) return false;
+    prepare_item(it, w_next, p, prefix, indptr, lane);
+    w_next += W;
+    return true;
+  };
   Item cur, nxt;
   cur.active = false;
   nxt.active = false;
-  if (w_next < total) {
-    prepare_item(nxt, w_next, p, prefix, indptr, lane);  // index loads only: allowed before the wait
-    w_next += W;
+  if (p.balanced && prefix[p.batch] != p.units) {
+    if (tid == 0) atomicOr(p.status, kFlagBadSequence);  // declared page total differs: nothing runs
+  } else {
+    prepare_next(nxt);  // index loads only: allowed before the wait
   }
   pdl_wait();  // q_rope and the pool pages come from the preceding kernel
   int issued = 0, consumed = 0;
 
   auto produce = [&]() -> bool {
-    if (!cur.active) {
+    while (!cur.active) {
       if (!nxt.active) return false;
       cur = nxt;
-      activate_item(cur, p.status, lane);
+      activate_item(cur, p, lane);
       nxt.active = false;
-      if (w_next < total) {
-        prepare_item(nxt, w_next, p, prefix, indptr, lane);
-        w_next += W;
-      }
+      prepare_next(nxt);
+      if (cur.drop) cur.active = false;
     }
     const int k = issued % nst;
     StageMeta mt;
@@ -612,7 +677,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     mt.j = cur.j;
     mt.g = cur.g;
     if (cur.p1 == cur.p0) {
-      mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | kMetaLastChunk | (1 << kMetaChunkShift);
+      const int nch = max(cur.nch, 1);
+      mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | (cur.j >= nch - 1 ? kMetaLastChunk : 0) |
+                 (nch << kMetaChunkShift);
       if (lane == 0) {
         meta[k] = mt;
         mbar_arrive(&bar[k]);
@@ -671,6 +738,21 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     cmp.init(lane);
   }
 
+  if (p.balanced && gw == 0) {
+    // sequences without pages own no page units: report them empty here
+    for (int s = 0; s < p.batch; ++s) {
+      if (indptr[s + 1] != indptr[s]) continue;
+      const long long row0 = (long long)s * p.hq;
+      if (p.merged) {
+        for (int i = lane; i < p.hq * D; i += 32) p.out[row0 * D + i] = __float2half_rn(0.f);
+        if (p.lse_out != nullptr)
+          for (int i = lane; i < p.hq; i += 32) p.lse_out[row0 + i] = -INFINITY;
+      } else {
+        for (int i = lane; i < p.hq * p.splits; i += 32) p.partial_lse[row0 * p.splits + i] = -INFINITY;
+      }
+    }
+  }
+
   for (int i = 0; i < nst; ++i)
     if (!produce()) break;
 
@@ -691,13 +773,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       return;
     }
     const int nch = (mt.flags >> kMetaChunkShift) & 0xffff;
-    if (mt.flags & kMetaEmpty) {
+    if (nch == 1 && (mt.flags & kMetaEmpty)) {
       for (int i = lane; i < p.group * D; i += 32) p.out[head_row0 * D + i] = __float2half_rn(0.f);
       if (p.lse_out != nullptr && lane < p.group) p.lse_out[head_row0 + lane] = -INFINITY;
     } else if (nch == 1) {
       cmp.finish_out(p.out, p.lse_out, head_row0);
     } else {
-      const bool wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
+      const bool wrote =
+          !(mt.flags & kMetaEmpty) && cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
       if (!wrote && lane < p.group) p.partial_lse[(head_row0 + lane) * p.splits + mt.j] = -INFINITY;
       // Publish this chunk, then count it; the chunk that completes the count merges them all.
       __threadfence();

@@ -88,10 +88,23 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
     *chunk = chunk_pages;
     return PKV_OK;
   }
-  // Automatic: chunk size so that the items fill the resident warps once (uniform lengths) or
-  // about four times (ragged lengths, where small items balance the long ones).
   const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, batch > 0 ? batch : 1);
   const long long warps = (long long)c->num_sms * cfg.warps;
+  // Automatic with the exact page total: the balanced partition, every warp of the grid taking an
+  // equal run of (sequence, KV head, page) units; a segment of n pages meets at most
+  // ceil(n * W / U) + 1 runs.
+  if (total_pages > 0) {
+    const long long U = (long long)total_pages * c->desc.num_kv_heads;
+    const long long W = std::min(warps, U);
+    const long long s_bal = ((long long)max_pages * W + U - 1) / U + 1;
+    if (U < 0x7fffffffLL && s_bal <= max_splits) {
+      *splits = (int)s_bal;
+      *chunk = -1;
+      return PKV_OK;
+    }
+  }
+  // Automatic without it: chunk size so that the items fill the resident warps once (uniform
+  // lengths) or about four times (ragged lengths, where small items balance the long ones).
   const long long uniform_pages = (long long)batch * max_pages;
   const long long pages = total_pages > 0 ? total_pages : uniform_pages;
   const bool ragged = total_pages > 0 && 10 * (long long)total_pages < 9 * uniform_pages;
@@ -355,9 +368,13 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   p.counters = counters;
   p.out = static_cast<__half*>(out);
   p.lse_out = lse_out;
+  p.balanced = chunk < 0 ? 1 : 0;
+  p.units = (long long)total_pages * c->desc.num_kv_heads;
   long long grid = (items + cfg.warps - 1) / cfg.warps;
-  if (grid > c->num_sms) grid = c->num_sms;
+  if (grid > c->num_sms || p.balanced) grid = c->num_sms;
   if (grid < 1) grid = 1;
+  p.part_warps = (int)std::min(grid * cfg.warps, std::max(p.units, 1LL));
+  if (p.balanced) p.chunk_pages = 0;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 

@@ -57,6 +57,12 @@ struct DecodeParams {
   int* counters;
   __half* out;
   float* lse_out;   // nullable
+  // Balanced mode: the page units of all (sequence, KV head) segments, in sequence, head, page
+  // order, are cut into part_warps equal runs (run w = units [w*U/W, (w+1)*U/W)); warp w of the
+  // grid processes run w.  units = U = hkv * page_indptr[batch] as declared by the host.
+  int balanced;
+  long long units;
+  int part_warps;
 };
 
 struct CombineParams {

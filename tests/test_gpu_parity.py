@@ -98,6 +98,24 @@ def test_partials_parity_explicit_plans(name, plan):
     H.assert_close_lse(g["lse"], lse)
 
 
+@pytest.mark.parametrize("name", ["tiny", "phi3_b1_ctx300", "ragged_d96", "gqa4_mixed_chunks", "gqa2_d96",
+                                  "gqa4_d64", "gqa8_d128", "mha_d64_long"])
+def test_partials_parity_balanced_partition(name):
+    """The automatic plan with the exact page total: every piece of the page-balanced partition."""
+    import oracle
+
+    step, host_pool, cache, tabs, g = _gpu_pool_after(SMALL[name], plan={})
+    S, chunk = cache.plan_decode(step.batch, step.max_pages_per_seq, int(step.page_indptr[-1]))
+    assert chunk == -1 and g["pl"].shape[2] == S
+    sms, warps = cache.device_info()
+    W = min(sms * warps, step.cfg.hkv * int(step.page_indptr[-1]))
+    gq = g["q_out"][H.query_rows(step)]
+    po, pl = oracle.split_attention_balanced(H.geometry(step), g["pool"], gq, step.page_indptr, step.page_indices,
+                                             step.last_page_len, W, S)
+    H.assert_close_lse(g["pl"], pl, "partial_lse")
+    H.assert_close_partial_o(g["po"], po, pl)
+
+
 @pytest.mark.parametrize("name", ["tiny", "phi3_b1_ctx300", "ragged_d96", "gqa4_mixed_chunks", "gqa8_d128",
                                   "gqa2_d96", "mha_d64_long"])
 @pytest.mark.parametrize("plan", [{}, {"num_splits": 3}, {"chunk_pages": 2}])

@@ -337,3 +337,33 @@ def test_scale_zero_gives_uniform_weights():
     out, lse = oracle.attention(_geom(pool, 2, 2, 8), pool, q, pi, px, last, sm_scale=0.0)
     V = f16(logical_kv(pool, pi, px, 0, 20, 1))
     np.testing.assert_allclose(out[0], V.mean(axis=1), atol=1e-13)
+
+
+@pytest.mark.parametrize("warps", [1, 3, 7, 40, 200])
+def test_balanced_partition_covers_each_segment_once_and_merges_to_unsplit(warps):
+    """The page-balanced partition: runs of equal size (within one page) whose pieces tile every
+    (sequence, KV head) segment exactly once; merging the pieces gives the unsplit result."""
+    rng = np.random.default_rng(31)
+    lengths = [1, 16, 17, 150, 333, 40]
+    hq, hkv, d = 4, 2, 16
+    pool, q, pi, px, last = random_paged_case(rng, lengths, hq, hkv, d)
+    g = _geom(pool, hq, hkv, d)
+    U = hkv * int(pi[-1])
+    if warps > U:
+        pytest.skip("more runs than units")
+    ref, ref_lse = oracle.attention(g, pool, q, pi, px, last)
+    S = -(-int(np.diff(pi).max()) * warps // U) + 1
+    po, pl = oracle.split_attention_balanced(g, pool, q, pi, px, last, warps, S)
+    out, out16, lse = oracle.combine(po, pl)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+    # run sizes differ by at most one page; pieces of a segment are contiguous and cover it
+    sizes = [(w + 1) * U // warps - w * U // warps for w in range(warps)]
+    assert max(sizes) - min(sizes) <= 1 and sum(sizes) == U
+    n_pieces = (~np.isinf(pl)).sum(axis=2)
+    for s_, L in enumerate(lengths):
+        n = int(pi[s_ + 1] - pi[s_])
+        for h in range(hq):
+            b = hkv * int(pi[s_]) + (h // (hq // hkv)) * n
+            expect = len({w for w in range(warps) for u in range(b, b + n) if w * U // warps <= u < (w + 1) * U // warps})
+            assert n_pieces[s_, h] == expect
