@@ -283,8 +283,16 @@ def run_ours(args):
 
     counters = torch.zeros(B * cfg.hkv, dtype=torch.int32, device=dev)
 
+    def layer_chain_fused(l):
+        """append, split-K decode and combine in one launch"""
+        q, k, v = qkv[l]
+        cache.append_decode_attention(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                                      tabs["page_indices"], tabs["last_page_len"], step.max_pages_per_seq,
+                                      counters, total_pages=total_pages, q_out=q_out[l], partial_o=po,
+                                      partial_lse=pl, out=outs[l], lse=lses[l])
+
     def layer_chain(l):
-        """append -> split-K decode with the combine merged into the same launch"""
+        """append -> split-K decode with the combine merged into the same launch (two launches)"""
         q, k, v = qkv[l]
         cache.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
                           tabs["page_indices"], q_out=q_out[l])
@@ -312,6 +320,10 @@ def run_ours(args):
         for l in layers:
             layer_chain_separate(l)
 
+    def step_fn_fused():
+        for l in layers:
+            layer_chain_fused(l)
+
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         step_fn()
@@ -325,6 +337,9 @@ def run_ours(args):
     graph_sep = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_sep, stream=stream):
         step_fn_separate()
+    graph_fused = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_fused, stream=stream):
+        step_fn_fused()
     torch.cuda.synchronize()
 
     def barrier():
@@ -351,16 +366,21 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
-    # the same step as three launches per layer (append, decode, combine), for reference
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph_sep.replay()
-        ev0.record()
-        for _ in range(args.steps):
-            graph_sep.replay()
-        ev1.record()
-    torch.cuda.synchronize()
-    step_sep_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    # the same step as three launches per layer (append, decode, combine) and as one (append,
+    # decode and combine fused), for reference
+    def time_graph(g):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            ev0.record()
+            for _ in range(args.steps):
+                g.replay()
+            ev1.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+
+    step_sep_ms = time_graph(graph_sep)
+    step_fused_ms = time_graph(graph_fused)
     code, flags = cache.check_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after the timed region: {pkv.status_string(code)} flags {flags:#x}")
@@ -460,6 +480,8 @@ def run_ours(args):
         "attention_us_per_step_per_layer": dec_ms * 1e3,
         "step_us_per_layer": step_ms * 1e3 / cfg.layers,
         "step": "per layer: pkv_append_rope + pkv_decode_attention_merged (2 launches)",
+        "one_kernel": {"value": world * kv_step / (step_fused_ms * 1e-3) / 1e9, "ms_per_step": step_fused_ms,
+                       "step": "per layer: pkv_append_decode_attention"},
         "separate_kernels": {"value": world * kv_step / (step_sep_ms * 1e-3) / 1e9, "ms_per_step": step_sep_ms,
                              "step": "per layer: pkv_append_rope + pkv_decode_attention + pkv_combine"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

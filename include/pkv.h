@@ -232,6 +232,27 @@ pkv_status pkv_decode_attention_merged(const pkv_cache* cache, int layer, const 
                                        float* lse_out, int* splits_used, pkv_stream_t stream);
 
 /*
+ * One layer's whole decode step in one launch: the append of pkv_append_rope, then
+ * pkv_decode_attention_merged over the updated cache, with the same results bit for bit.
+ * Arguments as pkv_append_rope (q, k, v are the raw new tokens; q_out receives the rotated q) and
+ * pkv_decode_attention_merged (the query of sequence s is its last new token, row
+ * append_indptr[s+1]-1; every sequence with pages must append at least one token).
+ * The work item that owns a page holding new tokens writes their rotated K and V for its KV head
+ * before it copies the page; every item rotates its query itself; the first item of each
+ * (sequence, KV head) writes that group's q_out rows and reports positions out of range.
+ * (Zero TVM Documentation, "Decode loop": QKV + RoPE + KV-append fused into one dispatch; here
+ * the append is fused with the attention that follows it instead.)
+ */
+pkv_status pkv_append_decode_attention(pkv_cache* cache, int layer, const void* q, const void* k,
+                                       const void* v, const int32_t* pos_map, const int32_t* append_indptr,
+                                       int num_tokens, const int32_t* page_indptr,
+                                       const int32_t* page_indices, const int32_t* last_page_len, int batch,
+                                       int max_pages_per_seq, int total_pages, int num_splits,
+                                       int chunk_pages, int max_splits, float sm_scale, void* q_out,
+                                       float* partial_o, float* partial_lse, int32_t* chunk_counters,
+                                       void* out, float* lse_out, int* splits_used, pkv_stream_t stream);
+
+/*
  * pkv_decode_attention_merged without caller workspace, for callers that cannot allocate device
  * memory on this path: a framework that reserved the whole device for its own allocator up
  * front, or a serving loop that must not risk an allocation failure or the implicit device

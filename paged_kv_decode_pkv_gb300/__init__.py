@@ -76,6 +76,9 @@ def lib():
         L.pkv_decode_attention_merged.restype = i
         L.pkv_decode_attention_merged.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, i, f, P, P, P, P, P,
                                                   ctypes.POINTER(i), P]
+        L.pkv_append_decode_attention.restype = i
+        L.pkv_append_decode_attention.argtypes = [P, i, P, P, P, P, P, i, P, P, P, i, i, i, i, i, i, f, P, P, P, P,
+                                                  P, P, ctypes.POINTER(i), P]
         L.pkv_decode_attention_noalloc.restype = i
         L.pkv_decode_attention_noalloc.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, f, P, P,
                                                    ctypes.POINTER(i), P]
@@ -253,6 +256,37 @@ class Cache:
             float(sm_scale), _ptr(partial_o), _ptr(partial_lse), _ptr(chunk_counters), _ptr(out), _ptr(lse),
             ctypes.byref(used), _stream(stream)), "pkv_decode_attention_merged")
         return out, lse
+
+    def append_decode_attention(self, layer, q, k, v, pos_map, append_indptr, page_indptr, page_indices,
+                                last_page_len, max_pages_per_seq, chunk_counters, total_pages=0, num_splits=0,
+                                chunk_pages=0, sm_scale=0.0, q_out=None, partial_o=None, partial_lse=None,
+                                out=None, lse=None, stream=None):
+        """pkv_append_decode_attention (append + merged decode in one launch); returns (q_out, out, lse)."""
+        import torch
+
+        B = int(page_indptr.numel()) - 1
+        dev = q.device
+        if partial_o is None or partial_lse is None:
+            S, _ = self.plan_decode(B, max_pages_per_seq, total_pages, num_splits, chunk_pages)
+            partial_o = torch.empty((B, self.num_qo_heads, S, self.head_dim), dtype=torch.float32, device=dev)
+            partial_lse = torch.empty((B, self.num_qo_heads, S), dtype=torch.float32, device=dev)
+        if q_out is None:
+            q_out = torch.empty_like(q)
+        if out is None:
+            out = torch.empty((B, self.num_qo_heads, self.head_dim), dtype=torch.float16, device=dev)
+        if lse is None:
+            lse = torch.empty((B, self.num_qo_heads), dtype=torch.float32, device=dev)
+        if chunk_counters.dtype != torch.int32 or chunk_counters.numel() < B * self.num_kv_heads:
+            raise ValueError("chunk_counters must be an int32 tensor of at least batch * num_kv_heads elements")
+        cap = int(partial_lse.numel()) // max(1, B * self.num_qo_heads)
+        used = ctypes.c_int()
+        _check(lib().pkv_append_decode_attention(
+            self.handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(pos_map), _ptr(append_indptr), int(pos_map.numel()),
+            _ptr(page_indptr), _ptr(page_indices), _ptr(last_page_len), B, max_pages_per_seq, total_pages,
+            num_splits, chunk_pages, max(cap, 1), float(sm_scale), _ptr(q_out), _ptr(partial_o), _ptr(partial_lse),
+            _ptr(chunk_counters), _ptr(out), _ptr(lse), ctypes.byref(used), _stream(stream)),
+            "pkv_append_decode_attention")
+        return q_out, out, lse
 
     def decode_attention_noalloc(self, layer, q_rope, page_indptr, page_indices, last_page_len,
                                  max_pages_per_seq, out, lse=None, q_indptr=None, total_pages=0, num_splits=0,

@@ -55,22 +55,40 @@ struct __align__(16) StageMeta {
 constexpr int kSmemBudget = 232448 - 1024;
 
 struct Layout {
-  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, indptr_off, total;
+  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, indptr_off, aptr_off, total;
 };
 
-__host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch) {
+// Shared memory: the stage ring, then per stage a query slot (fused mode: raw query rows followed
+// by the query position's (cos, sin) row), the mbarriers, the stage metadata, and per sequence the
+// work prefix, the page ranges and (fused mode) the new-token ranges.
+__host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch,
+                                              bool fused) {
   Layout L;
   const int n = warps * nstage;
   L.stage_bytes = 64 * head_dim;  // K and V of one page for one KV head
-  L.qslot_bytes = (group * head_dim * 2 + 127) & ~127;
+  L.qslot_bytes = (group * head_dim * 2 + (fused ? 4 * head_dim : 0) + 127) & ~127;
   L.q_off = n * L.stage_bytes;
   L.bar_off = L.q_off + n * L.qslot_bytes;
   L.meta_off = L.bar_off + n * 8;
   L.meta_off = (L.meta_off + 15) & ~15;
   L.prefix_off = L.meta_off + n * 16;
   L.indptr_off = L.prefix_off + (batch + 1) * 4;
-  L.total = L.indptr_off + (batch + 1) * 4 + 1024;  // + slack to align the base to 1024
+  L.aptr_off = L.indptr_off + (batch + 1) * 4;
+  L.total = L.aptr_off + (fused ? (batch + 1) * 4 : 0) + 1024;  // + slack to align the base to 1024
   return L;
+}
+
+// Rotated element i of a head row x (rotate-half RoPE with the row's (cos, sin) table cs), with
+// the same fp32 operations and rounding order as the append kernel.
+template <int D>
+__device__ __forceinline__ float rope_element(const __half* x, const float2* cs, int i) {
+  if (i < D / 2) {
+    const float a = __half2float(x[i]), b = __half2float(x[i + D / 2]);
+    return __fmaf_rn(a, cs[i].x, -__fmul_rn(b, cs[i].y));
+  }
+  const int ii = i - D / 2;
+  const float a = __half2float(x[ii]), b = __half2float(x[i]);
+  return __fmaf_rn(b, cs[ii].x, __fmul_rn(a, cs[ii].y));
 }
 
 // Chunks of a sequence with n pages; c receives the chunk size.  Returns 0 for an invalid n.
@@ -132,6 +150,32 @@ struct GroupOne {
         "mov.b32 {vl, vh}, %2;\n\t"
         "fma.rn.f32.f16 %0, %3, vl, %0;\n\tfma.rn.f32.f16 %1, %3, vh, %1;\n\t}"
         : "+f"(o0), "+f"(o1) : "r"(v), "h"(p16));
+  }
+
+  // Fused mode: rotate the raw query row in the slot with the (cos, sin) row that follows it.
+  __device__ void begin_rotate(const unsigned char* qslot, float scale_log2_) {
+    const __half* x = reinterpret_cast<const __half*>(qslot);
+    const float2* cs = reinterpret_cast<const float2*>(qslot + D * 2);
+#pragma unroll
+    for (int e = 0; e < HPL; ++e) {
+      const int i = li * DPL + 2 * e;
+      const __half2 h = __floats2half2_rn(rope_element<D>(x, cs, i), rope_element<D>(x, cs, i + 1));
+      q2[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+    scale_log2 = scale_log2_;
+  }
+
+  // Store the rotated query (fused mode) as the q_out row of head `row` of the query token.
+  __device__ void store_query(__half* q_out_row) const {
+    if (half == 0) {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(q_out_row + li * DPL);
+#pragma unroll
+      for (int e = 0; e < HPL; ++e) dst[e] = q2[e];
+    }
   }
 
   __device__ void begin(const unsigned char* qslot, float scale_log2_) {
@@ -332,6 +376,43 @@ struct GroupMma {
     return stage + u * REGION + (off ^ (((off >> 7) & SWZ) << 4));
   }
 
+  // Fused mode: fragments of the rotated query rows (raw rows in the slot, then the (cos, sin) row).
+  __device__ void begin_rotate(const unsigned char* qslot) {
+    const int c = 2 * (lane & 3);
+    const float2* cs = reinterpret_cast<const float2*>(qslot + group * D * 2);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (h < group) {
+        const __half* x = reinterpret_cast<const __half*>(qslot) + h * D;
+        const int i = ks * 16 + c;
+        const __half2 lo = __floats2half2_rn(rope_element<D>(x, cs, i), rope_element<D>(x, cs, i + 1));
+        const __half2 hi = __floats2half2_rn(rope_element<D>(x, cs, i + 8), rope_element<D>(x, cs, i + 9));
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(&lo);
+        qa[ks][1] = *reinterpret_cast<const uint32_t*>(&hi);
+      } else {
+        qa[ks][0] = 0u;
+        qa[ks][1] = 0u;
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  // Store the rotated query rows (fused mode): q_out_rows points at head g*G of the query token.
+  __device__ void store_query(__half* q_out_rows) const {
+    if (h < group) {
+      const int c = 2 * (lane & 3);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(q_out_rows + h * D + ks * 16 + c);
+        dst[0] = qa[ks][0];
+        dst[4] = qa[ks][1];
+      }
+    }
+  }
+
   __device__ void begin(const unsigned char* qslot) {
     const int c = 2 * (lane & 3);
 #pragma unroll
@@ -475,6 +556,9 @@ struct Item {
   int s, j, g, first, n, nch, p0, p1, pnext, win_base, window, last, q0, q1;
   bool active;
   bool drop;  // balanced mode: a piece of a sequence with more pieces than partial slots
+  // fused mode: positions of new tokens q0 + lane (window of 32), the query position, and the
+  // range of pages the new tokens fall in
+  int posw, qpos, pmin, pmax;
 };
 
 // Locate item w and start the global loads it needs (last-page length, query row, the first 32
@@ -547,11 +631,108 @@ __device__ __forceinline__ void issue_item_loads(Item& it, const DecodeParams& p
   it.active = true;
 }
 
+// Fused mode: the new tokens' positions (first 32) and the query position, from the shared copy of
+// append_indptr.
+__device__ __forceinline__ void issue_fused_loads(Item& it, const DecodeParams& p, const int* aptr, int lane) {
+  it.q0 = aptr[it.s];
+  it.q1 = aptr[it.s + 1];
+  const int t = it.q0 + lane;
+  it.posw = t < it.q1 ? p.pos_map[t] : -1;
+  it.qpos = (it.q1 - it.q0 > 32) ? p.pos_map[it.q1 - 1] : 0;
+}
+
+// Fused mode, at activation: the query position and the page range of the new tokens; the first
+// piece of a (sequence, KV head) also reports new tokens whose position is out of range.
+__device__ __forceinline__ void activate_fused(Item& it, const DecodeParams& p, int lane) {
+  const int T = it.q1 - it.q0;
+  if (T <= 32 && T > 0) it.qpos = __shfl_sync(0xffffffffu, it.posw, T - 1);
+  int lo = 0x7fffffff, hi = -1;
+  bool bad = false;
+  for (int w0 = 0; w0 < T; w0 += 32) {
+    const int t = it.q0 + w0 + lane;
+    const int pos = w0 == 0 ? it.posw : (t < it.q1 ? p.pos_map[t] : -1);
+    if (w0 + lane < T) {
+      const bool ok = pos >= 0 && pos < p.max_position && (pos >> 4) < it.n;
+      bad |= !ok;
+      if (ok) {
+        lo = min(lo, pos >> 4);
+        hi = max(hi, pos >> 4);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+  }
+  if (__any_sync(0xffffffffu, bad) && it.j == 0 && lane == 0) atomicOr(p.status, kFlagBadPosition);
+  it.pmin = lo;
+  it.pmax = hi;
+}
+
+// Fused mode: write the rotated K and V of KV head g of every new token that falls in page
+// `page_ord` (physical page pid) of the item's sequence, before that page's TMA copy is issued.
+template <int D>
+__device__ __forceinline__ void append_page(const Item& it, int page_ord, int pid, const DecodeParams& p, int lane) {
+  const int T = it.q1 - it.q0;
+  for (int w0 = 0; w0 < T; w0 += 32) {
+    const int t = it.q0 + w0 + lane;
+    const int pos = w0 == 0 ? it.posw : (t < it.q1 ? p.pos_map[t] : -1);
+    const bool mine = w0 + lane < T && pos >= 0 && pos < p.max_position && (pos >> 4) == page_ord;
+    unsigned ballot = __ballot_sync(0xffffffffu, mine);
+    while (ballot) {
+      const int src = __ffs(ballot) - 1;
+      ballot &= ballot - 1;
+      const int tok = it.q0 + w0 + src;
+      const int tpos = __shfl_sync(0xffffffffu, pos, src);
+      const __half* kr = p.k_new + ((long long)tok * p.hkv + it.g) * D;
+      const __half* vr = p.v_new + ((long long)tok * p.hkv + it.g) * D;
+      const float2* cs = p.rope + (long long)tpos * (D / 2);
+      const long long row = (((long long)pid * 2) * p.hkv + it.g) * kPageSize + (tpos & 15);
+      __half* kd = p.pool + row * D;
+      __half* vd = p.pool + (row + (long long)p.hkv * kPageSize) * D;
+      for (int i = lane; i < D / 2; i += 32) {
+        const float a = __half2float(kr[i]), b = __half2float(kr[i + D / 2]);
+        const float2 c = cs[i];
+        kd[i] = __float2half_rn(__fmaf_rn(a, c.x, -__fmul_rn(b, c.y)));
+        kd[i + D / 2] = __float2half_rn(__fmaf_rn(b, c.x, __fmul_rn(a, c.y)));
+      }
+      for (int i = lane; i < D; i += 32) vd[i] = vr[i];
+    }
+  }
+}
+
+// Fused mode: the q_out rows of the query heads g*G .. g*G+G-1 of every new token except the query
+// token (whose rows the consumer stores from its rotated fragments).
+template <int D>
+__device__ __forceinline__ void store_other_queries(int s, int g, const int* aptr, const DecodeParams& p, int lane) {
+  const int q0 = aptr[s], q1 = aptr[s + 1];
+  for (int t = q0; t < q1 - 1; ++t) {
+    const int pos = p.pos_map[t];
+    if (pos < 0 || pos >= p.max_position) continue;
+    const float2* cs = p.rope + (long long)pos * (D / 2);
+    for (int hh = 0; hh < p.group; ++hh) {
+      const __half* x = p.q + ((long long)t * p.hq + (long long)g * p.group + hh) * D;
+      __half* y = p.q_out + ((long long)t * p.hq + (long long)g * p.group + hh) * D;
+      for (int i = lane; i < D / 2; i += 32) {
+        const float a = __half2float(x[i]), b = __half2float(x[i + D / 2]);
+        const float2 c = cs[i];
+        y[i] = __float2half_rn(__fmaf_rn(a, c.x, -__fmul_rn(b, c.y)));
+        y[i + D / 2] = __float2half_rn(__fmaf_rn(b, c.x, __fmul_rn(a, c.y)));
+      }
+    }
+  }
+}
+
 // Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
 // item per KV head (its chunks are reported as -inf).
 __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, int lane) {
   bool ok = it.nch > 0;
   if (it.n > 0) ok = ok && it.last >= 1 && it.last <= kPageSize && it.q1 > it.q0;
+  if (p.fused && it.n > 0 && it.q1 > it.q0) {
+    activate_fused(it, p, lane);
+    ok = ok && it.qpos >= 0 && it.qpos < p.max_position;
+  }
   if (p.balanced && it.nch > p.splits) {
     // more pieces than partial slots (more pages than declared): the first piece reports the
     // sequence empty, the others are dropped
@@ -566,16 +747,17 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
   }
 }
 
-template <int D, bool MMA>
+template <int D, bool MMA, bool FUSED>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch);
+  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
   int* prefix = reinterpret_cast<int*>(base + L.prefix_off);
   int* indptr = reinterpret_cast<int*>(base + L.indptr_off);
+  int* aptr = reinterpret_cast<int*>(base + L.aptr_off);  // fused mode: append_indptr
   __shared__ int warp_sums[32];
 
   pdl_launch_dependents();
@@ -586,7 +768,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
 
   // Page ranges of every sequence, then items per sequence and their exclusive prefix sum (chunk
   // mode) or the first page unit of every sequence (balanced mode).
-  for (int i = tid; i <= p.batch; i += blockDim.x) indptr[i] = p.page_indptr[i];
+  for (int i = tid; i <= p.batch; i += blockDim.x) {
+    indptr[i] = p.page_indptr[i];
+    if constexpr (FUSED) aptr[i] = p.q_indptr[i];
+  }
   __syncthreads();
   if (p.balanced) {
     for (int i = tid; i <= p.batch; i += blockDim.x) prefix[i] = p.hkv * indptr[i];
@@ -628,6 +813,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   unsigned char* stages = base + (size_t)warp * nst * L.stage_bytes;
   unsigned char* qslots = base + L.q_off + (size_t)warp * nst * L.qslot_bytes;
   const uint32_t q_bytes = (uint32_t)(p.group * D * 2);
+  const uint32_t cs_bytes = FUSED ? (uint32_t)(4 * D) : 0u;  // the query position's (cos, sin) row
   const uint32_t page_bytes = (uint32_t)(64 * D);
   const uint64_t policy = l2_policy_evict_first();
 
@@ -644,11 +830,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if (u_next >= u_end) return false;
       prepare_piece(it, u_next, u_end, gw, p, prefix, indptr, lane);
       u_next += it.p1 - it.p0;
-      return true;
+    } else {
+      if (w_next >= total) return false;
+      prepare_item(it, w_next, p, prefix, indptr, lane);
+      w_next += W;
     }
-    if (w_next >= total) return false;
-    prepare_item(it, w_next, p, prefix, indptr, lane);
-    w_next += W;
+    if constexpr (FUSED) issue_fused_loads(it, p, aptr, lane);
     return true;
   };
   Item cur, nxt;
@@ -698,10 +885,18 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       const bool lastchunk = cur.j == cur.nch - 1;
       mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0) |
                  (cur.nch << kMetaChunkShift);
+      if constexpr (FUSED) {
+        // new tokens of this page: write their rotated K and V first, then let the copy read them
+        if (page_ok && cur.pnext >= cur.pmin && cur.pnext <= cur.pmax) {
+          append_page<D>(cur, cur.pnext, pid, p, lane);
+          fence_proxy_async_global();
+          __syncwarp();
+        }
+      }
       if (lane == 0) {
         if (!page_ok) atomicOr(p.status, kFlagBadPage);
         meta[k] = mt;
-        const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes : 0u);
+        const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes + cs_bytes : 0u);
         if (bytes) {
           mbar_arrive_expect_tx(&bar[k], bytes);
         } else {
@@ -710,6 +905,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         if (first) {
           const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
           bulk_load(qslots + k * L.qslot_bytes, qsrc, q_bytes, &bar[k]);
+          if constexpr (FUSED)
+            bulk_load(qslots + k * L.qslot_bytes + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes,
+                      &bar[k]);
         }
         if (page_ok) {
           unsigned char* dst = stages + (size_t)k * L.stage_bytes;
@@ -756,6 +954,19 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   for (int i = 0; i < nst; ++i)
     if (!produce()) break;
 
+  // Bounded wait for stage `c`; on expiry flag a timeout and drain (bounded) the copies in flight.
+  auto wait_stage = [&](int c) -> bool {
+    if (mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs)) return true;
+    if (lane == 0) atomicOr(p.status, kFlagTimeout);
+    for (int d = c + 1; d < issued; ++d) mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kWaitLimitNs / 16);
+    return false;
+  };
+
+  bool pending_merge = false;
+  long long pm_row0 = 0;
+  int pm_nch = 0;
+  int* pm_counter = nullptr;
+
   // Finish an item: write its partial (or, merged, its output / its share of the merge).
   auto finish_item = [&](const StageMeta& mt) {
     const long long head_row0 = (long long)mt.s * p.hq + (long long)mt.g * p.group;
@@ -790,19 +1001,54 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if (lane == 0) done = atomicAdd(counter, 1) + 1;
       done = __shfl_sync(kFull, done, 0);
       if (done == nch) {
+        // this chunk completed the group: merge once this warp's stages are released
         __threadfence();
-        merge_group<D>(p.partial_lse, p.partial_o, head_row0, p.group, p.splits, nch, lane, p.out, p.lse_out);
-        if (lane == 0) *counter = 0;  // ready for the next launch
+        pending_merge = true;
+        pm_row0 = head_row0;
+        pm_nch = nch;
+        pm_counter = counter;
       }
     }
   };
 
-  // Bounded wait for stage `c`; on expiry flag a timeout and drain (bounded) the copies in flight.
-  auto wait_stage = [&](int c) -> bool {
-    if (mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs)) return true;
-    if (lane == 0) atomicOr(p.status, kFlagTimeout);
-    for (int d = c + 1; d < issued; ++d) mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kWaitLimitNs / 16);
-    return false;
+  // Merge a completed group.  With the ring empty (the usual case at the end of a warp's run) the
+  // group's partial rows arrive in one bulk copy into the ring; otherwise they are read directly.
+  auto run_merge = [&]() {
+    const int rows_bytes = pm_nch * D * 4;
+    const bool smem_ok = issued == consumed && pm_nch <= 64 && p.group * rows_bytes <= nst * L.stage_bytes;
+    if (smem_ok) {
+      fence_proxy_async_global();  // the partials were written through the generic proxy
+      const int k = issued % nst;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar[k], (uint32_t)(p.group * rows_bytes));
+        for (int hh = 0; hh < p.group; ++hh)
+          bulk_load(stages + hh * rows_bytes, p.partial_o + (pm_row0 + hh) * p.splits * D, rows_bytes, &bar[k]);
+      }
+      float la[kMaxGroup], lb[kMaxGroup];
+#pragma unroll
+      for (int hh = 0; hh < kMaxGroup; ++hh) {
+        const float* lrow = p.partial_lse + (pm_row0 + hh) * p.splits;
+        la[hh] = (hh < p.group && lane < pm_nch) ? lrow[lane] : -INFINITY;
+        lb[hh] = (hh < p.group && lane + 32 < pm_nch) ? lrow[lane + 32] : -INFINITY;
+      }
+      if (!wait_stage(issued)) return false;
+      ++issued;
+      ++consumed;
+#pragma unroll
+      for (int hh = 0; hh < kMaxGroup; ++hh) {
+        if (hh >= p.group) break;
+        const long long row = pm_row0 + hh;
+        merge_row_smem<D>(la[hh], lb[hh], reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane,
+                          p.out + row * D, p.lse_out != nullptr ? p.lse_out + row : nullptr);
+      }
+      fence_proxy_async_smem();  // the reads above before later copies into the ring
+      __syncwarp();
+    } else {
+      merge_group<D>(p.partial_lse, p.partial_o, pm_row0, p.group, p.splits, pm_nch, lane, p.out, p.lse_out);
+    }
+    if (lane == 0) *pm_counter = 0;  // ready for the next launch
+    pending_merge = false;
+    return true;
   };
 
   while (consumed < issued) {
@@ -812,7 +1058,19 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     int used = 1;
     if (!(mt.flags & kMetaEmpty)) {
       if (mt.flags & kMetaFirst) {
-        if constexpr (MMA) {
+        if constexpr (FUSED) {
+          if constexpr (MMA) {
+            cmp.begin_rotate(qslots + k * L.qslot_bytes);
+          } else {
+            cmp.begin_rotate(qslots + k * L.qslot_bytes, p.scale_log2);
+          }
+          if (mt.j == 0) {
+            // the first piece of each (sequence, KV head) writes the rotated queries (q_out)
+            const int qrow = aptr[mt.s + 1] - 1;
+            cmp.store_query(p.q_out + ((long long)qrow * p.hq + (long long)mt.g * p.group) * D);
+            store_other_queries<D>(mt.s, mt.g, aptr, p, lane);
+          }
+        } else if constexpr (MMA) {
           cmp.begin(qslots + k * L.qslot_bytes);
         } else {
           cmp.begin(qslots + k * L.qslot_bytes, p.scale_log2);
@@ -847,37 +1105,44 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     consumed += used;
     fence_proxy_async_smem();  // this lane's reads/writes of the stages before their TMA refill
     __syncwarp();
+    if (pending_merge && !run_merge()) return;
     for (int u = 0; u < used; ++u) produce();
   }
 }
 
-template <int D, bool MMA>
+template <int D, bool MMA, bool FUSED>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&decode_kernel<D, MMA>);
+  return reinterpret_cast<void*>(&decode_kernel<D, MMA, FUSED>);
 }
 
-void* select_kernel(int head_dim, bool mma) {
+template <bool FUSED>
+void* select_kernel_t(int head_dim, bool mma) {
   switch (head_dim) {
-    case 64: return mma ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
-    case 96: return mma ? kernel_ptr<96, true>() : kernel_ptr<96, false>();
-    case 128: return mma ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+    case 64: return mma ? kernel_ptr<64, true, FUSED>() : kernel_ptr<64, false, FUSED>();
+    case 96: return mma ? kernel_ptr<96, true, FUSED>() : kernel_ptr<96, false, FUSED>();
+    case 128: return mma ? kernel_ptr<128, true, FUSED>() : kernel_ptr<128, false, FUSED>();
     default: return nullptr;
   }
 }
 
+void* select_kernel(int head_dim, bool mma, bool fused) {
+  return fused ? select_kernel_t<true>(head_dim, mma) : select_kernel_t<false>(head_dim, mma);
+}
+
 }  // namespace
 
-DecodeConfig decode_config(int group, int head_dim, int batch) {
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
   DecodeConfig c;
   c.mma = group >= 2;
+  c.fused = fused;
   c.warps = c.mma ? 6 : 8;
-  const Layout one = make_layout(c.warps, 1, head_dim, group, batch);
+  const Layout one = make_layout(c.warps, 1, head_dim, group, batch, fused);
   const int per_stage = c.warps * (one.stage_bytes + one.qslot_bytes + 8 + 16);
-  const int fixed = (batch + 1) * 8 + 1024 + 64;
+  const int fixed = (batch + 1) * (fused ? 12 : 8) + 1024 + 64;
   int nstage = (kSmemBudget - fixed) / per_stage;
   if (nstage > 8) nstage = 8;
   c.nstage = nstage;
-  c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch).total : 0;
+  c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused).total : 0;
   if (c.mma) {
     c.box_inner = head_dim == 96 ? 32 : 64;
     c.swizzle_bytes = head_dim == 96 ? 64 : 128;
@@ -889,7 +1154,7 @@ DecodeConfig decode_config(int group, int head_dim, int batch) {
 }
 
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
-  void* k = select_kernel(head_dim, cfg.mma);
+  void* k = select_kernel(head_dim, cfg.mma, cfg.fused);
   if (k == nullptr) return cudaErrorInvalidValue;
   const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e != cudaSuccess) return e;
@@ -898,7 +1163,7 @@ cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl) {
-  void* k = select_kernel(head_dim, cfg.mma);
+  void* k = select_kernel(head_dim, cfg.mma, cfg.fused);
   if (k == nullptr || cfg.smem_bytes == 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);

@@ -232,6 +232,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   // One 4-D tensor map per pool: dims (head_dim, slot, kv_head, page*2 + kv).
   const DecodeConfig cfg = pkv::decode_config(group, D, 1);
   e = pkv::decode_prepare(cfg, D);
+  if (e == cudaSuccess) e = pkv::decode_prepare(pkv::decode_config(group, D, 1, true), D);
   if (e == cudaSuccess) e = pkv::append_prepare();
   if (e == cudaSuccess) e = pkv::combine_prepare();
   if (e != cudaSuccess) {
@@ -316,12 +317,21 @@ pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int tot
 
 namespace {
 
-// Shared body of pkv_decode_attention and pkv_decode_attention_merged.
+// The append inputs of the fused entry point.
+struct FusedArgs {
+  const void* k;
+  const void* v;
+  const int32_t* pos_map;
+  void* q_out;
+};
+
+// Shared body of pkv_decode_attention, pkv_decode_attention_merged and pkv_append_decode_attention.
 pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
                          const int32_t* page_indptr, const int32_t* page_indices, const int32_t* last_page_len,
                          int batch, int max_pages, int total_pages, int num_splits, int chunk_pages, int max_splits,
                          float sm_scale, float* partial_o, float* partial_lse, int32_t* counters, void* out,
-                         float* lse_out, bool merged, int* splits_used, cudaStream_t stream) {
+                         float* lse_out, bool merged, int* splits_used, cudaStream_t stream,
+                         const FusedArgs* fused = nullptr) {
   if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return fail(PKV_ERR_INVALID_ARG, "cache or layer");
   int S = 0, chunk = 0;
   const pkv_status ps = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
@@ -340,8 +350,15 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   const long long items = (long long)batch * c->desc.num_kv_heads * S;
   if (items > 0x3fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
+  if (fused != nullptr &&
+      (fused->k == nullptr || fused->v == nullptr || fused->pos_map == nullptr || fused->q_out == nullptr ||
+       q_indptr == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (fused != nullptr && (!aligned(fused->k, 16) || !aligned(fused->v, 16) || !aligned(fused->q_out, 16) ||
+                           fused->q_out == q_rope))
+    return fail(PKV_ERR_INVALID_ARG, "misaligned or aliased q/k/v/q_out");
   const int D = c->desc.head_dim;
-  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch);
+  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch, fused != nullptr);
   if (cfg.nstage < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this batch");
   pkv::DecodeParams p;
   p.q = static_cast<const __half*>(q_rope);
@@ -375,6 +392,14 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   if (grid < 1) grid = 1;
   p.part_warps = (int)std::min(grid * cfg.warps, std::max(p.units, 1LL));
   if (p.balanced) p.chunk_pages = 0;
+  p.fused = fused != nullptr ? 1 : 0;
+  p.k_new = fused ? static_cast<const __half*>(fused->k) : nullptr;
+  p.v_new = fused ? static_cast<const __half*>(fused->v) : nullptr;
+  p.pos_map = fused ? fused->pos_map : nullptr;
+  p.q_out = fused ? static_cast<__half*>(fused->q_out) : nullptr;
+  p.pool = static_cast<__half*>(c->pools[layer]);
+  p.rope = reinterpret_cast<const float2*>(c->desc.rope_table);
+  p.max_position = c->desc.max_position;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 
@@ -390,6 +415,20 @@ pkv_status pkv_decode_attention(const pkv_cache* c, int layer, const void* q_rop
   return decode_common(c, layer, q_rope, q_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
                        total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse, nullptr,
                        nullptr, nullptr, false, splits_used, stream);
+}
+
+pkv_status pkv_append_decode_attention(pkv_cache* c, int layer, const void* q, const void* k, const void* v,
+                                       const int32_t* pos_map, const int32_t* append_indptr, int num_tokens,
+                                       const int32_t* page_indptr, const int32_t* page_indices,
+                                       const int32_t* last_page_len, int batch, int max_pages, int total_pages,
+                                       int num_splits, int chunk_pages, int max_splits, float sm_scale, void* q_out,
+                                       float* partial_o, float* partial_lse, int32_t* chunk_counters, void* out,
+                                       float* lse_out, int* splits_used, pkv_stream_t stream) {
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative num_tokens");
+  const FusedArgs fa{k, v, pos_map, q_out};
+  return decode_common(c, layer, q, append_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
+                       total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse,
+                       chunk_counters, out, lse_out, true, splits_used, stream, &fa);
 }
 
 pkv_status pkv_decode_attention_merged(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,

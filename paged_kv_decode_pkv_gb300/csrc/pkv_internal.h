@@ -63,6 +63,17 @@ struct DecodeParams {
   int balanced;
   long long units;
   int part_warps;
+  // Fused mode: the step's append runs inside the decode.  q is then the raw (unrotated) query,
+  // q_indptr the append_indptr (the query of a sequence is its last new token), and the kernel
+  // writes the rotated K and V of the new tokens into the pool and the rotated q into q_out.
+  int fused;
+  const __half* k_new;
+  const __half* v_new;
+  const int* pos_map;
+  __half* q_out;
+  __half* pool;
+  const float2* rope;
+  int max_position;
 };
 
 struct CombineParams {
@@ -76,6 +87,7 @@ struct CombineParams {
 // Decode launch geometry for a (group, head_dim) pair and a batch size.
 struct DecodeConfig {
   bool mma;             // tensor-core path (group >= 2)
+  bool fused;           // append folded into the decode
   int warps;            // warps per CTA
   int nstage;           // per-warp ring depth
   size_t smem_bytes;    // dynamic shared memory
@@ -83,7 +95,7 @@ struct DecodeConfig {
   int swizzle_bytes;    // 0 (none), 64 or 128
 };
 
-DecodeConfig decode_config(int group, int head_dim, int batch);
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused = false);
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim);  // function attributes
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl);
