@@ -44,7 +44,24 @@ def parse():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller variants of a workload, for profiler captures of the same kernels
+    ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size")
+    ap.add_argument("--pool-pages", type=int, default=0, help="override the pool size in pages")
     return ap.parse_args()
+
+
+def workload(args) -> W.Config:
+    cfg = W.CONFIGS[args.config]
+    changes = {}
+    if args.layers:
+        changes["layers"] = args.layers
+    if args.batch:
+        changes["batch"] = args.batch
+        changes["chunk_seqs"] = min(cfg.chunk_seqs, args.batch)
+    if args.pool_pages:
+        changes["pool_pages"] = args.pool_pages
+    return W.scaled(cfg, **changes) if changes else cfg
 
 
 def measured_peaks():
@@ -201,7 +218,7 @@ def run_reference(args):
 
     from tests import harness as H
 
-    cfg = W.CONFIGS[args.config]
+    cfg = workload(args)
     step = W.make_step(cfg)
     layers, seqs = reference_sample(step)
     sub = W.substep(step, seqs) if len(seqs) < step.batch else step
@@ -251,7 +268,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    cfg = W.CONFIGS[args.config]
+    cfg = workload(args)
     step = W.make_step(cfg, rank_seed(cfg, rank))
     layers = list(range(cfg.layers))
     pools = [W.device_pool(step, l) for l in layers]
