@@ -43,9 +43,11 @@ __device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const fl
   }
 }
 
+// The shared copy of append_indptr is dynamic (batch + 1 ints, none past kIndptrSmemCap) so that a
+// small launch fits beside a resident decode CTA and can start under programmatic dependent launch.
 template <int D>
 __global__ void __launch_bounds__(kThreads) append_rope_kernel(AppendParams p) {
-  __shared__ int s_indptr[kIndptrSmemCap + 1];
+  extern __shared__ int s_indptr[];
   __shared__ TokenSlot s_tok[kTokensPerCta];
   __shared__ float2 s_cs[kTokensPerCta][D / 2];  // (cos, sin) rows of the CTA's tokens
   pdl_launch_dependents();
@@ -156,7 +158,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.num_tokens + kTokensPerCta - 1) / kTokensPerCta);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = p.batch <= kIndptrSmemCap ? (size_t)(p.batch + 1) * sizeof(int) : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

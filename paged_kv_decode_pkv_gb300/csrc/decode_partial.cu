@@ -269,12 +269,12 @@ struct GroupOne {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint16_t pi = (uint16_t)__shfl_sync(kFull, (uint32_t)pbits, (lane & 16) | (2 * i));
-      if (2 * i + half < nvalid) {
-        uint32_t x[HPL];
-        load_row(Vb + (2 * i + half) * D * 2, li, x);
+      // rows past nvalid have p = 0 but may hold any bits (NaN): select zeros instead of branching
+      const bool valid = 2 * i + half < nvalid;
+      uint32_t x[HPL];
+      load_row(Vb + (2 * i + half) * D * 2, li, x);
 #pragma unroll
-        for (int e = 0; e < HPL; ++e) fma_pv(pi, x[e], o[2 * e], o[2 * e + 1]);
-      }
+      for (int e = 0; e < HPL; ++e) fma_pv(pi, valid ? x[e] : 0u, o[2 * e], o[2 * e + 1]);
     }
   }
 
@@ -750,8 +750,9 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
 template <int D, bool MMA, bool FUSED>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                         ~static_cast<uintptr_t>(1023));
+  // aligned to 1024 bytes by an offset from the shared array itself, so that every access below is
+  // compiled as a shared-memory access
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
@@ -848,6 +849,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   }
   pdl_wait();  // q_rope and the pool pages come from the preceding kernel
   int issued = 0, consumed = 0;
+  // ring slot and barrier phase parity of `issued` and of `consumed`
+  int ik = 0, ck = 0;
+  uint32_t iph = 0, cph = 0;
+  auto advance = [&](int& k, uint32_t& ph) {
+    if (++k == nst) {
+      k = 0;
+      ph ^= 1u;
+    }
+  };
 
   auto produce = [&]() -> bool {
     while (!cur.active) {
@@ -858,7 +868,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       prepare_next(nxt);
       if (cur.drop) cur.active = false;
     }
-    const int k = issued % nst;
+    const int k = ik;
     StageMeta mt;
     mt.s = cur.s;
     mt.j = cur.j;
@@ -925,6 +935,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if (lastp) cur.active = false;
     }
     ++issued;
+    advance(ik, iph);
     return true;
   };
 
@@ -954,9 +965,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   for (int i = 0; i < nst; ++i)
     if (!produce()) break;
 
-  // Bounded wait for stage `c`; on expiry flag a timeout and drain (bounded) the copies in flight.
-  auto wait_stage = [&](int c) -> bool {
-    if (mbar_wait_bounded(&bar[c % nst], (uint32_t)((c / nst) & 1), kWaitLimitNs)) return true;
+  // Bounded wait for stage number c (ring slot k, phase parity ph); on expiry flag a timeout and
+  // drain (bounded) the copies in flight.
+  auto wait_stage = [&](int c, int k, uint32_t ph) -> bool {
+    if (mbar_wait_bounded(&bar[k], ph, kWaitLimitNs)) return true;
     if (lane == 0) atomicOr(p.status, kFlagTimeout);
     for (int d = c + 1; d < issued; ++d) mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kWaitLimitNs / 16);
     return false;
@@ -1018,7 +1030,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     const bool smem_ok = issued == consumed && pm_nch <= 64 && p.group * rows_bytes <= nst * L.stage_bytes;
     if (smem_ok) {
       fence_proxy_async_global();  // the partials were written through the generic proxy
-      const int k = issued % nst;
+      const int k = ik;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar[k], (uint32_t)(p.group * rows_bytes));
         for (int hh = 0; hh < p.group; ++hh)
@@ -1031,9 +1043,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         la[hh] = (hh < p.group && lane < pm_nch) ? lrow[lane] : -INFINITY;
         lb[hh] = (hh < p.group && lane + 32 < pm_nch) ? lrow[lane + 32] : -INFINITY;
       }
-      if (!wait_stage(issued)) return false;
+      if (!wait_stage(issued, ik, iph)) return false;
       ++issued;
       ++consumed;
+      advance(ik, iph);
+      advance(ck, cph);
 #pragma unroll
       for (int hh = 0; hh < kMaxGroup; ++hh) {
         if (hh >= p.group) break;
@@ -1052,8 +1066,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   };
 
   while (consumed < issued) {
-    const int k = consumed % nst;
-    if (!wait_stage(consumed)) return;
+    const int k = ck;
+    if (!wait_stage(consumed, ck, cph)) return;
     const StageMeta mt = meta[k];
     int used = 1;
     if (!(mt.flags & kMetaEmpty)) {
@@ -1080,8 +1094,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if constexpr (!MMA) {
         // two pages of the same item at once when the next one is already in flight
         if (!(mt.flags & kMetaLast) && consumed + 1 < issued) {
-          if (!wait_stage(consumed + 1)) return;
-          const int k2 = (consumed + 1) % nst;
+          int k2 = ck;
+          uint32_t ph2 = cph;
+          advance(k2, ph2);
+          if (!wait_stage(consumed + 1, k2, ph2)) return;
           const StageMeta mt2 = meta[k2];
           const int nvalid2 = mt2.flags & kMetaValid;
           unsigned char* s1 = stages + (size_t)k * L.stage_bytes;
@@ -1103,6 +1119,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
     if (used == 1 && (mt.flags & kMetaLast)) finish_item(mt);
     consumed += used;
+    for (int u = 0; u < used; ++u) advance(ck, cph);
     fence_proxy_async_smem();  // this lane's reads/writes of the stages before their TMA refill
     __syncwarp();
     if (pending_merge && !run_merge()) return;
