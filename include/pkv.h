@@ -232,14 +232,19 @@ pkv_status pkv_decode_attention_merged(const pkv_cache* cache, int layer, const 
                                        float* lse_out, int* splits_used, pkv_stream_t stream);
 
 /*
- * One layer's whole decode step in one launch: the append of pkv_append_rope, then
- * pkv_decode_attention_merged over the updated cache, with the same results bit for bit.
- * Arguments as pkv_append_rope (q, k, v are the raw new tokens; q_out receives the rotated q) and
- * pkv_decode_attention_merged (the query of sequence s is its last new token, row
- * append_indptr[s+1]-1; every sequence with pages must append at least one token).
- * The work item that owns a page holding new tokens writes their rotated K and V for its KV head
- * before it copies the page; every item rotates its query itself; the first item of each
- * (sequence, KV head) writes that group's q_out rows and reports positions out of range.
+ * One layer's whole decode step: the append of pkv_append_rope, then pkv_decode_attention_merged
+ * over the updated cache, with the same results bit for bit.  Arguments as pkv_append_rope (q, k,
+ * v are the raw new tokens; q_out receives the rotated q) and pkv_decode_attention_merged (the
+ * query of sequence s is its last new token, row append_indptr[s+1]-1; every sequence with pages
+ * must append at least one token).
+ * When num_tokens == batch (one new token per sequence, the decode step) everything runs in one
+ * launch: the stage that starts a work item also brings the token's raw k and v, the consumer
+ * rotates k (the append kernel's arithmetic) and, on the page that holds the token, writes the
+ * rotated K and V rows into the staged copy and into the cache; every item rotates its query
+ * itself and the first item of each (sequence, KV head) writes that group's q_out rows and reports
+ * positions out of range.  A sequence whose append_indptr range is not exactly one token is then
+ * reported as PKV_FLAG_BAD_SEQUENCE.  Otherwise (a chunked append) the call issues the two
+ * launches of pkv_append_rope and pkv_decode_attention_merged.
  * (Zero TVM Documentation, "Decode loop": QKV + RoPE + KV-append fused into one dispatch; here
  * the append is fused with the attention that follows it instead.)
  */

@@ -31,6 +31,7 @@
 #include "merge.cuh"
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace pkv {
 namespace {
@@ -44,6 +45,9 @@ constexpr int kMetaFirst = 1 << 5;
 constexpr int kMetaLast = 1 << 6;
 constexpr int kMetaLastChunk = 1 << 7;
 constexpr int kMetaEmpty = 1 << 8;
+constexpr int kMetaNew = 1 << 9;     // one-launch mode: the stage also carries the new token's k and v
+constexpr int kMetaPatch = 1 << 10;  // one-launch mode: the page holds the new token (slot in bits 11..14)
+constexpr int kMetaSlotShift = 11;
 constexpr int kMetaChunkShift = 16;  // bits 16..31: chunks of the item's sequence
 
 struct __align__(16) StageMeta {
@@ -51,30 +55,42 @@ struct __align__(16) StageMeta {
 };
 
 // Dynamic shared memory budget: the 227 KB per-block opt-in maximum less room for the kernel's
-// static shared memory.
-constexpr int kSmemBudget = 232448 - 1024;
+// static shared memory (128 bytes).
+constexpr int kSmemBudget = 232448 - 256;
+
+// Alignment of the shared-memory base: 1024 bytes for the swizzled boxes of the tensor-core path,
+// 128 bytes for the plain boxes of the CUDA-core path.
+__host__ __device__ constexpr int smem_align(int group) { return group >= 2 ? 1024 : 128; }
 
 struct Layout {
-  int stage_bytes, qslot_bytes, q_off, bar_off, meta_off, prefix_off, indptr_off, aptr_off, total;
+  int stage_bytes, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, prefix_off, indptr_off, aptr_off,
+      total;
 };
 
-// Shared memory: the stage ring, then per stage a query slot (fused mode: raw query rows followed
-// by the query position's (cos, sin) row), the mbarriers, the stage metadata, and per sequence the
-// work prefix, the page ranges and (fused mode) the new-token ranges.
+// Items whose query rows may be in flight at once, per warp (one item slot each).
+constexpr int kItemSlots = 2;
+
+// Shared memory: the stage ring, then per warp kItemSlots item slots (the item's query rows;
+// one-launch mode also the query position's (cos, sin) row and the new token's raw k and v rows)
+// and (one-launch mode) the rotated K and V rows of the new token, the mbarriers, the stage
+// metadata, (one-launch mode) the page id of each stage, and per sequence the work prefix, the
+// page ranges and (one-launch mode) the new-token ranges.
 __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch,
                                               bool fused) {
   Layout L;
   const int n = warps * nstage;
   L.stage_bytes = 64 * head_dim;  // K and V of one page for one KV head
-  L.qslot_bytes = (group * head_dim * 2 + (fused ? 4 * head_dim : 0) + 127) & ~127;
+  L.qslot_bytes = (group * head_dim * 2 + (fused ? 8 * head_dim : 0) + 15) & ~15;
   L.q_off = n * L.stage_bytes;
-  L.bar_off = L.q_off + n * L.qslot_bytes;
+  L.patch_off = L.q_off + warps * kItemSlots * L.qslot_bytes;
+  L.bar_off = L.patch_off + (fused ? warps * 4 * head_dim : 0);
   L.meta_off = L.bar_off + n * 8;
   L.meta_off = (L.meta_off + 15) & ~15;
-  L.prefix_off = L.meta_off + n * 16;
+  L.pid_off = L.meta_off + n * 16;
+  L.prefix_off = L.pid_off + (fused ? n * 4 : 0);
   L.indptr_off = L.prefix_off + (batch + 1) * 4;
   L.aptr_off = L.indptr_off + (batch + 1) * 4;
-  L.total = L.aptr_off + (fused ? (batch + 1) * 4 : 0) + 1024;  // + slack to align the base to 1024
+  L.total = L.aptr_off + (fused ? (batch + 1) * 4 : 0) + smem_align(group);  // + slack to align the base
   return L;
 }
 
@@ -118,6 +134,11 @@ struct GroupOne {
     lane = lane_;
     half = lane >> 4;
     li = lane & 15;
+  }
+
+  // Shared-memory address of 16-byte chunk c (elements 8c..8c+7) of row t of K (kv 0) or V (kv 1).
+  __device__ static uint32_t row_chunk(uint32_t stage, int kv, int t, int c) {
+    return stage + (uint32_t)((kv * kPageSize + t) * D * 2 + 16 * c);
   }
 
   // The lane's DPL consecutive fp16 values of a row, as half2 pairs.
@@ -265,16 +286,27 @@ struct GroupOne {
     }
   }
 
-  __device__ void pv(const unsigned char* Vb, uint16_t pbits, int nvalid) {
+  // Slots past the sequence end may hold anything (even NaN): zero their V rows so that p = 0
+  // times V adds exactly nothing.
+  __device__ void zero_v_tail(unsigned char* Vb, int nvalid) const {
+    if (nvalid < kPageSize) {
+      constexpr int kChunksPerRow = D / 8;
+      const int n = (kPageSize - nvalid) * kChunksPerRow;
+      const uint32_t base = smem_u32(Vb + nvalid * D * 2);
+      for (int i = lane; i < n; i += 32)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + 16 * i), "r"(0u) : "memory");
+      __syncwarp();
+    }
+  }
+
+  __device__ void pv(const unsigned char* Vb, uint16_t pbits) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint16_t pi = (uint16_t)__shfl_sync(kFull, (uint32_t)pbits, (lane & 16) | (2 * i));
-      // rows past nvalid have p = 0 but may hold any bits (NaN): select zeros instead of branching
-      const bool valid = 2 * i + half < nvalid;
       uint32_t x[HPL];
       load_row(Vb + (2 * i + half) * D * 2, li, x);
 #pragma unroll
-      for (int e = 0; e < HPL; ++e) fma_pv(pi, valid ? x[e] : 0u, o[2 * e], o[2 * e + 1]);
+      for (int e = 0; e < HPL; ++e) fma_pv(pi, x[e], o[2 * e], o[2 * e + 1]);
     }
   }
 
@@ -283,7 +315,8 @@ struct GroupOne {
     return (row < nvalid) ? sc : -INFINITY;
   }
 
-  __device__ void page(const unsigned char* stage, int nvalid) {
+  __device__ void page(unsigned char* stage, int nvalid) {
+    zero_v_tail(stage + kPageSize * D * 2, nvalid);
     float acc[8];
     dots(stage, acc);
     float sc[1];
@@ -291,11 +324,13 @@ struct GroupOne {
     sc[0] = mask(sc[0], nvalid);
     uint16_t pb[1];
     softmax<1>(sc, pb);
-    pv(stage + kPageSize * D * 2, pb[0], nvalid);
+    pv(stage + kPageSize * D * 2, pb[0]);
   }
 
   // Two consecutive pages of one item at once: independent q.k work for both, one softmax update.
-  __device__ void page2(const unsigned char* sa, int na, const unsigned char* sb, int nb) {
+  __device__ void page2(unsigned char* sa, int na, unsigned char* sb, int nb) {
+    zero_v_tail(sa + kPageSize * D * 2, na);
+    zero_v_tail(sb + kPageSize * D * 2, nb);
     float acc[16];
     float (&a0)[8] = *reinterpret_cast<float(*)[8]>(&acc[0]);
     float (&a1)[8] = *reinterpret_cast<float(*)[8]>(&acc[8]);
@@ -307,8 +342,8 @@ struct GroupOne {
     sc[1] = mask(sc[1], nb);
     uint16_t pb[2];
     softmax<2>(sc, pb);
-    pv(sa + kPageSize * D * 2, pb[0], na);
-    pv(sb + kPageSize * D * 2, pb[1], nb);
+    pv(sa + kPageSize * D * 2, pb[0]);
+    pv(sb + kPageSize * D * 2, pb[1]);
   }
 
   // Writes the item's partial; returns false when nothing was accumulated.
@@ -375,6 +410,8 @@ struct GroupMma {
     const uint32_t off = (uint32_t)((kv * kPageSize + t) * (E * 2) + (dim % E) * 2);
     return stage + u * REGION + (off ^ (((off >> 7) & SWZ) << 4));
   }
+
+  __device__ static uint32_t row_chunk(uint32_t stage, int kv, int t, int c) { return chunk_addr(stage, kv, t, 8 * c); }
 
   // Fused mode: fragments of the rotated query rows (raw rows in the slot, then the (cos, sin) row).
   __device__ void begin_rotate(const unsigned char* qslot) {
@@ -556,9 +593,10 @@ struct Item {
   int s, j, g, first, n, nch, p0, p1, pnext, win_base, window, last, q0, q1;
   bool active;
   bool drop;  // balanced mode: a piece of a sequence with more pieces than partial slots
-  // fused mode: positions of new tokens q0 + lane (window of 32), the query position, and the
-  // range of pages the new tokens fall in
-  int posw, qpos, pmin, pmax;
+  // one-launch mode: the position of the sequence's single new token (also the query position),
+  // and whether its page lies in this item
+  int qpos;
+  bool has_new;
 };
 
 // Locate item w and start the global loads it needs (last-page length, query row, the first 32
@@ -631,97 +669,64 @@ __device__ __forceinline__ void issue_item_loads(Item& it, const DecodeParams& p
   it.active = true;
 }
 
-// Fused mode: the new tokens' positions (first 32) and the query position, from the shared copy of
-// append_indptr.
-__device__ __forceinline__ void issue_fused_loads(Item& it, const DecodeParams& p, const int* aptr, int lane) {
+// One-launch mode: the sequence's new-token range (from the shared copy of append_indptr) and the
+// new token's position.
+__device__ __forceinline__ void issue_fused_loads(Item& it, const DecodeParams& p, const int* aptr) {
   it.q0 = aptr[it.s];
   it.q1 = aptr[it.s + 1];
-  const int t = it.q0 + lane;
-  it.posw = t < it.q1 ? p.pos_map[t] : -1;
-  it.qpos = (it.q1 - it.q0 > 32) ? p.pos_map[it.q1 - 1] : 0;
+  it.qpos = it.q1 == it.q0 + 1 ? p.pos_map[it.q0] : -1;
 }
 
-// Fused mode, at activation: the query position and the page range of the new tokens; the first
-// piece of a (sequence, KV head) also reports new tokens whose position is out of range.
-__device__ __forceinline__ void activate_fused(Item& it, const DecodeParams& p, int lane) {
-  const int T = it.q1 - it.q0;
-  if (T <= 32 && T > 0) it.qpos = __shfl_sync(0xffffffffu, it.posw, T - 1);
-  int lo = 0x7fffffff, hi = -1;
-  bool bad = false;
-  for (int w0 = 0; w0 < T; w0 += 32) {
-    const int t = it.q0 + w0 + lane;
-    const int pos = w0 == 0 ? it.posw : (t < it.q1 ? p.pos_map[t] : -1);
-    if (w0 + lane < T) {
-      const bool ok = pos >= 0 && pos < p.max_position && (pos >> 4) < it.n;
-      bad |= !ok;
-      if (ok) {
-        lo = min(lo, pos >> 4);
-        hi = max(hi, pos >> 4);
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-  }
-  if (__any_sync(0xffffffffu, bad) && it.j == 0 && lane == 0) atomicOr(p.status, kFlagBadPosition);
-  it.pmin = lo;
-  it.pmax = hi;
+// One-launch mode, at activation: every sequence appends exactly one token; a position past the
+// cache or the sequence's pages is reported by the first piece of each (sequence, KV head).
+// Returns false when the query cannot be rotated (no single token or position out of the table).
+__device__ __forceinline__ bool activate_fused(Item& it, const DecodeParams& p, int lane) {
+  const bool single = it.q1 == it.q0 + 1;
+  const bool in_table = single && it.qpos >= 0 && it.qpos < p.max_position;
+  const bool in_pages = in_table && (it.qpos >> 4) < it.n;
+  if (single && !in_pages && it.j == 0 && lane == 0) atomicOr(p.status, kFlagBadPosition);
+  it.has_new = in_pages && (it.qpos >> 4) >= it.p0 && (it.qpos >> 4) < it.p1;
+  return in_table;
 }
 
-// Fused mode: write the rotated K and V of KV head g of every new token that falls in page
-// `page_ord` (physical page pid) of the item's sequence, before that page's TMA copy is issued.
+// One-launch mode: rotate the new token's raw k row (cs: its (cos, sin) row) and keep it with the
+// raw v row as the patch rows [K][V] of the item (the same arithmetic as the append kernel).
 template <int D>
-__device__ __forceinline__ void append_page(const Item& it, int page_ord, int pid, const DecodeParams& p, int lane) {
-  const int T = it.q1 - it.q0;
-  for (int w0 = 0; w0 < T; w0 += 32) {
-    const int t = it.q0 + w0 + lane;
-    const int pos = w0 == 0 ? it.posw : (t < it.q1 ? p.pos_map[t] : -1);
-    const bool mine = w0 + lane < T && pos >= 0 && pos < p.max_position && (pos >> 4) == page_ord;
-    unsigned ballot = __ballot_sync(0xffffffffu, mine);
-    while (ballot) {
-      const int src = __ffs(ballot) - 1;
-      ballot &= ballot - 1;
-      const int tok = it.q0 + w0 + src;
-      const int tpos = __shfl_sync(0xffffffffu, pos, src);
-      const __half* kr = p.k_new + ((long long)tok * p.hkv + it.g) * D;
-      const __half* vr = p.v_new + ((long long)tok * p.hkv + it.g) * D;
-      const float2* cs = p.rope + (long long)tpos * (D / 2);
-      const long long row = (((long long)pid * 2) * p.hkv + it.g) * kPageSize + (tpos & 15);
-      __half* kd = p.pool + row * D;
-      __half* vd = p.pool + (row + (long long)p.hkv * kPageSize) * D;
-      for (int i = lane; i < D / 2; i += 32) {
-        const float a = __half2float(kr[i]), b = __half2float(kr[i + D / 2]);
-        const float2 c = cs[i];
-        kd[i] = __float2half_rn(__fmaf_rn(a, c.x, -__fmul_rn(b, c.y)));
-        kd[i + D / 2] = __float2half_rn(__fmaf_rn(b, c.x, __fmul_rn(a, c.y)));
-      }
-      for (int i = lane; i < D; i += 32) vd[i] = vr[i];
-    }
+__device__ __forceinline__ void make_patch(const unsigned char* cs_row, const unsigned char* kv_raw,
+                                           unsigned char* patch, int lane) {
+  constexpr int kUnits = D / 16;  // rope units: chunk u pairs with chunk u + D/16
+  constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+  if (lane < kUnits) {
+    const uint4 lo = *reinterpret_cast<const uint4*>(kv_raw + 16 * lane);
+    const uint4 hi = *reinterpret_cast<const uint4*>(kv_raw + 16 * (lane + kUnits));
+    uint4 ylo, yhi;
+    rope8(lo, hi, reinterpret_cast<const float2*>(cs_row) + 8 * lane, ylo, yhi);
+    *reinterpret_cast<uint4*>(patch + 16 * lane) = ylo;
+    *reinterpret_cast<uint4*>(patch + 16 * (lane + kUnits)) = yhi;
+  } else if (lane < kUnits + kChunks) {
+    const int c = lane - kUnits;
+    *reinterpret_cast<uint4*>(patch + 2 * D + 16 * c) = *reinterpret_cast<const uint4*>(kv_raw + 2 * D + 16 * c);
   }
+  __syncwarp();
 }
 
-// Fused mode: the q_out rows of the query heads g*G .. g*G+G-1 of every new token except the query
-// token (whose rows the consumer stores from its rotated fragments).
-template <int D>
-__device__ __forceinline__ void store_other_queries(int s, int g, const int* aptr, const DecodeParams& p, int lane) {
-  const int q0 = aptr[s], q1 = aptr[s + 1];
-  for (int t = q0; t < q1 - 1; ++t) {
-    const int pos = p.pos_map[t];
-    if (pos < 0 || pos >= p.max_position) continue;
-    const float2* cs = p.rope + (long long)pos * (D / 2);
-    for (int hh = 0; hh < p.group; ++hh) {
-      const __half* x = p.q + ((long long)t * p.hq + (long long)g * p.group + hh) * D;
-      __half* y = p.q_out + ((long long)t * p.hq + (long long)g * p.group + hh) * D;
-      for (int i = lane; i < D / 2; i += 32) {
-        const float a = __half2float(x[i]), b = __half2float(x[i + D / 2]);
-        const float2 c = cs[i];
-        y[i] = __float2half_rn(__fmaf_rn(a, c.x, -__fmul_rn(b, c.y)));
-        y[i + D / 2] = __float2half_rn(__fmaf_rn(b, c.x, __fmul_rn(a, c.y)));
-      }
-    }
+// One-launch mode: write the patch rows into slot r of a staged page (layout of Compute) and into
+// the pool (page pid, KV head g), so later launches read the appended token from the cache.
+template <int D, class Compute>
+__device__ __forceinline__ void apply_patch(unsigned char* stage, const unsigned char* patch, int r, int pid, int g,
+                                            const DecodeParams& p, int lane) {
+  constexpr int kChunks = D / 8;
+  if (lane < 2 * kChunks) {
+    const int kv = lane >= kChunks ? 1 : 0;
+    const int c = lane - kv * kChunks;
+    const uint4 v = *reinterpret_cast<const uint4*>(patch + 16 * lane);
+    const uint32_t a = Compute::row_chunk(smem_u32(stage), kv, r, c);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+    __half* dst = p.pool + ((((long long)pid * 2 + kv) * p.hkv + g) * kPageSize + r) * D + 8 * c;
+    *reinterpret_cast<uint4*>(dst) = v;
   }
+  __syncwarp();
 }
 
 // Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
@@ -729,10 +734,8 @@ __device__ __forceinline__ void store_other_queries(int s, int g, const int* apt
 __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, int lane) {
   bool ok = it.nch > 0;
   if (it.n > 0) ok = ok && it.last >= 1 && it.last <= kPageSize && it.q1 > it.q0;
-  if (p.fused && it.n > 0 && it.q1 > it.q0) {
-    activate_fused(it, p, lane);
-    ok = ok && it.qpos >= 0 && it.qpos < p.max_position;
-  }
+  it.has_new = false;
+  if (p.fused && it.n > 0) ok = activate_fused(it, p, lane) && ok;
   if (p.balanced && it.nch > p.splits) {
     // more pieces than partial slots (more pages than declared): the first piece reports the
     // sequence empty, the others are dropped
@@ -744,15 +747,17 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
   if (!ok) {
     if (lane == 0) atomicOr(p.status, kFlagBadSequence);
     it.p0 = it.p1 = it.pnext = 0;
+    it.has_new = false;
   }
 }
 
 template <int D, bool MMA, bool FUSED>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
-  // aligned to 1024 bytes by an offset from the shared array itself, so that every access below is
+  // aligned (smem_align) by an offset from the shared array itself, so that every access below is
   // compiled as a shared-memory access
-  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr uint32_t kAlign = smem_align(MMA ? 2 : 1);
+  unsigned char* base = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
@@ -812,9 +817,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   uint64_t* bar = bars + warp * nst;
   StageMeta* meta = metas + warp * nst;
   unsigned char* stages = base + (size_t)warp * nst * L.stage_bytes;
-  unsigned char* qslots = base + L.q_off + (size_t)warp * nst * L.qslot_bytes;
+  unsigned char* qslots = base + L.q_off + (size_t)warp * kItemSlots * L.qslot_bytes;
   const uint32_t q_bytes = (uint32_t)(p.group * D * 2);
   const uint32_t cs_bytes = FUSED ? (uint32_t)(4 * D) : 0u;  // the query position's (cos, sin) row
+  const uint32_t kv_bytes = FUSED ? (uint32_t)(4 * D) : 0u;  // the new token's raw k and v rows
+  unsigned char* patch = base + L.patch_off + (size_t)warp * 4 * D;
+  int* meta_pid = reinterpret_cast<int*>(base + L.pid_off) + warp * p.nstage;
   const uint32_t page_bytes = (uint32_t)(64 * D);
   const uint64_t policy = l2_policy_evict_first();
 
@@ -836,7 +844,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       prepare_item(it, w_next, p, prefix, indptr, lane);
       w_next += W;
     }
-    if constexpr (FUSED) issue_fused_loads(it, p, aptr, lane);
+    if constexpr (FUSED) issue_fused_loads(it, p, aptr);
     return true;
   };
   Item cur, nxt;
@@ -849,6 +857,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   }
   pdl_wait();  // q_rope and the pool pages come from the preceding kernel
   int issued = 0, consumed = 0;
+  // Items whose first stage was issued / consumed: the first stage of item i brings its query rows
+  // into item slot i % kItemSlots, so at most kItemSlots items may be issued and not yet begun.
+  int items_issued = 0, items_begun = 0;
   // ring slot and barrier phase parity of `issued` and of `consumed`
   int ik = 0, ck = 0;
   uint32_t iph = 0, cph = 0;
@@ -868,6 +879,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       prepare_next(nxt);
       if (cur.drop) cur.active = false;
     }
+    if (cur.p1 != cur.p0 && cur.pnext == cur.p0 && items_issued - items_begun >= kItemSlots)
+      return false;  // both item slots are taken: wait until the consumer begins an item
     const int k = ik;
     StageMeta mt;
     mt.s = cur.s;
@@ -877,10 +890,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       const int nch = max(cur.nch, 1);
       mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | (cur.j >= nch - 1 ? kMetaLastChunk : 0) |
                  (nch << kMetaChunkShift);
-      if (lane == 0) {
-        meta[k] = mt;
-        mbar_arrive(&bar[k]);
-      }
+      st_shared_v4_if(lane == 0, &meta[k], mt.s, mt.j, mt.g, mt.flags);
+      mbar_arrive_if(lane == 0, &bar[k]);
       cur.active = false;
     } else {
       const bool first = cur.pnext == cur.p0, lastp = cur.pnext + 1 == cur.p1;
@@ -896,40 +907,43 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0) |
                  (cur.nch << kMetaChunkShift);
       if constexpr (FUSED) {
-        // new tokens of this page: write their rotated K and V first, then let the copy read them
-        if (page_ok && cur.pnext >= cur.pmin && cur.pnext <= cur.pmax) {
-          append_page<D>(cur, cur.pnext, pid, p, lane);
-          fence_proxy_async_global();
-          __syncwarp();
+        // The first stage also brings the new token's raw k and v; the consumer patches the page
+        // that holds the token in shared memory (the copy of that slot from the pool is stale).
+        if (first && cur.has_new) mt.flags |= kMetaNew;
+        if (cur.has_new && page_ok && cur.pnext == (cur.qpos >> 4)) {
+          mt.flags |= kMetaPatch | ((cur.qpos & 15) << kMetaSlotShift);
+          st_shared_u32_if(lane == 0, &meta_pid[k], pid);
         }
       }
-      if (lane == 0) {
-        if (!page_ok) atomicOr(p.status, kFlagBadPage);
-        meta[k] = mt;
-        const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes + cs_bytes : 0u);
-        if (bytes) {
-          mbar_arrive_expect_tx(&bar[k], bytes);
-        } else {
-          mbar_arrive(&bar[k]);
-        }
-        if (first) {
-          const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
-          bulk_load(qslots + k * L.qslot_bytes, qsrc, q_bytes, &bar[k]);
-          if constexpr (FUSED)
-            bulk_load(qslots + k * L.qslot_bytes + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes,
-                      &bar[k]);
-        }
-        if (page_ok) {
-          unsigned char* dst = stages + (size_t)k * L.stage_bytes;
-          if constexpr (MMA) {
-            constexpr int E = GroupMma<D>::E;
+      if (!page_ok && lane == 0) atomicOr(p.status, kFlagBadPage);
+      // lane 0 publishes the stage: metadata, then the barrier's byte count, then the copies (all
+      // predicated on the lane, no branch)
+      const bool l0 = lane == 0;
+      st_shared_v4_if(l0, &meta[k], mt.s, mt.j, mt.g, mt.flags);
+      const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes + cs_bytes : 0u) +
+                             ((mt.flags & kMetaNew) ? kv_bytes : 0u);
+      mbar_arrive_expect_tx_if(l0 && bytes != 0u, &bar[k], bytes);
+      mbar_arrive_if(l0 && bytes == 0u, &bar[k]);
+      unsigned char* qslot = qslots + (items_issued % kItemSlots) * L.qslot_bytes;
+      items_issued += first ? 1 : 0;
+      const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
+      bulk_load_if(l0 && first, qslot, qsrc, q_bytes, &bar[k]);
+      if constexpr (FUSED) {
+        bulk_load_if(l0 && first, qslot + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes, &bar[k]);
+        const bool kv = l0 && (mt.flags & kMetaNew);
+        const long long row = ((long long)cur.q0 * p.hkv + cur.g) * D;
+        bulk_load_if(kv, qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
+        bulk_load_if(kv, qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+      }
+      unsigned char* dst = stages + (size_t)k * L.stage_bytes;
+      if constexpr (MMA) {
+        constexpr int E = GroupMma<D>::E;
 #pragma unroll
-            for (int u = 0; u < D / E; ++u)
-              tma_load_4d(dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, cur.g, 2 * pid, policy);
-          } else {
-            tma_load_4d(dst, &map, &bar[k], 0, 0, cur.g, 2 * pid, policy);
-          }
-        }
+        for (int u = 0; u < D / E; ++u)
+          tma_load_4d_if(l0 && page_ok, dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, cur.g, 2 * pid,
+                         policy);
+      } else {
+        tma_load_4d_if(l0 && page_ok, dst, &map, &bar[k], 0, 0, cur.g, 2 * pid, policy);
       }
       ++cur.pnext;
       if (lastp) cur.active = false;
@@ -1006,15 +1020,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           !(mt.flags & kMetaEmpty) && cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
       if (!wrote && lane < p.group) p.partial_lse[(head_row0 + lane) * p.splits + mt.j] = -INFINITY;
       // Publish this chunk, then count it; the chunk that completes the count merges them all.
-      __threadfence();
+      // The warp barrier orders every lane's partial writes before lane 0's release; lane 0's
+      // acquire, then the barrier of the shuffle, order the merge's reads after the other chunks'.
       __syncwarp();
       int* counter = p.counters + (long long)mt.s * p.hkv + mt.g;
       int done = 0;
-      if (lane == 0) done = atomicAdd(counter, 1) + 1;
+      if (lane == 0) done = atom_add_acq_rel_gpu(counter, 1) + 1;
       done = __shfl_sync(kFull, done, 0);
       if (done == nch) {
         // this chunk completed the group: merge once this warp's stages are released
-        __threadfence();
         pending_merge = true;
         pm_row0 = head_row0;
         pm_nch = nch;
@@ -1027,7 +1041,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   // group's partial rows arrive in one bulk copy into the ring; otherwise they are read directly.
   auto run_merge = [&]() {
     const int rows_bytes = pm_nch * D * 4;
-    const bool smem_ok = issued == consumed && pm_nch <= 64 && p.group * rows_bytes <= nst * L.stage_bytes;
+    // the group's partial rows, then (tensor-core path) its split LSEs, 64 per head
+    const bool smem_ok = issued == consumed && pm_nch <= 64 &&
+                         p.group * rows_bytes + (MMA ? p.group * 256 : 0) <= nst * L.stage_bytes;
     if (smem_ok) {
       fence_proxy_async_global();  // the partials were written through the generic proxy
       const int k = ik;
@@ -1036,9 +1052,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         for (int hh = 0; hh < p.group; ++hh)
           bulk_load(stages + hh * rows_bytes, p.partial_o + (pm_row0 + hh) * p.splits * D, rows_bytes, &bar[k]);
       }
-      float la[kMaxGroup], lb[kMaxGroup];
+      // split LSEs: lane l holds splits l and l + 32 of each head (all loads in flight at once)
+      constexpr int kHeads = MMA ? kMaxGroup : 1;
+      float la[kHeads], lb[kHeads];
 #pragma unroll
-      for (int hh = 0; hh < kMaxGroup; ++hh) {
+      for (int hh = 0; hh < kHeads; ++hh) {
         const float* lrow = p.partial_lse + (pm_row0 + hh) * p.splits;
         la[hh] = (hh < p.group && lane < pm_nch) ? lrow[lane] : -INFINITY;
         lb[hh] = (hh < p.group && lane + 32 < pm_nch) ? lrow[lane + 32] : -INFINITY;
@@ -1048,12 +1066,27 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       ++consumed;
       advance(ik, iph);
       advance(ck, cph);
+      if constexpr (MMA) {
+        // park the LSEs behind the rows so that one (not unrolled) merge loop serves every head
+        float* lse_s = reinterpret_cast<float*>(stages + p.group * rows_bytes);
 #pragma unroll
-      for (int hh = 0; hh < kMaxGroup; ++hh) {
-        if (hh >= p.group) break;
-        const long long row = pm_row0 + hh;
-        merge_row_smem<D>(la[hh], lb[hh], reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane,
-                          p.out + row * D, p.lse_out != nullptr ? p.lse_out + row : nullptr);
+        for (int hh = 0; hh < kHeads; ++hh) {
+          if (hh < p.group) {
+            lse_s[hh * 64 + lane] = la[hh];
+            lse_s[hh * 64 + 32 + lane] = lb[hh];
+          }
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int hh = 0; hh < p.group; ++hh) {
+          const long long row = pm_row0 + hh;
+          merge_row_smem<D>(lse_s[hh * 64 + lane], lse_s[hh * 64 + 32 + lane],
+                            reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane, p.out + row * D,
+                            p.lse_out != nullptr ? p.lse_out + row : nullptr);
+        }
+      } else {
+        merge_row_smem<D>(la[0], lb[0], reinterpret_cast<const float*>(stages), pm_nch, lane, p.out + pm_row0 * D,
+                          p.lse_out != nullptr ? p.lse_out + pm_row0 : nullptr);
       }
       fence_proxy_async_smem();  // the reads above before later copies into the ring
       __syncwarp();
@@ -1069,61 +1102,75 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     const int k = ck;
     if (!wait_stage(consumed, ck, cph)) return;
     const StageMeta mt = meta[k];
+    StageMeta fin = mt;  // the last stage consumed in this step
     int used = 1;
     if (!(mt.flags & kMetaEmpty)) {
       if (mt.flags & kMetaFirst) {
+        const unsigned char* qs = qslots + (items_begun % kItemSlots) * L.qslot_bytes;
+        ++items_begun;  // the slot is read below, before this warp issues another copy
         if constexpr (FUSED) {
           if constexpr (MMA) {
-            cmp.begin_rotate(qslots + k * L.qslot_bytes);
+            cmp.begin_rotate(qs);
           } else {
-            cmp.begin_rotate(qslots + k * L.qslot_bytes, p.scale_log2);
+            cmp.begin_rotate(qs, p.scale_log2);
           }
           if (mt.j == 0) {
-            // the first piece of each (sequence, KV head) writes the rotated queries (q_out)
-            const int qrow = aptr[mt.s + 1] - 1;
+            // the first piece of each (sequence, KV head) writes the rotated query rows (q_out)
+            const int qrow = aptr[mt.s];
             cmp.store_query(p.q_out + ((long long)qrow * p.hq + (long long)mt.g * p.group) * D);
-            store_other_queries<D>(mt.s, mt.g, aptr, p, lane);
           }
+          if (mt.flags & kMetaNew) make_patch<D>(qs + q_bytes, qs + q_bytes + cs_bytes, patch, lane);
         } else if constexpr (MMA) {
-          cmp.begin(qslots + k * L.qslot_bytes);
+          cmp.begin(qs);
         } else {
-          cmp.begin(qslots + k * L.qslot_bytes, p.scale_log2);
+          cmp.begin(qs, p.scale_log2);
         }
       }
       const int nvalid = mt.flags & kMetaValid;
+      unsigned char* s1 = stages + (size_t)k * L.stage_bytes;
       if constexpr (!MMA) {
         // two pages of the same item at once when the next one is already in flight
+        int n2 = 0;
+        unsigned char* s2 = s1;
         if (!(mt.flags & kMetaLast) && consumed + 1 < issued) {
           int k2 = ck;
           uint32_t ph2 = cph;
           advance(k2, ph2);
           if (!wait_stage(consumed + 1, k2, ph2)) return;
-          const StageMeta mt2 = meta[k2];
-          const int nvalid2 = mt2.flags & kMetaValid;
-          unsigned char* s1 = stages + (size_t)k * L.stage_bytes;
-          unsigned char* s2 = stages + (size_t)k2 * L.stage_bytes;
-          if (nvalid > 0 && nvalid2 > 0) {
-            cmp.page2(s1, nvalid, s2, nvalid2);
-          } else {
-            if (nvalid > 0) cmp.page(s1, nvalid);
-            if (nvalid2 > 0) cmp.page(s2, nvalid2);
-          }
+          fin = meta[k2];
+          n2 = fin.flags & kMetaValid;
+          s2 = stages + (size_t)k2 * L.stage_bytes;
           used = 2;
-          if (mt2.flags & kMetaLast) finish_item(mt2);
-        } else if (nvalid > 0) {
-          cmp.page(stages + (size_t)k * L.stage_bytes, nvalid);
+          if constexpr (FUSED) {
+            if (fin.flags & kMetaPatch)
+              apply_patch<D, Compute>(s2, patch, (fin.flags >> kMetaSlotShift) & 15, meta_pid[k2], fin.g, p, lane);
+          }
+        }
+        if constexpr (FUSED) {
+          if (mt.flags & kMetaPatch)
+            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g, p, lane);
+        }
+        if (nvalid > 0 && n2 > 0) {
+          cmp.page2(s1, nvalid, s2, n2);
+        } else if (nvalid + n2 > 0) {
+          cmp.page(nvalid > 0 ? s1 : s2, nvalid > 0 ? nvalid : n2);
         }
       } else {
-        if (nvalid > 0) cmp.page(stages + (size_t)k * L.stage_bytes, nvalid, p.scale_log2);
+        if constexpr (FUSED) {
+          if (mt.flags & kMetaPatch)
+            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g, p, lane);
+        }
+        if (nvalid > 0) cmp.page(s1, nvalid, p.scale_log2);
       }
     }
-    if (used == 1 && (mt.flags & kMetaLast)) finish_item(mt);
+    if (fin.flags & kMetaLast) finish_item(fin);
     consumed += used;
     for (int u = 0; u < used; ++u) advance(ck, cph);
     fence_proxy_async_smem();  // this lane's reads/writes of the stages before their TMA refill
     __syncwarp();
     if (pending_merge && !run_merge()) return;
-    for (int u = 0; u < used; ++u) produce();
+    while (issued - consumed < nst && produce()) {
+    }
   }
 }
 
@@ -1152,12 +1199,23 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
   DecodeConfig c;
   c.mma = group >= 2;
   c.fused = fused;
-  c.warps = c.mma ? 6 : 8;
-  const Layout one = make_layout(c.warps, 1, head_dim, group, batch, fused);
-  const int per_stage = c.warps * (one.stage_bytes + one.qslot_bytes + 8 + 16);
-  const int fixed = (batch + 1) * (fused ? 12 : 8) + 1024 + 64;
-  int nstage = (kSmemBudget - fixed) / per_stage;
-  if (nstage > 8) nstage = 8;
+  // Warps: the most stages in flight per SM (warps x ring depth) that fit the plain layout, on a
+  // tie the deeper ring (the CUDA-core path always runs 8 warps, the tensor-core path 6 to 8).  The
+  // one-launch layout keeps the same warps, so both partition the work alike and give the same
+  // bits, and takes the ring depth that fits.
+  c.warps = 8;
+  int best = 0, best_n = 0;
+  for (int w = c.mma ? 6 : 8; w <= kMaxDecodeWarps; ++w) {
+    int n = 8;
+    while (n >= 2 && make_layout(w, n, head_dim, group, batch, false).total > kSmemBudget) --n;
+    if (n >= 2 && (w * n > best || (w * n == best && n > best_n))) {
+      best = w * n;
+      best_n = n;
+      c.warps = w;
+    }
+  }
+  int nstage = 8;
+  while (nstage >= 2 && make_layout(c.warps, nstage, head_dim, group, batch, fused).total > kSmemBudget) --nstage;
   c.nstage = nstage;
   c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused).total : 0;
   if (c.mma) {

@@ -93,9 +93,11 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
   // Automatic with the exact page total: the balanced partition, every warp of the grid taking an
   // equal run of (sequence, KV head, page) units; a segment of n pages meets at most
   // ceil(n * W / U) + 1 runs.
+  // The bound takes the most warps any decode launch runs (the one-launch layout may run more warps
+  // per CTA than the plain one), so one plan serves every entry point.
   if (total_pages > 0) {
     const long long U = (long long)total_pages * c->desc.num_kv_heads;
-    const long long W = std::min(warps, U);
+    const long long W = std::min((long long)c->num_sms * pkv::kMaxDecodeWarps, U);
     const long long s_bal = ((long long)max_pages * W + U - 1) / U + 1;
     if (U < 0x7fffffffLL && s_bal <= max_splits) {
       *splits = (int)s_bal;
@@ -425,6 +427,15 @@ pkv_status pkv_append_decode_attention(pkv_cache* c, int layer, const void* q, c
                                        float* partial_o, float* partial_lse, int32_t* chunk_counters, void* out,
                                        float* lse_out, int* splits_used, pkv_stream_t stream) {
   if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative num_tokens");
+  if (num_tokens != batch) {
+    // several new tokens per sequence (a chunked append): the append launch, then the merged decode
+    const pkv_status st = pkv_append_rope(c, layer, q, k, v, pos_map, append_indptr, num_tokens, batch,
+                                          page_indptr, page_indices, q_out, stream);
+    if (st != PKV_OK) return st;
+    return decode_common(c, layer, q_out, append_indptr, page_indptr, page_indices, last_page_len, batch,
+                         max_pages, total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o,
+                         partial_lse, chunk_counters, out, lse_out, true, splits_used, stream);
+  }
   const FusedArgs fa{k, v, pos_map, q_out};
   return decode_common(c, layer, q, append_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
                        total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse,

@@ -12,6 +12,7 @@ namespace pkv {
 constexpr int kPageSize = 16;
 constexpr int kMaxGroup = 8;        // Hq / Hkv handled by the kernels
 constexpr int kMaxDecodeBatch = 4096;  // sequences per decode call (per-CTA shared-memory prefix)
+constexpr int kMaxDecodeWarps = 8;     // warps per decode CTA, at most
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s
 
 // Device status word bits (mirrors PKV_FLAG_* of include/pkv.h).

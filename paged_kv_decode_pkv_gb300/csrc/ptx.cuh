@@ -103,6 +103,73 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// ---- predicated single-lane forms ---------------------------------------------------------------
+// Every lane of the warp executes these; only lanes whose `pred` is set perform the operation, so
+// work done by one elected lane needs no divergent branch.
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(bool pred, uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes), "r"((uint32_t)pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_if(bool pred, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"((uint32_t)pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_if(bool pred, void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                               int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %8, 0;\n\t"
+      "@p cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy),
+      "r"((uint32_t)pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "r"((uint32_t)pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4_if(bool pred, void* dst, int a, int b, int c, int d) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "@p st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n\t}" ::"r"(smem_u32(dst)),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"((uint32_t)pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32_if(bool pred, void* dst, int v) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p st.shared.b32 [%0], %1;\n\t}" ::"r"(smem_u32(dst)),
+      "r"(v), "r"((uint32_t)pred)
+      : "memory");
+}
+
+// ---- device-scope release/acquire counter --------------------------------------------------------
+
+// atomicAdd with acquire-release semantics at GPU scope: writes made before it (by this thread, or
+// by threads that synchronised with it at a barrier first) are visible to whoever reads the count,
+// and reads after it see what the earlier counters published.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // ---- programmatic dependent launch ------------------------------------------------------------
 
 // Block until the preceding grid in the stream has completed and its writes are visible

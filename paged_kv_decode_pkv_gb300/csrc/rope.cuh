@@ -1,0 +1,36 @@
+// Rotate-half RoPE of eight element pairs (Zero TVM Documentation, "KV cache": K is rotated before
+// the cache write; the rotation pairs element i with element i + head_dim/2 at angle
+// position * theta_i).  Shared by the append kernel and the one-launch decode so that both write
+// the same bits.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// lo: elements i..i+7 of a head row, hi: elements i+d/2..i+d/2+7, cs: the (cos, sin) pairs of
+// elements i..i+7 at the token's position.  Evaluated in fp32 with fused multiply-adds and
+// rounded once to fp16:
+//   x'_i = x_i cos - x_{i+d/2} sin ,   x'_{i+d/2} = x_{i+d/2} cos + x_i sin.
+__device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const float2* cs, uint4& out_lo,
+                                      uint4& out_hi) {
+  const __half2* a = reinterpret_cast<const __half2*>(&lo);
+  const __half2* b = reinterpret_cast<const __half2*>(&hi);
+  __half2* ya = reinterpret_cast<__half2*>(&out_lo);
+  __half2* yb = reinterpret_cast<__half2*>(&out_hi);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 xa = __half22float2(a[e]);
+    const float2 xb = __half22float2(b[e]);
+    const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];  // (cos, sin) of elements 2e and 2e+1
+    const float lo0 = __fmaf_rn(xa.x, c0.x, -__fmul_rn(xb.x, c0.y));
+    const float lo1 = __fmaf_rn(xa.y, c1.x, -__fmul_rn(xb.y, c1.y));
+    const float hi0 = __fmaf_rn(xb.x, c0.x, __fmul_rn(xa.x, c0.y));
+    const float hi1 = __fmaf_rn(xb.y, c1.x, __fmul_rn(xa.y, c1.y));
+    ya[e] = __floats2half2_rn(lo0, lo1);
+    yb[e] = __floats2half2_rn(hi0, hi1);
+  }
+}
+
+}  // namespace pkv

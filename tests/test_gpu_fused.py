@@ -77,3 +77,45 @@ def test_fused_step_reports_positions_out_of_range():
                                   total_pages=int(step.page_indptr[-1]))
     code, flags = cache.check_status()
     assert code == pkv.ERR_OUT_OF_RANGE and flags & pkv.FLAG_BAD_POSITION
+
+
+def _single_token_case():
+    import torch
+
+    cfg = SMALL["phi3_b1_ctx300"]
+    cfg = W.scaled(cfg, batch=3, lengths=("uniform", 40, 300), pool_pages=60)
+    step = W.make_step(cfg)
+    assert int(step.new_tokens.max()) == 1
+    pool = H.to_dev(W.host_pool(step, 0), torch.float16)
+    cache = H.make_cache(step, [0], [pool])
+    tabs = H.device_tables(step)
+    q, k, v = H.device_qkv(step, 0)
+    counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")
+    return step, cache, tabs, (q, k, v), counters
+
+
+def test_one_launch_reports_a_position_past_the_pages():
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    step, cache, tabs, (q, k, v), counters = _single_token_case()
+    bad = tabs["pos_map"].clone()
+    n_pages = int(step.page_indptr[1] - step.page_indptr[0])
+    bad[0] = n_pages * 16  # inside the RoPE table, past sequence 0's pages
+    cache.append_decode_attention(0, q, k, v, bad, tabs["append_indptr"], tabs["page_indptr"], tabs["page_indices"],
+                                  tabs["last_page_len"], step.max_pages_per_seq, counters,
+                                  total_pages=int(step.page_indptr[-1]))
+    code, flags = cache.check_status()
+    assert code == pkv.ERR_OUT_OF_RANGE and flags & pkv.FLAG_BAD_POSITION
+
+
+def test_one_launch_reports_a_sequence_without_exactly_one_token():
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    step, cache, tabs, (q, k, v), counters = _single_token_case()
+    indptr = tabs["append_indptr"].clone()
+    indptr[1] = 2  # sequence 0 takes two tokens, sequence 1 none: still batch tokens in total
+    cache.append_decode_attention(0, q, k, v, tabs["pos_map"], indptr, tabs["page_indptr"], tabs["page_indices"],
+                                  tabs["last_page_len"], step.max_pages_per_seq, counters,
+                                  total_pages=int(step.page_indptr[-1]))
+    code, flags = cache.check_status()
+    assert code == pkv.ERR_OUT_OF_RANGE and flags & pkv.FLAG_BAD_SEQUENCE
