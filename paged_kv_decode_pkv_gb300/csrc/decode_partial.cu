@@ -28,6 +28,8 @@
 //
 // Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
 // bounded time for its own copies in flight and returns.
+#include <algorithm>
+
 #include "merge.cuh"
 #include "pkv_internal.h"
 #include "ptx.cuh"
@@ -57,6 +59,10 @@ struct __align__(16) StageMeta {
 // Dynamic shared memory budget: the 227 KB per-block opt-in maximum less room for the kernel's
 // static shared memory (128 bytes).
 constexpr int kSmemBudget = 232448 - 256;
+
+// Shared memory of one SM, and the CTAs per SM the decode grid prefers.
+constexpr int kSmemPerSm = 233472;
+constexpr int kCtasPerSm = 2;
 
 // Alignment of the shared-memory base: 1024 bytes for the swizzled boxes of the tensor-core path,
 // 128 bytes for the plain boxes of the CUDA-core path.
@@ -1195,28 +1201,50 @@ void* select_kernel(int head_dim, bool mma, bool fused) {
 
 }  // namespace
 
+// Deepest ring (at most 8, at least 2, else 0) of a CTA of `warps` warps within `budget` bytes.
+int ring_depth(int warps, int head_dim, int group, int batch, bool fused, int budget) {
+  int n = 8;
+  while (n >= 2 && make_layout(warps, n, head_dim, group, batch, fused).total > budget) --n;
+  return n >= 2 ? n : 0;
+}
+
+// Dynamic shared memory a CTA may use when `ctas` CTAs share an SM (228 KB, 1 KB of it reserved per
+// resident CTA, and the kernel's static shared memory).
+int cta_budget(int ctas) { return std::min(kSmemBudget, (kSmemPerSm - ctas * 1024) / ctas - 256); }
+
 DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
   DecodeConfig c;
   c.mma = group >= 2;
   c.fused = fused;
-  // Warps: the most stages in flight per SM (warps x ring depth) that fit the plain layout, on a
-  // tie the deeper ring (the CUDA-core path always runs 8 warps, the tensor-core path 6 to 8).  The
-  // one-launch layout keeps the same warps, so both partition the work alike and give the same
-  // bits, and takes the ring depth that fits.
-  c.warps = 8;
-  int best = 0, best_n = 0;
+  // Warps per SM: the most stages in flight per SM (warps x ring depth) that fit the plain layout
+  // in one CTA, on a tie the deeper ring (the CUDA-core path always runs 8 warps, the tensor-core
+  // path 6 to 8).  Both layouts run the same warps per SM, so they partition the work alike and
+  // give the same bits; each takes the ring depth that fits.
+  int sm_warps = 8, best = 0, best_n = 0;
   for (int w = c.mma ? 6 : 8; w <= kMaxDecodeWarps; ++w) {
-    int n = 8;
-    while (n >= 2 && make_layout(w, n, head_dim, group, batch, false).total > kSmemBudget) --n;
+    const int n = ring_depth(w, head_dim, group, batch, false, kSmemBudget);
     if (n >= 2 && (w * n > best || (w * n == best && n > best_n))) {
       best = w * n;
       best_n = n;
-      c.warps = w;
+      sm_warps = w;
     }
   }
-  int nstage = 8;
-  while (nstage >= 2 && make_layout(c.warps, nstage, head_dim, group, batch, fused).total > kSmemBudget) --nstage;
-  c.nstage = nstage;
+  c.warps = sm_warps;
+  c.ctas_per_sm = 1;
+  c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, kSmemBudget);
+  // The SM's warps split over kCtasPerSm CTAs when the ring stays as deep: a CTA that is still
+  // merging at the end of a launch then holds only its share of the SM, and the next launch's CTAs
+  // start (and run their prologue) in the rest.
+  if (kCtasPerSm > 1 && sm_warps % kCtasPerSm == 0) {
+    const int w = sm_warps / kCtasPerSm;
+    const int n = ring_depth(w, head_dim, group, batch, fused, cta_budget(kCtasPerSm));
+    if (n >= c.nstage && n >= 2) {
+      c.warps = w;
+      c.ctas_per_sm = kCtasPerSm;
+      c.nstage = n;
+    }
+  }
+  const int nstage = c.nstage;
   c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused).total : 0;
   if (c.mma) {
     c.box_inner = head_dim == 96 ? 32 : 64;

@@ -89,7 +89,7 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
     return PKV_OK;
   }
   const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, batch > 0 ? batch : 1);
-  const long long warps = (long long)c->num_sms * cfg.warps;
+  const long long warps = (long long)c->num_sms * cfg.ctas_per_sm * cfg.warps;
   // Automatic with the exact page total: the balanced partition, every warp of the grid taking an
   // equal run of (sequence, KV head, page) units; a segment of n pages meets at most
   // ceil(n * W / U) + 1 runs.
@@ -271,7 +271,10 @@ void pkv_destroy(pkv_cache* c) { delete c; }
 pkv_status pkv_device_info(const pkv_cache* c, int* num_sms, int* decode_warps_per_sm) {
   if (c == nullptr) return PKV_ERR_INVALID_ARG;
   if (num_sms) *num_sms = c->num_sms;
-  if (decode_warps_per_sm) *decode_warps_per_sm = pkv::decode_config(c->group, c->desc.head_dim, 1).warps;
+  if (decode_warps_per_sm) {
+    const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, 1);
+    *decode_warps_per_sm = cfg.warps * cfg.ctas_per_sm;
+  }
   return PKV_OK;
 }
 
@@ -389,8 +392,9 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   p.lse_out = lse_out;
   p.balanced = chunk < 0 ? 1 : 0;
   p.units = (long long)total_pages * c->desc.num_kv_heads;
+  const long long full_grid = (long long)c->num_sms * cfg.ctas_per_sm;
   long long grid = (items + cfg.warps - 1) / cfg.warps;
-  if (grid > c->num_sms || p.balanced) grid = c->num_sms;
+  if (grid > full_grid || p.balanced) grid = full_grid;
   if (grid < 1) grid = 1;
   p.part_warps = (int)std::min(grid * cfg.warps, std::max(p.units, 1LL));
   if (p.balanced) p.chunk_pages = 0;

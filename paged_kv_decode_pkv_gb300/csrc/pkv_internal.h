@@ -90,6 +90,7 @@ struct DecodeConfig {
   bool mma;             // tensor-core path (group >= 2)
   bool fused;           // append folded into the decode
   int warps;            // warps per CTA
+  int ctas_per_sm;      // resident CTAs per SM (the grid of a full launch is SMs x this)
   int nstage;           // per-warp ring depth
   size_t smem_bytes;    // dynamic shared memory
   int box_inner;        // TMA box extent along head_dim (elements)
