@@ -192,7 +192,8 @@ size_t pkv_partial_bytes(int batch, int num_qo_heads, int splits, int head_dim);
  *   total_pages                        page_indptr[batch] if known on the host (then exact), else 0
  *   num_splits, chunk_pages, max_splits  split selection, see pkv_plan_decode
  *   sm_scale                           score scale; 0 selects 1/sqrt(head_dim)
- *   partial_o   fp32 [batch][Hq][S][head_dim]  S = *splits_used (capacity max_splits)
+ *   partial_o   fp32 [batch][Hq][S][head_dim]  S = *splits_used (capacity max_splits);
+ *                                      16-byte aligned, like q_rope and out
  *   partial_lse fp32 [batch][Hq][S]            natural-log LSE of each chunk
  *   splits_used (host, nullable)       receives S
  *

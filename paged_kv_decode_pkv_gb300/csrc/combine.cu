@@ -18,8 +18,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) combine_kernel(CombineParam
   if (sh >= (long long)p.batch * p.hq) return;
   pdl_wait();  // the partials come from the preceding kernel
   const int S = p.splits;
-  merge_row<D>(p.partial_lse + sh * S, p.partial_o + sh * S * D, S, lane, p.out + sh * D,
-               p.lse != nullptr ? p.lse + sh : nullptr);
+  merge_rows<D>(p.partial_lse + sh * S, p.partial_o + sh * S * D, S, lane, p.out + sh * D,
+                p.lse != nullptr ? p.lse + sh : nullptr);
 }
 
 }  // namespace

@@ -63,6 +63,8 @@ constexpr int kSmemBudget = 232448 - 256;
 // Shared memory of one SM, and the CTAs per SM the decode grid prefers.
 constexpr int kSmemPerSm = 233472;
 constexpr int kCtasPerSm = 2;
+// CUDA-core path: copy a page's K and V blocks with two plain bulk copies instead of one tensor copy.
+constexpr bool kPlainBulkPages = true;
 
 // Alignment of the shared-memory base: 1024 bytes for the swizzled boxes of the tensor-core path,
 // 128 bytes for the plain boxes of the CUDA-core path.
@@ -948,6 +950,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         for (int u = 0; u < D / E; ++u)
           tma_load_4d_if(l0 && page_ok, dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, cur.g, 2 * pid,
                          policy);
+      } else if constexpr (kPlainBulkPages) {
+        // the page's K block and V block of this KV head are each contiguous in the pool
+        const __half* kb = p.pool + (((long long)pid * 2 * p.hkv + cur.g) * kPageSize) * D;
+        bulk_load_hint_if(l0 && page_ok, dst, kb, page_bytes / 2, &bar[k], policy);
+        bulk_load_hint_if(l0 && page_ok, dst + page_bytes / 2, kb + (long long)p.hkv * kPageSize * D, page_bytes / 2,
+                          &bar[k], policy);
       } else {
         tma_load_4d_if(l0 && page_ok, dst, &map, &bar[k], 0, 0, cur.g, 2 * pid, policy);
       }
@@ -1047,9 +1055,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   // group's partial rows arrive in one bulk copy into the ring; otherwise they are read directly.
   auto run_merge = [&]() {
     const int rows_bytes = pm_nch * D * 4;
-    // the group's partial rows, then (tensor-core path) its split LSEs, 64 per head
+    // the group's partial rows, then its split LSEs, 64 per head
     const bool smem_ok = issued == consumed && pm_nch <= 64 &&
-                         p.group * rows_bytes + (MMA ? p.group * 256 : 0) <= nst * L.stage_bytes;
+                         p.group * (rows_bytes + 256) <= nst * L.stage_bytes;
     if (smem_ok) {
       fence_proxy_async_global();  // the partials were written through the generic proxy
       const int k = ik;
@@ -1058,7 +1066,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         for (int hh = 0; hh < p.group; ++hh)
           bulk_load(stages + hh * rows_bytes, p.partial_o + (pm_row0 + hh) * p.splits * D, rows_bytes, &bar[k]);
       }
-      // split LSEs: lane l holds splits l and l + 32 of each head (all loads in flight at once)
+      // split LSEs: lane l loads splits l and l + 32 of each head (all loads in flight at once) and
+      // parks them behind the rows
       constexpr int kHeads = MMA ? kMaxGroup : 1;
       float la[kHeads], lb[kHeads];
 #pragma unroll
@@ -1067,32 +1076,25 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         la[hh] = (hh < p.group && lane < pm_nch) ? lrow[lane] : -INFINITY;
         lb[hh] = (hh < p.group && lane + 32 < pm_nch) ? lrow[lane + 32] : -INFINITY;
       }
+      float* lse_s = reinterpret_cast<float*>(stages + p.group * rows_bytes);
+#pragma unroll
+      for (int hh = 0; hh < kHeads; ++hh) {
+        if (hh < p.group) {
+          lse_s[hh * 64 + lane] = la[hh];
+          lse_s[hh * 64 + 32 + lane] = lb[hh];
+        }
+      }
       if (!wait_stage(issued, ik, iph)) return false;
       ++issued;
       ++consumed;
       advance(ik, iph);
       advance(ck, cph);
-      if constexpr (MMA) {
-        // park the LSEs behind the rows so that one (not unrolled) merge loop serves every head
-        float* lse_s = reinterpret_cast<float*>(stages + p.group * rows_bytes);
-#pragma unroll
-        for (int hh = 0; hh < kHeads; ++hh) {
-          if (hh < p.group) {
-            lse_s[hh * 64 + lane] = la[hh];
-            lse_s[hh * 64 + 32 + lane] = lb[hh];
-          }
-        }
-        __syncwarp();
+      __syncwarp();
 #pragma unroll 1
-        for (int hh = 0; hh < p.group; ++hh) {
-          const long long row = pm_row0 + hh;
-          merge_row_smem<D>(lse_s[hh * 64 + lane], lse_s[hh * 64 + 32 + lane],
-                            reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane, p.out + row * D,
-                            p.lse_out != nullptr ? p.lse_out + row : nullptr);
-        }
-      } else {
-        merge_row_smem<D>(la[0], lb[0], reinterpret_cast<const float*>(stages), pm_nch, lane, p.out + pm_row0 * D,
-                          p.lse_out != nullptr ? p.lse_out + pm_row0 : nullptr);
+      for (int hh = 0; hh < p.group; ++hh) {
+        const long long row = pm_row0 + hh;
+        merge_rows<D>(lse_s + hh * 64, reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane,
+                      p.out + row * D, p.lse_out != nullptr ? p.lse_out + row : nullptr);
       }
       fence_proxy_async_smem();  // the reads above before later copies into the ring
       __syncwarp();

@@ -348,7 +348,7 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
       partial_o == nullptr || partial_lse == nullptr)
     return fail(PKV_ERR_INVALID_ARG, "null pointer");
   if (merged && (counters == nullptr || out == nullptr)) return fail(PKV_ERR_INVALID_ARG, "null pointer");
-  if (!aligned(q_rope, 16) || !aligned(partial_o, 8) || !aligned(partial_lse, 4) ||
+  if (!aligned(q_rope, 16) || !aligned(partial_o, 16) || !aligned(partial_lse, 4) ||
       (merged && (!aligned(out, 16) || !aligned(counters, 4))))
     return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
   if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale");

@@ -143,6 +143,17 @@ __device__ __forceinline__ void bulk_load_if(bool pred, void* dst, const void* s
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared with an L2 cache-eviction policy, predicated.
+__device__ __forceinline__ void bulk_load_hint_if(bool pred, void* dst, const void* src, uint32_t bytes,
+                                                  uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy), "r"((uint32_t)pred)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4_if(bool pred, void* dst, int a, int b, int c, int d) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
