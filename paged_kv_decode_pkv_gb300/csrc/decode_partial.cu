@@ -932,16 +932,19 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
                              ((mt.flags & kMetaNew) ? kv_bytes : 0u);
       mbar_arrive_expect_tx_if(l0 && bytes != 0u, &bar[k], bytes);
       mbar_arrive_if(l0 && bytes == 0u, &bar[k]);
-      unsigned char* qslot = qslots + (items_issued % kItemSlots) * L.qslot_bytes;
-      items_issued += first ? 1 : 0;
-      const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
-      bulk_load_if(l0 && first, qslot, qsrc, q_bytes, &bar[k]);
-      if constexpr (FUSED) {
-        bulk_load_if(l0 && first, qslot + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes, &bar[k]);
-        const bool kv = l0 && (mt.flags & kMetaNew);
-        const long long row = ((long long)cur.q0 * p.hkv + cur.g) * D;
-        bulk_load_if(kv, qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
-        bulk_load_if(kv, qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+      if (first) {
+        // the item's query rows (one-launch mode: with the (cos, sin) row and the new k and v)
+        unsigned char* qslot = qslots + (items_issued % kItemSlots) * L.qslot_bytes;
+        ++items_issued;
+        const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
+        bulk_load_if(l0, qslot, qsrc, q_bytes, &bar[k]);
+        if constexpr (FUSED) {
+          bulk_load_if(l0, qslot + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes, &bar[k]);
+          const bool kv = l0 && (mt.flags & kMetaNew);
+          const long long row = ((long long)cur.q0 * p.hkv + cur.g) * D;
+          bulk_load_if(kv, qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
+          bulk_load_if(kv, qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+        }
       }
       unsigned char* dst = stages + (size_t)k * L.stage_bytes;
       if constexpr (MMA) {
