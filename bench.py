@@ -32,7 +32,17 @@ METRIC = "decode-attention KV GB/s & % of GB300 HBM roofline; attention µs/step
 DEFAULT_CONFIG = 2
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_phi3_b1_ctx4096.md")
-DECODE_SOURCE = os.path.join(ROOT, "paged_kv_decode_pkv_gb300", "csrc", "decode_partial.cu")
+# the decode kernel's sources, in the order their bytes are hashed for the profile summary
+DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_decode_pkv_gb300", "csrc", f) for f in
+                  ("decode_partial.cu", "merge.cuh", "ptx.cuh", "rope.cuh", "pkv_internal.h")]
+
+
+def decode_sources_sha256() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def parse():
@@ -79,8 +89,8 @@ def ncu_traffic():
     kernel source changed since the counters were taken."""
     try:
         text = open(PROFILE_SUMMARY).read()
-        src = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
-        m_hash = re.search(r"decode_partial\.cu sha256:\s*([0-9a-f]{64})", text)
+        src = decode_sources_sha256()
+        m_hash = re.search(r"kernel sources sha256:\s*([0-9a-f]{64})", text)
         m_val = re.search(r"dram bytes per launch:\s*([0-9]+)", text)
         if m_hash and m_val and m_hash.group(1) == src:
             return int(m_val.group(1))
@@ -300,8 +310,10 @@ def run_ours(args):
 
     counters = torch.zeros(B * cfg.hkv, dtype=torch.int32, device=dev)
 
+    one_launch = T == B  # one new token per sequence: pkv_append_decode_attention is a single launch
+
     def layer_chain_fused(l):
-        """append, split-K decode and combine in one launch"""
+        """append, split-K decode and combine in one launch (two for chunked appends)"""
         q, k, v = qkv[l]
         cache.append_decode_attention(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
                                       tabs["page_indices"], tabs["last_page_len"], step.max_pages_per_seq,
@@ -343,20 +355,21 @@ def run_ours(args):
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
+        step_fn_fused()
         step_fn()
     torch.cuda.synchronize()
     code, flags = cache.check_status(stream)
     if code != 0:
         raise RuntimeError(f"device status {pkv.status_string(code)} flags {flags:#x}")
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()  # the headline step: pkv_append_decode_attention per layer
     with torch.cuda.graph(graph, stream=stream):
+        step_fn_fused()
+    graph_two = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_two, stream=stream):
         step_fn()
     graph_sep = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_sep, stream=stream):
         step_fn_separate()
-    graph_fused = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_fused, stream=stream):
-        step_fn_fused()
     torch.cuda.synchronize()
 
     def barrier():
@@ -383,8 +396,8 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
-    # the same step as three launches per layer (append, decode, combine) and as one (append,
-    # decode and combine fused), for reference
+    # the same step as two launches per layer (append; decode with the merge) and as three
+    # (append, decode, combine), for reference
     def time_graph(g):
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
@@ -397,22 +410,32 @@ def run_ours(args):
         return max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
 
     step_sep_ms = time_graph(graph_sep)
-    step_fused_ms = time_graph(graph_fused)
+    step_two_ms = time_graph(graph_two)
     code, flags = cache.check_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after the timed region: {pkv.status_string(code)} flags {flags:#x}")
     kv_step = step.kv_bytes() * cfg.layers
     value = world * kv_step / (step_ms * 1e-3) / 1e9
 
-    # ---- per-kernel durations: events around decode and combine on the launching stream -----------
+    # ---- per-kernel durations: events around each layer's decode launch on the launching stream ----
     # A second handle over the same pools launches without programmatic dependent launch, so each
     # kernel runs alone between its events; a GPU sleep in front of every step keeps the launches
-    # queued so that the events time the device, not the host's launch rate.
+    # queued so that the events time the device, not the host's launch rate.  The kernel is the
+    # headline step's: the one-launch decode (append, split-K decode and merge); with chunked
+    # appends, the merged decode after the append launch.
     plain = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
                       pools=pools, options=0)
 
     def layer_chain_plain(l, events):
         q, k, v = qkv[l]
+        if one_launch:
+            events[0].record()
+            plain.append_decode_attention(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                                          tabs["page_indices"], tabs["last_page_len"], step.max_pages_per_seq,
+                                          counters, total_pages=total_pages, q_out=q_out[l], partial_o=po,
+                                          partial_lse=pl, out=outs[l], lse=lses[l])
+            events[1].record()
+            return
         plain.append_rope(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
                           tabs["page_indices"], q_out=q_out[l])
         events[0].record()
@@ -450,7 +473,7 @@ def run_ours(args):
         for l in layers:
             for dst, src in zip(qkv[l], qkv_host[l]):
                 dst.copy_(src, non_blocking=True)
-            layer_chain(l)
+            layer_chain_fused(l)
             out_host[l].copy_(outs[l], non_blocking=True)
             lse_host[l].copy_(lses[l], non_blocking=True)
 
@@ -496,19 +519,23 @@ def run_ours(args):
         "hbm_roofline_frac_step": value / world / peak,
         "attention_us_per_step_per_layer": dec_ms * 1e3,
         "step_us_per_layer": step_ms * 1e3 / cfg.layers,
-        "step": "per layer: pkv_append_rope + pkv_decode_attention_merged (2 launches)",
-        "one_kernel": {"value": world * kv_step / (step_fused_ms * 1e-3) / 1e9, "ms_per_step": step_fused_ms,
-                       "step": "per layer: pkv_append_decode_attention"},
+        "step": "per layer: pkv_append_decode_attention (" +
+                ("1 launch: append, split-K decode and merge)" if one_launch else
+                 "2 launches for chunked appends: append, then split-K decode with the merge)"),
+        "two_kernels": {"value": world * kv_step / (step_two_ms * 1e-3) / 1e9, "ms_per_step": step_two_ms,
+                        "step": "per layer: pkv_append_rope + pkv_decode_attention_merged"},
         "separate_kernels": {"value": world * kv_step / (step_sep_ms * 1e-3) / 1e9, "ms_per_step": step_sep_ms,
                              "step": "per layer: pkv_append_rope + pkv_decode_attention + pkv_combine"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "decode_kernel (merged combine)",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_kernel, one-launch step (append, split-K decode, merge)" if one_launch
+                     else "decode_kernel (merged combine)",
                      "algorithmic_bytes_per_launch": kv_layer, "avg_launch_us": dec_ms * 1e3,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
         "e2e": {"value": world * kv_step / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "mode": "CUDA graph of the API calls",
                 "eager_value": world * kv_step / e2e_eager_s / 1e9, "eager_ms_per_step": e2e_eager_s * 1e3},
-        "gpu_launches": args.steps * cfg.layers * 2,
+        "gpu_launches": args.steps * cfg.layers * (1 if one_launch else 2),
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

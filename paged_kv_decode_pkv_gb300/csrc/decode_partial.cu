@@ -993,9 +993,6 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
   }
 
-  for (int i = 0; i < nst; ++i)
-    if (!produce()) break;
-
   // Bounded wait for stage number c (ring slot k, phase parity ph); on expiry flag a timeout and
   // drain (bounded) the copies in flight.
   auto wait_stage = [&](int c, int k, uint32_t ph) -> bool {
@@ -1109,7 +1106,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     return true;
   };
 
-  while (consumed < issued) {
+  // The ring is filled (and refilled after every step) at the top of the loop, the one place that
+  // issues copies, so the producer code exists once.
+  while (true) {
+    while (issued - consumed < nst && produce()) {
+    }
+    if (consumed == issued) break;
     const int k = ck;
     if (!wait_stage(consumed, ck, cph)) return;
     const StageMeta mt = meta[k];
@@ -1180,8 +1182,6 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     fence_proxy_async_smem();  // this lane's reads/writes of the stages before their TMA refill
     __syncwarp();
     if (pending_merge && !run_merge()) return;
-    while (issued - consumed < nst && produce()) {
-    }
   }
 }
 

@@ -16,10 +16,12 @@
 namespace pkv {
 
 // lse: [S] natural-log LSEs of the splits; rows: [S][D] normalised partial outputs (16-byte
-// aligned); out: the fp16 result row (8-byte aligned); lse_out: the merged LSE or nullptr.
+// aligned); out: the fp16 result row (8-byte aligned); lse_out: the merged LSE or nullptr.  Both
+// may point to global or shared memory.  Kept out of line: it runs once per merged row, and
+// inlined copies would crowd the streaming loop's instruction cache.
 template <int D>
-__device__ __forceinline__ void merge_rows(const float* lse, const float* rows, int S, int lane, __half* out,
-                                           float* lse_out) {
+__device__ __noinline__ void merge_rows(const float* lse, const float* rows, int S, int lane, __half* out,
+                                        float* lse_out) {
   constexpr unsigned kAll = 0xffffffffu;
   constexpr int kVec = D / 32;  // float4 vectors per lane
   // pass 1: lane l holds the LSEs of splits l and l + 32 (the rest, if any, in a loop)
