@@ -38,10 +38,15 @@ DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_decode_pkv_gb300", "csrc", f) for
 
 
 def decode_sources_sha256() -> str:
+    """sha256 of the decode kernel's code: its sources without blank and whole-line // comment
+    lines (a comment edit does not change the kernel)."""
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
         with open(f, "rb") as fh:
-            h.update(fh.read())
+            for line in fh.read().splitlines():
+                t = line.strip()
+                if t and not t.startswith(b"//"):
+                    h.update(line + b"\n")
     return h.hexdigest()
 
 

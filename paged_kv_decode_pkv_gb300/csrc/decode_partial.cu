@@ -4,18 +4,21 @@
 //
 // Work decomposition.  A work item is (sequence s, chunk j, KV head g): the pages
 // [j*c, min((j+1)*c, n_s)) of s for one KV head and all G = Hq/Hkv query heads that read it, so
-// every KV page is fetched once per KV head.  Items are enumerated sequence-major through a
-// prefix sum of items per sequence that each CTA builds in shared memory from page_indptr.  The
-// grid is persistent (one CTA per SM); every warp owns items gw, gw + W, gw + 2W, ... (W = warps
-// in the grid) and works alone: no CTA-wide barrier after the prologue.
+// every KV page is fetched once per KV head; with the exact page total the chunks are the pieces
+// of a page-balanced partition instead.  Items are enumerated sequence-major through a prefix sum
+// of items per sequence that each CTA builds in shared memory from page_indptr.  The grid is
+// persistent (one or two CTAs per SM); every warp owns items gw, gw + W, gw + 2W, ... (W = warps
+// in the grid) or one run of the balanced partition, and works alone: no CTA-wide barrier after
+// the prologue.
 //
 // Memory pipeline.  Each warp has a private ring of `nstage` shared-memory stages.  Lane 0 is the
-// producer: for each page it issues one TMA tensor copy per box of the page's K and V blocks
-// (fp16 [2][16][head_dim] of one KV head, a 4-D tensor map over the pool), plus a bulk copy of
-// the item's G query rows for the first page of an item, all completing on the stage's mbarrier.
-// The same warp consumes stages in order and refills each stage right after it is consumed, so
-// nstage pages per warp are in flight.  Per-stage metadata (sequence, chunk, head, valid slots,
-// first/last flags) travels through shared memory with the barrier's release/acquire order.
+// producer: for each page it issues the copies of the page's K and V blocks of one KV head (two
+// plain bulk copies on the CUDA-core path, swizzled 4-D tensor boxes on the tensor-core path),
+// plus, with the first page of an item, a bulk copy of the item's G query rows into one of two
+// per-warp item slots, all completing on the stage's mbarrier.  The same warp consumes stages in
+// order and refills the ring at the top of its loop, so nstage pages per warp are in flight.
+// Per-stage metadata (sequence, chunk, head, valid slots, first/last flags) travels through shared
+// memory with the barrier's release/acquire order.
 //
 // Compute.  G = 1 runs on CUDA cores: a half-warp covers one 16-slot row pair, each lane owns
 // head_dim/16 dimensions; q.k partials of 8 rows are reduced with a transposing butterfly (one
@@ -25,6 +28,11 @@
 // n-blocks, and the score accumulators are re-used directly as the A operand of P.V.  K/V boxes
 // use the 128-byte (64-byte for head_dim 96) TMA swizzle so the ldmatrix row reads are free of
 // bank conflicts.
+//
+// One-launch mode (template flag FUSED) also performs the append of a decode step: the first
+// stage of an item brings the new token's raw k and v and its (cos, sin) row, the consumer
+// rotates q and k there, and the staged copy of the page that holds the token is patched (and the
+// pool written) before it is used.
 //
 // Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
 // bounded time for its own copies in flight and returns.
