@@ -65,13 +65,13 @@ def _L():
         lib.orc_append.restype = i
         lib.orc_append.argtypes = [P, P, P, P, i, P, P, i, P, P, P, P]
         lib.orc_attention.restype = i
-        lib.orc_attention.argtypes = [P, P, P, i, P, P, P, d, P, P]
+        lib.orc_attention.argtypes = [P, P, P, i, P, P, P, d, i, P, P, P]
         lib.orc_split_attention.restype = i
-        lib.orc_split_attention.argtypes = [P, P, P, i, P, P, P, i, i, i, d, P, P]
+        lib.orc_split_attention.argtypes = [P, P, P, i, P, P, P, i, i, i, d, i, P, P]
         lib.orc_split_attention_balanced.restype = i
         lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, P, P]
         lib.orc_combine.restype = i
-        lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P]
+        lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P, P]
         lib.orc_threads.restype = i
         lib.orc_threads.argtypes = []
         lib.orc_init.restype = None
@@ -151,8 +151,18 @@ def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
 
 
-def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len, sm_scale=None):
-    """Unsplit decode attention: returns out (float64 [B, Hq, d]) and lse (float64 [B, Hq])."""
+def _sinks(sinks, hq):
+    if sinks is None:
+        return None, None
+    a = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64).reshape(hq))
+    return a, a.ctypes.data
+
+
+def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len, sm_scale=None,
+              window: int = 0, sinks=None):
+    """Unsplit decode attention: returns out (float64 [B, Hq, d]) and lse (float64 [B, Hq]).
+    window: attend to the `window` most recent positions (0 = all); sinks: per query head logits
+    (natural log, units of the scaled scores) joining the softmax denominator, or None."""
     sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
     pool, pp = _c(pool, np.uint16)
     q, pq = _c(q_rope, np.uint16)
@@ -163,7 +173,8 @@ def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page
     out = np.empty((B, geom.num_qo_heads, geom.head_dim), dtype=np.float64)
     lse = np.empty((B, geom.num_qo_heads), dtype=np.float64)
     g = geom.c()
-    rc = _L().orc_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, float(sm_scale),
+    sk, psk = _sinks(sinks, geom.num_qo_heads)
+    rc = _L().orc_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, float(sm_scale), int(window), psk,
                             out.ctypes.data, lse.ctypes.data)
     if rc:
         raise OracleError(rc)
@@ -172,8 +183,9 @@ def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page
 
 def split_attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len,
                     num_splits: int = 0, chunk_pages: int = 0, num_out_splits: int | None = None,
-                    sm_scale=None):
-    """Split-K partials: (partial_o float64 [B, Hq, S, d], partial_lse float64 [B, Hq, S])."""
+                    sm_scale=None, window: int = 0):
+    """Split-K partials: (partial_o float64 [B, Hq, S, d], partial_lse float64 [B, Hq, S]).
+    With a window the chunks cover each sequence's visible pages (see orc_split_attention)."""
     sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
     pool, pp = _c(pool, np.uint16)
     q, pq = _c(q_rope, np.uint16)
@@ -192,7 +204,8 @@ def split_attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, las
     pl = np.empty((B, geom.num_qo_heads, S), dtype=np.float64)
     g = geom.c()
     rc = _L().orc_split_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, int(num_splits),
-                                  int(chunk_pages), S, float(sm_scale), po.ctypes.data, pl.ctypes.data)
+                                  int(chunk_pages), S, float(sm_scale), int(window), po.ctypes.data,
+                                  pl.ctypes.data)
     if rc:
         raise OracleError(rc)
     return po, pl
@@ -219,15 +232,17 @@ def split_attention_balanced(geom: Geometry, pool, q_rope, page_indptr, page_ind
     return po, pl
 
 
-def combine(partial_o, partial_lse):
-    """LSE merge: returns (out float64 [B, Hq, d], out fp16 bits uint16, lse float64 [B, Hq])."""
+def combine(partial_o, partial_lse, sinks=None):
+    """LSE merge: returns (out float64 [B, Hq, d], out fp16 bits uint16, lse float64 [B, Hq]);
+    sinks: per query head logits joining the denominator, or None."""
     po, ppo = _c(partial_o, np.float64)
     pl, ppl = _c(partial_lse, np.float64)
     B, Hq, S, d = po.shape
+    sk, psk = _sinks(sinks, Hq)
     out = np.empty((B, Hq, d), dtype=np.float64)
     out16 = np.empty((B, Hq, d), dtype=np.uint16)
     lse = np.empty((B, Hq), dtype=np.float64)
-    rc = _L().orc_combine(ppo, ppl, B, Hq, S, d, out.ctypes.data, out16.ctypes.data, lse.ctypes.data)
+    rc = _L().orc_combine(ppo, ppl, B, Hq, S, d, psk, out.ctypes.data, out16.ctypes.data, lse.ctypes.data)
     if rc:
         raise OracleError(rc)
     return out, out16, lse

@@ -31,6 +31,14 @@
  *    a chunk with no token gives o = 0 and lse = -inf (natural log); the
  *    combine of all-empty chunks gives out = 0 and lse = -inf.
  *  - fp16 results are rounded to nearest, ties to even.
+ *  - Sliding window (Splash models page, the families' sliding_window and layer_types; Zero TVM
+ *    Documentation, "Decode loop": the unused fields of lengthInfo): a layer with window W > 0
+ *    lets the query at position len-1 attend to positions [max(0, len-W), len), the W most recent
+ *    tokens including itself; W = 0 is full attention.
+ *  - Attention sinks (Splash models page, a layer's attn_sinks, F32): one logit per query head,
+ *    in the units of the scaled scores, that joins the softmax's denominator and carries no
+ *    value: out = sum_t e^s_t V_t / (sum_t e^s_t + e^sink), lse = ln(sum_t e^s_t + e^sink).
+ *    Split partials are unaffected; the sink enters the combine.  -inf means no sink.
  */
 #include <math.h>
 #include <omp.h>
@@ -222,6 +230,24 @@ static int seq_len_of(const int32_t* page_indptr, const int32_t* last_page_len, 
   return ORC_OK;
 }
 
+/* First attended position of a sequence of length len under window W (0 = no window). */
+static int window_start(int len, int window) { return (window > 0 && len > window) ? len - window : 0; }
+
+/* Fold a sink logit into an attention result (o normalised over its tokens, lse their log-sum):
+ * o *= e^lse / (e^lse + e^sink), lse = ln(e^lse + e^sink); an empty result stays o = 0 with
+ * lse = sink. */
+static void apply_sink(double* o, double* lse, int d, double sink) {
+  if (sink == -INFINITY) return;
+  if (*lse == -INFINITY) {
+    *lse = sink;
+    return;
+  }
+  const double M = *lse > sink ? *lse : sink;
+  const double wa = exp(*lse - M), ws = exp(sink - M);
+  for (int i = 0; i < d; ++i) o[i] = o[i] * wa / (wa + ws);
+  *lse = M + log(wa + ws);
+}
+
 /* o[d] = sum_t softmax(score)_t V_t, lse = ln sum_t exp(score_t); empty range: o = 0, lse = -inf */
 static int attend(const orc_geom* g, const uint16_t* pool, const double* q, int s, int kv_head,
                   int t0, int t1, const int32_t* page_indptr, const int32_t* page_indices,
@@ -263,7 +289,8 @@ static int attend(const orc_geom* g, const uint16_t* pool, const double* q, int 
 /* Full (unsplit) decode attention.  q_rope: [B][Hq][d] fp16 bits; out: [B][Hq][d]; lse: [B][Hq]. */
 int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
                   const int32_t* page_indptr, const int32_t* page_indices,
-                  const int32_t* last_page_len, double sm_scale, double* out, double* lse) {
+                  const int32_t* last_page_len, double sm_scale, int window, const double* sinks,
+                  double* out, double* lse) {
   orc_init();
   const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads;
   if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0) return ORC_INVALID;
@@ -277,7 +304,9 @@ int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rop
     double* q = (double*)malloc(sizeof(double) * (size_t)d);
     for (int i = 0; i < d; ++i) q[i] = dec(q_rope[sh * d + i]);
     if (r == ORC_OK)
-      r = attend(g, pool, q, s, h / G, 0, len, page_indptr, page_indices, sm_scale, out + sh * d, lse + sh);
+      r = attend(g, pool, q, s, h / G, window_start(len, window), len, page_indptr, page_indices, sm_scale,
+                 out + sh * d, lse + sh);
+    if (r == ORC_OK && sinks != NULL) apply_sink(out + sh * d, lse + sh, d, sinks[h]);
     free(q);
     if (r != ORC_OK) {
 #pragma omp critical
@@ -287,20 +316,25 @@ int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rop
   return rc;
 }
 
-/* Split-K partial attention.  Chunk size in pages: chunk_pages if > 0 (uniform), otherwise
- * ceil(n_s / num_splits) for sequence s.  Chunk j covers pages [j*c, min((j+1)*c, n_s)).
- * partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S] with S = num_out_splits. */
+/* Split-K partial attention.  Under a window W the visible pages of sequence s are
+ * [f_s, n_s) with f_s = floor(window_start / 16), n'_s = n_s - f_s of them; without one f_s = 0.
+ * Chunk size in pages: chunk_pages if > 0 (uniform), otherwise ceil(n'_s / num_splits).  Chunk j
+ * covers visible pages [f_s + j*c, f_s + min((j+1)*c, n'_s)), and within them the attended
+ * positions only.  partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S] with S = num_out_splits. */
 int orc_split_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
                         const int32_t* page_indptr, const int32_t* page_indices,
                         const int32_t* last_page_len, int num_splits, int chunk_pages,
-                        int num_out_splits, double sm_scale, double* partial_o, double* partial_lse) {
+                        int num_out_splits, double sm_scale, int window, double* partial_o,
+                        double* partial_lse) {
   orc_init();
   const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads, S = num_out_splits;
   if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0 || S <= 0) return ORC_INVALID;
   if (chunk_pages <= 0 && num_splits <= 0) return ORC_INVALID;
   const int G = Hq / Hkv;
   for (int s = 0; s < B; ++s) {
-    int n = page_indptr[s + 1] - page_indptr[s];
+    int len;
+    if (seq_len_of(page_indptr, last_page_len, s, &len) != ORC_OK) return ORC_OUT_OF_RANGE;
+    int n = page_indptr[s + 1] - page_indptr[s] - window_start(len, window) / ORC_PAGE;
     int c = chunk_pages > 0 ? chunk_pages : (n + num_splits - 1) / num_splits;
     int chunks = (c > 0) ? (n + c - 1) / c : 0;
     if (chunks > S) return ORC_INVALID;
@@ -311,12 +345,14 @@ int orc_split_attention(const orc_geom* g, const uint16_t* pool, const uint16_t*
     int s = (int)(sh / Hq), h = (int)(sh % Hq);
     int len;
     int r = seq_len_of(page_indptr, last_page_len, s, &len);
-    int n = page_indptr[s + 1] - page_indptr[s];
+    const int ws = window_start(len, window), f = ws / ORC_PAGE;
+    int n = page_indptr[s + 1] - page_indptr[s] - f;
     int c = chunk_pages > 0 ? chunk_pages : (n + num_splits - 1) / num_splits;
     double* q = (double*)malloc(sizeof(double) * (size_t)d);
     for (int i = 0; i < d; ++i) q[i] = dec(q_rope[sh * d + i]);
     for (int j = 0; j < S && r == ORC_OK; ++j) {
-      int64_t t0 = (int64_t)j * c * ORC_PAGE, t1 = (int64_t)(j + 1) * c * ORC_PAGE;
+      int64_t t0 = ((int64_t)f + (int64_t)j * c) * ORC_PAGE, t1 = ((int64_t)f + (int64_t)(j + 1) * c) * ORC_PAGE;
+      if (t0 < ws) t0 = ws;
       if (t1 > len) t1 = len;
       if (t0 > len) t0 = len;
       r = attend(g, pool, q, s, h / G, (int)t0, (int)t1, page_indptr, page_indices, sm_scale,
@@ -388,9 +424,10 @@ int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const 
 }
 
 /* Log-sum-exp merge of the partials: out = sum_j w_j o_j / sum_j w_j with w_j = exp(lse_j - M),
- * M = max_j lse_j, lse = M + ln sum_j w_j.  out_f16 (nullable) gets out rounded to fp16. */
+ * M = max_j lse_j, lse = M + ln sum_j w_j; with a sink (sinks[h], nullable) the merged result then
+ * takes the sink into its denominator.  out_f16 (nullable) gets out rounded to fp16. */
 int orc_combine(const double* partial_o, const double* partial_lse, int B, int Hq, int S, int d,
-                double* out, uint16_t* out_f16, double* lse) {
+                const double* sinks, double* out, uint16_t* out_f16, double* lse) {
   if (B < 0 || Hq <= 0 || S <= 0 || d <= 0) return ORC_INVALID;
   for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
     const double* L = partial_lse + sh * S;
@@ -412,6 +449,7 @@ int orc_combine(const double* partial_o, const double* partial_lse, int B, int H
       for (int i = 0; i < d; ++i) o[i] /= W;
       lse[sh] = M + log(W);
     }
+    if (sinks != NULL) apply_sink(o, lse + sh, d, sinks[sh % Hq]);
     if (out_f16)
       for (int i = 0; i < d; ++i) out_f16[sh * d + i] = orc_f64_to_f16(o[i]);
   }

@@ -18,7 +18,12 @@ MUTANTS = [
     ("rope sign", "    y[i] = a * c - b * s;", "    y[i] = a * c + b * s;"),
     ("rope frequency exponent", "pow(theta, -2.0 * (double)i / (double)d)", "pow(theta, -1.0 * (double)i / (double)d)"),
     ("rope pairing", "double a = x[i], b = x[i + half];", "double a = x[i], b = x[d - 1 - i];"),
-    ("gqa head mapping", "s, h / G, 0, len,", "s, h % Hkv, 0, len,"),
+    ("gqa head mapping", "s, h / G, window_start(len, window), len,", "s, h % Hkv, window_start(len, window), len,"),
+    ("window off by one", "return (window > 0 && len > window) ? len - window : 0;",
+     "return (window > 0 && len > window) ? len - window + 1 : 0;"),
+    ("sink weight sign", "ws = exp(sink - M);", "ws = exp(M - sink);"),
+    ("sink dropped by the combine", "    if (sinks != NULL) apply_sink(o, lse + sh, d, sinks[sh % Hq]);\n", "\n"),
+    ("windowed chunk start", "      if (t0 < ws) t0 = ws;\n", "\n"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
     ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
      "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
@@ -45,6 +50,7 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
     subprocess.run(oracle.build_command(str(mutant), str(lib)), check=True)
     env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_window_sinks.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"the pins did not catch the planted mistake '{name}'"
