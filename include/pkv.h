@@ -95,6 +95,22 @@ typedef struct {
                             filled by pkv_create_cache; must outlive the cache */
   int* status_word;      /* device int32, zeroed by pkv_create_cache; must outlive the cache */
   int options;           /* PKV_OPT_* bits */
+  /* Per-layer attention variants (Splash models page: a family's sliding_window, its
+   * layer_types, and each layer's attn_sinks, F32).  Both may be NULL (every layer full
+   * attention, no sinks); both are read by pkv_create_cache, which copies them.
+   *   layer_window  host int32 [num_layers]: 0 = full attention; W > 0 = the query at position
+   *                 len-1 attends to positions [max(0, len-W), len), the W most recent tokens
+   *                 including itself.  Such a layer is split into chunks of its visible pages.
+   *   layer_sinks   host array [num_layers] of device pointers (each NULL or fp32 [num_qo_heads],
+   *                 caller-owned, alive while the cache is used): one logit per query head, in
+   *                 the units of the scaled scores (natural log), that joins the softmax's
+   *                 denominator and carries no value:
+   *                   out = sum_t e^s_t V_t / (sum_t e^s_t + e^sink),
+   *                   lse = ln(sum_t e^s_t + e^sink).
+   *                 The partials of pkv_decode_attention do not include it; pass the layer's
+   *                 sinks to pkv_combine.  The merged entry points apply it. */
+  const int32_t* layer_window;
+  const float* const* layer_sinks;
 } pkv_cache_desc;
 
 /* Bytes of one layer's pool. */
@@ -287,12 +303,14 @@ pkv_status pkv_decode_attention_noalloc(const pkv_cache* cache, int layer, const
  *   out[s][h][:] = fp16( sum_j w_j o_j / sum_j w_j ),   lse_out[s][h] = M + ln sum_j w_j.
  * Splits with lse_j = -inf are skipped (their o_j is not read); if every split is -inf,
  * out = 0 and lse_out = -inf.  out: fp16 [batch][Hq][head_dim]; lse_out: fp32 [batch][Hq]
- * or NULL.  num_splits >= 1; head_dim in {64, 96, 128}.
+ * or NULL.  num_splits >= 1; head_dim in {64, 96, 128}.  sinks: NULL, or the layer's device
+ * fp32 [Hq] attention sinks (see pkv_cache_desc), which join M and the denominator:
+ * M = max(max_j lse_j, sink_h), out = sum_j w_j o_j / (sum_j w_j + exp(sink_h - M)).
  * The cache supplies the launch options (PKV_OPT_PDL); it may be NULL for plain launches.
  */
 pkv_status pkv_combine(const pkv_cache* cache, const float* partial_o, const float* partial_lse,
-                       int batch, int num_qo_heads, int num_splits, int head_dim, void* out,
-                       float* lse_out, pkv_stream_t stream);
+                       const float* sinks, int batch, int num_qo_heads, int num_splits, int head_dim,
+                       void* out, float* lse_out, pkv_stream_t stream);
 
 /*
  * Synchronise `stream`, read and clear the cache's status word.  Returns PKV_OK when no bit was

@@ -35,7 +35,8 @@ class _Desc(ctypes.Structure):
                 ("num_qo_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("max_position", ctypes.c_int), ("rope_theta", ctypes.c_double),
                 ("layer_pools", ctypes.POINTER(ctypes.c_void_p)), ("rope_table", ctypes.c_void_p),
-                ("status_word", ctypes.c_void_p), ("options", ctypes.c_int)]
+                ("status_word", ctypes.c_void_p), ("options", ctypes.c_int),
+                ("layer_window", ctypes.POINTER(ctypes.c_int32)), ("layer_sinks", ctypes.POINTER(ctypes.c_void_p))]
 
 
 _lib = None
@@ -83,7 +84,7 @@ def lib():
         L.pkv_decode_attention_noalloc.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, f, P, P,
                                                    ctypes.POINTER(i), P]
         L.pkv_combine.restype = i
-        L.pkv_combine.argtypes = [P, P, P, i, i, i, i, P, P, P]
+        L.pkv_combine.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
         L.pkv_check_status.restype = i
         L.pkv_check_status.argtypes = [P, P, ctypes.POINTER(i)]
         _lib = L
@@ -127,10 +128,12 @@ class Cache:
     """A paged KV cache over caller-owned device memory (torch tensors).
 
     ``pools`` is a list of fp16 tensors [num_pages, 2, num_kv_heads, 16, head_dim] (allocated
-    here when omitted).  The RoPE table and the status word are allocated here as tensors."""
+    here when omitted).  The RoPE table and the status word are allocated here as tensors.
+    ``windows``: per layer sliding window (0 = full attention), or None; ``sinks``: per layer
+    None or an fp32 tensor [num_qo_heads] of attention-sink logits (kept alive here), or None."""
 
     def __init__(self, num_layers, num_pages, num_qo_heads, num_kv_heads, head_dim, max_position,
-                 rope_theta, pools=None, options: int = 0, device=None):
+                 rope_theta, pools=None, options: int = 0, device=None, windows=None, sinks=None):
         import torch
 
         device = torch.device("cuda") if device is None else torch.device(device)
@@ -151,10 +154,27 @@ class Cache:
         self.rope_table = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=device)
         self.status_word = torch.zeros(1, dtype=torch.int32, device=device)
         self._pool_ptrs = (ctypes.c_void_p * self.num_layers)(*[t.data_ptr() for t in self.pools])
+        win_ptr = ctypes.POINTER(ctypes.c_int32)()
+        sink_ptr = ctypes.POINTER(ctypes.c_void_p)()
+        self.windows = [0] * self.num_layers if windows is None else [int(w) for w in windows]
+        self.sinks = [None] * self.num_layers if sinks is None else list(sinks)
+        if len(self.windows) != self.num_layers or len(self.sinks) != self.num_layers:
+            raise ValueError("windows and sinks take one entry per layer")
+        for t in self.sinks:
+            if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (self.num_qo_heads,)
+                                  or not t.is_contiguous() or t.device.type != "cuda"):
+                raise ValueError("sinks must be contiguous float32 CUDA tensors of shape [num_qo_heads]")
+        if windows is not None:
+            self._windows = (ctypes.c_int32 * self.num_layers)(*self.windows)
+            win_ptr = ctypes.cast(self._windows, ctypes.POINTER(ctypes.c_int32))
+        if sinks is not None:
+            self._sink_ptrs = (ctypes.c_void_p * self.num_layers)(
+                *[None if t is None else t.data_ptr() for t in self.sinks])
+            sink_ptr = ctypes.cast(self._sink_ptrs, ctypes.POINTER(ctypes.c_void_p))
         d = _Desc(self.num_layers, self.num_pages, PAGE_SIZE, self.num_qo_heads, self.num_kv_heads,
                   self.head_dim, self.max_position, self.rope_theta,
                   ctypes.cast(self._pool_ptrs, ctypes.POINTER(ctypes.c_void_p)),
-                  self.rope_table.data_ptr(), self.status_word.data_ptr(), int(options))
+                  self.rope_table.data_ptr(), self.status_word.data_ptr(), int(options), win_ptr, sink_ptr)
         handle = ctypes.c_void_p()
         with torch.cuda.device(device):
             _check(lib().pkv_create_cache(ctypes.byref(d), ctypes.byref(handle)), "pkv_create_cache")
@@ -304,8 +324,8 @@ class Cache:
             _ptr(out), _ptr(lse), ctypes.byref(used), _stream(stream)), "pkv_decode_attention_noalloc")
         return out, lse
 
-    def combine(self, partial_o, partial_lse, out=None, lse=None, stream=None):
-        """pkv_combine; returns (out fp16 [B,Hq,d], lse fp32 [B,Hq])."""
+    def combine(self, partial_o, partial_lse, out=None, lse=None, stream=None, sinks=None):
+        """pkv_combine; returns (out fp16 [B,Hq,d], lse fp32 [B,Hq]); sinks: fp32 [Hq] or None."""
         import torch
 
         B, Hq, S, d = (int(x) for x in partial_o.shape)
@@ -313,8 +333,8 @@ class Cache:
             out = torch.empty((B, Hq, d), dtype=torch.float16, device=partial_o.device)
         if lse is None:
             lse = torch.empty((B, Hq), dtype=torch.float32, device=partial_o.device)
-        _check(lib().pkv_combine(self.handle, _ptr(partial_o), _ptr(partial_lse), B, Hq, S, d, _ptr(out),
-                                 _ptr(lse), _stream(stream)), "pkv_combine")
+        _check(lib().pkv_combine(self.handle, _ptr(partial_o), _ptr(partial_lse), _ptr(sinks), B, Hq, S, d,
+                                 _ptr(out), _ptr(lse), _stream(stream)), "pkv_combine")
         return out, lse
 
     def check_status(self, stream=None):
@@ -324,8 +344,8 @@ class Cache:
         return code, flags.value
 
 
-def combine(partial_o, partial_lse, out=None, lse=None, stream=None):
-    """pkv_combine without a cache (plain launches)."""
+def combine(partial_o, partial_lse, out=None, lse=None, stream=None, sinks=None):
+    """pkv_combine without a cache (plain launches); sinks: fp32 [Hq] or None."""
     import torch
 
     B, Hq, S, d = (int(x) for x in partial_o.shape)
@@ -333,6 +353,6 @@ def combine(partial_o, partial_lse, out=None, lse=None, stream=None):
         out = torch.empty((B, Hq, d), dtype=torch.float16, device=partial_o.device)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=partial_o.device)
-    _check(lib().pkv_combine(None, _ptr(partial_o), _ptr(partial_lse), B, Hq, S, d, _ptr(out), _ptr(lse),
-                             _stream(stream)), "pkv_combine")
+    _check(lib().pkv_combine(None, _ptr(partial_o), _ptr(partial_lse), _ptr(sinks), B, Hq, S, d, _ptr(out),
+                             _ptr(lse), _stream(stream)), "pkv_combine")
     return out, lse

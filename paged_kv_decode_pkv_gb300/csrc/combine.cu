@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) combine_kernel(CombineParam
   pdl_wait();  // the partials come from the preceding kernel
   const int S = p.splits;
   merge_rows<D>(p.partial_lse + sh * S, p.partial_o + sh * S * D, S, lane, p.out + sh * D,
-                p.lse != nullptr ? p.lse + sh : nullptr);
+                p.lse != nullptr ? p.lse + sh : nullptr, p.sinks != nullptr ? p.sinks[sh % p.hq] : -INFINITY);
 }
 
 }  // namespace

@@ -60,8 +60,12 @@ constexpr int kMetaPatch = 1 << 10;  // one-launch mode: the page holds the new 
 constexpr int kMetaSlotShift = 11;
 constexpr int kMetaChunkShift = 16;  // bits 16..31: chunks of the item's sequence
 
+// Stage metadata: sequence, chunk, KV head and (low half of gl's high bits) the first attended slot
+// of the page (a sliding window's start inside its first visible page), flags.
 struct __align__(16) StageMeta {
-  int s, j, g, flags;
+  int s, j, gl, flags;
+  __device__ int g() const { return gl & 0xffff; }
+  __device__ int lo() const { return gl >> 16; }
 };
 
 // Dynamic shared memory budget: the 227 KB per-block opt-in maximum less room for the kernel's
@@ -80,7 +84,7 @@ __host__ __device__ constexpr int smem_align(int group) { return group >= 2 ? 10
 
 struct Layout {
   int stage_bytes, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, prefix_off, indptr_off, aptr_off,
-      total;
+      wstart_off, total;
 };
 
 // Items whose query rows may be in flight at once, per warp (one item slot each).
@@ -90,9 +94,10 @@ constexpr int kItemSlots = 2;
 // one-launch mode also the query position's (cos, sin) row and the new token's raw k and v rows)
 // and (one-launch mode) the rotated K and V rows of the new token, the mbarriers, the stage
 // metadata, (one-launch mode) the page id of each stage, and per sequence the work prefix, the
-// page ranges and (one-launch mode) the new-token ranges.
+// page ranges, (one-launch mode) the new-token ranges and (sliding window) the first visible page
+// and its first attended slot.
 __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch,
-                                              bool fused) {
+                                              bool fused, bool windowed = false) {
   Layout L;
   const int n = warps * nstage;
   L.stage_bytes = 64 * head_dim;  // K and V of one page for one KV head
@@ -106,7 +111,8 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
   L.prefix_off = L.pid_off + (fused ? n * 4 : 0);
   L.indptr_off = L.prefix_off + (batch + 1) * 4;
   L.aptr_off = L.indptr_off + (batch + 1) * 4;
-  L.total = L.aptr_off + (fused ? (batch + 1) * 4 : 0) + smem_align(group);  // + slack to align the base
+  L.wstart_off = L.aptr_off + (fused ? (batch + 1) * 4 : 0);
+  L.total = L.wstart_off + (windowed ? batch * 4 : 0) + smem_align(group);  // + slack to align the base
   return L;
 }
 
@@ -326,25 +332,26 @@ struct GroupOne {
     }
   }
 
-  __device__ float mask(float sc, int nvalid) const {
+  // Rows outside [lo, nvalid) do not take part (lo: a sliding window's first slot, usually 0).
+  __device__ float mask(float sc, int lo, int nvalid) const {
     const int row = 2 * ((li >> 1) & 7) + half;
-    return (row < nvalid) ? sc : -INFINITY;
+    return (row >= lo && row < nvalid) ? sc : -INFINITY;
   }
 
-  __device__ void page(unsigned char* stage, int nvalid) {
+  __device__ void page(unsigned char* stage, int lo, int nvalid) {
     zero_v_tail(stage + kPageSize * D * 2, nvalid);
     float acc[8];
     dots(stage, acc);
     float sc[1];
     reduce_rows<1>(acc, sc);
-    sc[0] = mask(sc[0], nvalid);
+    sc[0] = mask(sc[0], lo, nvalid);
     uint16_t pb[1];
     softmax<1>(sc, pb);
     pv(stage + kPageSize * D * 2, pb[0]);
   }
 
   // Two consecutive pages of one item at once: independent q.k work for both, one softmax update.
-  __device__ void page2(unsigned char* sa, int na, unsigned char* sb, int nb) {
+  __device__ void page2(unsigned char* sa, int la, int na, unsigned char* sb, int nb) {
     zero_v_tail(sa + kPageSize * D * 2, na);
     zero_v_tail(sb + kPageSize * D * 2, nb);
     float acc[16];
@@ -354,8 +361,8 @@ struct GroupOne {
     dots(sb, a1);
     float sc[2];
     reduce_rows<2>(acc, sc);
-    sc[0] = mask(sc[0], na);
-    sc[1] = mask(sc[1], nb);
+    sc[0] = mask(sc[0], la, na);
+    sc[1] = mask(sc[1], 0, nb);
     uint16_t pb[2];
     softmax<2>(sc, pb);
     pv(sa + kPageSize * D * 2, pb[0]);
@@ -485,7 +492,7 @@ struct GroupMma {
     l = 0.f;
   }
 
-  __device__ void page(unsigned char* stage_ptr, int nvalid, float scale_log2) {
+  __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2) {
     const uint32_t stage = smem_u32(stage_ptr);
     if (nvalid < kPageSize) {
       // Slots past the sequence end may hold anything (even NaN): zero their V rows so that
@@ -516,10 +523,10 @@ struct GroupMma {
     }
     const int c = 2 * (lane & 3);
     float s[4] = {sc[0][0] * scale_log2, sc[0][1] * scale_log2, sc[1][0] * scale_log2, sc[1][1] * scale_log2};
-    s[0] = (c < nvalid) ? s[0] : -INFINITY;
-    s[1] = (c + 1 < nvalid) ? s[1] : -INFINITY;
-    s[2] = (c + 8 < nvalid) ? s[2] : -INFINITY;
-    s[3] = (c + 9 < nvalid) ? s[3] : -INFINITY;
+    s[0] = (c >= lo && c < nvalid) ? s[0] : -INFINITY;
+    s[1] = (c + 1 >= lo && c + 1 < nvalid) ? s[1] : -INFINITY;
+    s[2] = (c + 8 >= lo && c + 8 < nvalid) ? s[2] : -INFINITY;
+    s[3] = (c + 9 >= lo && c + 9 < nvalid) ? s[3] : -INFINITY;
     float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
@@ -613,6 +620,9 @@ struct Item {
   // and whether its page lies in this item
   int qpos;
   bool has_new;
+  // sliding window: the first visible page of the sequence (page ordinals of the item count from
+  // it) and the first attended slot of that page
+  int f, lo;
 };
 
 // Locate item w and start the global loads it needs (last-page length, query row, the first 32
@@ -620,7 +630,7 @@ struct Item {
 __device__ __forceinline__ void issue_item_loads(Item& it, const DecodeParams& p, int lane);
 
 __device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams& p, const int* prefix,
-                                             const int* indptr, int lane) {
+                                             const int* indptr, const int* wstart, int lane) {
   const int s = find_sequence(prefix, p.batch, w);
   const int r = w - prefix[s];
   it.s = s;
@@ -628,6 +638,16 @@ __device__ __forceinline__ void prepare_item(Item& it, int w, const DecodeParams
   it.g = r - it.j * p.hkv;
   it.first = indptr[s];
   it.n = indptr[s + 1] - it.first;
+  it.f = 0;
+  it.lo = 0;
+  if (wstart != nullptr) {
+    // sliding window: the item's pages are the sequence's visible pages
+    const int ws = wstart[s];
+    it.f = ws & 0xffffff;
+    it.lo = ws >> 24;
+    it.first += it.f;
+    it.n -= it.f;
+  }
   int c = 1;
   it.nch = seq_chunks(p, it.n, c);
   if (it.nch > 0 && it.n > 0) {
@@ -657,6 +677,8 @@ __device__ __forceinline__ void prepare_piece(Item& it, long long u, long long u
   it.g = g;
   it.first = indptr[s];
   it.n = n;
+  it.f = 0;
+  it.lo = 0;
   it.p0 = page;
   it.p1 = (int)min((long long)n, (long long)page + (u_end - u));
   const long long b = (long long)prefix[s] + (long long)g * n;  // first unit of the segment
@@ -699,9 +721,10 @@ __device__ __forceinline__ void issue_fused_loads(Item& it, const DecodeParams& 
 __device__ __forceinline__ bool activate_fused(Item& it, const DecodeParams& p, int lane) {
   const bool single = it.q1 == it.q0 + 1;
   const bool in_table = single && it.qpos >= 0 && it.qpos < p.max_position;
-  const bool in_pages = in_table && (it.qpos >> 4) < it.n;
+  const int vpage = (it.qpos >> 4) - it.f;  // among the item's (visible) pages
+  const bool in_pages = in_table && vpage >= 0 && vpage < it.n;
   if (single && !in_pages && it.j == 0 && lane == 0) atomicOr(p.status, kFlagBadPosition);
-  it.has_new = in_pages && (it.qpos >> 4) >= it.p0 && (it.qpos >> 4) < it.p1;
+  it.has_new = in_pages && vpage >= it.p0 && vpage < it.p1;
   return in_table;
 }
 
@@ -774,12 +797,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   // compiled as a shared-memory access
   constexpr uint32_t kAlign = smem_align(MMA ? 2 : 1);
   unsigned char* base = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
-  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED);
+  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED, p.window > 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
   int* prefix = reinterpret_cast<int*>(base + L.prefix_off);
   int* indptr = reinterpret_cast<int*>(base + L.indptr_off);
   int* aptr = reinterpret_cast<int*>(base + L.aptr_off);  // fused mode: append_indptr
+  const bool windowed = p.window > 0;
+  // sliding window: per sequence, first visible page | first attended slot << 24
+  int* wstart = windowed ? reinterpret_cast<int*>(base + L.wstart_off) : nullptr;
   __shared__ int warp_sums[32];
 
   pdl_launch_dependents();
@@ -795,6 +821,25 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     if constexpr (FUSED) aptr[i] = p.q_indptr[i];
   }
   __syncthreads();
+  if (windowed) {
+    // the query at position len - 1 attends to [len - window, len): pages from (len - window) / 16
+    for (int s = tid; s < p.batch; s += blockDim.x) {
+      const int n = indptr[s + 1] - indptr[s];
+      int ws = 0;
+      if (n > 0) {
+        const int last = p.last_page_len[s];
+        const int len = (n - 1) * kPageSize + last;
+        if (last >= 1 && last <= kPageSize && len > p.window) ws = len - p.window;
+      }
+      wstart[s] = (ws >> 4) | ((ws & 15) << 24);
+    }
+    __syncthreads();
+  }
+  // pages an item walks: the sequence's pages, or its visible pages under a window
+  auto seq_pages = [&](int s) {
+    const int n = indptr[s + 1] - indptr[s];
+    return windowed ? n - (wstart[s] & 0xffffff) : n;
+  };
   if (p.balanced) {
     for (int i = tid; i <= p.batch; i += blockDim.x) prefix[i] = p.hkv * indptr[i];
   } else {
@@ -803,7 +848,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     int local = 0;
     for (int s = s0; s < s1; ++s) {
       int c;
-      const int nch = seq_chunks(p, indptr[s + 1] - indptr[s], c);
+      const int nch = seq_chunks(p, seq_pages(s), c);
       local += p.hkv * (nch > 0 ? nch : 1);
     }
     int incl = local;
@@ -820,7 +865,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     for (int s = s0; s < s1; ++s) {
       prefix[s] = run;
       int c;
-      const int nch = seq_chunks(p, indptr[s + 1] - indptr[s], c);
+      const int nch = seq_chunks(p, seq_pages(s), c);
       run += p.hkv * (nch > 0 ? nch : 1);
     }
     if (tid == blockDim.x - 1) prefix[p.batch] = run;
@@ -857,7 +902,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       u_next += it.p1 - it.p0;
     } else {
       if (w_next >= total) return false;
-      prepare_item(it, w_next, p, prefix, indptr, lane);
+      prepare_item(it, w_next, p, prefix, indptr, wstart, lane);
       w_next += W;
     }
     if constexpr (FUSED) issue_fused_loads(it, p, aptr);
@@ -901,12 +946,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     StageMeta mt;
     mt.s = cur.s;
     mt.j = cur.j;
-    mt.g = cur.g;
+    mt.gl = cur.g;
     if (cur.p1 == cur.p0) {
       const int nch = max(cur.nch, 1);
       mt.flags = kMetaFirst | kMetaLast | kMetaEmpty | (cur.j >= nch - 1 ? kMetaLastChunk : 0) |
                  (nch << kMetaChunkShift);
-      st_shared_v4_if(lane == 0, &meta[k], mt.s, mt.j, mt.g, mt.flags);
+      st_shared_v4_if(lane == 0, &meta[k], mt.s, mt.j, mt.gl, mt.flags);
       mbar_arrive_if(lane == 0, &bar[k]);
       cur.active = false;
     } else {
@@ -926,7 +971,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         // The first stage also brings the new token's raw k and v; the consumer patches the page
         // that holds the token in shared memory (the copy of that slot from the pool is stale).
         if (first && cur.has_new) mt.flags |= kMetaNew;
-        if (cur.has_new && page_ok && cur.pnext == (cur.qpos >> 4)) {
+        if (cur.has_new && page_ok && cur.pnext == (cur.qpos >> 4) - cur.f) {
           mt.flags |= kMetaPatch | ((cur.qpos & 15) << kMetaSlotShift);
           st_shared_u32_if(lane == 0, &meta_pid[k], pid);
         }
@@ -935,7 +980,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       // lane 0 publishes the stage: metadata, then the barrier's byte count, then the copies (all
       // predicated on the lane, no branch)
       const bool l0 = lane == 0;
-      st_shared_v4_if(l0, &meta[k], mt.s, mt.j, mt.g, mt.flags);
+      if (cur.pnext == 0) mt.gl |= cur.lo << 16;  // a window's first attended slot
+      st_shared_v4_if(l0, &meta[k], mt.s, mt.j, mt.gl, mt.flags);
       const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes + cs_bytes : 0u) +
                              ((mt.flags & kMetaNew) ? kv_bytes : 0u);
       mbar_arrive_expect_tx_if(l0 && bytes != 0u, &bar[k], bytes);
@@ -994,7 +1040,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if (p.merged) {
         for (int i = lane; i < p.hq * D; i += 32) p.out[row0 * D + i] = __float2half_rn(0.f);
         if (p.lse_out != nullptr)
-          for (int i = lane; i < p.hq; i += 32) p.lse_out[row0 + i] = -INFINITY;
+          for (int i = lane; i < p.hq; i += 32)
+            p.lse_out[row0 + i] = p.sinks != nullptr ? p.sinks[i] : -INFINITY;  // no token: the sink alone
       } else {
         for (int i = lane; i < p.hq * p.splits; i += 32) p.partial_lse[row0 * p.splits + i] = -INFINITY;
       }
@@ -1012,12 +1059,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
 
   bool pending_merge = false;
   long long pm_row0 = 0;
-  int pm_nch = 0;
+  int pm_nch = 0, pm_head0 = 0;  // pm_head0: the group's first query head in the layer
   int* pm_counter = nullptr;
 
   // Finish an item: write its partial (or, merged, its output / its share of the merge).
   auto finish_item = [&](const StageMeta& mt) {
-    const long long head_row0 = (long long)mt.s * p.hq + (long long)mt.g * p.group;
+    const long long head_row0 = (long long)mt.s * p.hq + (long long)mt.g() * p.group;
     if (!p.merged) {
       bool wrote = false;
       if (!(mt.flags & kMetaEmpty)) wrote = cmp.finish(p.partial_o, p.partial_lse, head_row0, p.splits, mt.j);
@@ -1032,10 +1079,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       return;
     }
     const int nch = (mt.flags >> kMetaChunkShift) & 0xffff;
-    if (nch == 1 && (mt.flags & kMetaEmpty)) {
+    // With sinks a single chunk also takes the merge path, so that its result is the combine's.
+    if (nch == 1 && (mt.flags & kMetaEmpty) && p.sinks == nullptr) {
       for (int i = lane; i < p.group * D; i += 32) p.out[head_row0 * D + i] = __float2half_rn(0.f);
       if (p.lse_out != nullptr && lane < p.group) p.lse_out[head_row0 + lane] = -INFINITY;
-    } else if (nch == 1) {
+    } else if (nch == 1 && p.sinks == nullptr) {
       cmp.finish_out(p.out, p.lse_out, head_row0);
     } else {
       const bool wrote =
@@ -1045,7 +1093,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       // The warp barrier orders every lane's partial writes before lane 0's release; lane 0's
       // acquire, then the barrier of the shuffle, order the merge's reads after the other chunks'.
       __syncwarp();
-      int* counter = p.counters + (long long)mt.s * p.hkv + mt.g;
+      int* counter = p.counters + (long long)mt.s * p.hkv + mt.g();
       int done = 0;
       if (lane == 0) done = atom_add_acq_rel_gpu(counter, 1) + 1;
       done = __shfl_sync(kFull, done, 0);
@@ -1053,6 +1101,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         // this chunk completed the group: merge once this warp's stages are released
         pending_merge = true;
         pm_row0 = head_row0;
+        pm_head0 = mt.g() * p.group;
         pm_nch = nch;
         pm_counter = counter;
       }
@@ -1102,12 +1151,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       for (int hh = 0; hh < p.group; ++hh) {
         const long long row = pm_row0 + hh;
         merge_rows<D>(lse_s + hh * 64, reinterpret_cast<const float*>(stages + hh * rows_bytes), pm_nch, lane,
-                      p.out + row * D, p.lse_out != nullptr ? p.lse_out + row : nullptr);
+                      p.out + row * D, p.lse_out != nullptr ? p.lse_out + row : nullptr,
+                      p.sinks != nullptr ? p.sinks[pm_head0 + hh] : -INFINITY);
       }
       fence_proxy_async_smem();  // the reads above before later copies into the ring
       __syncwarp();
     } else {
-      merge_group<D>(p.partial_lse, p.partial_o, pm_row0, p.group, p.splits, pm_nch, lane, p.out, p.lse_out);
+      merge_group<D>(p.partial_lse, p.partial_o, pm_row0, p.group, p.splits, pm_nch, lane, p.out, p.lse_out,
+                     p.sinks, pm_head0);
     }
     if (lane == 0) *pm_counter = 0;  // ready for the next launch
     pending_merge = false;
@@ -1138,7 +1189,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           if (mt.j == 0) {
             // the first piece of each (sequence, KV head) writes the rotated query rows (q_out)
             const int qrow = aptr[mt.s];
-            cmp.store_query(p.q_out + ((long long)qrow * p.hq + (long long)mt.g * p.group) * D);
+            cmp.store_query(p.q_out + ((long long)qrow * p.hq + (long long)mt.g() * p.group) * D);
           }
           if (mt.flags & kMetaNew) make_patch<D>(qs + q_bytes, qs + q_bytes + cs_bytes, patch, lane);
         } else if constexpr (MMA) {
@@ -1164,24 +1215,24 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           used = 2;
           if constexpr (FUSED) {
             if (fin.flags & kMetaPatch)
-              apply_patch<D, Compute>(s2, patch, (fin.flags >> kMetaSlotShift) & 15, meta_pid[k2], fin.g, p, lane);
+              apply_patch<D, Compute>(s2, patch, (fin.flags >> kMetaSlotShift) & 15, meta_pid[k2], fin.g(), p, lane);
           }
         }
         if constexpr (FUSED) {
           if (mt.flags & kMetaPatch)
-            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g, p, lane);
+            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
         if (nvalid > 0 && n2 > 0) {
-          cmp.page2(s1, nvalid, s2, n2);
+          cmp.page2(s1, mt.lo(), nvalid, s2, n2);
         } else if (nvalid + n2 > 0) {
-          cmp.page(nvalid > 0 ? s1 : s2, nvalid > 0 ? nvalid : n2);
+          cmp.page(nvalid > 0 ? s1 : s2, nvalid > 0 ? mt.lo() : 0, nvalid > 0 ? nvalid : n2);
         }
       } else {
         if constexpr (FUSED) {
           if (mt.flags & kMetaPatch)
-            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g, p, lane);
+            apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
-        if (nvalid > 0) cmp.page(s1, nvalid, p.scale_log2);
+        if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
       }
     }
     if (fin.flags & kMetaLast) finish_item(fin);
@@ -1215,9 +1266,9 @@ void* select_kernel(int head_dim, bool mma, bool fused) {
 }  // namespace
 
 // Deepest ring (at most 8, at least 2, else 0) of a CTA of `warps` warps within `budget` bytes.
-int ring_depth(int warps, int head_dim, int group, int batch, bool fused, int budget) {
+int ring_depth(int warps, int head_dim, int group, int batch, bool fused, bool windowed, int budget) {
   int n = 8;
-  while (n >= 2 && make_layout(warps, n, head_dim, group, batch, fused).total > budget) --n;
+  while (n >= 2 && make_layout(warps, n, head_dim, group, batch, fused, windowed).total > budget) --n;
   return n >= 2 ? n : 0;
 }
 
@@ -1225,7 +1276,7 @@ int ring_depth(int warps, int head_dim, int group, int batch, bool fused, int bu
 // resident CTA, and the kernel's static shared memory).
 int cta_budget(int ctas) { return std::min(kSmemBudget, (kSmemPerSm - ctas * 1024) / ctas - 256); }
 
-DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool windowed) {
   DecodeConfig c;
   c.mma = group >= 2;
   c.fused = fused;
@@ -1235,7 +1286,7 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
   // give the same bits; each takes the ring depth that fits.
   int sm_warps = 8, best = 0, best_n = 0;
   for (int w = c.mma ? 6 : 8; w <= kMaxDecodeWarps; ++w) {
-    const int n = ring_depth(w, head_dim, group, batch, false, kSmemBudget);
+    const int n = ring_depth(w, head_dim, group, batch, false, false, kSmemBudget);
     if (n >= 2 && (w * n > best || (w * n == best && n > best_n))) {
       best = w * n;
       best_n = n;
@@ -1244,13 +1295,13 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
   }
   c.warps = sm_warps;
   c.ctas_per_sm = 1;
-  c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, kSmemBudget);
+  c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget);
   // The SM's warps split over kCtasPerSm CTAs when the ring stays as deep: a CTA that is still
   // merging at the end of a launch then holds only its share of the SM, and the next launch's CTAs
   // start (and run their prologue) in the rest.
   if (kCtasPerSm > 1 && sm_warps % kCtasPerSm == 0) {
     const int w = sm_warps / kCtasPerSm;
-    const int n = ring_depth(w, head_dim, group, batch, fused, cta_budget(kCtasPerSm));
+    const int n = ring_depth(w, head_dim, group, batch, fused, windowed, cta_budget(kCtasPerSm));
     if (n >= c.nstage && n >= 2) {
       c.warps = w;
       c.ctas_per_sm = kCtasPerSm;
@@ -1258,7 +1309,8 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused) {
     }
   }
   const int nstage = c.nstage;
-  c.smem_bytes = nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused).total : 0;
+  c.smem_bytes =
+      nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused, windowed).total : 0;
   if (c.mma) {
     c.box_inner = head_dim == 96 ? 32 : 64;
     c.swizzle_bytes = head_dim == 96 ? 64 : 128;

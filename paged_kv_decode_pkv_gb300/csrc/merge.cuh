@@ -7,7 +7,8 @@
 // of eight lanes; group g accumulates splits g, g + 4, g + 8, ... in order, each lane owning
 // head_dim/8 consecutive dimensions as float4 vectors (with up to 64 splits the weights of pass 1
 // arrive by shuffle, beyond that every lane recomputes its w_j, the same value); the four group
-// sums are then added in a fixed order, (g0 + g1) + (g2 + g3).  Used by the combine kernel (rows and
+// sums are then added in a fixed order, (g0 + g1) + (g2 + g3).  A sink logit (a layer's attention
+// sink, -inf for none) joins the maximum and adds its weight to the denominator, carrying no value.  Used by the combine kernel (rows and
 // LSEs in global memory) and by the merged decode (in shared memory), so both give the same bits.
 #pragma once
 
@@ -21,7 +22,7 @@ namespace pkv {
 // inlined copies would crowd the streaming loop's instruction cache.
 template <int D>
 __device__ __noinline__ void merge_rows(const float* lse, const float* rows, int S, int lane, __half* out,
-                                        float* lse_out) {
+                                        float* lse_out, float sink) {
   constexpr unsigned kAll = 0xffffffffu;
   constexpr int kVec = D / 32;  // float4 vectors per lane
   // pass 1: lane l holds the LSEs of splits l and l + 32 (the rest, if any, in a loop)
@@ -31,6 +32,7 @@ __device__ __noinline__ void merge_rows(const float* lse, const float* rows, int
   for (int j = lane + 64; j < S; j += 32) M = fmaxf(M, lse[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+  M = fmaxf(M, sink);
   float4 acc[kVec];
 #pragma unroll
   for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -88,6 +90,7 @@ __device__ __noinline__ void merge_rows(const float* lse, const float* rows, int
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kAll, W, o);
+  if (sink != -INFINITY) W += expf(sink - M);
 #pragma unroll
   for (int o = 8; o <= 16; o <<= 1) {
 #pragma unroll
@@ -116,11 +119,12 @@ __device__ __noinline__ void merge_rows(const float* lse, const float* rows, int
 // of line so its registers do not weigh on the streaming loop.
 template <int D>
 __device__ __noinline__ void merge_group(const float* partial_lse, const float* partial_o, long long head_row0,
-                                         int group, int splits, int nch, int lane, __half* out, float* lse_out) {
+                                         int group, int splits, int nch, int lane, __half* out, float* lse_out,
+                                         const float* sinks, int head0) {
   for (int hh = 0; hh < group; ++hh) {
     const long long row = head_row0 + hh;
     merge_rows<D>(partial_lse + row * splits, partial_o + row * splits * D, nch, lane, out + row * D,
-                  lse_out != nullptr ? lse_out + row : nullptr);
+                  lse_out != nullptr ? lse_out + row : nullptr, sinks != nullptr ? sinks[head0 + hh] : -INFINITY);
   }
 }
 

@@ -15,6 +15,8 @@
 struct pkv_cache {
   pkv_cache_desc desc;
   std::vector<void*> pools;
+  std::vector<int> windows;         // per layer, 0 = full attention
+  std::vector<const float*> sinks;  // per layer, device fp32 [Hq] or null
   std::vector<CUtensorMap> maps;  // one per layer pool
   int device = 0;
   int num_sms = 0;
@@ -194,6 +196,11 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   for (int l = 0; l < d->num_layers; ++l)
     if (d->layer_pools[l] == nullptr || !aligned(d->layer_pools[l], 256)) return PKV_ERR_INVALID_ARG;
   if (d->options & ~PKV_OPT_PDL) return PKV_ERR_INVALID_ARG;
+  for (int l = 0; l < d->num_layers; ++l) {
+    if (d->layer_window != nullptr && d->layer_window[l] < 0) return PKV_ERR_INVALID_ARG;
+    if (d->layer_sinks != nullptr && d->layer_sinks[l] != nullptr && !aligned(d->layer_sinks[l], 4))
+      return PKV_ERR_INVALID_ARG;
+  }
 
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -203,6 +210,14 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   c->desc = *d;
   c->pools.assign(d->layer_pools, d->layer_pools + d->num_layers);
   c->desc.layer_pools = nullptr;
+  c->windows.assign(d->num_layers, 0);
+  c->sinks.assign(d->num_layers, nullptr);
+  for (int l = 0; l < d->num_layers; ++l) {
+    if (d->layer_window != nullptr) c->windows[l] = d->layer_window[l];
+    if (d->layer_sinks != nullptr) c->sinks[l] = d->layer_sinks[l];
+  }
+  c->desc.layer_window = nullptr;
+  c->desc.layer_sinks = nullptr;
   c->group = group;
   c->pdl = (d->options & PKV_OPT_PDL) != 0;
   cudaError_t e = cudaGetDevice(&c->device);
@@ -341,6 +356,21 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   int S = 0, chunk = 0;
   const pkv_status ps = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
   if (ps != PKV_OK) return fail(ps, "split plan arguments");
+  const int window = c->windows[layer];
+  if (window > 0) {
+    // A windowed layer walks each sequence's visible pages, at most ceil(window / 16) + 1 of
+    // them, in chunks (the page-balanced partition counts whole sequences): per-sequence chunks
+    // for an explicit split count, else chunks no longer than those the plan gave, so the split
+    // count stays within the plan's (and within pkv_plan_decode's, the partial buffers' size).
+    const int max_vis = std::max(1, std::min(max_pages, (window + PKV_PAGE_SIZE - 1) / PKV_PAGE_SIZE + 1));
+    if (num_splits <= 0) {
+      const int c_pages = chunk > 0 ? chunk : std::max(1, (max_vis + S - 1) / S);
+      chunk = c_pages;
+      S = (max_vis + c_pages - 1) / c_pages;
+    } else {
+      chunk = 0;
+    }
+  }
   if (splits_used) *splits_used = S;
   if (batch == 0) return PKV_OK;
   if (batch > pkv::kMaxDecodeBatch) return fail(PKV_ERR_UNSUPPORTED, "batch above 4096 sequences");
@@ -363,7 +393,7 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
                            fused->q_out == q_rope))
     return fail(PKV_ERR_INVALID_ARG, "misaligned or aliased q/k/v/q_out");
   const int D = c->desc.head_dim;
-  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch, fused != nullptr);
+  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch, fused != nullptr, window > 0);
   if (cfg.nstage < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this batch");
   pkv::DecodeParams p;
   p.q = static_cast<const __half*>(q_rope);
@@ -406,6 +436,8 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   p.pool = static_cast<__half*>(c->pools[layer]);
   p.rope = reinterpret_cast<const float2*>(c->desc.rope_table);
   p.max_position = c->desc.max_position;
+  p.window = window;
+  p.sinks = c->sinks[layer];
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 
@@ -457,8 +489,8 @@ pkv_status pkv_decode_attention_merged(const pkv_cache* c, int layer, const void
                        chunk_counters, out, lse_out, true, splits_used, stream);
 }
 
-pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* partial_lse, int batch,
-                       int num_qo_heads, int num_splits, int head_dim, void* out, float* lse_out,
+pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* partial_lse, const float* sinks,
+                       int batch, int num_qo_heads, int num_splits, int head_dim, void* out, float* lse_out,
                        pkv_stream_t stream) {
   if (batch < 0 || num_qo_heads < 1 || num_splits < 1) return PKV_ERR_INVALID_ARG;
   if (!head_dim_ok(head_dim)) return PKV_ERR_UNSUPPORTED;
@@ -470,6 +502,7 @@ pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* 
   p.partial_lse = partial_lse;
   p.out = static_cast<__half*>(out);
   p.lse = lse_out;
+  p.sinks = sinks;
   p.batch = batch;
   p.hq = num_qo_heads;
   p.splits = num_splits;

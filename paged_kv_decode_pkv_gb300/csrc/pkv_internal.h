@@ -75,6 +75,11 @@ struct DecodeParams {
   __half* pool;
   const float2* rope;
   int max_position;
+  // Layer variants: a sliding window of `window` positions (0 = full attention; chunk mode only,
+  // the chunks then cover each sequence's visible pages) and per query head sink logits (natural
+  // log, units of the scaled scores; nullable) that join the merge's denominator.
+  int window;
+  const float* sinks;
 };
 
 struct CombineParams {
@@ -82,6 +87,7 @@ struct CombineParams {
   const float* partial_lse;
   __half* out;
   float* lse;
+  const float* sinks;  // nullable: per query head sink logits
   int batch, hq, splits, head_dim;
 };
 
@@ -97,7 +103,7 @@ struct DecodeConfig {
   int swizzle_bytes;    // 0 (none), 64 or 128
 };
 
-DecodeConfig decode_config(int group, int head_dim, int batch, bool fused = false);
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused = false, bool windowed = false);
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim);  // function attributes
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl);
