@@ -202,7 +202,8 @@ def oracle_sample(step: W.Step, seconds: float, max_layers: int):
         g = H.geometry(sub)
         t0 = time.perf_counter()
         q_out = oracle.append(g, q, k, v, sub.pos_map, sub.append_indptr, sub.page_indptr, sub.page_indices, pool)
-        oracle.attention(g, pool, q_out[H.query_rows(sub)], sub.page_indptr, sub.page_indices, sub.last_page_len)
+        oracle.attention(g, pool, q_out[H.query_rows(sub)], sub.page_indptr, sub.page_indices, sub.last_page_len,
+                         window=step.cfg.window, sinks=oracle_sinks(step, layer))
         done_time += time.perf_counter() - t0
         done_bytes += sub.kv_bytes()
         layers += 1
@@ -211,6 +212,10 @@ def oracle_sample(step: W.Step, seconds: float, max_layers: int):
     what = (f"{layers} layer(s) x {len(seqs)} of {step.batch} sequence(s) of {step.cfg.name}: fp64 append + "
             f"unsplit attention, {done_bytes / 1e9:.3f} GB of KV")
     return done_bytes / done_time / 1e9, oracle.threads(), what
+
+
+def oracle_sinks(step: W.Step, layer: int):
+    return W.sink_logits(step, layer).astype(np.float64) if step.cfg.sinks else None
 
 
 def reference_sample(step: W.Step, budget_bytes: float = 2e9):
@@ -240,15 +245,16 @@ def run_reference(args):
     g = H.geometry(sub)
     rows = W.token_rows(step, seqs)
     inputs = [(W.host_pool_pages(sub, l, np.arange(sub.num_pages)), *W.new_qkv(step, l, rows=rows)) for l in layers]
+    sinks = [oracle_sinks(step, l) for l in layers]
     times = []
     for i in range(args.warmup + args.steps):
         pools = [x[0].copy() for x in inputs]
         t0 = time.perf_counter()
-        for pool, (_, q, k, v) in zip(pools, inputs):
+        for pool, (_, q, k, v), sk in zip(pools, inputs, sinks):
             q_out = oracle.append(g, q, k, v, sub.pos_map, sub.append_indptr, sub.page_indptr, sub.page_indices,
                                   pool)
             oracle.attention(g, pool, q_out[H.query_rows(sub)], sub.page_indptr, sub.page_indices,
-                             sub.last_page_len)
+                             sub.last_page_len, window=cfg.window, sinks=sk)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     t = statistics.mean(times)
@@ -287,8 +293,11 @@ def run_ours(args):
     step = W.make_step(cfg, rank_seed(cfg, rank))
     layers = list(range(cfg.layers))
     pools = [W.device_pool(step, l) for l in layers]
+    # layer variants of the workload: sliding window and attention sinks
+    windows = [cfg.window] * cfg.layers if cfg.window else None
+    sinks = [torch.from_numpy(W.sink_logits(step, l)).to(dev) for l in layers] if cfg.sinks else None
     cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=pkv.OPT_PDL)
+                      pools=pools, options=pkv.OPT_PDL, windows=windows, sinks=sinks)
     B, T = step.batch, step.num_tokens
     total_pages = int(step.page_indptr[-1])
     S, chunk = cache.plan_decode(B, step.max_pages_per_seq, total_pages)
@@ -344,7 +353,7 @@ def run_ours(args):
         cache.decode_attention(l, q_out[l], tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
                                step.max_pages_per_seq, q_indptr=tabs["append_indptr"] if use_q_indptr else None,
                                total_pages=total_pages, partial_o=po, partial_lse=pl)
-        cache.combine(po, pl, out=outs[l], lse=lses[l])
+        cache.combine(po, pl, out=outs[l], lse=lses[l], sinks=None if sinks is None else sinks[l])
 
     def step_fn():
         for l in layers:
@@ -429,7 +438,7 @@ def run_ours(args):
     # headline step's: the one-launch decode (append, split-K decode and merge); with chunked
     # appends, the merged decode after the append launch.
     plain = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=0)
+                      pools=pools, options=0, windows=windows, sinks=sinks)
 
     def layer_chain_plain(l, events):
         q, k, v = qkv[l]
@@ -523,6 +532,8 @@ def run_ours(args):
                    "kv_heads": cfg.hkv, "head_dim": cfg.head_dim, "page_size": 16,
                    "context_tokens": int(step.seq_len.sum()), "kv_bytes_per_step": kv_step,
                    "splits": S, "chunk_pages": chunk,
+                   **({"window": cfg.window} if cfg.window else {}),
+                   **({"attention_sinks": "per layer and query head"} if cfg.sinks else {}),
                    "l2": f"inputs larger than L2: {kv_step / 1e9:.2f} GB of KV per step",
                    "launch": "CUDA graph of the step, programmatic dependent launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

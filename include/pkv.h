@@ -182,6 +182,12 @@ pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const voi
  *   both 0, total_pages == 0  a uniform chunk size from the batch, the KV heads, max_pages_per_seq
  *                             and the SM count, so that the work items fill the resident warps.
  *   The split count never exceeds max_splits (the balanced partition is not used when it would).
+ * A layer with a sliding window (pkv_cache_desc.layer_window) walks each sequence's visible pages
+ * (at most V = ceil(W/16) + 1): num_splits and chunk_pages apply to them; with neither, the
+ * balanced partition of the visible page units (the kernel counts them; splits = V + 1), or, if
+ * that exceeds max_splits, chunks of about four work items per resident warp.  *splits is the
+ * most any layer of the cache produces (the capacity partial buffers need); *chunk_pages_out
+ * describes the layers without a window.
  * (Zero TVM Documentation, "How it works": split-K over KV chunks with a fixed ?splitk=N; the
  * choice from length and SM count is this library's.)
  */

@@ -69,7 +69,7 @@ def _L():
         lib.orc_split_attention.restype = i
         lib.orc_split_attention.argtypes = [P, P, P, i, P, P, P, i, i, i, d, i, P, P]
         lib.orc_split_attention_balanced.restype = i
-        lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, P, P]
+        lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, i, P, P]
         lib.orc_combine.restype = i
         lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P, P]
         lib.orc_threads.restype = i
@@ -212,8 +212,9 @@ def split_attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, las
 
 
 def split_attention_balanced(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page_len,
-                             num_warps: int, num_out_splits: int, sm_scale=None):
-    """Partials of the page-balanced partition into ``num_warps`` equal runs of page units."""
+                             num_warps: int, num_out_splits: int, sm_scale=None, window: int = 0):
+    """Partials of the page-balanced partition into ``num_warps`` equal runs of page units (the
+    visible pages under a window)."""
     sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
     pool, pp = _c(pool, np.uint16)
     q, pq = _c(q_rope, np.uint16)
@@ -226,7 +227,7 @@ def split_attention_balanced(geom: Geometry, pool, q_rope, page_indptr, page_ind
     pl = np.empty((B, geom.num_qo_heads, S), dtype=np.float64)
     g = geom.c()
     rc = _L().orc_split_attention_balanced(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, int(num_warps), S,
-                                           float(sm_scale), po.ctypes.data, pl.ctypes.data)
+                                           float(sm_scale), int(window), po.ctypes.data, pl.ctypes.data)
     if rc:
         raise OracleError(rc)
     return po, pl

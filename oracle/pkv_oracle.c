@@ -370,20 +370,39 @@ int orc_split_attention(const orc_geom* g, const uint16_t* pool, const uint16_t*
 /* Split-K partial attention with the page-balanced partition: the page units of all
  * (sequence, KV head) segments, ordered sequence-major, then KV head, then page, are cut into
  * num_warps contiguous runs, run w being units [floor(w*U/W), floor((w+1)*U/W)) with
- * U = Hkv * page_indptr[B].  Piece k of a segment is its intersection with the k-th run that
- * meets it.  partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S]; slots without a piece are
- * (0, -inf).  Requires num_warps <= U (every run non-empty). */
+ * U = Hkv * (total pages).  Piece k of a segment is its intersection with the k-th run that
+ * meets it.  Under a window W > 0 a sequence's units are its visible pages [f_s, n_s) (see
+ * orc_split_attention) and U counts those.  partial_o: [B][Hq][S][d], partial_lse: [B][Hq][S];
+ * slots without a piece are (0, -inf).  Requires num_warps <= U (every run non-empty). */
 int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int B,
                                  const int32_t* page_indptr, const int32_t* page_indices,
                                  const int32_t* last_page_len, int num_warps, int num_out_splits,
-                                 double sm_scale, double* partial_o, double* partial_lse) {
+                                 double sm_scale, int window, double* partial_o, double* partial_lse) {
   orc_init();
   const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads, S = num_out_splits;
   if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0 || S <= 0 || num_warps <= 0) return ORC_INVALID;
   const int G = Hq / Hkv;
-  const int64_t U = (int64_t)Hkv * page_indptr[B];
+  /* visible pages of each sequence and their exclusive prefix */
+  int64_t* vstart = (int64_t*)malloc(sizeof(int64_t) * (size_t)(B + 1));
+  int* vfirst = (int*)malloc(sizeof(int) * (size_t)(B > 0 ? B : 1));
+  vstart[0] = 0;
+  for (int s = 0; s < B; ++s) {
+    int len = 0;
+    if (seq_len_of(page_indptr, last_page_len, s, &len) != ORC_OK) {
+      free(vstart);
+      free(vfirst);
+      return ORC_OUT_OF_RANGE;
+    }
+    vfirst[s] = window_start(len, window) / ORC_PAGE;
+    vstart[s + 1] = vstart[s] + (page_indptr[s + 1] - page_indptr[s] - vfirst[s]);
+  }
+  const int64_t U = (int64_t)Hkv * vstart[B];
   const int64_t W = num_warps;
-  if (U > 0 && W > U) return ORC_INVALID;
+  if (U > 0 && W > U) {
+    free(vstart);
+    free(vfirst);
+    return ORC_INVALID;
+  }
   int rc = ORC_OK;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t sh = 0; sh < (int64_t)B * Hq; ++sh) {
@@ -396,8 +415,9 @@ int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const 
       for (int i = 0; i < d; ++i) partial_o[(sh * S + j) * d + i] = 0.0;
       partial_lse[sh * S + j] = -INFINITY;
     }
-    const int64_t n = page_indptr[s + 1] - page_indptr[s];
-    const int64_t b = (int64_t)Hkv * page_indptr[s] + (int64_t)kvh * n; /* first unit of the segment */
+    const int64_t n = vstart[s + 1] - vstart[s];
+    const int64_t b = (int64_t)Hkv * vstart[s] + (int64_t)kvh * n; /* first unit of the segment */
+    const int64_t f = vfirst[s], ws = window_start(len, window);
     int k = 0;
     for (int64_t w = 0; w < W && r == ORC_OK && n > 0; ++w) {
       const int64_t u0 = w * U / W, u1 = (w + 1) * U / W;
@@ -407,7 +427,8 @@ int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const 
         r = ORC_INVALID;
         break;
       }
-      int64_t t0 = (lo - b) * ORC_PAGE, t1 = (hi - b) * ORC_PAGE;
+      int64_t t0 = (f + lo - b) * ORC_PAGE, t1 = (f + hi - b) * ORC_PAGE;
+      if (t0 < ws) t0 = ws;
       if (t1 > len) t1 = len;
       if (t0 > len) t0 = len;
       r = attend(g, pool, q, s, kvh, (int)t0, (int)t1, page_indptr, page_indices, sm_scale,
@@ -420,6 +441,8 @@ int orc_split_attention_balanced(const orc_geom* g, const uint16_t* pool, const 
       rc = r;
     }
   }
+  free(vstart);
+  free(vfirst);
   return rc;
 }
 

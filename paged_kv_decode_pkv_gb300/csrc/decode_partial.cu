@@ -665,25 +665,32 @@ __device__ __forceinline__ long long first_run(long long b, long long U, long lo
   return ((b + 1) * W + U - 1) / U - 1;
 }
 
-// Balanced mode: the piece of warp gw that starts at unit u of its run [u, u_end).
+// Balanced mode: the piece of warp gw that starts at unit u of its run [u, u_end); U units in PW
+// runs.  Under a sliding window the units are the visible pages (wstart non-null).
 __device__ __forceinline__ void prepare_piece(Item& it, long long u, long long u_end, int gw, const DecodeParams& p,
-                                              const int* prefix, const int* indptr, int lane) {
+                                              const int* prefix, const int* indptr, const int* wstart,
+                                              long long U, long long PW, int lane) {
   const int s = find_sequence(prefix, p.batch, (int)u);
-  const int n = indptr[s + 1] - indptr[s];
+  int f = 0, lo = 0;
+  if (wstart != nullptr) {
+    f = wstart[s] & 0xffffff;
+    lo = wstart[s] >> 24;
+  }
+  const int n = indptr[s + 1] - indptr[s] - f;
   const long long r = u - prefix[s];
   const int g = (int)(r / n);
   const int page = (int)(r - (long long)g * n);
   it.s = s;
   it.g = g;
-  it.first = indptr[s];
+  it.first = indptr[s] + f;
   it.n = n;
-  it.f = 0;
-  it.lo = 0;
+  it.f = f;
+  it.lo = lo;
   it.p0 = page;
   it.p1 = (int)min((long long)n, (long long)page + (u_end - u));
   const long long b = (long long)prefix[s] + (long long)g * n;  // first unit of the segment
-  const long long wf = first_run(b, p.units, p.part_warps);
-  const long long wl = first_run(b + n - 1, p.units, p.part_warps);
+  const long long wf = first_run(b, U, PW);
+  const long long wl = first_run(b + n - 1, U, PW);
   it.j = (int)(gw - wf);
   it.nch = (int)(wl - wf + 1);
   it.drop = false;
@@ -840,17 +847,20 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     const int n = indptr[s + 1] - indptr[s];
     return windowed ? n - (wstart[s] & 0xffffff) : n;
   };
-  if (p.balanced) {
+  if (p.balanced && !windowed) {
     for (int i = tid; i <= p.batch; i += blockDim.x) prefix[i] = p.hkv * indptr[i];
   } else {
+    // exclusive scan of the units (balanced: visible page units) or items (chunk mode) per sequence
     const int per = (p.batch + blockDim.x - 1) / blockDim.x;
     const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
     int local = 0;
-    for (int s = s0; s < s1; ++s) {
+    auto units_of = [&](int s) {
+      if (p.balanced) return p.hkv * seq_pages(s);
       int c;
       const int nch = seq_chunks(p, seq_pages(s), c);
-      local += p.hkv * (nch > 0 ? nch : 1);
-    }
+      return p.hkv * (nch > 0 ? nch : 1);
+    };
+    for (int s = s0; s < s1; ++s) local += units_of(s);
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -864,9 +874,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     int run = warp_base + incl - local;
     for (int s = s0; s < s1; ++s) {
       prefix[s] = run;
-      int c;
-      const int nch = seq_chunks(p, seq_pages(s), c);
-      run += p.hkv * (nch > 0 ? nch : 1);
+      run += units_of(s);
     }
     if (tid == blockDim.x - 1) prefix[p.batch] = run;
   }
@@ -890,15 +898,18 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   // Producer state: the item being issued (cur) and the next one, whose loads are in flight.
   const int gw = blockIdx.x * p.warps + warp;
   int w_next = gw;
+  // balanced mode: U page units in PW runs (under a window both come from the visible pages)
+  const long long U = windowed ? (long long)total : p.units;
+  const long long PW = windowed ? min((long long)W, U) : (long long)p.part_warps;
   long long u_next = 0, u_end = 0;  // balanced mode: the rest of this warp's run of page units
-  if (p.balanced && gw < p.part_warps) {
-    u_next = (long long)gw * p.units / p.part_warps;
-    u_end = (long long)(gw + 1) * p.units / p.part_warps;
+  if (p.balanced && gw < PW) {
+    u_next = (long long)gw * U / PW;
+    u_end = (long long)(gw + 1) * U / PW;
   }
   auto prepare_next = [&](Item& it) -> bool {
     if (p.balanced) {
       if (u_next >= u_end) return false;
-      prepare_piece(it, u_next, u_end, gw, p, prefix, indptr, lane);
+      prepare_piece(it, u_next, u_end, gw, p, prefix, indptr, wstart, U, PW, lane);
       u_next += it.p1 - it.p0;
     } else {
       if (w_next >= total) return false;
@@ -911,7 +922,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   Item cur, nxt;
   cur.active = false;
   nxt.active = false;
-  if (p.balanced && prefix[p.batch] != p.units) {
+  if (p.balanced && !windowed && prefix[p.batch] != p.units) {
     if (tid == 0) atomicOr(p.status, kFlagBadSequence);  // declared page total differs: nothing runs
   } else {
     prepare_next(nxt);  // index loads only: allowed before the wait

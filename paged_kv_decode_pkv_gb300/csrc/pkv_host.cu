@@ -136,6 +136,51 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
   return PKV_OK;
 }
 
+// Plan of a layer with a sliding window of `window` positions: each sequence walks its visible
+// pages (at most ceil(window / 16) + 1 of them).  Explicit split counts and chunk sizes apply to
+// them; otherwise the page-balanced partition of the visible pages (the kernel counts them), or,
+// when its split bound exceeds max_splits, chunks of about four work items per resident warp.
+pkv_status plan_windowed(const pkv_cache* c, int window, int batch, int max_pages, int num_splits, int chunk_pages,
+                         int max_splits, int* splits, int* chunk) {
+  if (batch < 0 || max_pages < 0 || num_splits < 0 || chunk_pages < 0 || max_splits < 1) return PKV_ERR_INVALID_ARG;
+  if (num_splits > 0 && chunk_pages > 0) return PKV_ERR_INVALID_ARG;
+  const int max_vis = std::max(1, std::min(max_pages, (window + PKV_PAGE_SIZE - 1) / PKV_PAGE_SIZE + 1));
+  if (num_splits > 0) {
+    if (num_splits > max_splits) return PKV_ERR_INVALID_ARG;
+    *splits = num_splits;
+    *chunk = 0;
+    return PKV_OK;
+  }
+  if (chunk_pages <= 0 && max_vis + 1 <= max_splits) {
+    // the page-balanced partition over the visible pages, whose total the kernel counts itself; a
+    // segment of n' visible pages meets at most n' + 1 runs
+    *splits = max_vis + 1;
+    *chunk = -1;
+    return PKV_OK;
+  }
+  long long cp = chunk_pages;
+  if (cp <= 0) {
+    const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, batch > 0 ? batch : 1);
+    const long long warps = (long long)c->num_sms * cfg.ctas_per_sm * cfg.warps;
+    const long long units = (long long)std::max(batch, 1) * c->desc.num_kv_heads * max_vis;
+    cp = std::max(1LL, (units + 4 * warps - 1) / (4 * warps));
+    if ((max_vis + cp - 1) / cp > max_splits) cp = (max_vis + max_splits - 1) / max_splits;
+  }
+  const long long s = (max_vis + cp - 1) / cp;
+  if (s > max_splits) return PKV_ERR_INVALID_ARG;
+  *splits = (int)s;
+  *chunk = (int)cp;
+  return PKV_OK;
+}
+
+// The plan of one layer (sliding window or not).
+pkv_status plan_layer(const pkv_cache* c, int layer, int batch, int max_pages, int total_pages, int num_splits,
+                      int chunk_pages, int max_splits, int* splits, int* chunk) {
+  const int window = c->windows[layer];
+  if (window > 0) return plan_windowed(c, window, batch, max_pages, num_splits, chunk_pages, max_splits, splits, chunk);
+  return plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, splits, chunk);
+}
+
 }  // namespace
 
 namespace pkv {
@@ -330,7 +375,17 @@ pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k
 pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,
                            int chunk_pages, int max_splits, int* splits, int* chunk_out) {
   if (c == nullptr || splits == nullptr || chunk_out == nullptr) return PKV_ERR_INVALID_ARG;
-  return plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, splits, chunk_out);
+  const pkv_status st = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, splits, chunk_out);
+  if (st != PKV_OK) return st;
+  // the split count is the most any layer produces (windowed layers plan their own chunks)
+  for (int l = 0; l < c->desc.num_layers; ++l) {
+    if (c->windows[l] <= 0) continue;
+    int s = 0, ch = 0;
+    const pkv_status sw = plan_windowed(c, c->windows[l], batch, max_pages, num_splits, chunk_pages, max_splits, &s, &ch);
+    if (sw != PKV_OK) return sw;
+    *splits = std::max(*splits, s);
+  }
+  return PKV_OK;
 }
 
 }  // extern "C"
@@ -354,23 +409,10 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
                          const FusedArgs* fused = nullptr) {
   if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return fail(PKV_ERR_INVALID_ARG, "cache or layer");
   int S = 0, chunk = 0;
-  const pkv_status ps = plan(c, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
+  const pkv_status ps =
+      plan_layer(c, layer, batch, max_pages, total_pages, num_splits, chunk_pages, max_splits, &S, &chunk);
   if (ps != PKV_OK) return fail(ps, "split plan arguments");
   const int window = c->windows[layer];
-  if (window > 0) {
-    // A windowed layer walks each sequence's visible pages, at most ceil(window / 16) + 1 of
-    // them, in chunks (the page-balanced partition counts whole sequences): per-sequence chunks
-    // for an explicit split count, else chunks no longer than those the plan gave, so the split
-    // count stays within the plan's (and within pkv_plan_decode's, the partial buffers' size).
-    const int max_vis = std::max(1, std::min(max_pages, (window + PKV_PAGE_SIZE - 1) / PKV_PAGE_SIZE + 1));
-    if (num_splits <= 0) {
-      const int c_pages = chunk > 0 ? chunk : std::max(1, (max_vis + S - 1) / S);
-      chunk = c_pages;
-      S = (max_vis + c_pages - 1) / c_pages;
-    } else {
-      chunk = 0;
-    }
-  }
   if (splits_used) *splits_used = S;
   if (batch == 0) return PKV_OK;
   if (batch > pkv::kMaxDecodeBatch) return fail(PKV_ERR_UNSUPPORTED, "batch above 4096 sequences");

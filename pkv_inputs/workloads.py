@@ -66,6 +66,8 @@ class Config:
     chunk_seqs: int = 0       # sequences that append a chunk instead of one token
     chunk_tokens: int = 0
     num_splits: int = 0       # explicit split count; 0 = the planner chooses
+    window: int = 0           # sliding window of every layer (0 = full attention)
+    sinks: bool = False       # per-layer attention-sink logits, one per query head
 
     @property
     def group(self) -> int:
@@ -86,6 +88,11 @@ CONFIGS = {
     5: Config(5, "gqa32x8_d128_b128_loguniform16_65536_chunk512", layers=1, batch=128, hq=32,
               hkv=8, head_dim=128, theta=1e6, lengths=("loguniform", 16, 65536),
               page_table="permuted", pool_pages=600000, chunk_seqs=16, chunk_tokens=512),
+    # the 32/8 x 128 attention with a 2048-token window of the Splash page's drafts, with
+    # attention sinks on every layer (its families' attn_sinks)
+    6: Config(6, "gqa32x8_d128_b32_ctx8192_window2048_sinks_8layers", layers=8, batch=32, hq=32, hkv=8,
+              head_dim=128, theta=1e6, lengths=("fixed", 8192), page_table="identity", pool_pages=16384,
+              window=2048, sinks=True),
 }
 
 
@@ -126,8 +133,10 @@ class Step:
         return int(n.max()) if n.size else 0
 
     def kv_bytes(self) -> int:
-        """Algorithmic KV bytes one decode pass reads per layer (each page once per KV head)."""
-        return int(self.seq_len.sum()) * self.cfg.hkv * self.cfg.head_dim * 2 * 2
+        """Algorithmic KV bytes one decode pass reads per layer (each attended token once per KV
+        head; under a sliding window only the window's tokens)."""
+        seen = np.minimum(self.seq_len, self.cfg.window) if self.cfg.window > 0 else self.seq_len
+        return int(seen.sum()) * self.cfg.hkv * self.cfg.head_dim * 2 * 2
 
 
 def _lengths(cfg: Config, seed: int) -> np.ndarray:
@@ -237,6 +246,15 @@ def new_qkv(step: Step, layer: int, rows=None):
                     cfg.outlier_pct).reshape(-1, hkv, d)
     v = fill_blocks(rows, hkv * d, key(s, base + TAG_V_NEW), cfg.value_scale).reshape(-1, hkv, d)
     return q, k, v
+
+
+TAG_SINKS = 7  # per layer, beside the new-token tags
+
+
+def sink_logits(step: Step, layer: int) -> np.ndarray:
+    """The layer's attention-sink logits, float32 [Hq]: seeded N(0,1) draws (fp16-representable)."""
+    bits = fill_range(step.cfg.hq, key(step.seed, layer * 16 + TAG_SINKS))
+    return bits.view(np.float16).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------------------------

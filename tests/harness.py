@@ -127,8 +127,9 @@ def query_rows(step: W.Step) -> np.ndarray:
 # oracle side
 
 
-def oracle_chain(step: W.Step, pool, q, k, v, num_splits=0, chunk_pages=0):
-    """The oracle's own append on a copy of ``pool`` followed by split attention and combine."""
+def oracle_chain(step: W.Step, pool, q, k, v, num_splits=0, chunk_pages=0, window=0, sinks=None):
+    """The oracle's own append on a copy of ``pool`` followed by split attention and combine
+    (window / sinks: the layer's sliding window and attention-sink logits)."""
     g = geometry(step)
     pool = pool.copy()
     q_out = oracle.append(g, q, k, v, step.pos_map, step.append_indptr, step.page_indptr, step.page_indices, pool)
@@ -136,18 +137,19 @@ def oracle_chain(step: W.Step, pool, q, k, v, num_splits=0, chunk_pages=0):
     res = {"pool": pool, "q_out": q_out}
     if num_splits or chunk_pages:
         po, pl = oracle.split_attention(g, pool, qd, step.page_indptr, step.page_indices, step.last_page_len,
-                                        num_splits=num_splits, chunk_pages=chunk_pages)
+                                        num_splits=num_splits, chunk_pages=chunk_pages, window=window)
         res["partial_o"], res["partial_lse"] = po, pl
-        res["out"], res["out16"], res["lse"] = oracle.combine(po, pl)
+        res["out"], res["out16"], res["lse"] = oracle.combine(po, pl, sinks=sinks)
     else:
         res["out"], res["lse"] = oracle.attention(g, pool, qd, step.page_indptr, step.page_indices,
-                                                  step.last_page_len)
+                                                  step.last_page_len, window=window, sinks=sinks)
     return res
 
 
-def oracle_attention_on(step: W.Step, pool, q_rope_rows):
+def oracle_attention_on(step: W.Step, pool, q_rope_rows, window=0, sinks=None):
     g = geometry(step)
-    return oracle.attention(g, pool, q_rope_rows, step.page_indptr, step.page_indices, step.last_page_len)
+    return oracle.attention(g, pool, q_rope_rows, step.page_indptr, step.page_indices, step.last_page_len,
+                            window=window, sinks=sinks)
 
 
 def default_scale(step: W.Step) -> float:

@@ -158,18 +158,31 @@ def test_device_generator_matches_host():
 
 
 def _full_size_check(cid, layers_to_check, seqs_fn):
+    """The workload at its full size, launched as bench.py launches it (pkv_append_decode_attention
+    per layer, programmatic dependent launch, the planner's automatic split), checked on sampled
+    sequences regenerated on the host."""
     import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
 
     cfg = W.CONFIGS[cid]
     step = W.make_step(cfg)
     tabs = H.device_tables(step)
     layers = list(range(cfg.layers))
     pools = [W.device_pool(step, l) for l in layers]
-    cache = H.make_cache(step, layers, pools)
+    sinks_host = [W.sink_logits(step, l) for l in layers] if cfg.sinks else None
+    sinks = [torch.from_numpy(x).cuda() for x in sinks_host] if cfg.sinks else None
+    cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+                      pools=pools, options=pkv.OPT_PDL, windows=[cfg.window] * cfg.layers if cfg.window else None,
+                      sinks=sinks)
+    tp = int(step.page_indptr[-1])
+    counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")
     outs = {}
     for l in layers:
         q, k, v = H.device_qkv(step, l)
-        q_out, po, pl, out, lse = H.run_chain(cache, l, tabs, q, k, v, step)
+        q_out, out, lse = cache.append_decode_attention(
+            l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"], tabs["page_indices"],
+            tabs["last_page_len"], step.max_pages_per_seq, counters, total_pages=tp)
         if l in layers_to_check:
             outs[l] = (q_out, out, lse)
     torch.cuda.synchronize()
@@ -180,9 +193,10 @@ def _full_size_check(cid, layers_to_check, seqs_fn):
     rows = W.token_rows(step, seqs)
     for l in layers_to_check:
         q_out, out, lse = outs[l]
+        sk = None if sinks_host is None else sinks_host[l].astype(np.float64)
         pool_sub = W.host_pool_pages(sub, l, np.arange(sub.num_pages))
         q, k, v = W.new_qkv(step, l, rows=rows)
-        ref = H.oracle_chain(sub, pool_sub, q, k, v)
+        ref = H.oracle_chain(sub, pool_sub, q, k, v, window=cfg.window, sinks=sk)
         origin = torch.from_numpy(sub.page_origin).cuda()
         gpu_pages = pools[l].index_select(0, origin).view(torch.int16).cpu().numpy().view(np.uint16)
         gpu_qout = q_out.view(torch.int16)[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
@@ -192,7 +206,8 @@ def _full_size_check(cid, layers_to_check, seqs_fn):
         g_lse = lse[sel].cpu().numpy()
         H.assert_close_out(g_out, ref["out"], f"config {cid} layer {l} out")
         H.assert_close_lse(g_lse, ref["lse"], f"config {cid} layer {l} lse")
-        out_i, lse_i = H.oracle_attention_on(sub, gpu_pages, gpu_qout[H.query_rows(sub)])
+        out_i, lse_i = H.oracle_attention_on(sub, gpu_pages, gpu_qout[H.query_rows(sub)], window=cfg.window,
+                                             sinks=sk)
         H.assert_close_out(g_out, out_i, f"config {cid} layer {l} out (GPU cache)")
     del pools, cache
     torch.cuda.empty_cache()
@@ -215,3 +230,7 @@ def test_full_size_mixed_serving():
         chunk = np.flatnonzero(st.new_tokens > 1)
         return sorted({int(np.argmax(st.seq_len)), int(np.argmin(st.seq_len)), int(chunk[0]), int(chunk[-1]), 5})
     _full_size_check(5, [0], pick)
+
+
+def test_full_size_sliding_window_with_sinks():
+    _full_size_check(6, [0, 7], lambda st: [0, 31])

@@ -142,3 +142,37 @@ def test_windowed_one_launch_step_is_bit_identical(name, window):
     assert np.array_equal(_bits(q_out_a), _bits(q_out_b)), "q_out"
     assert np.array_equal(_bits(out_a), _bits(out_b)), "out"
     assert np.array_equal(_bits(lse_a), _bits(lse_b)), "lse"
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_d96", "gqa4_d64", "gqa8_d128", "mha_d64_long"])
+@pytest.mark.parametrize("window", [1, 17, 100])
+def test_windowed_balanced_partials_match_oracle(name, window):
+    """The automatic plan of a windowed layer: the page-balanced partition of the visible pages,
+    every piece compared."""
+    import torch
+
+    step, host_pool, sinks_host, sinks, cache_over = _setup(name, window, True, seed_extra=13)
+    pool = H.to_dev(host_pool, torch.float16)
+    cache = cache_over(pool)
+    tabs = H.device_tables(step)
+    q, k, v = H.device_qkv(step, 0)
+    q_out = cache.append_rope(0, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                              tabs["page_indices"])
+    po, pl, S = cache.decode_attention(0, q_out, tabs["page_indptr"], tabs["page_indices"], tabs["last_page_len"],
+                                       step.max_pages_per_seq, q_indptr=tabs["q_indptr"],
+                                       total_pages=int(step.page_indptr[-1]))
+    out_c, lse_c = cache.combine(po, pl, sinks=sinks)
+    torch.cuda.synchronize()
+    assert cache.check_status() == (0, 0)
+    sms, warps = cache.device_info()
+    L = step.seq_len
+    visible = int(sum(-(-int(x) // 16) - max(0, int(x) - window) // 16 for x in L)) * step.cfg.hkv
+    gpool = _bits(pool).view(np.uint16)
+    gq = _bits(q_out).view(np.uint16)[H.query_rows(step)]
+    rpo, rpl = oracle.split_attention_balanced(H.geometry(step), gpool, gq, step.page_indptr, step.page_indices,
+                                               step.last_page_len, min(sms * warps, visible), S, window=window)
+    H.assert_close_lse(pl.cpu().numpy(), rpl, "partial_lse")
+    H.assert_close_partial_o(po.cpu().numpy(), rpo, rpl)
+    ref_out, _, ref_lse = oracle.combine(rpo, rpl, sinks=sinks_host.astype(np.float64))
+    H.assert_close_out(_bits(out_c).view(np.uint16), ref_out)
+    H.assert_close_lse(lse_c.cpu().numpy(), ref_lse)

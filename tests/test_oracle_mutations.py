@@ -23,7 +23,9 @@ MUTANTS = [
      "return (window > 0 && len > window) ? len - window + 1 : 0;"),
     ("sink weight sign", "ws = exp(sink - M);", "ws = exp(M - sink);"),
     ("sink dropped by the combine", "    if (sinks != NULL) apply_sink(o, lse + sh, d, sinks[sh % Hq]);\n", "\n"),
-    ("windowed chunk start", "      if (t0 < ws) t0 = ws;\n", "\n"),
+    ("windowed chunk start", "      if (t0 < ws) t0 = ws;\n      if (t1 > len) t1 = len;\n      if (t0 > len) t0 = len;\n      r = attend(g, pool, q, s, h / G,",
+     "      if (t1 > len) t1 = len;\n      if (t0 > len) t0 = len;\n      r = attend(g, pool, q, s, h / G,"),
+    ("windowed balanced start", "    const int64_t f = vfirst[s], ws = window_start(len, window);", "    const int64_t f = 0, ws = window_start(len, window);"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
     ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
      "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),

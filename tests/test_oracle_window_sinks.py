@@ -141,3 +141,21 @@ def test_windowed_chunks_cover_only_visible_pages():
     np.testing.assert_allclose(po[0, :, 0], ro, atol=1e-12)
     np.testing.assert_allclose(pl[0, :, 0], rl, atol=1e-12)
     assert np.all(pl[0, :, 4:] == -np.inf)      # 4 visible pages: chunks 4..6 are empty
+
+
+@pytest.mark.parametrize("window", [1, 17, 60])
+@pytest.mark.parametrize("warps", [1, 5, 40])
+def test_windowed_balanced_partition_merges_to_unsplit(window, warps):
+    rng = np.random.default_rng(38 + window + warps)
+    hq, hkv, d = 4, 2, 16
+    pool, q, pi, px, last = random_paged_case(rng, LENGTHS, hq, hkv, d)
+    g = _geom(pool, hq, hkv, d)
+    sinks = rng.standard_normal(hq)
+    ref, ref_lse = oracle.attention(g, pool, q, pi, px, last, window=window, sinks=sinks)
+    S = int(np.diff(pi).max()) + 1
+    # runs are non-empty: at most as many as visible page units (the kernel takes the same minimum)
+    visible = sum(-(-L // 16) - max(0, L - window) // 16 for L in LENGTHS) * hkv
+    po, pl = oracle.split_attention_balanced(g, pool, q, pi, px, last, min(warps, visible), S, window=window)
+    out, out16, lse = oracle.combine(po, pl, sinks=sinks)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
