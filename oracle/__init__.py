@@ -72,6 +72,8 @@ def _L():
         lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, i, P, P]
         lib.orc_combine.restype = i
         lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P, P]
+        lib.orc_qkv_project.restype = i
+        lib.orc_qkv_project.argtypes = [P, P, P, i, i, i, P]
         lib.orc_threads.restype = i
         lib.orc_threads.argtypes = []
         lib.orc_init.restype = None
@@ -145,6 +147,36 @@ def append(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, page_in
     if rc:
         raise OracleError(rc)
     return q_out
+
+
+def qkv_project(x, w_packed, scales):
+    """Q4F16_1 projection: x fp16 bits [T, hidden], w uint32 [N, hidden/8], scales fp16 bits
+    [N, hidden/32] -> y fp16 bits [T, N] (see orc_qkv_project)."""
+    x, px = _c(x, np.uint16)
+    w, pw = _c(w_packed, np.uint32)
+    sc, ps = _c(scales, np.uint16)
+    T, hidden = x.shape
+    N = w.shape[0]
+    if w.shape != (N, hidden // 8) or sc.shape != (N, hidden // 32):
+        raise ValueError("weight / scale shapes do not match the input")
+    y = np.empty((T, N), dtype=np.uint16)
+    rc = _L().orc_qkv_project(px, pw, ps, T, hidden, N, y.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return y
+
+
+def qkv_append(geom: Geometry, x, w_packed, scales, pos_map, append_indptr, page_indptr, page_indices, pool):
+    """The fused step of the pages' decode loop: the Q4F16_1 QKV projection, then RoPE and the KV
+    append.  Returns (y, q_out): y fp16 bits [T, (Hq + 2Hkv) d] (q, k, v rows), q_out as append()."""
+    y = qkv_project(x, w_packed, scales)
+    T = y.shape[0]
+    hq, hkv, d = geom.num_qo_heads, geom.num_kv_heads, geom.head_dim
+    q = y[:, :hq * d].reshape(T, hq, d)
+    k = y[:, hq * d:(hq + hkv) * d].reshape(T, hkv, d)
+    v = y[:, (hq + hkv) * d:].reshape(T, hkv, d)
+    q_out = append(geom, q, k, v, pos_map, append_indptr, page_indptr, page_indices, pool)
+    return y, q_out
 
 
 def default_scale(head_dim: int) -> float:

@@ -215,6 +215,41 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* QKV projection with Q4F16_1 weights (Zero TVM Documentation, "Q4F16 quantization format": eight
+ * int4 values per uint32, element i in bits 4i..4i+3, one fp16 scale per 32 weights, weight value
+ * f16(nibble - 7) * scale evaluated in fp16; "Decode loop": the QKV matmul feeds RoPE and the KV
+ * append in one dispatch).
+ * Readings: the weight is row-major by output feature, packed along the input:
+ *   w[n][k / 8] holds input k of output n in nibble k % 8, scales[n][k / 32];
+ * the fp16 product (nibble - 7) * scale is rounded to nearest even (an fp16 multiply), the dot
+ * product over the input is exact here (fp64), and the projection is rounded to fp16, the q, k, v
+ * rows [q heads | k heads | v heads] of width head_dim that the append then takes.
+ * x: fp16 [T][hidden]; y: fp16 [T][N]. */
+int orc_qkv_project(const uint16_t* x, const uint32_t* w, const uint16_t* scales, int T, int hidden, int N,
+                    uint16_t* y) {
+  orc_init();
+  if (T < 0 || hidden <= 0 || hidden % 32 || N <= 0) return ORC_INVALID;
+  const int words = hidden / 8, groups = hidden / 32;
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)hidden);
+    for (int k = 0; k < hidden; ++k) {
+      const uint32_t packed = w[(int64_t)n * words + k / 8];
+      const int nibble = (int)((packed >> (4 * (k % 8))) & 0xFu);
+      const double scale = dec(scales[(int64_t)n * groups + k / 32]);
+      wrow[k] = dec(orc_f64_to_f16((double)(nibble - 7) * scale));
+    }
+    for (int t = 0; t < T; ++t) {
+      double acc = 0.0;
+      for (int k = 0; k < hidden; ++k) acc += dec(x[(int64_t)t * hidden + k]) * wrow[k];
+      y[(int64_t)t * N + n] = orc_f64_to_f16(acc);
+    }
+    free(wrow);
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Attention of one query head over logical tokens [t0, t1) of sequence s.                     */
 
 static int seq_len_of(const int32_t* page_indptr, const int32_t* last_page_len, int s, int* len) {

@@ -26,6 +26,14 @@ MUTANTS = [
     ("windowed chunk start", "      if (t0 < ws) t0 = ws;\n      if (t1 > len) t1 = len;\n      if (t0 > len) t0 = len;\n      r = attend(g, pool, q, s, h / G,",
      "      if (t1 > len) t1 = len;\n      if (t0 > len) t0 = len;\n      r = attend(g, pool, q, s, h / G,"),
     ("windowed balanced start", "    const int64_t f = vfirst[s], ws = window_start(len, window);", "    const int64_t f = 0, ws = window_start(len, window);"),
+    ("int4 nibble order", "const int nibble = (int)((packed >> (4 * (k % 8))) & 0xFu);",
+     "const int nibble = (int)((packed >> (4 * (7 - k % 8))) & 0xFu);"),
+    ("int4 centering", "wrow[k] = dec(orc_f64_to_f16((double)(nibble - 7) * scale));",
+     "wrow[k] = dec(orc_f64_to_f16((double)(nibble - 8) * scale));"),
+    ("int4 product not rounded to fp16", "wrow[k] = dec(orc_f64_to_f16((double)(nibble - 7) * scale));",
+     "wrow[k] = (double)(nibble - 7) * scale;"),
+    ("int4 scale group", "const double scale = dec(scales[(int64_t)n * groups + k / 32]);",
+     "const double scale = dec(scales[(int64_t)n * groups + k / 64]);"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
     ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
      "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
@@ -53,6 +61,7 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
     env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_window_sinks.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_window_sinks.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_qkv.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"the pins did not catch the planted mistake '{name}'"
