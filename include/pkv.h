@@ -166,6 +166,34 @@ pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const voi
                            void* q_out, pkv_stream_t stream);
 
 /*
+ * QKV projection with Q4F16_1 weights, fused with RoPE and the KV append (Zero TVM Documentation,
+ * "Decode loop": the QKV matmul, RoPE and the KV append in one dispatch; "Q4F16 quantization
+ * format": eight int4 values per uint32, element i in bits 4i..4i+3, one fp16 scale per 32
+ * weights, weight value f16(nibble - 7) * scale evaluated in fp16).
+ *   x        fp16 [num_tokens][hidden] (16-byte aligned), hidden a multiple of 32, <= 4096
+ *   w        uint32 [N][hidden / 8] (16-byte aligned), N = (Hq + 2 Hkv) * head_dim output rows
+ *            ordered [q heads | k heads | v heads]; input k of row n is nibble k % 8 of
+ *            w[n][k / 8]
+ *   scales   fp16 [N][hidden / 32]
+ * For every token and output row n: y = fp16(sum_k x_k * f16((nibble - 7) * scale)), the
+ * products rounded to fp16 as the format states and summed in fp32.  The q, k and v rows of y
+ * then go through pkv_append_rope (same arguments and errors), bit for bit as if y had been
+ * written and pkv_append_rope called on it.  The weights are read before the programmatic
+ * dependent launch wait (they are not produced by the preceding kernel).
+ */
+pkv_status pkv_qkv_append_rope(pkv_cache* cache, int layer, const void* x, const uint32_t* w, const void* scales,
+                               int hidden, const int32_t* pos_map, const int32_t* append_indptr, int num_tokens,
+                               int batch, const int32_t* page_indptr, const int32_t* page_indices, void* q_out,
+                               pkv_stream_t stream);
+
+/*
+ * The projection of pkv_qkv_append_rope alone: y fp16 [num_tokens][N] (16-byte aligned), the
+ * same bits the fused call rotates and appends.  Arguments as there.
+ */
+pkv_status pkv_qkv_project(const pkv_cache* cache, const void* x, const uint32_t* w, const void* scales,
+                           int hidden, int num_tokens, void* y, pkv_stream_t stream);
+
+/*
  * Split plan (host only, no device access).  Returns in *splits the number of partial slots per
  * (sequence, query head) that pkv_decode_attention will produce for these arguments, and in
  * *chunk_pages the uniform chunk size in pages (0 when num_splits > 0 selects per-sequence

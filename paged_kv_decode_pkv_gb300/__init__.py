@@ -83,6 +83,10 @@ def lib():
         L.pkv_decode_attention_noalloc.restype = i
         L.pkv_decode_attention_noalloc.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, f, P, P,
                                                    ctypes.POINTER(i), P]
+        L.pkv_qkv_project.restype = i
+        L.pkv_qkv_project.argtypes = [P, P, P, P, i, i, P, P]
+        L.pkv_qkv_append_rope.restype = i
+        L.pkv_qkv_append_rope.argtypes = [P, i, P, P, P, i, P, P, i, i, P, P, P, P]
         L.pkv_combine.restype = i
         L.pkv_combine.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
         L.pkv_check_status.restype = i
@@ -336,6 +340,32 @@ class Cache:
         _check(lib().pkv_combine(self.handle, _ptr(partial_o), _ptr(partial_lse), _ptr(sinks), B, Hq, S, d,
                                  _ptr(out), _ptr(lse), _stream(stream)), "pkv_combine")
         return out, lse
+
+    def qkv_project(self, x, w, scales, y=None, stream=None):
+        """pkv_qkv_project: x fp16 [T, hidden], w int32/uint32 [N, hidden/8], scales fp16
+        [N, hidden/32] -> y fp16 [T, N]."""
+        import torch
+
+        T, hidden = (int(v) for v in x.shape)
+        if y is None:
+            y = torch.empty((T, int(w.shape[0])), dtype=torch.float16, device=x.device)
+        _check(lib().pkv_qkv_project(self.handle, _ptr(x), _ptr(w), _ptr(scales), hidden, T, _ptr(y),
+                                     _stream(stream)), "pkv_qkv_project")
+        return y
+
+    def qkv_append_rope(self, layer, x, w, scales, pos_map, append_indptr, page_indptr, page_indices,
+                        q_out=None, stream=None):
+        """pkv_qkv_append_rope: the Q4F16_1 projection of x, then RoPE and the append; returns q_out."""
+        import torch
+
+        T, hidden = (int(v) for v in x.shape)
+        B = int(append_indptr.numel()) - 1
+        if q_out is None:
+            q_out = torch.empty((T, self.num_qo_heads, self.head_dim), dtype=torch.float16, device=x.device)
+        _check(lib().pkv_qkv_append_rope(self.handle, layer, _ptr(x), _ptr(w), _ptr(scales), hidden, _ptr(pos_map),
+                                         _ptr(append_indptr), T, B, _ptr(page_indptr), _ptr(page_indices),
+                                         _ptr(q_out), _stream(stream)), "pkv_qkv_append_rope")
+        return q_out
 
     def check_status(self, stream=None):
         """pkv_check_status; returns (status code, flag bits) without raising."""

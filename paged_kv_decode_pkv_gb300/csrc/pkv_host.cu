@@ -295,6 +295,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   const DecodeConfig cfg = pkv::decode_config(group, D, 1);
   e = pkv::decode_prepare(cfg, D);
   if (e == cudaSuccess) e = pkv::decode_prepare(pkv::decode_config(group, D, 1, true), D);
+  if (e == cudaSuccess) e = pkv::qkv_prepare();
   if (e == cudaSuccess) e = pkv::append_prepare();
   if (e == cudaSuccess) e = pkv::combine_prepare();
   if (e != cudaSuccess) {
@@ -370,6 +371,69 @@ pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k
   p.max_position = c->desc.max_position;
   p.num_pages = c->desc.num_pages;
   return launch_status("append_rope launch", pkv::launch_append(p, stream, c->pdl));
+}
+
+namespace {
+
+// Shared checks and parameters of the QKV entry points.
+pkv_status qkv_params(const pkv_cache* c, const void* x, const uint32_t* w, const void* scales, int hidden,
+                      int num_tokens, pkv::QkvParams* p) {
+  if (c == nullptr || num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "null cache or negative num_tokens");
+  if (hidden <= 0 || hidden % 32 || hidden > pkv::kQkvMaxHidden)
+    return fail(PKV_ERR_UNSUPPORTED, "hidden must be a positive multiple of 32, at most 4096");
+  if (num_tokens > 0 && (x == nullptr || w == nullptr || scales == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(scales, 2)) return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  *p = pkv::QkvParams{};
+  p->x = static_cast<const __half*>(x);
+  p->w = w;
+  p->scales = static_cast<const __half*>(scales);
+  p->num_tokens = num_tokens;
+  p->hidden = hidden;
+  p->hq = c->desc.num_qo_heads;
+  p->hkv = c->desc.num_kv_heads;
+  p->head_dim = c->desc.head_dim;
+  p->max_position = c->desc.max_position;
+  p->num_pages = c->desc.num_pages;
+  p->rope = reinterpret_cast<const float2*>(c->desc.rope_table);
+  p->status = c->desc.status_word;
+  return PKV_OK;
+}
+
+}  // namespace
+
+pkv_status pkv_qkv_append_rope(pkv_cache* c, int layer, const void* x, const uint32_t* w, const void* scales,
+                               int hidden, const int32_t* pos_map, const int32_t* append_indptr, int num_tokens,
+                               int batch, const int32_t* page_indptr, const int32_t* page_indices, void* q_out,
+                               pkv_stream_t stream) {
+  pkv::QkvParams p;
+  const pkv_status st = qkv_params(c, x, w, scales, hidden, num_tokens, &p);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= c->desc.num_layers || batch < 0) return fail(PKV_ERR_INVALID_ARG, "layer or batch");
+  if (num_tokens == 0 || batch == 0) return PKV_OK;
+  if (pos_map == nullptr || append_indptr == nullptr || page_indptr == nullptr || page_indices == nullptr ||
+      q_out == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q_out, 16)) return fail(PKV_ERR_INVALID_ARG, "misaligned q_out");
+  p.pos_map = pos_map;
+  p.append_indptr = append_indptr;
+  p.page_indptr = page_indptr;
+  p.page_indices = page_indices;
+  p.batch = batch;
+  p.q_out = static_cast<__half*>(q_out);
+  p.pool = static_cast<__half*>(c->pools[layer]);
+  return launch_status("qkv launch", pkv::launch_qkv(p, stream, c->pdl));
+}
+
+pkv_status pkv_qkv_project(const pkv_cache* c, const void* x, const uint32_t* w, const void* scales, int hidden,
+                           int num_tokens, void* y, pkv_stream_t stream) {
+  pkv::QkvParams p;
+  const pkv_status st = qkv_params(c, x, w, scales, hidden, num_tokens, &p);
+  if (st != PKV_OK) return st;
+  if (num_tokens == 0) return PKV_OK;
+  if (y == nullptr || !aligned(y, 16)) return fail(PKV_ERR_INVALID_ARG, "null or misaligned y");
+  p.y_out = static_cast<__half*>(y);
+  return launch_status("qkv launch", pkv::launch_qkv(p, stream, c->pdl));
 }
 
 pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,

@@ -36,6 +36,25 @@ struct AppendParams {
   int num_tokens, batch, hq, hkv, head_dim, max_position, num_pages;
 };
 
+// QKV projection (Q4F16_1) fused with RoPE and the KV append.
+struct QkvParams {
+  const __half* x;           // [num_tokens][hidden]
+  const uint32_t* w;         // [N][hidden / 8], N = (hq + 2 hkv) * head_dim
+  const __half* scales;      // [N][hidden / 32]
+  __half* y_out;             // nullable: write the projection [num_tokens][N] instead of appending
+  const int* pos_map;
+  const int* append_indptr;
+  const int* page_indptr;
+  const int* page_indices;
+  __half* q_out;
+  __half* pool;              // null with y_out
+  const float2* rope;
+  int* status;
+  int num_tokens, batch, hidden, hq, hkv, head_dim, max_position, num_pages;
+};
+constexpr int kQkvMaxHidden = 4096;          // four input parts of 1024 (x two row halves = 8 warps)
+constexpr int kQkvMaxSmem = 2 * kQkvMaxHidden * 2 + 4 * 2 * 16 * 4;
+
 struct DecodeParams {
   const __half* q;
   const int* q_indptr;  // nullable
@@ -110,6 +129,8 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const D
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl);
 cudaError_t append_prepare();   // function attributes (shared-memory carveout)
 cudaError_t combine_prepare();
+cudaError_t qkv_prepare();
+cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 
 }  // namespace pkv

@@ -1,0 +1,287 @@
+// QKV projection with Q4F16_1 weights, fused with RoPE and the KV append (Zero TVM
+// Documentation, "Decode loop": the QKV matmul, RoPE and the KV-append in one dispatch; "Q4F16
+// quantization format": eight int4 values per uint32, element i in bits 4i..4i+3, one fp16 scale
+// per 32 weights, weight value f16(nibble - 7) * scale evaluated in fp16).
+//
+// Weights are row-major by output feature and packed along the input: w[n][k / 8] holds input k
+// of output n in nibble k % 8, scales[n][k / 32].  Output rows are [q heads | k heads | v heads],
+// head_dim rows each.
+//
+// Work decomposition.  A CTA owns 16 output rows of one head, the rope pairs 8b + i and
+// head_dim/2 + 8b + i (i < 8), so it can rotate what it computes.  Its warps split the rows in
+// two halves of 8 and the input into parts of 1024 (a lane takes 32 consecutive inputs: one
+// 16-byte weight load and one scale per row); every lane loads its 8 rows' weights up front.  Per
+// word the eight nibbles become four half2 pairs {i, i+4} with mask-and-or (1024 + nibble as an
+// fp16), an exact subtraction of 1031 and an fp16 multiply by the scale (the format's fp16
+// product, rounded to nearest); the input is stored in shared memory in the same pair order and
+// the products accumulate in fp32.  The warps' partial sums are reduced in a fixed order, rounded
+// to fp16 (the projection's value), rotated with the append kernel's arithmetic and written: q
+// rows to q_out, k and v rows into the pool.  Tokens are processed two at a time.
+#include "pkv_internal.h"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTok = 2;        // tokens per pass
+constexpr int kPartIn = 1024;  // inputs per warp (32 lanes x 32)
+
+struct QkvSlot {
+  long long k_off;  // pool element offset of [page][0][0][slot][0]; -1 = skip the token
+  int pos;
+};
+
+// fp16 pairs {x, y} as one 32-bit word
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// acc += a.lo * b.lo + a.hi * b.hi (fp16 operands, fp32 accumulation)
+__device__ __forceinline__ float fma2(uint32_t a, uint32_t b, float acc) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(acc) : "r"(a), "r"(b));
+  return acc;
+}
+
+// Weights of the eight nibbles of `word` as four fp16 pairs {j, j+4}: f16(nibble - 7) * scale.
+__device__ __forceinline__ void dequant_word(uint32_t word, __half2 scale2, uint32_t (&wp)[4]) {
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6407));  // 1031
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t bits = ((word >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // {1024 + n_j, 1024 + n_j+4}
+    __half2 h = *reinterpret_cast<const __half2*>(&bits);
+    h = __hsub2(h, bias);        // exact: nibble - 7
+    h = __hmul2(h, scale2);      // the fp16 product, rounded to nearest
+    wp[j] = h2u(h);
+  }
+}
+
+// Sum of acc[r][t] over the 32 lanes for the 8 rows r at once: each exchange halves the rows a
+// lane keeps (lane bit 4 keeps rows 4..7, bit 3 the upper half of those, bit 2 the upper one),
+// so lane l ends with row (l >> 2) & 7; 9 shuffles instead of 40.
+__device__ __forceinline__ float reduce8(const float (&acc)[8][kTok], int t, int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float v4[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+    v4[a] = (b4 ? acc[a + 4][t] : acc[a][t]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[a][t] : acc[a + 4][t], 16);
+  float v2[2];
+#pragma unroll
+  for (int a = 0; a < 2; ++a) v2[a] = (b3 ? v4[a + 2] : v4[a]) + __shfl_xor_sync(0xffffffffu, b3 ? v4[a] : v4[a + 2], 8);
+  float v1 = (b2 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? v2[0] : v2[1], 4);
+  v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+  return v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __half* xs = reinterpret_cast<__half*>(smem);                       // [kTok][hidden], pair order
+  float* red = reinterpret_cast<float*>(smem + (size_t)kTok * p.hidden * 2);  // [parts][kTok][16]
+  __shared__ QkvSlot slots[kTok];
+  pdl_launch_dependents();
+
+  const int lane = threadIdx.x & 31;
+  const int parts = blockDim.x >> 6;                 // warps per row half
+  const int half = (threadIdx.x >> 5) / parts;       // 0: rows 8b + i, 1: rows D/2 + 8b + i
+  const int warp = (threadIdx.x >> 5) - half * parts;  // input part
+  const int blocks_per_head = D / 16;
+  const int hh = blockIdx.x / blocks_per_head;  // head among q, k, v heads
+  const int b = blockIdx.x - hh * blocks_per_head;
+  const int N = (p.hq + 2 * p.hkv) * D;
+  const int words = p.hidden / 8, groups = p.hidden / 32;
+  const int group = warp * 32 + lane;  // this lane's 32 inputs
+  const bool active = group < groups;
+
+  // this warp's rows: hh * D + half * D/2 + 8b + r, r < 8
+  const long long row0 = (long long)hh * D + half * (D / 2) + 8 * b;
+
+  // weights and scales of the 8 rows: inputs of the weights, no wait needed
+  uint4 wv[8];
+  __half2 sc2[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const long long row = row0 + r;
+    if (active) {
+      wv[r] = *reinterpret_cast<const uint4*>(p.w + row * words + group * 4);
+      sc2[r] = __half2half2(p.scales[row * groups + group]);
+    } else {
+      wv[r] = make_uint4(0, 0, 0, 0);
+      sc2[r] = __float2half2_rn(0.f);
+    }
+  }
+  pdl_wait();  // the input rows and the pool may come from the preceding kernel
+
+  for (int t0 = 0; t0 < p.num_tokens; t0 += kTok) {
+    const int nt = min(kTok, p.num_tokens - t0);
+    // the tokens' input rows, each word's eight values stored as the pairs {j, j+4}
+    for (int i = threadIdx.x; i < nt * words; i += blockDim.x) {
+      const int t = i / words, m = i - t * words;
+      const uint4 v = *reinterpret_cast<const uint4*>(p.x + (long long)(t0 + t) * p.hidden + 8 * m);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};  // pairs (0,1), (2,3), (4,5), (6,7)
+      uint4 o;
+      o.x = __byte_perm(e[0], e[2], 0x5410);  // {x0, x4}
+      o.y = __byte_perm(e[0], e[2], 0x7632);  // {x1, x5}
+      o.z = __byte_perm(e[1], e[3], 0x5410);  // {x2, x6}
+      o.w = __byte_perm(e[1], e[3], 0x7632);  // {x3, x7}
+      *reinterpret_cast<uint4*>(xs + (size_t)t * p.hidden + 8 * m) = o;
+    }
+    if (threadIdx.x < kTok) {
+      // token -> sequence -> page slot (the append kernel's checks)
+      const int t = t0 + threadIdx.x;
+      QkvSlot ts{-1, 0};
+      if (threadIdx.x < nt && p.pool != nullptr) {
+        int lo = 0, hi = p.batch;
+        if (p.append_indptr[0] <= t && t < p.append_indptr[p.batch]) {
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.append_indptr[mid] <= t) lo = mid; else hi = mid;
+          }
+          const int pos = p.pos_map[t];
+          const int first = p.page_indptr[lo];
+          const int n_pages = p.page_indptr[lo + 1] - first;
+          if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
+            atomicOr(p.status, kFlagBadPosition);
+          } else {
+            const int page = p.page_indices[first + (pos >> 4)];
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.status, kFlagBadPage);
+            } else {
+              ts.k_off = ((long long)page * 2 * p.hkv * kPageSize + (pos & 15)) * D;
+              ts.pos = pos;
+            }
+          }
+        } else {
+          atomicOr(p.status, kFlagBadSequence);
+        }
+      }
+      slots[threadIdx.x] = ts;
+    }
+    __syncthreads();
+
+    // partial sums: acc[r][t] over this lane's 32 inputs, then over the warp
+    float acc[8][kTok];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) acc[r][t] = 0.f;
+    if (active) {
+      // the lane's 32 inputs of each token (four words' worth, in pair order)
+      uint4 xw[kTok][4];
+#pragma unroll
+      for (int t = 0; t < kTok; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          xw[t][q] = t < nt ? *reinterpret_cast<const uint4*>(xs + (size_t)t * p.hidden + 32 * group + 8 * q)
+                            : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t word = q == 0 ? wv[r].x : q == 1 ? wv[r].y : q == 2 ? wv[r].z : wv[r].w;
+          uint32_t wp[4];
+          dequant_word(word, sc2[r], wp);
+#pragma unroll
+          for (int t = 0; t < kTok; ++t) {
+            float a = acc[r][t];
+            a = fma2(wp[0], xw[t][q].x, a);
+            a = fma2(wp[1], xw[t][q].y, a);
+            a = fma2(wp[2], xw[t][q].z, a);
+            a = fma2(wp[3], xw[t][q].w, a);
+            acc[r][t] = a;
+          }
+        }
+      }
+    }
+    // transposing butterfly: after it lanes 4r .. 4r + 3 hold row r summed over the warp
+#pragma unroll
+    for (int t = 0; t < kTok; ++t) {
+      if (t < nt) {
+        const float sum = reduce8(acc, t, lane);
+        if ((lane & 3) == 0) red[(warp * kTok + t) * 16 + 8 * half + ((lane >> 2) & 7)] = sum;
+      }
+    }
+    __syncthreads();
+
+    // the projection (fp16), then RoPE and the append for the CTA's rows
+    for (int i = threadIdx.x; i < nt * 8; i += blockDim.x) {
+      const int t = i >> 3, r = i & 7;
+      float ylo = 0.f, yhi = 0.f;
+      for (int w = 0; w < parts; ++w) {
+        ylo += red[(w * kTok + t) * 16 + r];
+        yhi += red[(w * kTok + t) * 16 + 8 + r];
+      }
+      const __half hlo = __float2half_rn(ylo), hhi = __float2half_rn(yhi);
+      const int e = 8 * b + r;  // element of the head's first half
+      const long long tok = t0 + t;
+      if (p.y_out != nullptr) {
+        p.y_out[tok * N + hh * D + e] = hlo;
+        p.y_out[tok * N + hh * D + D / 2 + e] = hhi;
+        continue;
+      }
+      const QkvSlot ts = slots[t];
+      if (ts.k_off < 0) continue;
+      __half olo = hlo, ohi = hhi;
+      if (hh < p.hq + p.hkv) {
+        // rotate-half RoPE of the pair (e, e + D/2) at the token's position
+        float ra, rb;
+        rope_pair(__half2float(hlo), __half2float(hhi), p.rope[(long long)ts.pos * (D / 2) + e], ra, rb);
+        olo = __float2half_rn(ra);
+        ohi = __float2half_rn(rb);
+      }
+      __half* dst;
+      if (hh < p.hq) {
+        dst = p.q_out + (tok * p.hq + hh) * D;
+      } else if (hh < p.hq + p.hkv) {
+        dst = p.pool + ts.k_off + (long long)(hh - p.hq) * kPageSize * D;  // K block of head hh - hq
+      } else {
+        dst = p.pool + ts.k_off + (long long)(hh - p.hq) * kPageSize * D;  // V block: (hkv + g) blocks in
+      }
+      dst[e] = olo;
+      dst[D / 2 + e] = ohi;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t qkv_prepare() {
+  const void* k[] = {(const void*)&qkv_append_kernel<64>, (const void*)&qkv_append_kernel<96>,
+                     (const void*)&qkv_append_kernel<128>};
+  for (const void* f : k) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvMaxSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+size_t qkv_smem_bytes(int hidden, int parts) {
+  return (size_t)kTok * hidden * 2 + (size_t)parts * kTok * 16 * sizeof(float);
+}
+
+cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl) {
+  if (p.num_tokens <= 0) return cudaSuccess;
+  const int parts = (p.hidden + kPartIn - 1) / kPartIn;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.hq + 2 * p.hkv) * (p.head_dim / 16)));
+  cfg.blockDim = dim3(64 * parts);
+  cfg.dynamicSmemBytes = qkv_smem_bytes(p.hidden, parts);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (p.head_dim) {
+    case 64: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<64>, p);
+    case 96: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<96>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<128>, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

@@ -9,6 +9,12 @@
 
 namespace pkv {
 
+// One rotation pair: a = x_i, b = x_{i+d/2}, (c, s) = (cos, sin) of element i at the position.
+__device__ __forceinline__ void rope_pair(float a, float b, float2 cs, float& out_a, float& out_b) {
+  out_a = __fmaf_rn(a, cs.x, -__fmul_rn(b, cs.y));
+  out_b = __fmaf_rn(b, cs.x, __fmul_rn(a, cs.y));
+}
+
 // lo: elements i..i+7 of a head row, hi: elements i+d/2..i+d/2+7, cs: the (cos, sin) pairs of
 // elements i..i+7 at the token's position.  Evaluated in fp32 with fused multiply-adds and
 // rounded once to fp16:
@@ -24,10 +30,9 @@ __device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const fl
     const float2 xa = __half22float2(a[e]);
     const float2 xb = __half22float2(b[e]);
     const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];  // (cos, sin) of elements 2e and 2e+1
-    const float lo0 = __fmaf_rn(xa.x, c0.x, -__fmul_rn(xb.x, c0.y));
-    const float lo1 = __fmaf_rn(xa.y, c1.x, -__fmul_rn(xb.y, c1.y));
-    const float hi0 = __fmaf_rn(xb.x, c0.x, __fmul_rn(xa.x, c0.y));
-    const float hi1 = __fmaf_rn(xb.y, c1.x, __fmul_rn(xa.y, c1.y));
+    float lo0, lo1, hi0, hi1;
+    rope_pair(xa.x, xb.x, c0, lo0, hi0);
+    rope_pair(xa.y, xb.y, c1, lo1, hi1);
     ya[e] = __floats2half2_rn(lo0, lo1);
     yb[e] = __floats2half2_rn(hi0, hi1);
   }

@@ -249,6 +249,30 @@ def new_qkv(step: Step, layer: int, rows=None):
 
 
 TAG_SINKS = 7  # per layer, beside the new-token tags
+TAG_QKV_W, TAG_QKV_SCALE, TAG_HIDDEN = 8, 9, 10
+
+
+def qkv_hidden(cfg: Config) -> int:
+    """Hidden width feeding the QKV projection: Hq * head_dim (the Phi-3 shape: 3072)."""
+    return cfg.hq * cfg.head_dim
+
+
+def qkv_weights(step: Step, layer: int):
+    """Q4F16_1 weights of the layer's QKV projection: packed uint32 [N, hidden/8] (uniform random
+    nibbles) and fp16 scale bits [N, hidden/32] (seeded N(0,1) x 0.003)."""
+    cfg = step.cfg
+    hidden = qkv_hidden(cfg)
+    n = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
+    w = (words(key(step.seed, layer * 16 + TAG_QKV_W), n * hidden // 8) & 0xFFFFFFFF).astype(np.uint32)
+    sc = fill_range(n * (hidden // 32), key(step.seed, layer * 16 + TAG_QKV_SCALE), scale=0.003)
+    return w.reshape(n, hidden // 8), sc.reshape(n, hidden // 32)
+
+
+def hidden_states(step: Step, layer: int, rows=None):
+    """The new tokens' inputs of the QKV projection, fp16 bits [T, hidden] (seeded N(0,1))."""
+    hidden = qkv_hidden(step.cfg)
+    rows = np.arange(step.num_tokens, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    return fill_blocks(rows, hidden, key(step.seed, layer * 16 + TAG_HIDDEN))
 
 
 def sink_logits(step: Step, layer: int) -> np.ndarray:
