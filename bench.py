@@ -275,6 +275,70 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------------
 
 
+def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages, stream,
+                time_graph, dev):
+    """The Q4F16_1 QKV projection fused with RoPE and the KV append (pkv_qkv_append_rope), one
+    launch per layer in a CUDA graph, each layer with its own weights; and the same followed by
+    the merged decode (the attention segment of the pages' decode loop).  Weight bytes per layer:
+    packed nibbles, fp16 scales and the inputs; HBM-bound."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    hidden = W.qkv_hidden(cfg)
+    if hidden > 4096 or hidden % 32:
+        return None
+    ws = []
+    for l in layers:
+        w, sc = W.qkv_weights(step, l)
+        x = W.hidden_states(step, l)
+        ws.append((torch.from_numpy(x).view(torch.float16).to(dev), torch.from_numpy(w.view(np.int32)).to(dev),
+                   torch.from_numpy(sc).view(torch.float16).to(dev)))
+    use_q_indptr = int(step.new_tokens.max()) > 1
+
+    def proj_step():
+        for l in layers:
+            x, w, sc = ws[l]
+            cache.qkv_append_rope(l, x, w, sc, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                                  tabs["page_indices"], q_out=q_out[l])
+
+    def proj_decode_step():
+        for l in layers:
+            x, w, sc = ws[l]
+            cache.qkv_append_rope(l, x, w, sc, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                                  tabs["page_indices"], q_out=q_out[l])
+            cache.decode_attention_merged(l, q_out[l], tabs["page_indptr"], tabs["page_indices"],
+                                          tabs["last_page_len"], step.max_pages_per_seq, counters,
+                                          q_indptr=tabs["append_indptr"] if use_q_indptr else None,
+                                          total_pages=total_pages, partial_o=po, partial_lse=pl, out=outs[l],
+                                          lse=lses[l])
+
+    with torch.cuda.stream(stream):
+        proj_decode_step()
+    torch.cuda.synchronize()
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after the projection: {pkv.status_string(code)} flags {flags:#x}")
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        proj_step()
+    with torch.cuda.graph(g2, stream=stream):
+        proj_decode_step()
+    torch.cuda.synchronize()
+    proj_ms = time_graph(g1)
+    both_ms = time_graph(g2)
+    n_rows = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
+    wbytes = n_rows * hidden // 2 + n_rows * (hidden // 32) * 2 + step.num_tokens * hidden * 2
+    peak, _ = measured_peaks()
+    per_layer_us = proj_ms * 1e3 / cfg.layers
+    gbs = wbytes * cfg.layers / (proj_ms * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "bytes_per_layer": wbytes, "us_per_layer": per_layer_us,
+            "roofline_frac": gbs / peak, "hidden": hidden, "rows": n_rows,
+            "step": "per layer: pkv_qkv_append_rope (Q4F16_1 projection + RoPE + append, one launch)",
+            "with_decode_us_per_layer": both_ms * 1e3 / cfg.layers,
+            "with_decode": "per layer: pkv_qkv_append_rope + pkv_decode_attention_merged"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -518,6 +582,10 @@ def run_ours(args):
         barrier()
         return max_over_ranks((time.perf_counter() - t0) / args.steps)
 
+    # ---- the pages' fused QKV dispatch: Q4F16_1 projection + RoPE + append, then the decode -----
+    qkv_proj = qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages,
+                           stream, time_graph, dev)
+
     e2e_s = timed_e2e(e2e_graph.replay)
     e2e_eager_s = timed_e2e(e2e_step)
     code, flags = cache.check_status(stream)
@@ -560,6 +628,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "mode": "CUDA graph of the API calls",
                 "eager_value": world * kv_step / e2e_eager_s / 1e9, "eager_ms_per_step": e2e_eager_s * 1e3},
         "gpu_launches": args.steps * cfg.layers * (1 if one_launch else 2),
+        "qkv_projection": qkv_proj,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

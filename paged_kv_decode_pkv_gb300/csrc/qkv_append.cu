@@ -16,7 +16,9 @@
 // product, rounded to nearest); the input is stored in shared memory in the same pair order and
 // the products accumulate in fp32.  The warps' partial sums are reduced in a fixed order, rounded
 // to fp16 (the projection's value), rotated with the append kernel's arithmetic and written: q
-// rows to q_out, k and v rows into the pool.  Tokens are processed two at a time.
+// rows to q_out, k and v rows into the pool.  Tokens are processed two at a time (one: a kernel
+// specialised for a single token).  The token slots are looked up before the programmatic
+// dependent launch wait (page tables and positions are not produced by the preceding kernel).
 #include "pkv_internal.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -24,7 +26,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kTok = 2;        // tokens per pass
+constexpr int kTokMax = 2;     // tokens per pass of the multi-token kernel (1 for a single token)
 constexpr int kPartIn = 1024;  // inputs per warp (32 lanes x 32)
 
 struct QkvSlot {
@@ -32,8 +34,6 @@ struct QkvSlot {
   int pos;
 };
 
-// fp16 pairs {x, y} as one 32-bit word
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // acc += a.lo * b.lo + a.hi * b.hi (fp16 operands, fp32 accumulation)
 __device__ __forceinline__ float fma2(uint32_t a, uint32_t b, float acc) {
@@ -45,21 +45,24 @@ __device__ __forceinline__ float fma2(uint32_t a, uint32_t b, float acc) {
 }
 
 // Weights of the eight nibbles of `word` as four fp16 pairs {j, j+4}: f16(nibble - 7) * scale.
-__device__ __forceinline__ void dequant_word(uint32_t word, __half2 scale2, uint32_t (&wp)[4]) {
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6407));  // 1031
+// (word >> 4j) & 0x000F000F | 0x64006400 is the fp16 pair {1024 + n_j, 1024 + n_j+4}; subtracting
+// 1031 is exact, the multiply by the scale pair is the format's fp16 product, rounded to nearest.
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t scale2, uint32_t (&wp)[4]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t bits = ((word >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // {1024 + n_j, 1024 + n_j+4}
-    __half2 h = *reinterpret_cast<const __half2*>(&bits);
-    h = __hsub2(h, bias);        // exact: nibble - 7
-    h = __hmul2(h, scale2);      // the fp16 product, rounded to nearest
-    wp[j] = h2u(h);
+    asm("{\n\t.reg .b32 t;\n\t"
+        "lop3.b32 t, %1, 0x000F000F, 0x64006400, 0xEA;\n\t"
+        "sub.rn.f16x2 t, t, %2;\n\t"
+        "mul.rn.f16x2 %0, t, %3;\n\t}"
+        : "=r"(wp[j])
+        : "r"(word >> (4 * j)), "r"(0x64076407u), "r"(scale2));
   }
 }
 
 // Sum of acc[r][t] over the 32 lanes for the 8 rows r at once: each exchange halves the rows a
 // lane keeps (lane bit 4 keeps rows 4..7, bit 3 the upper half of those, bit 2 the upper one),
 // so lane l ends with row (l >> 2) & 7; 9 shuffles instead of 40.
+template <int kTok>
 __device__ __forceinline__ float reduce8(const float (&acc)[8][kTok], int t, int lane) {
   const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
   float v4[4];
@@ -74,12 +77,13 @@ __device__ __forceinline__ float reduce8(const float (&acc)[8][kTok], int t, int
   return v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
+template <int D, int kTok>
+__global__ void __launch_bounds__(256, kTok == 1 ? 3 : 2) qkv_append_kernel(QkvParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   __half* xs = reinterpret_cast<__half*>(smem);                       // [kTok][hidden], pair order
   float* red = reinterpret_cast<float*>(smem + (size_t)kTok * p.hidden * 2);  // [parts][kTok][16]
-  __shared__ QkvSlot slots[kTok];
+  __shared__ QkvSlot slots[kTokMax];
+  __shared__ float2 cs[kTokMax][8];  // (cos, sin) of elements 8b .. 8b + 7 at each token's position
   pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31;
@@ -99,18 +103,52 @@ __global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
 
   // weights and scales of the 8 rows: inputs of the weights, no wait needed
   uint4 wv[8];
-  __half2 sc2[8];
+  uint32_t sc2[8];  // the row's scale as an fp16 pair
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const long long row = row0 + r;
     if (active) {
       wv[r] = *reinterpret_cast<const uint4*>(p.w + row * words + group * 4);
-      sc2[r] = __half2half2(p.scales[row * groups + group]);
+      const uint32_t h = __half_as_ushort(p.scales[row * groups + group]);
+      sc2[r] = h | (h << 16);
     } else {
       wv[r] = make_uint4(0, 0, 0, 0);
-      sc2[r] = __float2half2_rn(0.f);
+      sc2[r] = 0u;
     }
   }
+  // token t -> sequence -> page slot, into slots[i] (the append kernel's checks)
+  auto lookup_slot = [&](int t, int i) {
+    QkvSlot ts{-1, 0};
+    if (t < p.num_tokens && p.pool != nullptr) {
+      int lo = 0, hi = p.batch;
+      if (p.append_indptr[0] <= t && t < p.append_indptr[p.batch]) {
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.append_indptr[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int pos = p.pos_map[t];
+        const int first = p.page_indptr[lo];
+        const int n_pages = p.page_indptr[lo + 1] - first;
+        if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
+          atomicOr(p.status, kFlagBadPosition);
+        } else {
+          const int page = p.page_indices[first + (pos >> 4)];
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.status, kFlagBadPage);
+          } else {
+            ts.k_off = ((long long)page * 2 * p.hkv * kPageSize + (pos & 15)) * D;
+            ts.pos = pos;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cs[i][e] = p.rope[(long long)pos * (D / 2) + 8 * b + e];
+          }
+        }
+      } else {
+        atomicOr(p.status, kFlagBadSequence);
+      }
+    }
+    slots[i] = ts;
+  };
+  if (threadIdx.x < kTok) lookup_slot(threadIdx.x, threadIdx.x);  // the first tokens, before the wait
   pdl_wait();  // the input rows and the pool may come from the preceding kernel
 
   for (int t0 = 0; t0 < p.num_tokens; t0 += kTok) {
@@ -127,37 +165,7 @@ __global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
       o.w = __byte_perm(e[1], e[3], 0x7632);  // {x3, x7}
       *reinterpret_cast<uint4*>(xs + (size_t)t * p.hidden + 8 * m) = o;
     }
-    if (threadIdx.x < kTok) {
-      // token -> sequence -> page slot (the append kernel's checks)
-      const int t = t0 + threadIdx.x;
-      QkvSlot ts{-1, 0};
-      if (threadIdx.x < nt && p.pool != nullptr) {
-        int lo = 0, hi = p.batch;
-        if (p.append_indptr[0] <= t && t < p.append_indptr[p.batch]) {
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.append_indptr[mid] <= t) lo = mid; else hi = mid;
-          }
-          const int pos = p.pos_map[t];
-          const int first = p.page_indptr[lo];
-          const int n_pages = p.page_indptr[lo + 1] - first;
-          if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
-            atomicOr(p.status, kFlagBadPosition);
-          } else {
-            const int page = p.page_indices[first + (pos >> 4)];
-            if (page < 0 || page >= p.num_pages) {
-              atomicOr(p.status, kFlagBadPage);
-            } else {
-              ts.k_off = ((long long)page * 2 * p.hkv * kPageSize + (pos & 15)) * D;
-              ts.pos = pos;
-            }
-          }
-        } else {
-          atomicOr(p.status, kFlagBadSequence);
-        }
-      }
-      slots[threadIdx.x] = ts;
-    }
+    if (t0 > 0 && threadIdx.x < kTok) lookup_slot(t0 + threadIdx.x, threadIdx.x);
     __syncthreads();
 
     // partial sums: acc[r][t] over this lane's 32 inputs, then over the warp
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
 #pragma unroll
     for (int t = 0; t < kTok; ++t) {
       if (t < nt) {
-        const float sum = reduce8(acc, t, lane);
+        const float sum = reduce8<kTok>(acc, t, lane);
         if ((lane & 3) == 0) red[(warp * kTok + t) * 16 + 8 * half + ((lane >> 2) & 7)] = sum;
       }
     }
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
       if (hh < p.hq + p.hkv) {
         // rotate-half RoPE of the pair (e, e + D/2) at the token's position
         float ra, rb;
-        rope_pair(__half2float(hlo), __half2float(hhi), p.rope[(long long)ts.pos * (D / 2) + e], ra, rb);
+        rope_pair(__half2float(hlo), __half2float(hhi), cs[t][r], ra, rb);
         olo = __float2half_rn(ra);
         ohi = __float2half_rn(rb);
       }
@@ -248,8 +256,9 @@ __global__ void __launch_bounds__(256) qkv_append_kernel(QkvParams p) {
 }  // namespace
 
 cudaError_t qkv_prepare() {
-  const void* k[] = {(const void*)&qkv_append_kernel<64>, (const void*)&qkv_append_kernel<96>,
-                     (const void*)&qkv_append_kernel<128>};
+  const void* k[] = {(const void*)&qkv_append_kernel<64, 1>, (const void*)&qkv_append_kernel<96, 1>,
+                     (const void*)&qkv_append_kernel<128, 1>, (const void*)&qkv_append_kernel<64, kTokMax>,
+                     (const void*)&qkv_append_kernel<96, kTokMax>, (const void*)&qkv_append_kernel<128, kTokMax>};
   for (const void* f : k) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvMaxSmem);
     if (e != cudaSuccess) return e;
@@ -259,8 +268,8 @@ cudaError_t qkv_prepare() {
   return cudaSuccess;
 }
 
-size_t qkv_smem_bytes(int hidden, int parts) {
-  return (size_t)kTok * hidden * 2 + (size_t)parts * kTok * 16 * sizeof(float);
+size_t qkv_smem_bytes(int hidden, int parts, int tok) {
+  return (size_t)tok * hidden * 2 + (size_t)parts * tok * 16 * sizeof(float);
 }
 
 cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl) {
@@ -269,7 +278,8 @@ cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.hq + 2 * p.hkv) * (p.head_dim / 16)));
   cfg.blockDim = dim3(64 * parts);
-  cfg.dynamicSmemBytes = qkv_smem_bytes(p.hidden, parts);
+  const bool one = p.num_tokens == 1;
+  cfg.dynamicSmemBytes = qkv_smem_bytes(p.hidden, parts, one ? 1 : kTokMax);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -277,9 +287,12 @@ cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   switch (p.head_dim) {
-    case 64: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<64>, p);
-    case 96: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<96>, p);
-    case 128: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<128>, p);
+    case 64: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<64, 1>, p)
+                        : cudaLaunchKernelEx(&cfg, qkv_append_kernel<64, kTokMax>, p);
+    case 96: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<96, 1>, p)
+                        : cudaLaunchKernelEx(&cfg, qkv_append_kernel<96, kTokMax>, p);
+    case 128: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<128, 1>, p)
+                         : cudaLaunchKernelEx(&cfg, qkv_append_kernel<128, kTokMax>, p);
     default: return cudaErrorInvalidValue;
   }
 }
