@@ -72,6 +72,8 @@ def _L():
         lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, i, P, P]
         lib.orc_combine.restype = i
         lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P, P]
+        lib.orc_prefill_attention.restype = i
+        lib.orc_prefill_attention.argtypes = [P, P, P, i, i, P, P, P, P, P, d, i, P, P, P]
         lib.orc_qkv_project.restype = i
         lib.orc_qkv_project.argtypes = [P, P, P, i, i, i, P]
         lib.orc_threads.restype = i
@@ -208,6 +210,30 @@ def attention(geom: Geometry, pool, q_rope, page_indptr, page_indices, last_page
     sk, psk = _sinks(sinks, geom.num_qo_heads)
     rc = _L().orc_attention(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, float(sm_scale), int(window), psk,
                             out.ctypes.data, lse.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return out, lse
+
+
+def prefill_attention(geom: Geometry, pool, q_rope, append_indptr, pos_map, page_indptr, page_indices,
+                      last_page_len, sm_scale=None, window: int = 0, sinks=None):
+    """Chunked-prefill attention: every token t (rows of q_rope [T, Hq, d]) attends causally to the
+    positions <= pos_map[t] of its sequence.  Returns out float64 [T, Hq, d], lse float64 [T, Hq]."""
+    sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
+    pool, pp = _c(pool, np.uint16)
+    q, pq = _c(q_rope, np.uint16)
+    ai, pai = _c(append_indptr, np.int32)
+    pm, ppm = _c(pos_map, np.int32)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    lp, plp = _c(last_page_len, np.int32)
+    T, B = q.shape[0], ai.size - 1
+    out = np.empty((T, geom.num_qo_heads, geom.head_dim), dtype=np.float64)
+    lse = np.empty((T, geom.num_qo_heads), dtype=np.float64)
+    g = geom.c()
+    sk, psk = _sinks(sinks, geom.num_qo_heads)
+    rc = _L().orc_prefill_attention(ctypes.byref(g), pp, pq, T, B, pai, ppm, ppi, ppx, plp, float(sm_scale),
+                                    int(window), psk, out.ctypes.data, lse.ctypes.data)
     if rc:
         raise OracleError(rc)
     return out, lse

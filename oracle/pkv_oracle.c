@@ -351,6 +351,60 @@ int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rop
   return rc;
 }
 
+/* Chunked-prefill attention (the step after the append when a sequence appends several tokens:
+ * SURVEY's NEXT-1; Zero TVM Documentation, "Decode loop": a token attends to itself and to every
+ * earlier position of its sequence).  Token t of sequence s (append_indptr) at position
+ * p = pos_map[t] attends to the positions [window_start(p + 1, W), p] of s, the cache after the
+ * append holding them; sinks as in orc_attention.  q_rope: [T][Hq][d] fp16 bits; out: [T][Hq][d];
+ * lse: [T][Hq].  A position outside [0, len_s) is rejected. */
+int orc_prefill_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rope, int T, int B,
+                          const int32_t* append_indptr, const int32_t* pos_map, const int32_t* page_indptr,
+                          const int32_t* page_indices, const int32_t* last_page_len, double sm_scale,
+                          int window, const double* sinks, double* out, double* lse) {
+  orc_init();
+  const int d = g->head_dim, Hq = g->num_qo_heads, Hkv = g->num_kv_heads;
+  if (d <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || B < 0 || T < 0) return ORC_INVALID;
+  if (append_indptr[0] != 0 || append_indptr[B] != T) return ORC_INVALID;
+  const int G = Hq / Hkv;
+  int* seq_of = (int*)malloc(sizeof(int) * (size_t)(T > 0 ? T : 1));
+  for (int s = 0; s < B; ++s) {
+    if (append_indptr[s + 1] < append_indptr[s]) {
+      free(seq_of);
+      return ORC_INVALID;
+    }
+    int len;
+    if (seq_len_of(page_indptr, last_page_len, s, &len) != ORC_OK) {
+      free(seq_of);
+      return ORC_OUT_OF_RANGE;
+    }
+    for (int t = append_indptr[s]; t < append_indptr[s + 1]; ++t) {
+      if (pos_map[t] < 0 || pos_map[t] >= len) {
+        free(seq_of);
+        return ORC_OUT_OF_RANGE;
+      }
+      seq_of[t] = s;
+    }
+  }
+  int rc = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t th = 0; th < (int64_t)T * Hq; ++th) {
+    const int t = (int)(th / Hq), h = (int)(th % Hq);
+    const int s = seq_of[t], p = pos_map[t];
+    double* q = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) q[i] = dec(q_rope[th * d + i]);
+    int r = attend(g, pool, q, s, h / G, window_start(p + 1, window), p + 1, page_indptr, page_indices, sm_scale,
+                   out + th * d, lse + th);
+    if (r == ORC_OK && sinks != NULL) apply_sink(out + th * d, lse + th, d, sinks[h]);
+    free(q);
+    if (r != ORC_OK) {
+#pragma omp critical
+      rc = r;
+    }
+  }
+  free(seq_of);
+  return rc;
+}
+
 /* Split-K partial attention.  Under a window W the visible pages of sequence s are
  * [f_s, n_s) with f_s = floor(window_start / 16), n'_s = n_s - f_s of them; without one f_s = 0.
  * Chunk size in pages: chunk_pages if > 0 (uniform), otherwise ceil(n'_s / num_splits).  Chunk j

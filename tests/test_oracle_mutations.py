@@ -34,6 +34,7 @@ MUTANTS = [
      "wrow[k] = (double)(nibble - 7) * scale;"),
     ("int4 scale group", "const double scale = dec(scales[(int64_t)n * groups + k / 32]);",
      "const double scale = dec(scales[(int64_t)n * groups + k / 64]);"),
+    ("prefill not causal", "window_start(p + 1, window), p + 1, page_indptr,", "window_start(p + 1, window), p + 2, page_indptr,"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
     ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
      "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
@@ -62,6 +63,7 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_window_sinks.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_qkv.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_qkv.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_prefill.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"the pins did not catch the planted mistake '{name}'"
