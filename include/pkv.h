@@ -166,6 +166,27 @@ pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const voi
                            void* q_out, pkv_stream_t stream);
 
 /*
+ * Chunked-prefill attention (the step after a multi-token append: every appended token attends
+ * causally to its sequence; Zero TVM Documentation, "Decode loop": a token attends to itself and
+ * to the earlier positions of its sequence).  Token t of sequence s (append_indptr), at position
+ * p = pos_map[t] < len_s, attends to the positions [max(0, p + 1 - W), p] of s (W = the layer's
+ * window, 0 = all) in the cache after the append; the layer's sinks join the denominator:
+ *   out[t][h][:] = fp16( sum_u e^{s_u} V_u / (sum_u e^{s_u} + e^{sink_h}) ),
+ *   lse_out[t][h] = ln(sum_u e^{s_u} + e^{sink_h}),   s_u = sm_scale * q_t,h . K_u.
+ *   q_rope   fp16 [num_tokens][Hq][head_dim] (e.g. q_out of pkv_append_rope), 16-byte aligned
+ *   out      fp16 [num_tokens][Hq][head_dim], 16-byte aligned;  lse_out fp32 [num_tokens][Hq] or NULL
+ * Tiles of (sequence, KV head, 16 / G tokens) run mma.sync over the pages the tile attends to.
+ * Device-detected errors: page ids out of range, positions outside [0, len_s), bad
+ * last_page_len (the token's rows are left unwritten).  With one token per sequence at its last
+ * position this equals the merged decode up to rounding.
+ */
+pkv_status pkv_prefill_attention(const pkv_cache* cache, int layer, const void* q_rope,
+                                 const int32_t* append_indptr, const int32_t* pos_map, int num_tokens,
+                                 const int32_t* page_indptr, const int32_t* page_indices,
+                                 const int32_t* last_page_len, int batch, float sm_scale, void* out,
+                                 float* lse_out, pkv_stream_t stream);
+
+/*
  * QKV projection with Q4F16_1 weights, fused with RoPE and the KV append (Zero TVM Documentation,
  * "Decode loop": the QKV matmul, RoPE and the KV append in one dispatch; "Q4F16 quantization
  * format": eight int4 values per uint32, element i in bits 4i..4i+3, one fp16 scale per 32

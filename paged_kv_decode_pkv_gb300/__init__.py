@@ -83,6 +83,8 @@ def lib():
         L.pkv_decode_attention_noalloc.restype = i
         L.pkv_decode_attention_noalloc.argtypes = [P, i, P, P, P, P, P, i, i, i, i, i, f, P, P,
                                                    ctypes.POINTER(i), P]
+        L.pkv_prefill_attention.restype = i
+        L.pkv_prefill_attention.argtypes = [P, i, P, P, P, i, P, P, P, i, ctypes.c_float, P, P, P]
         L.pkv_qkv_project.restype = i
         L.pkv_qkv_project.argtypes = [P, P, P, P, i, i, P, P]
         L.pkv_qkv_append_rope.restype = i
@@ -339,6 +341,23 @@ class Cache:
             lse = torch.empty((B, Hq), dtype=torch.float32, device=partial_o.device)
         _check(lib().pkv_combine(self.handle, _ptr(partial_o), _ptr(partial_lse), _ptr(sinks), B, Hq, S, d,
                                  _ptr(out), _ptr(lse), _stream(stream)), "pkv_combine")
+        return out, lse
+
+    def prefill_attention(self, layer, q_rope, append_indptr, pos_map, page_indptr, page_indices, last_page_len,
+                          sm_scale=0.0, out=None, lse=None, stream=None):
+        """pkv_prefill_attention: every appended token attends causally; returns (out, lse)."""
+        import torch
+
+        T = int(q_rope.shape[0])
+        B = int(append_indptr.numel()) - 1
+        if out is None:
+            out = torch.empty((T, self.num_qo_heads, self.head_dim), dtype=torch.float16, device=q_rope.device)
+        if lse is None:
+            lse = torch.empty((T, self.num_qo_heads), dtype=torch.float32, device=q_rope.device)
+        _check(lib().pkv_prefill_attention(self.handle, layer, _ptr(q_rope), _ptr(append_indptr), _ptr(pos_map), T,
+                                           _ptr(page_indptr), _ptr(page_indices), _ptr(last_page_len), B,
+                                           float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)),
+               "pkv_prefill_attention")
         return out, lse
 
     def qkv_project(self, x, w, scales, y=None, stream=None):

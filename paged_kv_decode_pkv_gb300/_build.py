@@ -10,7 +10,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_host.cu", "append_rope.cu", "decode_partial.cu", "combine.cu", "decode_noalloc.cu", "qkv_append.cu"]
+SOURCES = ["pkv_host.cu", "append_rope.cu", "decode_partial.cu", "combine.cu", "decode_noalloc.cu", "qkv_append.cu", "prefill.cu"]
 ARCH = "103a"
 
 

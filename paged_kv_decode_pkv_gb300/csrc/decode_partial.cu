@@ -75,8 +75,6 @@ constexpr int kSmemBudget = 232448 - 256;
 // Shared memory of one SM, and the CTAs per SM the decode grid prefers.
 constexpr int kSmemPerSm = 233472;
 constexpr int kCtasPerSm = 2;
-// CUDA-core path: copy a page's K and V blocks with two plain bulk copies instead of one tensor copy.
-constexpr bool kPlainBulkPages = true;
 
 // Alignment of the shared-memory base: 1024 bytes for the swizzled boxes of the tensor-core path,
 // 128 bytes for the plain boxes of the CUDA-core path.
@@ -1018,14 +1016,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         for (int u = 0; u < D / E; ++u)
           tma_load_4d_if(l0 && page_ok, dst + u * GroupMma<D>::REGION, &map, &bar[k], u * E, 0, cur.g, 2 * pid,
                          policy);
-      } else if constexpr (kPlainBulkPages) {
+      } else {
         // the page's K block and V block of this KV head are each contiguous in the pool
         const __half* kb = p.pool + (((long long)pid * 2 * p.hkv + cur.g) * kPageSize) * D;
         bulk_load_hint_if(l0 && page_ok, dst, kb, page_bytes / 2, &bar[k], policy);
         bulk_load_hint_if(l0 && page_ok, dst + page_bytes / 2, kb + (long long)p.hkv * kPageSize * D, page_bytes / 2,
                           &bar[k], policy);
-      } else {
-        tma_load_4d_if(l0 && page_ok, dst, &map, &bar[k], 0, 0, cur.g, 2 * pid, policy);
       }
       ++cur.pnext;
       if (lastp) cur.active = false;
@@ -1322,13 +1318,10 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
   const int nstage = c.nstage;
   c.smem_bytes =
       nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused, windowed).total : 0;
-  if (c.mma) {
-    c.box_inner = head_dim == 96 ? 32 : 64;
-    c.swizzle_bytes = head_dim == 96 ? 64 : 128;
-  } else {
-    c.box_inner = head_dim;
-    c.swizzle_bytes = 0;
-  }
+  // The pool's tensor map always has the swizzled boxes the tensor-core layouts read (the
+  // CUDA-core path copies plain runs instead; the prefill kernel uses the map for every group).
+  c.box_inner = head_dim == 96 ? 32 : 64;
+  c.swizzle_bytes = head_dim == 96 ? 64 : 128;
   return c;
 }
 

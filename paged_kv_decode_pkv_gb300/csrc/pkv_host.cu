@@ -296,6 +296,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   e = pkv::decode_prepare(cfg, D);
   if (e == cudaSuccess) e = pkv::decode_prepare(pkv::decode_config(group, D, 1, true), D);
   if (e == cudaSuccess) e = pkv::qkv_prepare();
+  if (e == cudaSuccess) e = pkv::prefill_prepare();
   if (e == cudaSuccess) e = pkv::append_prepare();
   if (e == cudaSuccess) e = pkv::combine_prepare();
   if (e != cudaSuccess) {
@@ -434,6 +435,48 @@ pkv_status pkv_qkv_project(const pkv_cache* c, const void* x, const uint32_t* w,
   if (y == nullptr || !aligned(y, 16)) return fail(PKV_ERR_INVALID_ARG, "null or misaligned y");
   p.y_out = static_cast<__half*>(y);
   return launch_status("qkv launch", pkv::launch_qkv(p, stream, c->pdl));
+}
+
+pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_rope, const int32_t* append_indptr,
+                                 const int32_t* pos_map, int num_tokens, const int32_t* page_indptr,
+                                 const int32_t* page_indices, const int32_t* last_page_len, int batch,
+                                 float sm_scale, void* out, float* lse_out, pkv_stream_t stream) {
+  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers || num_tokens < 0 || batch < 0)
+    return fail(PKV_ERR_INVALID_ARG, "cache, layer or sizes");
+  if (num_tokens == 0 || batch == 0) return PKV_OK;
+  if (batch > pkv::kMaxDecodeBatch) return fail(PKV_ERR_UNSUPPORTED, "batch above 4096 sequences");
+  if (q_rope == nullptr || append_indptr == nullptr || pos_map == nullptr || page_indptr == nullptr ||
+      page_indices == nullptr || last_page_len == nullptr || out == nullptr)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q_rope, 16) || !aligned(out, 16)) return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(PKV_ERR_INVALID_ARG, "sm_scale");
+  const int D = c->desc.head_dim;
+  const pkv::PrefillConfig cfg = pkv::prefill_config(D, batch);
+  if (cfg.nstage < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this batch");
+  pkv::PrefillParams p{};
+  p.q = static_cast<const __half*>(q_rope);
+  p.append_indptr = append_indptr;
+  p.pos_map = pos_map;
+  p.page_indptr = page_indptr;
+  p.page_indices = page_indices;
+  p.last_page_len = last_page_len;
+  p.out = static_cast<__half*>(out);
+  p.lse = lse_out;
+  p.status = c->desc.status_word;
+  p.sinks = c->sinks[layer];
+  p.batch = batch;
+  p.num_tokens = num_tokens;
+  p.hq = c->desc.num_qo_heads;
+  p.hkv = c->desc.num_kv_heads;
+  p.group = c->group;
+  p.num_pages = c->desc.num_pages;
+  p.tpt = 16 / c->group;
+  p.window = c->windows[layer];
+  p.nstage = cfg.nstage;
+  const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const int grid = c->num_sms * 2;
+  return launch_status("prefill launch", pkv::launch_prefill(p, c->maps[layer], cfg, D, grid, stream, c->pdl));
 }
 
 pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,

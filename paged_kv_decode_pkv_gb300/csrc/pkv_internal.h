@@ -55,6 +55,34 @@ struct QkvParams {
 constexpr int kQkvMaxHidden = 4096;          // four input parts of 1024 (x two row halves = 8 warps)
 constexpr int kQkvMaxSmem = 2 * kQkvMaxHidden * 2 + 4 * 2 * 16 * 4;
 
+// Chunked-prefill attention: every appended token attends causally over its sequence's pages.
+struct PrefillParams {
+  const __half* q;  // [num_tokens][hq][head_dim], rotated
+  const int* append_indptr;
+  const int* pos_map;
+  const int* page_indptr;
+  const int* page_indices;
+  const int* last_page_len;
+  __half* out;      // [num_tokens][hq][head_dim]
+  float* lse;       // [num_tokens][hq], nullable
+  int* status;
+  const float* sinks;  // nullable, per query head
+  int batch, num_tokens, hq, hkv, group, num_pages;
+  int tpt;          // tokens per tile: 16 / group
+  int window;       // 0 = full attention
+  int nstage;
+  float scale_log2;
+};
+constexpr int kPrefillWarps = 4;
+struct PrefillConfig {
+  int nstage;
+  size_t smem_bytes;
+};
+PrefillConfig prefill_config(int head_dim, int batch);
+cudaError_t prefill_prepare();
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& map, const PrefillConfig& cfg, int head_dim,
+                           int grid, cudaStream_t stream, bool pdl);
+
 struct DecodeParams {
   const __half* q;
   const int* q_indptr;  // nullable
