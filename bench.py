@@ -275,6 +275,47 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------------
 
 
+def prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, dev):
+    """Chunked-prefill attention of every appended token (pkv_prefill_attention), one launch per
+    layer in a CUDA graph, on workloads whose sequences append several tokens.  Tensor-bound at
+    long contexts: flops = 4 * Hq * head_dim * sum over tokens of the positions each attends to."""
+    import torch
+
+    if int(step.new_tokens.max()) <= 1:
+        return None
+    T = step.num_tokens
+    outs = [torch.empty((T, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
+    lses = [torch.empty((T, cfg.hq), dtype=torch.float32, device=dev) for _ in layers]
+
+    def run():
+        for l in layers:
+            cache.prefill_attention(l, q_out[l], tabs["append_indptr"], tabs["pos_map"], tabs["page_indptr"],
+                                    tabs["page_indices"], tabs["last_page_len"], out=outs[l], lse=lses[l])
+
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    torch.cuda.synchronize()
+    ms = time_graph(g)
+    seen = step.pos_map.astype(np.int64) + 1
+    if cfg.window:
+        seen = np.minimum(seen, cfg.window)
+    flops = 4.0 * cfg.hq * cfg.head_dim * float(seen.sum())
+    tflops = flops * cfg.layers / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        peak, kind = 1900.0, "fallback"
+    return {"value": tflops, "unit": "TFLOP/s", "bound": "tensor", "peak": peak, "frac": tflops / peak,
+            "peak_source": kind + "; fp16 mma runs at the bf16 rate", "us_per_layer": ms * 1e3 / cfg.layers,
+            "flops_per_layer": flops, "tokens": T,
+            "step": "per layer: pkv_prefill_attention (every appended token, causal; mma.sync m16n8k16)"}
+
+
 def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages, stream,
                 time_graph, dev):
     """The Q4F16_1 QKV projection fused with RoPE and the KV append (pkv_qkv_append_rope), one
@@ -583,6 +624,7 @@ def run_ours(args):
         return max_over_ranks((time.perf_counter() - t0) / args.steps)
 
     # ---- the pages' fused QKV dispatch: Q4F16_1 projection + RoPE + append, then the decode -----
+    prefill = prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, dev)
     qkv_proj = qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages,
                            stream, time_graph, dev)
 
@@ -629,6 +671,7 @@ def run_ours(args):
                 "eager_value": world * kv_step / e2e_eager_s / 1e9, "eager_ms_per_step": e2e_eager_s * 1e3},
         "gpu_launches": args.steps * cfg.layers * (1 if one_launch else 2),
         "qkv_projection": qkv_proj,
+        **({"prefill": prefill} if prefill is not None else {}),
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
