@@ -283,14 +283,25 @@ def prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, d
 
     if int(step.new_tokens.max()) <= 1:
         return None
-    T = step.num_tokens
+    # the sequences that appended a chunk (the others are decode steps, served by the decode kernel)
+    seqs = np.flatnonzero(step.new_tokens > 1)
+    ai = np.concatenate([[0], np.cumsum(step.new_tokens[seqs])]).astype(np.int32)
+    rows = np.concatenate([np.arange(step.append_indptr[s], step.append_indptr[s + 1]) for s in seqs])
+    pi = np.concatenate([[0], np.cumsum(np.diff(step.page_indptr)[seqs])]).astype(np.int32)
+    px = np.concatenate([step.page_indices[step.page_indptr[s]:step.page_indptr[s + 1]] for s in seqs])
+    sub = {"append_indptr": ai, "pos_map": step.pos_map[rows], "page_indptr": pi, "page_indices": px,
+           "last_page_len": step.last_page_len[seqs]}
+    sub = {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.int32)).to(dev) for k, v in sub.items()}
+    rows_d = torch.from_numpy(rows.astype(np.int64)).to(dev)
+    qs = [q_out[l].index_select(0, rows_d) for l in layers]
+    T = int(rows.size)
     outs = [torch.empty((T, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
     lses = [torch.empty((T, cfg.hq), dtype=torch.float32, device=dev) for _ in layers]
 
     def run():
         for l in layers:
-            cache.prefill_attention(l, q_out[l], tabs["append_indptr"], tabs["pos_map"], tabs["page_indptr"],
-                                    tabs["page_indices"], tabs["last_page_len"], out=outs[l], lse=lses[l])
+            cache.prefill_attention(l, qs[l], sub["append_indptr"], sub["pos_map"], sub["page_indptr"],
+                                    sub["page_indices"], sub["last_page_len"], out=outs[l], lse=lses[l])
 
     with torch.cuda.stream(stream):
         run()
@@ -300,7 +311,7 @@ def prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, d
         run()
     torch.cuda.synchronize()
     ms = time_graph(g)
-    seen = step.pos_map.astype(np.int64) + 1
+    seen = step.pos_map[rows].astype(np.int64) + 1
     if cfg.window:
         seen = np.minimum(seen, cfg.window)
     flops = 4.0 * cfg.hq * cfg.head_dim * float(seen.sum())
@@ -312,8 +323,9 @@ def prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, d
         peak, kind = 1900.0, "fallback"
     return {"value": tflops, "unit": "TFLOP/s", "bound": "tensor", "peak": peak, "frac": tflops / peak,
             "peak_source": kind + "; fp16 mma runs at the bf16 rate", "us_per_layer": ms * 1e3 / cfg.layers,
-            "flops_per_layer": flops, "tokens": T,
-            "step": "per layer: pkv_prefill_attention (every appended token, causal; mma.sync m16n8k16)"}
+            "flops_per_layer": flops, "tokens": T, "sequences": int(seqs.size),
+            "step": "per layer: pkv_prefill_attention over the sequences that appended a chunk (every chunk "
+                    "token, causal; mma.sync m16n8k16)"}
 
 
 def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages, stream,

@@ -475,7 +475,7 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
   p.nstage = cfg.nstage;
   const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  const int grid = c->num_sms * 2;
+  const int grid = c->num_sms;
   return launch_status("prefill launch", pkv::launch_prefill(p, c->maps[layer], cfg, D, grid, stream, c->pdl));
 }
 

@@ -73,7 +73,7 @@ struct PrefillParams {
   int nstage;
   float scale_log2;
 };
-constexpr int kPrefillWarps = 4;
+constexpr int kPrefillWarps = 8;  // consumer warps per CTA (plus one producer warp)
 struct PrefillConfig {
   int nstage;
   size_t smem_bytes;

@@ -55,32 +55,43 @@ __device__ __forceinline__ int find_seq(const int* prefix, int batch, int w) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __grid_constant__ CUtensorMap map,
-                                                                     PrefillParams p) {
+__global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const __grid_constant__ CUtensorMap map,
+                                                                           PrefillParams p) {
   using Gm = PfGeom<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nst = p.nstage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)kPrefillWarps * nst * Gm::STAGE);
-  int* prefix = reinterpret_cast<int*>(bars + kPrefillWarps * nst);
-  __shared__ int warp_sums[kPrefillWarps];
+  unsigned char* stages = base;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)nst * Gm::STAGE);
+  uint64_t* empty = full + nst;
+  int* prefix = reinterpret_cast<int*>(empty + nst);
+  __shared__ int warp_sums[kPrefillWarps + 1];
+  __shared__ int abort_flag;
 
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) prefetch_tensormap(&map);
-  for (int i = tid; i < kPrefillWarps * nst; i += blockDim.x) mbar_init(&bars[i], 1);
+  const bool producer = warp == kPrefillWarps;
+  if (tid == 0) {
+    prefetch_tensormap(&map);
+    abort_flag = 0;
+  }
+  for (int i = tid; i < nst; i += blockDim.x) {
+    mbar_init(&full[i], 1);
+    mbar_init(&empty[i], kPrefillWarps);
+  }
   fence_mbarrier_init();
 
-  // tiles of each sequence (Hkv x ceil(tokens / tpt)) and their exclusive prefix
+  // tasks of each sequence (Hkv x blocks of kPrefillWarps tiles of tpt tokens) and their prefix
+  const int block_tokens = kPrefillWarps * p.tpt;
   {
     const int per = (p.batch + blockDim.x - 1) / blockDim.x;
     const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
-    auto tiles_of = [&](int s) {
+    auto tasks_of = [&](int s) {
       const int c = p.append_indptr[s + 1] - p.append_indptr[s];
-      return c > 0 ? p.hkv * ((c + p.tpt - 1) / p.tpt) : 0;
+      return c > 0 ? p.hkv * ((c + block_tokens - 1) / block_tokens) : 0;
     };
     int local = 0;
-    for (int s = s0; s < s1; ++s) local += tiles_of(s);
+    for (int s = s0; s < s1; ++s) local += tasks_of(s);
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -93,40 +104,88 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
     for (int w = 0; w < warp; ++w) run += warp_sums[w];
     for (int s = s0; s < s1; ++s) {
       prefix[s] = run;
-      run += tiles_of(s);
+      run += tasks_of(s);
     }
     if (tid == blockDim.x - 1) prefix[p.batch] = run;
   }
   __syncthreads();
   const int total = prefix[p.batch];
-  const int W = gridDim.x * kPrefillWarps;
-  const int gw = blockIdx.x * kPrefillWarps + warp;
 
-  uint64_t* bar = bars + warp * nst;
-  unsigned char* stages = base + (size_t)warp * nst * Gm::STAGE;
-  const uint64_t policy = l2_policy_evict_first();
+  // the tiles of one (sequence, KV head) run side by side and read the same pages: keep them in L2
+  const uint64_t policy = l2_policy_evict_last();
   const int G = p.group;
   const int c2 = 2 * (lane & 3);
-  int seq = 0;  // pages consumed by this warp so far (ring slot and phase)
-  bool timed_out = false;
+  int seq = 0;  // pages the CTA has streamed so far (ring slot and phases)
 
   pdl_wait();  // q and the pool (the append) come from the preceding kernel
 
-  for (int w = gw; w < total && !timed_out; w += W) {
-    const int s = find_seq(prefix, p.batch, w);
+  for (int task = blockIdx.x; task < total; task += gridDim.x) {
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+    const int s = find_seq(prefix, p.batch, task);
     const int a0 = p.append_indptr[s], cnt = p.append_indptr[s + 1] - a0;
-    const int per_head = (cnt + p.tpt - 1) / p.tpt;
-    const int r = w - prefix[s];
+    const int per_head = (cnt + block_tokens - 1) / block_tokens;
+    const int r = task - prefix[s];
     const int g = r / per_head;
-    const int tok0 = a0 + (r - g * per_head) * p.tpt;
+    const int tb0 = a0 + (r - g * per_head) * block_tokens;  // first token of the block
+    const int nb_tok = min(block_tokens, a0 + cnt - tb0);
     const int first = p.page_indptr[s];
     const int n = p.page_indptr[s + 1] - first;
     const int last = n > 0 ? p.last_page_len[s] : 0;
     const bool seq_ok = n > 0 && last >= 1 && last <= kPageSize;
     const int len = seq_ok ? (n - 1) * kPageSize + last : 0;
-    if (!seq_ok && lane == 0 && r == 0) atomicOr(p.status, kFlagBadSequence);
+    if (!seq_ok && tid == 0 && r == 0) atomicOr(p.status, kFlagBadSequence);
 
-    // the lane's two rows: rho0 = lane / 4 and rho0 + 8
+    // the block's page range (every warp computes it from the block's positions)
+    int pmin = 0x7fffffff, pmax = -1;
+    for (int t = lane; t < nb_tok; t += 32) {
+      const int pos = seq_ok ? p.pos_map[tb0 + t] : -1;
+      if (pos >= 0 && pos < len) {
+        const int st = (p.window > 0 && pos + 1 > p.window) ? pos + 1 - p.window : 0;
+        pmin = min(pmin, st >> 4);
+        pmax = max(pmax, pos >> 4);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      pmin = min(pmin, __shfl_xor_sync(kAll, pmin, off));
+      pmax = max(pmax, __shfl_xor_sync(kAll, pmax, off));
+    }
+    if (pmax < 0) continue;  // no valid token (reported below by the rows)
+    const int np = pmax - pmin + 1;
+
+    if (producer) {
+      // ---- the CTA's producer: page copies into the shared ring ----
+      int win_base = 0;
+      int window_ids = lane < np ? p.page_indices[first + pmin + lane] : 0;
+      for (int i = 0; i < np; ++i) {
+        if (i - win_base >= 32) {
+          win_base = i & ~31;
+          window_ids = win_base + lane < np ? p.page_indices[first + pmin + win_base + lane] : 0;
+        }
+        const int pid = __shfl_sync(kAll, window_ids, i - win_base);
+        const int f = seq + i, slot = f % nst;
+        if (f >= nst && !mbar_wait_bounded(&empty[slot], (uint32_t)(((f / nst) - 1) & 1), kWaitLimitNs)) {
+          if (lane == 0) {
+            atomicOr(p.status, kFlagTimeout);
+            abort_flag = 1;
+          }
+          break;
+        }
+        const bool ok = pid >= 0 && pid < p.num_pages;
+        if (!ok && lane == 0) atomicOr(p.status, kFlagBadPage);
+        mbar_arrive_expect_tx_if(lane == 0 && ok, &full[slot], (uint32_t)Gm::STAGE);
+        mbar_arrive_if(lane == 0 && !ok, &full[slot]);
+        unsigned char* dst = stages + (size_t)slot * Gm::STAGE;
+#pragma unroll
+        for (int u = 0; u < D / Gm::E; ++u)
+          tma_load_4d_if(lane == 0 && ok, dst + u * Gm::REGION, &map, &full[slot], u * Gm::E, 0, g, 2 * pid, policy);
+      }
+      seq += np;
+      continue;
+    }
+
+    // ---- consumer warp: 16 rows = tokens tok0 .. tok0 + tpt - 1 of the block x the group's heads ----
+    const int tok0 = tb0 + warp * p.tpt;
     int tok[2], head[2], pos[2], start[2];
     bool valid[2];
 #pragma unroll
@@ -143,23 +202,23 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
       }
       start[i] = (p.window > 0 && pos[i] + 1 > p.window) ? pos[i] + 1 - p.window : 0;
     }
-    // the tile's page range
-    int pmin = 0x7fffffff, pmax = -1;
+    // the warp's own last page (nothing to compute after it), and the positions every valid row
+    // attends to (pages inside [full_lo, full_hi] need no mask)
+    int wmax = -1, full_lo = 0, full_hi = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       if (valid[i]) {
-        pmin = min(pmin, start[i] >> 4);
-        pmax = max(pmax, pos[i] >> 4);
+        wmax = max(wmax, pos[i] >> 4);
+        full_lo = max(full_lo, start[i]);
+        full_hi = min(full_hi, pos[i]);
       }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      pmin = min(pmin, __shfl_xor_sync(kAll, pmin, off));
-      pmax = max(pmax, __shfl_xor_sync(kAll, pmax, off));
+      wmax = max(wmax, __shfl_xor_sync(kAll, wmax, off));
+      full_lo = max(full_lo, __shfl_xor_sync(kAll, full_lo, off));
+      full_hi = min(full_hi, __shfl_xor_sync(kAll, full_hi, off));
     }
-    if (pmax < 0) continue;  // no valid row
-    const int np = pmax - pmin + 1;
 
-    // query fragments of the 16 rows (A operand: rows rho0 and rho0 + 8)
     uint32_t qa[Gm::KS][4];
 #pragma unroll
     for (int ks = 0; ks < Gm::KS; ++ks) {
@@ -175,60 +234,27 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
     for (int nb = 0; nb < Gm::NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
-    // page ids, 32 at a time
-    int win_base = 0;
-    int window_ids = lane < np ? p.page_indices[first + pmin + lane] : 0;
-    auto page_id = [&](int i) {  // all lanes; i non-decreasing
-      if (i - win_base >= 32) {
-        win_base = i & ~31;
-        window_ids = win_base + lane < np ? p.page_indices[first + pmin + win_base + lane] : 0;
-      }
-      return __shfl_sync(kAll, window_ids, i - win_base);
-    };
-    auto issue = [&](int i, int slot) {
-      const int pid = page_id(i);
-      const bool ok = pid >= 0 && pid < p.num_pages;
-      if (!ok && lane == 0) atomicOr(p.status, kFlagBadPage);
-      mbar_arrive_expect_tx_if(lane == 0 && ok, &bar[slot], (uint32_t)Gm::STAGE);
-      mbar_arrive_if(lane == 0 && !ok, &bar[slot]);
-      unsigned char* dst = stages + (size_t)slot * Gm::STAGE;
-#pragma unroll
-      for (int u = 0; u < D / Gm::E; ++u)
-        tma_load_4d_if(lane == 0 && ok, dst + u * Gm::REGION, &map, &bar[slot], u * Gm::E, 0, g, 2 * pid, policy);
-      return ok;
-    };
-    uint32_t okmask = 0;  // bit i % 32 of pages in flight: copy issued
-    const int pre = min(nst, np);
-    for (int i = 0; i < pre; ++i)
-      if (issue(i, (seq + i) % nst)) okmask |= 1u << (i & 31);
-
+    bool stop = false;
     for (int i = 0; i < np; ++i) {
-      const int slot = (seq + i) % nst;
-      const uint32_t ph = (uint32_t)(((seq + i) / nst) & 1);
-      if (!mbar_wait_bounded(&bar[slot], ph, kWaitLimitNs)) {
-        if (lane == 0) atomicOr(p.status, kFlagTimeout);
-        for (int j = i + 1; j < min(np, i + nst); ++j)
-          mbar_wait_bounded(&bar[(seq + j) % nst], (uint32_t)(((seq + j) / nst) & 1), kWaitLimitNs / 16);
-        timed_out = true;
+      const int f = seq + i, slot = f % nst;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((f / nst) & 1), kWaitLimitNs)) {
+        if (lane == 0) {
+          atomicOr(p.status, kFlagTimeout);
+          abort_flag = 1;
+        }
+        stop = true;
         break;
       }
       const int ord = pmin + i;
-      const bool page_ok = okmask & (1u << (i & 31));
       const uint32_t stage = smem_u32(stages + (size_t)slot * Gm::STAGE);
-      if (page_ok) {
+      if (ord <= wmax) {
         const int nvalid = ord == n - 1 ? last : kPageSize;
-        if (nvalid < kPageSize) {
-          // slots past the sequence end may hold anything: zero their V rows (P = 0 there)
-          constexpr int kChunks = D / 8;
-          for (int c = lane; c < (kPageSize - nvalid) * kChunks; c += 32) {
-            const uint32_t a = Gm::chunk_addr(stage, 1, nvalid + c / kChunks, (c % kChunks) * 8);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-          }
-          __syncwarp();
-        }
-        // S = Q K^T: two n-blocks of 8 slots
+        // S = Q K^T: two n-blocks of 8 slots (V rows past the end are masked through P below,
+        // and their values are zeroed so that P = 0 times anything stays 0)
+        // (even and odd k-steps accumulate apart: four independent mma chains instead of two)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
+          float sc_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
           const int mi = lane >> 3, rr = lane & 7;
           const int t = (mi >> 1) * 8 + rr;
           const int dsub = (mi & 1) * 8;
@@ -236,49 +262,67 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
           for (int ks = 0; ks < Gm::KS; ++ks) {
             uint32_t b0, b1, b2, b3;
             ldmatrix_x4(Gm::chunk_addr(stage, 0, t, ks * 16 + dsub), b0, b1, b2, b3);
-            mma_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            float (&c0)[4] = (ks & 1) ? sc_odd[0] : sc[0];
+            float (&c1)[4] = (ks & 1) ? sc_odd[1] : sc[1];
+            mma_16816(c0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_16816(c1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
           }
-        }
-        // mask and online softmax, rows rho0 (i = 0: sc[*][0..1]) and rho0 + 8 (i = 1: sc[*][2..3])
-        float pr[2][4];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          float v[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int col = (e >> 1) * 8 + c2 + (e & 1);  // slot
-            const int tpos = ord * kPageSize + col;
-            const float x = sc[e >> 1][2 * i + (e & 1)] * p.scale_log2;
-            v[e] = (valid[i] && tpos >= start[i] && tpos <= pos[i]) ? x : -INFINITY;
+            sc[0][e] += sc_odd[0][e];
+            sc[1][e] += sc_odd[1][e];
+          }
+        }
+        // a page every valid row sees whole needs no mask (rows without a token are never written)
+        const bool whole = ord * kPageSize >= full_lo && ord * kPageSize + kPageSize - 1 <= full_hi &&
+                           nvalid == kPageSize;
+        float pr[2][4];
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2) {
+          float v[4];
+          if (whole) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = sc[e >> 1][2 * i2 + (e & 1)] * p.scale_log2;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = (e >> 1) * 8 + c2 + (e & 1);
+              const int tpos = ord * kPageSize + col;
+              const float x = sc[e >> 1][2 * i2 + (e & 1)] * p.scale_log2;
+              v[e] = (valid[i2] && tpos >= start[i2] && tpos <= pos[i2]) ? x : -INFINITY;
+            }
           }
           float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
           mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
           mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
-          if (mx > m[i] + kLazy) {
-            const float alpha = exp2f(m[i] - mx);
-            l[i] *= alpha;
+          if (mx > m[i2] + kLazy) {
+            const float alpha = exp2f(m[i2] - mx);
+            l[i2] *= alpha;
 #pragma unroll
             for (int nb = 0; nb < Gm::NB; ++nb) {
-              acc[nb][2 * i] *= alpha;
-              acc[nb][2 * i + 1] *= alpha;
+              acc[nb][2 * i2] *= alpha;
+              acc[nb][2 * i2 + 1] *= alpha;
             }
-            m[i] = mx;
+            m[i2] = mx;
           }
-#pragma unroll
           // a row may see no position yet (its window starts further on): its P is 0, not NaN
-          for (int e = 0; e < 4; ++e) pr[i][e] = v[e] == -INFINITY ? 0.f : exp2f(v[e] - m[i]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pr[i2][e] = v[e] == -INFINITY ? 0.f : exp2f(v[e] - m[i2]);
         }
-        // P as fp16 (l adds the same rounded values): A fragments for P V
         uint32_t pa[4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const __half2 lo = __floats2half2_rn(pr[i][0], pr[i][1]);  // slots c2, c2 + 1
-          const __half2 hi = __floats2half2_rn(pr[i][2], pr[i][3]);  // slots c2 + 8, c2 + 9
+        for (int i2 = 0; i2 < 2; ++i2) {
+          const __half2 lo = __floats2half2_rn(pr[i2][0], pr[i2][1]);
+          const __half2 hi = __floats2half2_rn(pr[i2][2], pr[i2][3]);
           const float2 flo = __half22float2(lo), fhi = __half22float2(hi);
-          l[i] += (flo.x + flo.y) + (fhi.x + fhi.y);
-          pa[i] = *reinterpret_cast<const uint32_t*>(&lo);
-          pa[2 + i] = *reinterpret_cast<const uint32_t*>(&hi);
+          l[i2] += (flo.x + flo.y) + (fhi.x + fhi.y);
+          pa[i2] = *reinterpret_cast<const uint32_t*>(&lo);
+          pa[2 + i2] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        if (nvalid < kPageSize) {
+          // the ring is shared: instead of zeroing V rows past the end, zero their P (already 0
+          // through the mask) and read those V rows as zero via a guarded copy of the fragment
+          // inputs below
         }
         {
           const int mi = lane >> 3, rr = lane & 7;
@@ -288,20 +332,29 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
           for (int mm = 0; mm < D / 16; ++mm) {
             uint32_t v0, v1, v2, v3;
             ldmatrix_x4_trans(Gm::chunk_addr(stage, 1, t, mm * 16 + dsub), v0, v1, v2, v3);
+            if (nvalid < kPageSize) {
+              // V fragments of slots past the sequence end may hold anything (NaN): zero them
+              // (ldmatrix.trans gives this lane slots tr and tr + 8 of its two 8x8 matrices)
+              const int tr = 2 * (lane & 3);
+              if (tr >= nvalid) v0 = 0u;
+              if (tr + 1 >= nvalid) v0 &= 0x0000FFFFu;
+              if (tr + 8 >= nvalid) v1 = 0u;
+              if (tr + 9 >= nvalid) v1 &= 0x0000FFFFu;
+              if (tr >= nvalid) v2 = 0u;
+              if (tr + 1 >= nvalid) v2 &= 0x0000FFFFu;
+              if (tr + 8 >= nvalid) v3 = 0u;
+              if (tr + 9 >= nvalid) v3 &= 0x0000FFFFu;
+            }
             mma_16816(acc[2 * mm], pa[0], pa[1], pa[2], pa[3], v0, v1);
             mma_16816(acc[2 * mm + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
           }
         }
       }
-      fence_proxy_async_smem();  // this lane's reads/writes of the stage before its refill
       __syncwarp();
-      if (i + nst < np) {
-        if (issue(i + nst, slot)) okmask |= 1u << ((i + nst) & 31);
-        else okmask &= ~(1u << ((i + nst) & 31));
-      }
+      if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage
     }
-    if (timed_out) break;
     seq += np;
+    if (stop) break;
 
     // finish the two rows: out = acc / l (with the sink in the denominator), lse
 #pragma unroll
@@ -328,20 +381,24 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_kernel(const __gri
         p.lse[(long long)tok[i] * p.hq + head[i]] = any ? (mm + log2f(lt)) * kLn2 : -INFINITY;
     }
   }
+  // the producer leaves only when its copies have landed: wait (bounded) for the last fills
+  if (producer && *reinterpret_cast<volatile int*>(&abort_flag)) {
+    for (int f = max(0, seq - nst); f < seq; ++f)
+      mbar_wait_bounded(&full[f % nst], (uint32_t)((f / nst) & 1), kWaitLimitNs / 16);
+  }
 }
 
 template <int D>
 size_t prefill_smem(int nstage, int batch) {
-  return 1024 + (size_t)kPrefillWarps * nstage * PfGeom<D>::STAGE + (size_t)kPrefillWarps * nstage * 8 +
-         (size_t)(batch + 1) * 4;
+  return 1024 + (size_t)nstage * PfGeom<D>::STAGE + (size_t)nstage * 16 + (size_t)(batch + 1) * 4;
 }
 
 }  // namespace
 
 PrefillConfig prefill_config(int head_dim, int batch) {
   PrefillConfig c;
-  const int budget = (233472 - 2 * 1024) / 2 - 256;  // two CTAs per SM
-  c.nstage = 4;
+  const int budget = 232448 - 256;  // one CTA (nine warps) per SM
+  c.nstage = 8;
   auto smem = [&](int n) {
     return head_dim == 64 ? prefill_smem<64>(n, batch) : head_dim == 96 ? prefill_smem<96>(n, batch)
                                                                          : prefill_smem<128>(n, batch);
@@ -367,7 +424,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& map, const
                            int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);
-  lc.blockDim = dim3(kPrefillWarps * 32);
+  lc.blockDim = dim3((kPrefillWarps + 1) * 32);  // consumers and one producer warp
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
