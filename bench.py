@@ -434,7 +434,7 @@ def run_ours(args):
     windows = [cfg.window] * cfg.layers if cfg.window else None
     sinks = [torch.from_numpy(W.sink_logits(step, l)).to(dev) for l in layers] if cfg.sinks else None
     cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=pkv.OPT_PDL, windows=windows, sinks=sinks)
+                      pools=pools, options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES, windows=windows, sinks=sinks)
     B, T = step.batch, step.num_tokens
     total_pages = int(step.page_indptr[-1])
     S, chunk = cache.plan_decode(B, step.max_pages_per_seq, total_pages)
@@ -673,7 +673,7 @@ def run_ours(args):
                    **({"window": cfg.window} if cfg.window else {}),
                    **({"attention_sinks": "per layer and query head"} if cfg.sinks else {}),
                    "l2": f"inputs larger than L2: {kv_step / 1e9:.2f} GB of KV per step",
-                   "launch": "CUDA graph of the step, programmatic dependent launch",
+                   "launch": "CUDA graph of the step, programmatic dependent launch, early page copies",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_roofline_frac_step": value / world / peak,
         "attention_us_per_step_per_layer": launch_ms * 1e3,

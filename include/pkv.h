@@ -68,6 +68,13 @@ typedef enum {
                            reading q, k, v, the pool and the partials, but read their int32 page
                            tables (page_indptr, append_indptr, last_page_len, q_indptr) earlier:
                            do not produce those arrays in the kernel launched right before. */
+#define PKV_OPT_EARLY_PAGES 0x2 /* with PKV_OPT_PDL, the one-launch step (pkv_append_decode_attention
+                                   with one token per sequence) starts copying the layer's cached
+                                   pages before that wait, so the copies overlap the end of the
+                                   previous kernel; the new tokens' q, k, v are read after it.  The
+                                   kernel launched right before must not write this layer's pool.
+                                   Applied when Hq / Hkv >= 2 (tensor-core path), where it measured
+                                   faster; ignored otherwise. */
 
 typedef struct pkv_cache pkv_cache; /* opaque, host-only */
 

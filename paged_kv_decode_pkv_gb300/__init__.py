@@ -22,6 +22,7 @@ PAGE_SIZE = 16
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_RANGE, ERR_CUDA, ERR_TIMEOUT = range(6)
 FLAG_BAD_PAGE, FLAG_BAD_POSITION, FLAG_BAD_SEQUENCE, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 OPT_PDL = 0x1
+OPT_EARLY_PAGES = 0x2  # PKV_OPT_EARLY_PAGES
 
 
 class PkvError(RuntimeError):

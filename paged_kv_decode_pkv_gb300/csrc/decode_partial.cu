@@ -81,8 +81,8 @@ constexpr int kCtasPerSm = 2;
 __host__ __device__ constexpr int smem_align(int group) { return group >= 2 ? 1024 : 128; }
 
 struct Layout {
-  int stage_bytes, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, prefix_off, indptr_off, aptr_off,
-      wstart_off, total;
+  int stage_bytes, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, defer_off, prefix_off, indptr_off,
+      aptr_off, wstart_off, total;
 };
 
 // Items whose query rows may be in flight at once, per warp (one item slot each).
@@ -106,7 +106,8 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
   L.meta_off = L.bar_off + n * 8;
   L.meta_off = (L.meta_off + 15) & ~15;
   L.pid_off = L.meta_off + n * 16;
-  L.prefix_off = L.pid_off + (fused ? n * 4 : 0);
+  L.defer_off = (L.pid_off + (fused ? n * 4 : 0) + 15) & ~15;  // 16-byte entries are stored as vectors
+  L.prefix_off = L.defer_off + (fused ? n * 32 : 0);
   L.indptr_off = L.prefix_off + (batch + 1) * 4;
   L.aptr_off = L.indptr_off + (batch + 1) * 4;
   L.wstart_off = L.aptr_off + (fused ? (batch + 1) * 4 : 0);
@@ -925,7 +926,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   } else {
     prepare_next(nxt);  // index loads only: allowed before the wait
   }
-  pdl_wait();  // q_rope and the pool pages come from the preceding kernel
+  // One-launch mode with early pages: the ring is filled before the launch wait (the cache's pages
+  // of earlier steps are not written by the preceding kernel), the items' rows after it.
+  bool waited = !(FUSED && p.early);
+  int ndefer = 0;
+  int* defer = reinterpret_cast<int*>(base + L.defer_off) + warp * p.nstage * 8;
+  if (waited) pdl_wait();  // q_rope and the pool pages come from the preceding kernel
   int issued = 0, consumed = 0;
   // Items whose first stage was issued / consumed: the first stage of item i brings its query rows
   // into item slot i % kItemSlots, so at most kItemSlots items may be issued and not yet begun.
@@ -997,16 +1003,26 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       mbar_arrive_if(l0 && bytes == 0u, &bar[k]);
       if (first) {
         // the item's query rows (one-launch mode: with the (cos, sin) row and the new k and v)
-        unsigned char* qslot = qslots + (items_issued % kItemSlots) * L.qslot_bytes;
+        const int qslot_off = (items_issued % kItemSlots) * L.qslot_bytes;
+        unsigned char* qslot = qslots + qslot_off;
         ++items_issued;
-        const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
-        bulk_load_if(l0, qslot, qsrc, q_bytes, &bar[k]);
-        if constexpr (FUSED) {
-          bulk_load_if(l0, qslot + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes, &bar[k]);
-          const bool kv = l0 && (mt.flags & kMetaNew);
-          const long long row = ((long long)cur.q0 * p.hkv + cur.g) * D;
-          bulk_load_if(kv, qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
-          bulk_load_if(kv, qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+        if (FUSED && !waited) {
+          // before the launch wait (early pages): the page copy goes now, the item's rows, which the
+          // preceding kernel may write, right after the wait (the stage's byte count includes them)
+          int* e = defer + ndefer * 8;
+          st_shared_v4_if(l0, e, k, qslot_off, cur.q1 - 1, cur.g);
+          st_shared_v4_if(l0, e + 4, cur.qpos, mt.flags, cur.q0, 0);
+          ++ndefer;
+        } else {
+          const __half* qsrc = p.q + ((long long)(cur.q1 - 1) * p.hq + (long long)cur.g * p.group) * D;
+          bulk_load_if(l0, qslot, qsrc, q_bytes, &bar[k]);
+          if constexpr (FUSED) {
+            bulk_load_if(l0, qslot + q_bytes, p.rope + (long long)cur.qpos * (D / 2), cs_bytes, &bar[k]);
+            const bool kv = l0 && (mt.flags & kMetaNew);
+            const long long row = ((long long)cur.q0 * p.hkv + cur.g) * D;
+            bulk_load_if(kv, qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
+            bulk_load_if(kv, qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+          }
         }
       }
       unsigned char* dst = stages + (size_t)k * L.stage_bytes;
@@ -1037,6 +1053,29 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     cmp.init(lane, p.group);
   } else {
     cmp.init(lane);
+  }
+
+  if (!waited) {
+    while (issued < nst && produce()) {
+    }
+    pdl_wait();  // the new token's q, k, v come from the preceding kernel
+    waited = true;
+    __syncwarp();
+    if (lane == 0) {
+      for (int i = 0; i < ndefer; ++i) {
+        const int* e = defer + i * 8;
+        const int k = e[0], row_q = e[2], g = e[3], qpos = e[4], flags = e[5], q0 = e[6];
+        unsigned char* qslot = qslots + e[1];
+        bulk_load(qslot, p.q + ((long long)row_q * p.hq + (long long)g * p.group) * D, q_bytes, &bar[k]);
+        bulk_load(qslot + q_bytes, p.rope + (long long)qpos * (D / 2), cs_bytes, &bar[k]);
+        if (flags & kMetaNew) {
+          const long long row = ((long long)q0 * p.hkv + g) * D;
+          bulk_load(qslot + q_bytes + cs_bytes, p.k_new + row, kv_bytes / 2, &bar[k]);
+          bulk_load(qslot + q_bytes + cs_bytes + kv_bytes / 2, p.v_new + row, kv_bytes / 2, &bar[k]);
+        }
+      }
+    }
+    __syncwarp();
   }
 
   if (p.balanced && gw == 0) {

@@ -240,7 +240,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   if (!aligned(d->rope_table, 16)) return PKV_ERR_INVALID_ARG;
   for (int l = 0; l < d->num_layers; ++l)
     if (d->layer_pools[l] == nullptr || !aligned(d->layer_pools[l], 256)) return PKV_ERR_INVALID_ARG;
-  if (d->options & ~PKV_OPT_PDL) return PKV_ERR_INVALID_ARG;
+  if (d->options & ~(PKV_OPT_PDL | PKV_OPT_EARLY_PAGES)) return PKV_ERR_INVALID_ARG;
   for (int l = 0; l < d->num_layers; ++l) {
     if (d->layer_window != nullptr && d->layer_window[l] < 0) return PKV_ERR_INVALID_ARG;
     if (d->layer_sinks != nullptr && d->layer_sinks[l] != nullptr && !aligned(d->layer_sinks[l], 4))
@@ -587,6 +587,9 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   p.max_position = c->desc.max_position;
   p.window = window;
   p.sinks = c->sinks[layer];
+  // Early page copies measured faster on the tensor-core path (GQA long context: 6 400 -> 6 600 GB/s)
+  // and slower on the CUDA-core path (single stream: 3 230 -> 3 125 GB/s), so only there.
+  p.early = (fused != nullptr && (c->desc.options & PKV_OPT_EARLY_PAGES) && c->group >= 2) ? 1 : 0;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 

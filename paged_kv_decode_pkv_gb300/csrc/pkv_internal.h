@@ -127,6 +127,7 @@ struct DecodeParams {
   // log, units of the scaled scores; nullable) that join the merge's denominator.
   int window;
   const float* sinks;
+  int early;  // one-launch mode: copy pages before the launch wait (PKV_OPT_EARLY_PAGES)
 };
 
 struct CombineParams {

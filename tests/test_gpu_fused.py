@@ -18,9 +18,12 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("plan", [{}, {"num_splits": 3}, {"chunk_pages": 2}])
-def test_fused_step_is_bit_identical_to_append_then_merged_decode(name, plan):
+@pytest.mark.parametrize("plan,early", [({}, False), ({"num_splits": 3}, False), ({"chunk_pages": 2}, False),
+                                        ({}, True)])
+def test_fused_step_is_bit_identical_to_append_then_merged_decode(name, plan, early):
     import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
 
     cfg = SMALL[name]
     if cfg.num_splits and not plan:
@@ -30,7 +33,8 @@ def test_fused_step_is_bit_identical_to_append_then_merged_decode(name, plan):
     pool_a = H.to_dev(host_pool, torch.float16)
     pool_b = H.to_dev(host_pool, torch.float16)
     cache_a = H.make_cache(step, [0], [pool_a])
-    cache_b = H.make_cache(step, [0], [pool_b])
+    # early pages: the one-launch kernel copies the cache before its launch wait (with PDL)
+    cache_b = H.make_cache(step, [0], [pool_b], options=(pkv.OPT_PDL | pkv.OPT_EARLY_PAGES) if early else 0)
     tabs = H.device_tables(step)
     q, k, v = H.device_qkv(step, 0)
     tp = int(step.page_indptr[-1])
