@@ -72,6 +72,16 @@ def _L():
         lib.orc_split_attention_balanced.argtypes = [P, P, P, i, P, P, P, i, i, d, i, P, P]
         lib.orc_combine.restype = i
         lib.orc_combine.argtypes = [P, P, i, i, i, i, P, P, P, P]
+        lib.orc_quantize_row.restype = None
+        lib.orc_quantize_row.argtypes = [P, i, P, P]
+        lib.orc_append_int8.restype = i
+        lib.orc_append_int8.argtypes = [P, P, P, P, i, P, P, i, P, P, P, P]
+        lib.orc_dequantize_pool.restype = None
+        lib.orc_dequantize_pool.argtypes = [P, P, P]
+        lib.orc_attention_int8.restype = i
+        lib.orc_attention_int8.argtypes = [P, P, P, i, P, P, P, d, i, P, P, P]
+        lib.orc_split_attention_int8.restype = i
+        lib.orc_split_attention_int8.argtypes = [P, P, P, i, P, P, P, i, i, i, d, i, P, P]
         lib.orc_prefill_attention.restype = i
         lib.orc_prefill_attention.argtypes = [P, P, P, i, i, P, P, P, P, P, d, i, P, P, P]
         lib.orc_qkv_project.restype = i
@@ -149,6 +159,93 @@ def append(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, page_in
     if rc:
         raise OracleError(rc)
     return q_out
+
+
+def int8_block_bytes(head_dim: int) -> int:
+    """Bytes of one int8 block: the 16 slots' codes [16][d] and fp32 scales [16]."""
+    return 16 * head_dim + 64
+
+
+def quantize_row(x):
+    """Row quantizer of the int8 cache: x fp16 bits [d] -> (codes int8 [d], scale float32)."""
+    x, px = _c(x, np.uint16)
+    codes = np.empty(x.size, dtype=np.int8)
+    sc = np.empty(1, dtype=np.float32)
+    _L().orc_quantize_row(px, x.size, codes.ctypes.data, sc.ctypes.data)
+    return codes, sc[0]
+
+
+def append_int8(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, page_indices, pool8):
+    """Append into an int8 pool (uint8 [P, 2, Hkv, 16*d + 64], in place); returns q_out."""
+    q, pq = _c(q, np.uint16)
+    k, pk = _c(k, np.uint16)
+    v, pv = _c(v, np.uint16)
+    pm, ppm = _c(pos_map, np.int32)
+    ai, pai = _c(append_indptr, np.int32)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    if not (pool8.flags["C_CONTIGUOUS"] and pool8.dtype == np.uint8):
+        raise ValueError("pool8 must be a C-contiguous uint8 array")
+    T = q.shape[0]
+    q_out = np.empty_like(q)
+    g = geom.c()
+    rc = _L().orc_append_int8(ctypes.byref(g), pq, pk, pv, T, ppm, pai, ai.size - 1, ppi, ppx, pool8.ctypes.data,
+                              q_out.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return q_out
+
+
+def dequantize_pool(geom: Geometry, pool8):
+    """fp64 values of an int8 pool, laid out like the fp16 pool [P, 2, Hkv, 16, d]."""
+    p8, pp = _c(pool8, np.uint8)
+    out = np.empty((geom.num_pages, 2, geom.num_kv_heads, 16, geom.head_dim), dtype=np.float64)
+    g = geom.c()
+    _L().orc_dequantize_pool(ctypes.byref(g), pp, out.ctypes.data)
+    return out
+
+
+def attention_int8(geom: Geometry, pool8, q_rope, page_indptr, page_indices, last_page_len, sm_scale=None,
+                   window: int = 0, sinks=None):
+    """attention() over an int8 pool."""
+    sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
+    p8, pp = _c(pool8, np.uint8)
+    q, pq = _c(q_rope, np.uint16)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    lp, plp = _c(last_page_len, np.int32)
+    B = pi.size - 1
+    out = np.empty((B, geom.num_qo_heads, geom.head_dim), dtype=np.float64)
+    lse = np.empty((B, geom.num_qo_heads), dtype=np.float64)
+    g = geom.c()
+    sk, psk = _sinks(sinks, geom.num_qo_heads)
+    rc = _L().orc_attention_int8(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, float(sm_scale), int(window), psk,
+                                 out.ctypes.data, lse.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return out, lse
+
+
+def split_attention_int8(geom: Geometry, pool8, q_rope, page_indptr, page_indices, last_page_len,
+                         num_splits: int = 0, chunk_pages: int = 0, num_out_splits: int = 1, sm_scale=None,
+                         window: int = 0):
+    """split_attention() over an int8 pool."""
+    sm_scale = default_scale(geom.head_dim) if sm_scale is None else sm_scale
+    p8, pp = _c(pool8, np.uint8)
+    q, pq = _c(q_rope, np.uint16)
+    pi, ppi = _c(page_indptr, np.int32)
+    px, ppx = _c(page_indices, np.int32)
+    lp, plp = _c(last_page_len, np.int32)
+    B = pi.size - 1
+    S = num_out_splits
+    po = np.empty((B, geom.num_qo_heads, S, geom.head_dim), dtype=np.float64)
+    pl = np.empty((B, geom.num_qo_heads, S), dtype=np.float64)
+    g = geom.c()
+    rc = _L().orc_split_attention_int8(ctypes.byref(g), pp, pq, B, ppi, ppx, plp, int(num_splits), int(chunk_pages),
+                                       S, float(sm_scale), int(window), po.ctypes.data, pl.ctypes.data)
+    if rc:
+        raise OracleError(rc)
+    return po, pl
 
 
 def qkv_project(x, w_packed, scales):

@@ -215,6 +215,88 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* int8 KV pages (SURVEY's NEXT-2; Zero TVM Documentation, "The memory-bandwidth ceiling": int8
+ * KV is exposed behind a flag; the format is this build's reading).
+ * Layout per layer: uint8 pool8[num_pages][2][Hkv][16 * d + 64]: a block holds the 16 slots'
+ * int8 codes [16][d] and then their fp32 scales [16].
+ * Row quantizer (one row = one token, one KV head, K or V, of d fp16 values x_i; K after RoPE and
+ * its fp16 rounding, as the fp16 cache stores it): amax = max |x_i|; s = fp32(amax / 127) (fp32
+ * division, nearest); code_i = clamp(rint_even(fp32(x_i / s)), -127, 127); amax = 0 gives s = 0 and
+ * codes 0.  The decision is taken in fp32, the precision of the kernel.  The value of a slot is
+ * code * s. */
+static int64_t block8(const orc_geom* g, int64_t page, int kv, int head) {
+  return ((page * 2 + kv) * g->num_kv_heads + head) * (int64_t)(16 * g->head_dim + 64);
+}
+
+void orc_quantize_row(const uint16_t* x, int d, int8_t* codes, float* scale) {
+  orc_init();
+  float amax = 0.f;
+  for (int i = 0; i < d; ++i) {
+    const float a = fabsf((float)dec(x[i]));
+    if (a > amax) amax = a;
+  }
+  const float s = amax / 127.0f;
+  *scale = s;
+  for (int i = 0; i < d; ++i) {
+    if (s == 0.f) {
+      codes[i] = 0;
+      continue;
+    }
+    float q = nearbyintf((float)dec(x[i]) / s);
+    if (q > 127.f) q = 127.f;
+    if (q < -127.f) q = -127.f;
+    codes[i] = (int8_t)q;
+  }
+}
+
+/* The append into an int8 pool: orc_append's rotation and placement, then the row quantizer. */
+int orc_append_int8(const orc_geom* g, const uint16_t* q, const uint16_t* k, const uint16_t* v, int T,
+                    const int32_t* pos_map, const int32_t* append_indptr, int B, const int32_t* page_indptr,
+                    const int32_t* page_indices, uint8_t* pool8, uint16_t* q_out) {
+  orc_init();
+  const int d = g->head_dim, Hkv = g->num_kv_heads;
+  /* the fp16 append into a scratch pool of the same geometry gives the rows to quantize */
+  const int64_t rows = (int64_t)g->num_pages * 2 * Hkv * ORC_PAGE;
+  uint16_t* scratch = (uint16_t*)calloc((size_t)rows * d, sizeof(uint16_t));
+  int rc = orc_append(g, q, k, v, T, pos_map, append_indptr, B, page_indptr, page_indices, scratch, q_out);
+  if (rc == ORC_OK) {
+    for (int s = 0; s < B; ++s) {
+      for (int t = append_indptr[s]; t < append_indptr[s + 1]; ++t) {
+        const int p = pos_map[t];
+        const int64_t page = page_indices[page_indptr[s] + p / ORC_PAGE];
+        const int slot = p % ORC_PAGE;
+        for (int h = 0; h < Hkv; ++h) {
+          for (int kv = 0; kv < 2; ++kv) {
+            uint8_t* blk = pool8 + block8(g, page, kv, h);
+            float sc;
+            orc_quantize_row(scratch + pool_row(g, page, kv, h, slot), d, (int8_t*)(blk + slot * d), &sc);
+            memcpy(blk + 16 * d + 4 * slot, &sc, 4);
+          }
+        }
+      }
+    }
+  }
+  free(scratch);
+  return rc;
+}
+
+/* Dequantize an int8 pool into fp64 rows laid out like the fp16 pool: out[page][kv][head][slot][d]. */
+void orc_dequantize_pool(const orc_geom* g, const uint8_t* pool8, double* out) {
+  const int d = g->head_dim, Hkv = g->num_kv_heads;
+  for (int64_t page = 0; page < g->num_pages; ++page)
+    for (int kv = 0; kv < 2; ++kv)
+      for (int h = 0; h < Hkv; ++h) {
+        const uint8_t* blk = pool8 + block8(g, page, kv, h);
+        for (int slot = 0; slot < ORC_PAGE; ++slot) {
+          float sc;
+          memcpy(&sc, blk + 16 * d + 4 * slot, 4);
+          for (int i = 0; i < d; ++i)
+            out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i] * (double)sc;
+        }
+      }
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* QKV projection with Q4F16_1 weights (Zero TVM Documentation, "Q4F16 quantization format": eight
  * int4 values per uint32, element i in bits 4i..4i+3, one fp16 scale per 32 weights, weight value
  * f16(nibble - 7) * scale evaluated in fp16; "Decode loop": the QKV matmul feeds RoPE and the KV
@@ -284,6 +366,13 @@ static void apply_sink(double* o, double* lse, int d, double sink) {
 }
 
 /* o[d] = sum_t softmax(score)_t V_t, lse = ln sum_t exp(score_t); empty range: o = 0, lse = -inf */
+/* The cache the attention reads: fp16 rows, or (int8 caches) their dequantized fp64 values. */
+static const double* g_pool64 = NULL; /* set only inside the int8 entry points (single-threaded setup) */
+
+static double kv_at(const uint16_t* pool, int64_t row, int i) {
+  return g_pool64 != NULL ? g_pool64[row + i] : dec(pool[row + i]);
+}
+
 static int attend(const orc_geom* g, const uint16_t* pool, const double* q, int s, int kv_head,
                   int t0, int t1, const int32_t* page_indptr, const int32_t* page_indices,
                   double sm_scale, double* o, double* lse) {
@@ -301,19 +390,19 @@ static int attend(const orc_geom* g, const uint16_t* pool, const double* q, int 
       free(score);
       return ORC_OUT_OF_RANGE;
     }
-    const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);
+    const int64_t krow = pool_row(g, page, 0, kv_head, t % ORC_PAGE);
     double dot = 0.0;
-    for (int i = 0; i < d; ++i) dot += q[i] * dec(K[i]);
+    for (int i = 0; i < d; ++i) dot += q[i] * kv_at(pool, krow, i);
     score[t - t0] = sm_scale * dot;
     if (score[t - t0] > m) m = score[t - t0];
   }
   double l = 0.0;
   for (int t = t0; t < t1; ++t) {
     int page = page_indices[page_indptr[s] + t / ORC_PAGE];
-    const uint16_t* V = pool + pool_row(g, page, 1, kv_head, t % ORC_PAGE);
+    const int64_t vrow = pool_row(g, page, 1, kv_head, t % ORC_PAGE);
     double w = exp(score[t - t0] - m);
     l += w;
-    for (int i = 0; i < d; ++i) o[i] += w * dec(V[i]);
+    for (int i = 0; i < d; ++i) o[i] += w * kv_at(pool, vrow, i);
   }
   for (int i = 0; i < d; ++i) o[i] /= l;
   *lse = m + log(l);
@@ -566,4 +655,35 @@ int orc_combine(const double* partial_o, const double* partial_lse, int B, int H
       for (int i = 0; i < d; ++i) out_f16[sh * d + i] = orc_f64_to_f16(o[i]);
   }
   return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Attention over an int8 pool: the same definitions over the dequantized values code * s. */
+int orc_attention_int8(const orc_geom* g, const uint8_t* pool8, const uint16_t* q_rope, int B,
+                       const int32_t* page_indptr, const int32_t* page_indices, const int32_t* last_page_len,
+                       double sm_scale, int window, const double* sinks, double* out, double* lse) {
+  double* p64 = (double*)malloc(sizeof(double) * (size_t)g->num_pages * 2 * g->num_kv_heads * ORC_PAGE *
+                                (size_t)g->head_dim);
+  orc_dequantize_pool(g, pool8, p64);
+  g_pool64 = p64;
+  int rc = orc_attention(g, NULL, q_rope, B, page_indptr, page_indices, last_page_len, sm_scale, window, sinks,
+                         out, lse);
+  g_pool64 = NULL;
+  free(p64);
+  return rc;
+}
+
+int orc_split_attention_int8(const orc_geom* g, const uint8_t* pool8, const uint16_t* q_rope, int B,
+                             const int32_t* page_indptr, const int32_t* page_indices,
+                             const int32_t* last_page_len, int num_splits, int chunk_pages, int num_out_splits,
+                             double sm_scale, int window, double* partial_o, double* partial_lse) {
+  double* p64 = (double*)malloc(sizeof(double) * (size_t)g->num_pages * 2 * g->num_kv_heads * ORC_PAGE *
+                                (size_t)g->head_dim);
+  orc_dequantize_pool(g, pool8, p64);
+  g_pool64 = p64;
+  int rc = orc_split_attention(g, NULL, q_rope, B, page_indptr, page_indices, last_page_len, num_splits,
+                               chunk_pages, num_out_splits, sm_scale, window, partial_o, partial_lse);
+  g_pool64 = NULL;
+  free(p64);
+  return rc;
 }

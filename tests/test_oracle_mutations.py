@@ -35,9 +35,13 @@ MUTANTS = [
     ("int4 scale group", "const double scale = dec(scales[(int64_t)n * groups + k / 32]);",
      "const double scale = dec(scales[(int64_t)n * groups + k / 64]);"),
     ("prefill not causal", "window_start(p + 1, window), p + 1, page_indptr,", "window_start(p + 1, window), p + 2, page_indptr,"),
+    ("int8 rounding truncates", "float q = nearbyintf((float)dec(x[i]) / s);", "float q = truncf((float)dec(x[i]) / s);"),
+    ("int8 scale divisor", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
+    ("int8 scale offset", "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i] * (double)sc;",
+     "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i];"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
-    ("slot index", "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
-     "const uint16_t* K = pool + pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
+    ("slot index", "const int64_t krow = pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
+     "const int64_t krow = pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
     ("softmax scale dropped", "score[t - t0] = sm_scale * dot;", "score[t - t0] = dot;"),
     ("combine lse", "lse[sh] = M + log(W);", "lse[sh] = log(W);"),
     ("fp16 rounding truncates", "double n = nearbyint(a / quantum);", "double n = floor(a / quantum);"),
@@ -64,6 +68,7 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_window_sinks.py"),
                         os.path.join(ROOT, "tests", "test_oracle_qkv.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_prefill.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_prefill.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_int8.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"the pins did not catch the planted mistake '{name}'"
