@@ -68,6 +68,17 @@ typedef enum {
                            reading q, k, v, the pool and the partials, but read their int32 page
                            tables (page_indptr, append_indptr, last_page_len, q_indptr) earlier:
                            do not produce those arrays in the kernel launched right before. */
+#define PKV_OPT_INT8_KV 0x4 /* int8 KV pages (SURVEY's NEXT-2 reading; the Zero TVM page exposes int8
+                               KV behind a flag): each layer's pool is uint8 blocks
+                               [num_pages][2][Hkv][16 * head_dim + 64] holding the 16 slots' int8
+                               codes [16][head_dim] then their fp32 scales [16].  The append
+                               quantizes each new K row (after RoPE and its fp16 rounding) and V row:
+                               s = max|x| / 127 (fp32), code = clamp(rint(x / s), -127, 127) (fp32);
+                               attention runs on the exact codes and applies the scales in fp32 to
+                               the scores (K) and the probabilities (V).  Needs
+                               Hq / Hkv >= 2 (tensor-core path); pkv_append_decode_attention runs as
+                               two launches; pkv_prefill_attention and pkv_qkv_append_rope return
+                               PKV_ERR_UNSUPPORTED. */
 #define PKV_OPT_EARLY_PAGES 0x2 /* with PKV_OPT_PDL, the one-launch step (pkv_append_decode_attention
                                    with one token per sequence) starts copying the layer's cached
                                    pages before that wait, so the copies overlap the end of the
@@ -122,6 +133,9 @@ typedef struct {
 
 /* Bytes of one layer's pool. */
 size_t pkv_pool_bytes(int num_pages, int num_kv_heads, int head_dim);
+
+/* Bytes of one layer's int8 pool (PKV_OPT_INT8_KV): num_pages * 2 * Hkv * (16 * head_dim + 64). */
+size_t pkv_pool_bytes_int8(int num_pages, int num_kv_heads, int head_dim);
 
 /* Bytes of the RoPE table: max_position * (head_dim / 2) (cos, sin) pairs of fp32, computed on
  * the host in fp64 as cos/sin(p * theta^(-2i/head_dim)) and rounded once to fp32. */

@@ -76,6 +76,8 @@ def _L():
         lib.orc_quantize_row.argtypes = [P, i, P, P]
         lib.orc_append_int8.restype = i
         lib.orc_append_int8.argtypes = [P, P, P, P, i, P, P, i, P, P, P, P]
+        lib.orc_quantize_pool.restype = None
+        lib.orc_quantize_pool.argtypes = [P, P, P]
         lib.orc_dequantize_pool.restype = None
         lib.orc_dequantize_pool.argtypes = [P, P, P]
         lib.orc_attention_int8.restype = i
@@ -194,6 +196,15 @@ def append_int8(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, pa
     if rc:
         raise OracleError(rc)
     return q_out
+
+
+def quantize_pool(geom: Geometry, pool):
+    """Every slot row of an fp16 pool [P, 2, Hkv, 16, d] quantized: uint8 [P, 2, Hkv, 16*d + 64]."""
+    p16, pp = _c(pool, np.uint16)
+    out = np.empty((geom.num_pages, 2, geom.num_kv_heads, int8_block_bytes(geom.head_dim)), dtype=np.uint8)
+    g = geom.c()
+    _L().orc_quantize_pool(ctypes.byref(g), pp, out.ctypes.data)
+    return out
 
 
 def dequantize_pool(geom: Geometry, pool8):

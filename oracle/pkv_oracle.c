@@ -280,6 +280,23 @@ int orc_append_int8(const orc_geom* g, const uint16_t* q, const uint16_t* k, con
   return rc;
 }
 
+/* Quantize every slot row of an fp16 pool into an int8 pool (cache contents before a step). */
+void orc_quantize_pool(const orc_geom* g, const uint16_t* pool, uint8_t* pool8) {
+  orc_init();
+  const int d = g->head_dim, Hkv = g->num_kv_heads;
+#pragma omp parallel for schedule(static)
+  for (int64_t page = 0; page < g->num_pages; ++page)
+    for (int kv = 0; kv < 2; ++kv)
+      for (int h = 0; h < Hkv; ++h) {
+        uint8_t* blk = pool8 + block8(g, page, kv, h);
+        for (int slot = 0; slot < ORC_PAGE; ++slot) {
+          float sc;
+          orc_quantize_row(pool + pool_row(g, page, kv, h, slot), d, (int8_t*)(blk + slot * d), &sc);
+          memcpy(blk + 16 * d + 4 * slot, &sc, 4);
+        }
+      }
+}
+
 /* Dequantize an int8 pool into fp64 rows laid out like the fp16 pool: out[page][kv][head][slot][d]. */
 void orc_dequantize_pool(const orc_geom* g, const uint8_t* pool8, double* out) {
   const int d = g->head_dim, Hkv = g->num_kv_heads;

@@ -23,6 +23,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_RANGE, ERR_CUDA, ERR_TIMEOUT = 
 FLAG_BAD_PAGE, FLAG_BAD_POSITION, FLAG_BAD_SEQUENCE, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 OPT_PDL = 0x1
 OPT_EARLY_PAGES = 0x2  # PKV_OPT_EARLY_PAGES
+OPT_INT8_KV = 0x4  # PKV_OPT_INT8_KV
 
 
 class PkvError(RuntimeError):
@@ -148,14 +149,18 @@ class Cache:
         self.num_qo_heads, self.num_kv_heads = int(num_qo_heads), int(num_kv_heads)
         self.head_dim, self.max_position = int(head_dim), int(max_position)
         self.rope_theta = float(rope_theta)
-        shape = (self.num_pages, 2, self.num_kv_heads, PAGE_SIZE, self.head_dim)
+        self.int8 = bool(int(options) & OPT_INT8_KV)
+        if self.int8:  # uint8 blocks: codes [16][d] then fp32 scales [16]
+            shape, dtype = (self.num_pages, 2, self.num_kv_heads, 16 * self.head_dim + 64), torch.uint8
+        else:
+            shape, dtype = (self.num_pages, 2, self.num_kv_heads, PAGE_SIZE, self.head_dim), torch.float16
         if pools is None:
-            pools = [torch.empty(shape, dtype=torch.float16, device=device) for _ in range(self.num_layers)]
+            pools = [torch.empty(shape, dtype=dtype, device=device) for _ in range(self.num_layers)]
         if len(pools) != self.num_layers:
             raise ValueError("one pool per layer is required")
         for t in pools:
-            if t.dtype != torch.float16 or tuple(t.shape) != shape or not t.is_contiguous():
-                raise ValueError(f"pools must be contiguous float16 tensors of shape {shape}")
+            if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"pools must be contiguous {dtype} tensors of shape {shape}")
         self.pools = list(pools)
         nbytes = rope_table_bytes(self.max_position, self.head_dim)
         self.rope_table = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=device)

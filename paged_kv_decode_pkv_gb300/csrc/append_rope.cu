@@ -154,3 +154,141 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) 
 }
 
 }  // namespace pkv
+
+// ------------------------------------------------------------------------------------------------
+// The append into an int8 cache (PKV_OPT_INT8_KV).  Layout per layer: uint8 blocks
+// [num_pages][2][Hkv][16 * d + 64], a block holding the 16 slots' int8 codes [16][d] and then their
+// fp32 scales [16].  Row quantizer: amax = max |x_i| of the row's fp16 values (K after RoPE and its
+// fp16 rounding, as the fp16 cache stores it; V as given), s = amax / 127 (fp32 division),
+// code_i = clamp(rint_even(x_i / s), -127, 127) (fp32 division), amax = 0 giving s = 0 and codes 0.
+// One warp per (token, row): Hq query rows (rotated to q_out, fp16), Hkv K rows, Hkv V rows.
+
+namespace pkv {
+namespace {
+
+constexpr int kQ8Warps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kQ8Warps * 32) append_rope_q8_kernel(AppendParams p) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int rows_per_token = p.hq + 2 * p.hkv;
+  const long long job = (long long)blockIdx.x * kQ8Warps + (threadIdx.x >> 5);
+  if (job >= (long long)p.num_tokens * rows_per_token) return;
+  const int t = (int)(job / rows_per_token);
+  const int row = (int)(job - (long long)t * rows_per_token);
+  // token -> sequence -> page slot (the fp16 append's checks; the first row of a token reports)
+  long long blk_page = -1;
+  int pos = 0;
+  {
+    int lo = 0, hi = p.batch;
+    if (p.append_indptr[0] <= t && t < p.append_indptr[p.batch]) {
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.append_indptr[mid] <= t) lo = mid; else hi = mid;
+      }
+      pos = p.pos_map[t];
+      const int first = p.page_indptr[lo];
+      const int n_pages = p.page_indptr[lo + 1] - first;
+      if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
+        if (row == 0 && lane == 0) atomicOr(p.status, kFlagBadPosition);
+      } else {
+        const int page = p.page_indices[first + (pos >> 4)];
+        if (page < 0 || page >= p.num_pages) {
+          if (row == 0 && lane == 0) atomicOr(p.status, kFlagBadPage);
+        } else {
+          blk_page = page;
+        }
+      }
+    } else if (row == 0 && lane == 0) {
+      atomicOr(p.status, kFlagBadSequence);
+    }
+  }
+  pdl_wait();  // q, k, v and the pool may be produced or read by the preceding kernel
+  if (blk_page < 0) return;
+
+  const bool is_q = row < p.hq;
+  const bool is_k = !is_q && row < p.hq + p.hkv;
+  const int head = is_q ? row : is_k ? row - p.hq : row - p.hq - p.hkv;
+  const __half* src = is_q ? p.q + ((long long)t * p.hq + head) * D
+                    : (is_k ? p.k : p.v) + ((long long)t * p.hkv + head) * D;
+  const float2* cs = p.rope + (long long)pos * (D / 2);
+  // the row's values as the fp16 cache would hold them: pairs (j, j + D/2), j = lane, lane + 32
+  constexpr int kPairs = (D / 2 + 31) / 32;
+  __half lo_v[kPairs], hi_v[kPairs];
+#pragma unroll
+  for (int u = 0; u < kPairs; ++u) {
+    const int j = lane + 32 * u;
+    if (j < D / 2) {
+      __half a = src[j], b = src[j + D / 2];
+      if (!(row >= p.hq + p.hkv)) {  // q and k rows are rotated
+        float ra, rb;
+        rope_pair(__half2float(a), __half2float(b), cs[j], ra, rb);
+        a = __float2half_rn(ra);
+        b = __float2half_rn(rb);
+      }
+      lo_v[u] = a;
+      hi_v[u] = b;
+    }
+  }
+  if (is_q) {
+    __half* dst = p.q_out + ((long long)t * p.hq + head) * D;
+#pragma unroll
+    for (int u = 0; u < kPairs; ++u) {
+      const int j = lane + 32 * u;
+      if (j < D / 2) {
+        dst[j] = lo_v[u];
+        dst[j + D / 2] = hi_v[u];
+      }
+    }
+    return;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < kPairs; ++u)
+    if (lane + 32 * u < D / 2) amax = fmaxf(amax, fmaxf(fabsf(__half2float(lo_v[u])), fabsf(__half2float(hi_v[u]))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = amax / 127.0f;
+  const int kv = is_k ? 0 : 1;
+  unsigned char* blk = p.pool8 + ((blk_page * 2 + kv) * p.hkv + head) * (long long)(16 * D + 64);
+  const int slot = pos & 15;
+  auto code = [&](__half h) -> signed char {
+    if (s == 0.f) return 0;
+    const float q = rintf(__half2float(h) / s);
+    return (signed char)fminf(127.f, fmaxf(-127.f, q));
+  };
+#pragma unroll
+  for (int u = 0; u < kPairs; ++u) {
+    const int j = lane + 32 * u;
+    if (j < D / 2) {
+      blk[slot * D + j] = (unsigned char)code(lo_v[u]);
+      blk[slot * D + j + D / 2] = (unsigned char)code(hi_v[u]);
+    }
+  }
+  if (lane == 0) *reinterpret_cast<float*>(blk + 16 * D + 4 * slot) = s;
+}
+
+}  // namespace
+
+cudaError_t launch_append_q8(const AppendParams& p, cudaStream_t stream, bool pdl) {
+  if (p.num_tokens <= 0 || p.batch <= 0) return cudaSuccess;
+  const long long jobs = (long long)p.num_tokens * (p.hq + 2 * p.hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((jobs + kQ8Warps - 1) / kQ8Warps));
+  cfg.blockDim = dim3(kQ8Warps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (p.head_dim) {
+    case 64: return cudaLaunchKernelEx(&cfg, append_rope_q8_kernel<64>, p);
+    case 96: return cudaLaunchKernelEx(&cfg, append_rope_q8_kernel<96>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, append_rope_q8_kernel<128>, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

@@ -81,8 +81,8 @@ constexpr int kCtasPerSm = 2;
 __host__ __device__ constexpr int smem_align(int group) { return group >= 2 ? 1024 : 128; }
 
 struct Layout {
-  int stage_bytes, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, defer_off, prefix_off, indptr_off,
-      aptr_off, wstart_off, total;
+  int stage_bytes, ring_off, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, defer_off, prefix_off,
+      indptr_off, aptr_off, wstart_off, total;
 };
 
 // Items whose query rows may be in flight at once, per warp (one item slot each).
@@ -95,12 +95,15 @@ constexpr int kItemSlots = 2;
 // page ranges, (one-launch mode) the new-token ranges and (sliding window) the first visible page
 // and its first attended slot.
 __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_dim, int group, int batch,
-                                              bool fused, bool windowed = false) {
+                                              bool fused, bool windowed = false, bool q8 = false) {
   Layout L;
   const int n = warps * nstage;
-  L.stage_bytes = 64 * head_dim;  // K and V of one page for one KV head
+  // K and V of one page for one KV head (int8 cache: the two int8 blocks as stored, expanded per
+  // page into the warp's fp16 tile, which then comes first)
+  L.stage_bytes = q8 ? 2 * int8_block_bytes(head_dim) : 64 * head_dim;
+  L.ring_off = q8 ? warps * 64 * head_dim : 0;
   L.qslot_bytes = (group * head_dim * 2 + (fused ? 8 * head_dim : 0) + 15) & ~15;
-  L.q_off = n * L.stage_bytes;
+  L.q_off = L.ring_off + n * L.stage_bytes;
   L.patch_off = L.q_off + warps * kItemSlots * L.qslot_bytes;
   L.bar_off = L.patch_off + (fused ? warps * 4 * head_dim : 0);
   L.meta_off = L.bar_off + n * 8;
@@ -418,6 +421,7 @@ struct GroupMma {
   uint32_t qa[KS][2];
   float acc[NB][4];
   float m, l;
+  float vref;  // int8 cache: acc holds sum p * scale * code / vref (vref = the largest V scale so far)
   int lane, h, group;
 
   __device__ void init(int lane_, int group_) {
@@ -457,6 +461,7 @@ struct GroupMma {
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     m = -INFINITY;
     l = 0.f;
+    vref = 0.f;
   }
 
   // Store the rotated query rows (fused mode): q_out_rows points at head g*G of the query token.
@@ -489,9 +494,13 @@ struct GroupMma {
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     m = -INFINITY;
     l = 0.f;
+    vref = 0.f;
   }
 
-  __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2) {
+  // ks, vs (int8 cache): the 16 slots' K and V scales; the staged tile then holds the exact codes,
+  // K scales multiply the scores, V scales the probabilities (relative to vref, raised lazily).
+  __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2, const float* ks = nullptr,
+                       const float* vs = nullptr) {
     const uint32_t stage = smem_u32(stage_ptr);
     if (nvalid < kPageSize) {
       // Slots past the sequence end may hold anything (even NaN): zero their V rows so that
@@ -522,6 +531,12 @@ struct GroupMma {
     }
     const int c = 2 * (lane & 3);
     float s[4] = {sc[0][0] * scale_log2, sc[0][1] * scale_log2, sc[1][0] * scale_log2, sc[1][1] * scale_log2};
+    if (ks != nullptr) {
+      s[0] = sc[0][0] * ks[c] * scale_log2;
+      s[1] = sc[0][1] * ks[c + 1] * scale_log2;
+      s[2] = sc[1][0] * ks[c + 8] * scale_log2;
+      s[3] = sc[1][1] * ks[c + 9] * scale_log2;
+    }
     s[0] = (c >= lo && c < nvalid) ? s[0] : -INFINITY;
     s[1] = (c + 1 >= lo && c + 1 < nvalid) ? s[1] : -INFINITY;
     s[2] = (c + 8 >= lo && c + 8 < nvalid) ? s[2] : -INFINITY;
@@ -542,12 +557,37 @@ struct GroupMma {
       }
       m = mx;
     }
-    const __half2 p01 = __floats2half2_rn(exp2f(s[0] - m), exp2f(s[1] - m));
-    const __half2 p23 = __floats2half2_rn(exp2f(s[2] - m), exp2f(s[3] - m));
+    const float e0 = exp2f(s[0] - m), e1 = exp2f(s[1] - m), e2 = exp2f(s[2] - m), e3 = exp2f(s[3] - m);
+    const __half2 p01 = __floats2half2_rn(e0, e1);
+    const __half2 p23 = __floats2half2_rn(e2, e3);
     const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
     l += (f01.x + f01.y) + (f23.x + f23.y);
-    const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
-    const uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
+    uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
+    uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
+    if (vs != nullptr) {
+      // P times each slot's V scale over vref (raised, with a rescale of acc, only when a scale
+      // exceeds it by 2^7, so P * scale / vref stays below 2^15, inside fp16)
+      const float v0 = (c >= lo && c < nvalid) ? vs[c] : 0.f, v1 = (c + 1 >= lo && c + 1 < nvalid) ? vs[c + 1] : 0.f;
+      const float v2 = (c + 8 >= lo && c + 8 < nvalid) ? vs[c + 8] : 0.f;
+      const float v3 = (c + 9 >= lo && c + 9 < nvalid) ? vs[c + 9] : 0.f;
+      float vm = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+      vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 1));
+      vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 2));
+      if (vm > vref * 128.f) {
+        const float alpha = vref / vm;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          acc[nb][0] *= alpha;
+          acc[nb][1] *= alpha;
+        }
+        vref = vm;
+      }
+      const float inv = vref > 0.f ? 1.f / vref : 0.f;
+      const __half2 q01 = __floats2half2_rn(e0 * (v0 * inv), e1 * (v1 * inv));
+      const __half2 q23 = __floats2half2_rn(e2 * (v2 * inv), e3 * (v3 * inv));
+      pa0 = *reinterpret_cast<const uint32_t*>(&q01);
+      pa2 = *reinterpret_cast<const uint32_t*>(&q23);
+    }
     {
       const int mi = lane >> 3, r = lane & 7;
       const int t = (mi & 1) * 8 + r;
@@ -569,7 +609,7 @@ struct GroupMma {
     const bool any = __shfl_sync(kFull, lt, 0) > 0.f;  // every head row saw the same tokens
     if (!any) return false;
     if (h < group) {
-      const float inv = 1.f / lt;
+      const float inv = (vref > 0.f ? vref : 1.f) / lt;
       const long long row = head_row0 + h;
       float* dst = po + (row * S + j) * D + 2 * (lane & 3);
 #pragma unroll
@@ -586,7 +626,7 @@ struct GroupMma {
     lt += __shfl_xor_sync(kFull, lt, 2);
     if (h < group) {
       const bool any = lt > 0.f;
-      const float inv = any ? 1.f / lt : 0.f;
+      const float inv = any ? (vref > 0.f ? vref : 1.f) / lt : 0.f;
       const long long row = head_row0 + h;
       __half* dst = out + row * D + 2 * (lane & 3);
 #pragma unroll
@@ -774,6 +814,37 @@ __device__ __forceinline__ void apply_patch(unsigned char* stage, const unsigned
   __syncwarp();
 }
 
+// int8 cache: expand a staged page's codes (the K and V blocks as stored: codes [16][d], then fp32
+// scales [16]) into the fp16 tile layout the tensor-core path reads; the codes are exact in fp16
+// ((code ^ 0x80) + 1024 - 1152) and the scales are applied to the scores and probabilities.
+template <int D>
+__device__ __forceinline__ void expand_q8(const unsigned char* landing, unsigned char* tile, int lane) {
+  constexpr int kBlk = int8_block_bytes(D);
+  constexpr int kChunks = D / 8;  // 16-byte fp16 chunks of a row
+  const uint32_t tb = smem_u32(tile);
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+  for (int c = lane; c < 2 * kPageSize * kChunks; c += 32) {
+    const int kv = c / (kPageSize * kChunks);
+    const int rem = c - kv * kPageSize * kChunks;
+    const int t = rem / kChunks, cc = rem - t * kChunks;
+    const unsigned char* blk = landing + kv * kBlk;
+    const uint2 w = *reinterpret_cast<const uint2*>(blk + t * D + 8 * cc);
+    const uint32_t u0 = w.x ^ 0x80808080u, u1 = w.y ^ 0x80808080u;
+    const uint32_t b[4] = {__byte_perm(u0, 0x64646464u, 0x5140), __byte_perm(u0, 0x64646464u, 0x5342),
+                           __byte_perm(u1, 0x64646464u, 0x5140), __byte_perm(u1, 0x64646464u, 0x5342)};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&b[j]), bias);  // exact codes
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const uint32_t a = GroupMma<D>::chunk_addr(tb, kv, t, 8 * cc);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                 : "memory");
+  }
+  __syncwarp();
+}
+
 // Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
 // item per KV head (its chunks are reported as -inf).
 __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, int lane) {
@@ -796,14 +867,14 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
   }
 }
 
-template <int D, bool MMA, bool FUSED>
+template <int D, bool MMA, bool FUSED, bool Q8>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
   // aligned (smem_align) by an offset from the shared array itself, so that every access below is
   // compiled as a shared-memory access
   constexpr uint32_t kAlign = smem_align(MMA ? 2 : 1);
   unsigned char* base = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
-  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED, p.window > 0);
+  const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED, p.window > 0, Q8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
   StageMeta* metas = reinterpret_cast<StageMeta*>(base + L.meta_off);
   int* prefix = reinterpret_cast<int*>(base + L.prefix_off);
@@ -884,14 +955,16 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   const int nst = p.nstage;
   uint64_t* bar = bars + warp * nst;
   StageMeta* meta = metas + warp * nst;
-  unsigned char* stages = base + (size_t)warp * nst * L.stage_bytes;
+  unsigned char* stages = base + L.ring_off + (size_t)warp * nst * L.stage_bytes;
   unsigned char* qslots = base + L.q_off + (size_t)warp * kItemSlots * L.qslot_bytes;
   const uint32_t q_bytes = (uint32_t)(p.group * D * 2);
   const uint32_t cs_bytes = FUSED ? (uint32_t)(4 * D) : 0u;  // the query position's (cos, sin) row
   const uint32_t kv_bytes = FUSED ? (uint32_t)(4 * D) : 0u;  // the new token's raw k and v rows
   unsigned char* patch = base + L.patch_off + (size_t)warp * 4 * D;
   int* meta_pid = reinterpret_cast<int*>(base + L.pid_off) + warp * p.nstage;
-  const uint32_t page_bytes = (uint32_t)(64 * D);
+  constexpr int kBlk = int8_block_bytes(D);
+  const uint32_t page_bytes = Q8 ? (uint32_t)(2 * kBlk) : (uint32_t)(64 * D);
+  unsigned char* tile = base + (size_t)warp * 64 * D;  // int8 cache: the page expanded to fp16
   const uint64_t policy = l2_policy_evict_first();
 
   // Producer state: the item being issued (cur) and the next one, whose loads are in flight.
@@ -1026,7 +1099,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         }
       }
       unsigned char* dst = stages + (size_t)k * L.stage_bytes;
-      if constexpr (MMA) {
+      if constexpr (Q8) {
+        // the page's int8 K block and V block of this KV head, as stored
+        const unsigned char* kb = p.pool8 + (((long long)pid * 2) * p.hkv + cur.g) * kBlk;
+        bulk_load_hint_if(l0 && page_ok, dst, kb, kBlk, &bar[k], policy);
+        bulk_load_hint_if(l0 && page_ok, dst + kBlk, kb + (long long)p.hkv * kBlk, kBlk, &bar[k], policy);
+      } else if constexpr (MMA) {
         constexpr int E = GroupMma<D>::E;
 #pragma unroll
         for (int u = 0; u < D / E; ++u)
@@ -1278,7 +1356,16 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           if (mt.flags & kMetaPatch)
             apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
-        if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
+        if constexpr (Q8) {
+          if (nvalid > 0) {
+            expand_q8<D>(s1, tile, lane);
+            const float* ksc = reinterpret_cast<const float*>(s1 + 16 * D);
+            const float* vsc = reinterpret_cast<const float*>(s1 + kBlk + 16 * D);
+            cmp.page(tile, mt.lo(), nvalid, p.scale_log2, ksc, vsc);
+          }
+        } else {
+          if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
+        }
       }
     }
     if (fin.flags & kMetaLast) finish_item(fin);
@@ -1290,9 +1377,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   }
 }
 
-template <int D, bool MMA, bool FUSED>
+template <int D, bool MMA, bool FUSED, bool Q8 = false>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&decode_kernel<D, MMA, FUSED>);
+  return reinterpret_cast<void*>(&decode_kernel<D, MMA, FUSED, Q8>);
 }
 
 template <bool FUSED>
@@ -1305,16 +1392,25 @@ void* select_kernel_t(int head_dim, bool mma) {
   }
 }
 
-void* select_kernel(int head_dim, bool mma, bool fused) {
+void* select_kernel(int head_dim, bool mma, bool fused, bool q8) {
+  if (q8) {  // int8 cache: tensor-core path, separate launches only
+    if (!mma || fused) return nullptr;
+    switch (head_dim) {
+      case 64: return kernel_ptr<64, true, false, true>();
+      case 96: return kernel_ptr<96, true, false, true>();
+      case 128: return kernel_ptr<128, true, false, true>();
+      default: return nullptr;
+    }
+  }
   return fused ? select_kernel_t<true>(head_dim, mma) : select_kernel_t<false>(head_dim, mma);
 }
 
 }  // namespace
 
 // Deepest ring (at most 8, at least 2, else 0) of a CTA of `warps` warps within `budget` bytes.
-int ring_depth(int warps, int head_dim, int group, int batch, bool fused, bool windowed, int budget) {
+int ring_depth(int warps, int head_dim, int group, int batch, bool fused, bool windowed, int budget, bool q8 = false) {
   int n = 8;
-  while (n >= 2 && make_layout(warps, n, head_dim, group, batch, fused, windowed).total > budget) --n;
+  while (n >= 2 && make_layout(warps, n, head_dim, group, batch, fused, windowed, q8).total > budget) --n;
   return n >= 2 ? n : 0;
 }
 
@@ -1322,8 +1418,9 @@ int ring_depth(int warps, int head_dim, int group, int batch, bool fused, bool w
 // resident CTA, and the kernel's static shared memory).
 int cta_budget(int ctas) { return std::min(kSmemBudget, (kSmemPerSm - ctas * 1024) / ctas - 256); }
 
-DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool windowed) {
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool windowed, bool q8) {
   DecodeConfig c;
+  c.q8 = q8;
   c.mma = group >= 2;
   c.fused = fused;
   // Warps per SM: the most stages in flight per SM (warps x ring depth) that fit the plain layout
@@ -1341,13 +1438,13 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
   }
   c.warps = sm_warps;
   c.ctas_per_sm = 1;
-  c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget);
+  c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget, q8);
   // The SM's warps split over kCtasPerSm CTAs when the ring stays as deep: a CTA that is still
   // merging at the end of a launch then holds only its share of the SM, and the next launch's CTAs
   // start (and run their prologue) in the rest.
   if (kCtasPerSm > 1 && sm_warps % kCtasPerSm == 0) {
     const int w = sm_warps / kCtasPerSm;
-    const int n = ring_depth(w, head_dim, group, batch, fused, windowed, cta_budget(kCtasPerSm));
+    const int n = ring_depth(w, head_dim, group, batch, fused, windowed, cta_budget(kCtasPerSm), q8);
     if (n >= c.nstage && n >= 2) {
       c.warps = w;
       c.ctas_per_sm = kCtasPerSm;
@@ -1356,7 +1453,7 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
   }
   const int nstage = c.nstage;
   c.smem_bytes =
-      nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused, windowed).total : 0;
+      nstage >= 2 ? (size_t)make_layout(c.warps, nstage, head_dim, group, batch, fused, windowed, q8).total : 0;
   // The pool's tensor map always has the swizzled boxes the tensor-core layouts read (the
   // CUDA-core path copies plain runs instead; the prefill kernel uses the map for every group).
   c.box_inner = head_dim == 96 ? 32 : 64;
@@ -1365,7 +1462,7 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
 }
 
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
-  void* k = select_kernel(head_dim, cfg.mma, cfg.fused);
+  void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8);
   if (k == nullptr) return cudaErrorInvalidValue;
   const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e != cudaSuccess) return e;
@@ -1374,7 +1471,7 @@ cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl) {
-  void* k = select_kernel(head_dim, cfg.mma, cfg.fused);
+  void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8);
   if (k == nullptr || cfg.smem_bytes == 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);

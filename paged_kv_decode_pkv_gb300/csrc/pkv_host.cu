@@ -22,6 +22,7 @@ struct pkv_cache {
   int num_sms = 0;
   int group = 1;
   bool pdl = false;
+  bool int8 = false;  // PKV_OPT_INT8_KV: int8 blocks with per-slot scales
 };
 
 namespace {
@@ -202,6 +203,11 @@ size_t pkv_pool_bytes(int num_pages, int num_kv_heads, int head_dim) {
   return (size_t)num_pages * 2 * num_kv_heads * PKV_PAGE_SIZE * head_dim * 2;
 }
 
+size_t pkv_pool_bytes_int8(int num_pages, int num_kv_heads, int head_dim) {
+  if (num_pages <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return (size_t)num_pages * 2 * num_kv_heads * pkv::int8_block_bytes(head_dim);
+}
+
 size_t pkv_rope_table_bytes(int max_position, int head_dim) {
   if (max_position <= 0 || head_dim <= 0 || head_dim % 2) return 0;
   return (size_t)max_position * (head_dim / 2) * 2 * sizeof(float);
@@ -240,7 +246,9 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   if (!aligned(d->rope_table, 16)) return PKV_ERR_INVALID_ARG;
   for (int l = 0; l < d->num_layers; ++l)
     if (d->layer_pools[l] == nullptr || !aligned(d->layer_pools[l], 256)) return PKV_ERR_INVALID_ARG;
-  if (d->options & ~(PKV_OPT_PDL | PKV_OPT_EARLY_PAGES)) return PKV_ERR_INVALID_ARG;
+  if (d->options & ~(PKV_OPT_PDL | PKV_OPT_EARLY_PAGES | PKV_OPT_INT8_KV)) return PKV_ERR_INVALID_ARG;
+  if ((d->options & PKV_OPT_INT8_KV) && d->num_qo_heads / d->num_kv_heads < 2)
+    return fail(PKV_ERR_UNSUPPORTED, "int8 KV cache: the tensor-core path (Hq / Hkv >= 2) only");
   for (int l = 0; l < d->num_layers; ++l) {
     if (d->layer_window != nullptr && d->layer_window[l] < 0) return PKV_ERR_INVALID_ARG;
     if (d->layer_sinks != nullptr && d->layer_sinks[l] != nullptr && !aligned(d->layer_sinks[l], 4))
@@ -265,6 +273,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   c->desc.layer_sinks = nullptr;
   c->group = group;
   c->pdl = (d->options & PKV_OPT_PDL) != 0;
+  c->int8 = (d->options & PKV_OPT_INT8_KV) != 0;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e != cudaSuccess) {
@@ -295,6 +304,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   const DecodeConfig cfg = pkv::decode_config(group, D, 1);
   e = pkv::decode_prepare(cfg, D);
   if (e == cudaSuccess) e = pkv::decode_prepare(pkv::decode_config(group, D, 1, true), D);
+  if (e == cudaSuccess && c->int8) e = pkv::decode_prepare(pkv::decode_config(group, D, 1, false, false, true), D);
   if (e == cudaSuccess) e = pkv::qkv_prepare();
   if (e == cudaSuccess) e = pkv::prefill_prepare();
   if (e == cudaSuccess) e = pkv::append_prepare();
@@ -304,7 +314,8 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
     return cuda_fail("setting kernel attributes", e);
   }
   c->maps.resize(d->num_layers);
-  for (int l = 0; l < d->num_layers; ++l) {
+  if (c->int8) memset(c->maps.data(), 0, sizeof(CUtensorMap) * c->maps.size());  // int8 pages use plain copies
+  for (int l = 0; l < d->num_layers && !c->int8; ++l) {
     const cuuint64_t gdim[4] = {(cuuint64_t)D, (cuuint64_t)PKV_PAGE_SIZE, (cuuint64_t)d->num_kv_heads,
                                 (cuuint64_t)d->num_pages * 2};
     const cuuint64_t gstride[3] = {(cuuint64_t)D * 2, (cuuint64_t)PKV_PAGE_SIZE * D * 2,
@@ -371,6 +382,12 @@ pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k
   p.head_dim = c->desc.head_dim;
   p.max_position = c->desc.max_position;
   p.num_pages = c->desc.num_pages;
+  if (c->int8) {
+    p.pool = nullptr;
+    p.pool8 = static_cast<unsigned char*>(c->pools[layer]);
+    return launch_status("append_rope launch", pkv::launch_append_q8(p, stream, c->pdl));
+  }
+  p.pool8 = nullptr;
   return launch_status("append_rope launch", pkv::launch_append(p, stream, c->pdl));
 }
 
@@ -411,6 +428,7 @@ pkv_status pkv_qkv_append_rope(pkv_cache* c, int layer, const void* x, const uin
   const pkv_status st = qkv_params(c, x, w, scales, hidden, num_tokens, &p);
   if (st != PKV_OK) return st;
   if (layer < 0 || layer >= c->desc.num_layers || batch < 0) return fail(PKV_ERR_INVALID_ARG, "layer or batch");
+  if (c->int8) return fail(PKV_ERR_UNSUPPORTED, "int8 cache: use pkv_qkv_project and pkv_append_rope");
   if (num_tokens == 0 || batch == 0) return PKV_OK;
   if (pos_map == nullptr || append_indptr == nullptr || page_indptr == nullptr || page_indices == nullptr ||
       q_out == nullptr)
@@ -443,6 +461,7 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
                                  float sm_scale, void* out, float* lse_out, pkv_stream_t stream) {
   if (c == nullptr || layer < 0 || layer >= c->desc.num_layers || num_tokens < 0 || batch < 0)
     return fail(PKV_ERR_INVALID_ARG, "cache, layer or sizes");
+  if (c->int8) return fail(PKV_ERR_UNSUPPORTED, "int8 cache: prefill attention reads fp16 pages");
   if (num_tokens == 0 || batch == 0) return PKV_OK;
   if (batch > pkv::kMaxDecodeBatch) return fail(PKV_ERR_UNSUPPORTED, "batch above 4096 sequences");
   if (q_rope == nullptr || append_indptr == nullptr || pos_map == nullptr || page_indptr == nullptr ||
@@ -542,7 +561,8 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
                            fused->q_out == q_rope))
     return fail(PKV_ERR_INVALID_ARG, "misaligned or aliased q/k/v/q_out");
   const int D = c->desc.head_dim;
-  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch, fused != nullptr, window > 0);
+  if (c->int8 && fused != nullptr) return fail(PKV_ERR_UNSUPPORTED, "int8 cache: one-launch layout");
+  const DecodeConfig cfg = pkv::decode_config(c->group, D, batch, fused != nullptr, window > 0, c->int8);
   if (cfg.nstage < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this batch");
   pkv::DecodeParams p;
   p.q = static_cast<const __half*>(q_rope);
@@ -590,6 +610,8 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   // Early page copies measured faster on the tensor-core path (GQA long context: 6 400 -> 6 600 GB/s)
   // and slower on the CUDA-core path (single stream: 3 230 -> 3 125 GB/s), so only there.
   p.early = (fused != nullptr && (c->desc.options & PKV_OPT_EARLY_PAGES) && c->group >= 2) ? 1 : 0;
+  p.pool8 = c->int8 ? static_cast<const unsigned char*>(c->pools[layer]) : nullptr;
+  if (c->int8) p.pool = nullptr;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
 }
 
@@ -615,8 +637,9 @@ pkv_status pkv_append_decode_attention(pkv_cache* c, int layer, const void* q, c
                                        float* partial_o, float* partial_lse, int32_t* chunk_counters, void* out,
                                        float* lse_out, int* splits_used, pkv_stream_t stream) {
   if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative num_tokens");
-  if (num_tokens != batch) {
-    // several new tokens per sequence (a chunked append): the append launch, then the merged decode
+  if (num_tokens != batch || c->int8) {
+    // several new tokens per sequence (a chunked append), or an int8 cache: the append launch, then
+    // the merged decode
     const pkv_status st = pkv_append_rope(c, layer, q, k, v, pos_map, append_indptr, num_tokens, batch,
                                           page_indptr, page_indices, q_out, stream);
     if (st != PKV_OK) return st;

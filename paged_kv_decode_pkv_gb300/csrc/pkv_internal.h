@@ -34,6 +34,7 @@ struct AppendParams {
   const float2* rope;  // [max_position][head_dim / 2] (cos, sin)
   int* status;
   int num_tokens, batch, hq, hkv, head_dim, max_position, num_pages;
+  unsigned char* pool8;  // int8 cache (PKV_OPT_INT8_KV): blocks [num_pages][2][hkv][16 * d + 64]
 };
 
 // QKV projection (Q4F16_1) fused with RoPE and the KV append.
@@ -128,6 +129,7 @@ struct DecodeParams {
   int window;
   const float* sinks;
   int early;  // one-launch mode: copy pages before the launch wait (PKV_OPT_EARLY_PAGES)
+  const unsigned char* pool8;  // int8 cache: blocks [num_pages][2][hkv][16 * d + 64]
 };
 
 struct CombineParams {
@@ -143,6 +145,7 @@ struct CombineParams {
 struct DecodeConfig {
   bool mma;             // tensor-core path (group >= 2)
   bool fused;           // append folded into the decode
+  bool q8;              // int8 cache
   int warps;            // warps per CTA
   int ctas_per_sm;      // resident CTAs per SM (the grid of a full launch is SMs x this)
   int nstage;           // per-warp ring depth
@@ -151,11 +154,14 @@ struct DecodeConfig {
   int swizzle_bytes;    // 0 (none), 64 or 128
 };
 
-DecodeConfig decode_config(int group, int head_dim, int batch, bool fused = false, bool windowed = false);
+DecodeConfig decode_config(int group, int head_dim, int batch, bool fused = false, bool windowed = false,
+                           bool q8 = false);
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim);  // function attributes
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_append_q8(const AppendParams& p, cudaStream_t stream, bool pdl);
+__host__ __device__ constexpr int int8_block_bytes(int head_dim) { return 16 * head_dim + 64; }
 cudaError_t append_prepare();   // function attributes (shared-memory carveout)
 cudaError_t combine_prepare();
 cudaError_t qkv_prepare();

@@ -81,3 +81,18 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkv, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         pkv.lib()
+
+
+def test_int8_cache_needs_a_query_group(lib):
+    """The int8 cache runs on the tensor-core path only: one query head per KV head is refused
+    before any device call."""
+    import ctypes
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    pools = (ctypes.c_void_p * 1)(256)
+    d = pkv._Desc(1, 10, 16, 8, 8, 128, 100, 1e4, ctypes.cast(pools, ctypes.POINTER(ctypes.c_void_p)), 256, 256,
+                  pkv.OPT_INT8_KV)
+    out = ctypes.c_void_p()
+    assert lib.pkv_create_cache(ctypes.byref(d), ctypes.byref(out)) == pkv.ERR_UNSUPPORTED
+    assert lib.pkv_pool_bytes_int8(10, 8, 128) == 10 * 2 * 8 * (16 * 128 + 64)

@@ -151,3 +151,18 @@ def test_int8_split_and_combine_equal_unsplit():
     out, _, lse = oracle.combine(po, pl)
     np.testing.assert_allclose(out, ref, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def test_quantize_pool_matches_the_row_quantizer():
+    rng = np.random.default_rng(7)
+    pool, q, pi, px, last = random_paged_case(rng, [20, 5], 2, 2, 16)
+    g = oracle.Geometry(pool.shape[0], 2, 2, 16, 1 << 20, 1e4)
+    pool8 = oracle.quantize_pool(g, pool)
+    for page in range(pool.shape[0]):
+        for kv in range(2):
+            for h in range(2):
+                for slot in range(16):
+                    codes, sc = oracle.quantize_row(pool[page, kv, h, slot])
+                    blk = pool8[page, kv, h]
+                    assert np.array_equal(blk[slot * 16:(slot + 1) * 16].view(np.int8), codes)
+                    assert blk[256 + 4 * slot:256 + 4 * slot + 4].view(np.float32)[0] == sc or (np.isnan(sc))
