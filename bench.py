@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size")
     ap.add_argument("--pool-pages", type=int, default=0, help="override the pool size in pages")
+    ap.add_argument("--int8", action="store_true",
+                    help="int8 KV cache (PKV_OPT_INT8_KV; workloads with Hq / Hkv >= 2): the history is "
+                         "appended through the library's quantizing append; bytes are the int8 blocks read")
     return ap.parse_args()
 
 
@@ -392,6 +395,60 @@ def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, o
             "with_decode": "per layer: pkv_qkv_append_rope + pkv_decode_attention_merged"}
 
 
+def kv_bytes_layer(step: W.Step, int8: bool) -> int:
+    """Algorithmic KV bytes one layer's decode reads: fp16 K and V, or (int8 cache) the int8 codes
+    and the fp32 scale of every attended slot."""
+    if not int8:
+        return step.kv_bytes()
+    cfg = step.cfg
+    seen = np.minimum(step.seq_len, cfg.window) if cfg.window > 0 else step.seq_len
+    return int(seen.sum()) * cfg.hkv * 2 * (cfg.head_dim + 4)
+
+
+def int8_pools(step: W.Step, cfg, layers, dev):
+    """int8 pools whose history (every position but the step's new tokens) went through the
+    library's quantizing append: seeded raw k and v rows appended sequence by sequence."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+    from pkv_inputs import dev_fill_range, key
+
+    if cfg.hq // cfg.hkv < 2:
+        raise SystemExit("--int8 needs a workload with Hq / Hkv >= 2")
+    blk = 16 * cfg.head_dim + 64
+    pools = [torch.zeros((step.num_pages, 2, cfg.hkv, blk), dtype=torch.uint8, device=dev) for _ in layers]
+    builder = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+                        pools=pools, options=pkv.OPT_INT8_KV)
+    pi = torch.from_numpy(step.page_indptr.astype(np.int32)).to(dev)
+    px = torch.from_numpy(step.page_indices.astype(np.int32)).to(dev)
+    cached = (step.seq_len - step.new_tokens).astype(np.int64)
+    for l in layers:
+        for s in range(step.batch):
+            n = int(cached[s])
+            if n <= 0:
+                continue
+            rows = n * cfg.hkv * cfg.head_dim
+            k = torch.empty(rows, dtype=torch.float16, device=dev)
+            v = torch.empty(rows, dtype=torch.float16, device=dev)
+            seed = step.seed + 1000003 * (l + 1)
+            dev_fill_range(k.data_ptr(), rows, key(seed, 2 * s), 0, cfg.value_scale)
+            dev_fill_range(v.data_ptr(), rows, key(seed, 2 * s + 1), 0, cfg.value_scale)
+            q = torch.zeros((n, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev)
+            seq_pi = torch.tensor([0, int(step.page_indptr[s + 1] - step.page_indptr[s])], dtype=torch.int32,
+                                  device=dev)
+            seq_px = px[int(step.page_indptr[s]):int(step.page_indptr[s + 1])].contiguous()
+            pos = torch.arange(n, dtype=torch.int32, device=dev)
+            ai = torch.tensor([0, n], dtype=torch.int32, device=dev)
+            builder.append_rope(l, q, k.view(n, cfg.hkv, cfg.head_dim), v.view(n, cfg.hkv, cfg.head_dim), pos, ai,
+                                seq_pi, seq_px)
+    torch.cuda.synchronize()
+    code, flags = builder.check_status()
+    if code != 0:
+        raise RuntimeError(f"int8 history append: status {code} flags {flags:#x}")
+    del builder, pi
+    return pools
+
+
 def staged(arrays, dev):
     """One pinned host buffer and one device buffer holding `arrays` at 256-byte aligned offsets;
     returns (host, device, device views with each array's shape and dtype: fp16 for uint16 bits)."""
@@ -429,12 +486,13 @@ def run_ours(args):
     cfg = workload(args)
     step = W.make_step(cfg, rank_seed(cfg, rank))
     layers = list(range(cfg.layers))
-    pools = [W.device_pool(step, l) for l in layers]
+    pools = int8_pools(step, cfg, layers, dev) if args.int8 else [W.device_pool(step, l) for l in layers]
     # layer variants of the workload: sliding window and attention sinks
     windows = [cfg.window] * cfg.layers if cfg.window else None
     sinks = [torch.from_numpy(W.sink_logits(step, l)).to(dev) for l in layers] if cfg.sinks else None
     cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES, windows=windows, sinks=sinks)
+                      pools=pools, options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES | (pkv.OPT_INT8_KV if args.int8 else 0),
+                      windows=windows, sinks=sinks)
     B, T = step.batch, step.num_tokens
     total_pages = int(step.page_indptr[-1])
     S, chunk = cache.plan_decode(B, step.max_pages_per_seq, total_pages)
@@ -566,7 +624,7 @@ def run_ours(args):
     code, flags = cache.check_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after the timed region: {pkv.status_string(code)} flags {flags:#x}")
-    kv_step = step.kv_bytes() * cfg.layers
+    kv_step = kv_bytes_layer(step, args.int8) * cfg.layers
     value = world * kv_step / (step_ms * 1e-3) / 1e9
 
     # ---- per-kernel durations: events around each layer's decode launch on the launching stream ----
@@ -576,7 +634,7 @@ def run_ours(args):
     # headline step's: the one-launch decode (append, split-K decode and merge); with chunked
     # appends, the merged decode after the append launch.
     plain = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=0, windows=windows, sinks=sinks)
+                      pools=pools, options=pkv.OPT_INT8_KV if args.int8 else 0, windows=windows, sinks=sinks)
 
     def layer_chain_plain(l, events):
         q, k, v = qkv[l]
@@ -609,7 +667,7 @@ def run_ours(args):
                 i += 1
     torch.cuda.synchronize()
     dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    kv_layer = step.kv_bytes()
+    kv_layer = kv_bytes_layer(step, args.int8)
     # With one launch per layer the timed region is nothing but this kernel, launched back to back
     # (programmatic dependent launch overlaps each prologue with the previous launch), so its
     # average launch duration there is the step time over the launches.  With chunked appends the
@@ -652,8 +710,8 @@ def run_ours(args):
         return max_over_ranks((time.perf_counter() - t0) / args.steps)
 
     # ---- the pages' fused QKV dispatch: Q4F16_1 projection + RoPE + append, then the decode -----
-    prefill = prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, dev)
-    qkv_proj = qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages,
+    prefill = None if args.int8 else prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, dev)
+    qkv_proj = None if args.int8 else qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages,
                            stream, time_graph, dev)
 
     e2e_s = timed_e2e(e2e_graph.replay)
@@ -665,12 +723,14 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16 data, f32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": "int8 KV codes, f16 queries, f32 accumulate" if args.int8 else "f16 data, f32 accumulate", "data": "synthetic",
         "config": {"workload": cfg.name, "layers": cfg.layers, "batch": B, "q_heads": cfg.hq,
                    "kv_heads": cfg.hkv, "head_dim": cfg.head_dim, "page_size": 16,
                    "context_tokens": int(step.seq_len.sum()), "kv_bytes_per_step": kv_step,
                    "splits": S, "chunk_pages": chunk,
                    **({"window": cfg.window} if cfg.window else {}),
+                   **({"kv_cache": "int8 blocks (codes + fp32 scale per slot); bytes are those read",
+                       "fp16_equivalent_kv_bytes_per_step": step.kv_bytes() * cfg.layers} if args.int8 else {}),
                    **({"attention_sinks": "per layer and query head"} if cfg.sinks else {}),
                    "l2": f"inputs larger than L2: {kv_step / 1e9:.2f} GB of KV per step",
                    "launch": "CUDA graph of the step, programmatic dependent launch, early page copies",
