@@ -342,8 +342,8 @@ def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, o
     import paged_kv_decode_pkv_gb300 as pkv
 
     hidden = W.qkv_hidden(cfg)
-    if hidden > 4096 or hidden % 32:
-        return None
+    if hidden > 4096 or hidden % 32 or step.num_tokens > 256:
+        return None  # a large token count makes the projection a GEMM, which this kernel is not
     ws = []
     for l in layers:
         w, sc = W.qkv_weights(step, l)
