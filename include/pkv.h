@@ -84,8 +84,8 @@ typedef enum {
                                    pages before that wait, so the copies overlap the end of the
                                    previous kernel; the new tokens' q, k, v are read after it.  The
                                    kernel launched right before must not write this layer's pool.
-                                   Applied when Hq / Hkv >= 2 (tensor-core path), where it measured
-                                   faster; ignored otherwise. */
+                                   The whole ring goes early when Hq / Hkv >= 2 (tensor-core path),
+                                   two stages per warp otherwise (the depths that measured fastest). */
 
 typedef struct pkv_cache pkv_cache; /* opaque, host-only */
 

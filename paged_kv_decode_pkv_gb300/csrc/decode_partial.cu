@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   }
 
   if (!waited) {
-    while (issued < nst && produce()) {
+    while (issued < min(nst, p.early) && produce()) {
     }
     pdl_wait();  // the new token's q, k, v come from the preceding kernel
     waited = true;

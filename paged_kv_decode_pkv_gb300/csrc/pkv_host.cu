@@ -29,6 +29,9 @@ namespace {
 
 using pkv::DecodeConfig;
 
+constexpr int kEarlyStagesOneHead = 2;  // early stages per warp on the CUDA-core path
+constexpr int kEarlyStagesGroup = 8;    // and on the tensor-core path (the whole ring)
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -607,9 +610,13 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   p.max_position = c->desc.max_position;
   p.window = window;
   p.sinks = c->sinks[layer];
-  // Early page copies measured faster on the tensor-core path (GQA long context: 6 400 -> 6 600 GB/s)
-  // and slower on the CUDA-core path (single stream: 3 230 -> 3 125 GB/s), so only there.
-  p.early = (fused != nullptr && (c->desc.options & PKV_OPT_EARLY_PAGES) && c->group >= 2) ? 1 : 0;
+  // Early page copies, measured: tensor-core path, the whole ring (GQA long context 6 400 -> 6 580
+  // GB/s; 1 to 3 stages were slower); CUDA-core path, two stages per warp (single stream 3 230 ->
+  // 3 510 GB/s; one stage 3 390, three 3 435, the whole ring 3 125, where the early copies slow the
+  // previous launch's merge tail).
+  p.early = 0;
+  if (fused != nullptr && (c->desc.options & PKV_OPT_EARLY_PAGES))
+    p.early = c->group >= 2 ? kEarlyStagesGroup : kEarlyStagesOneHead;
   p.pool8 = c->int8 ? static_cast<const unsigned char*>(c->pools[layer]) : nullptr;
   if (c->int8) p.pool = nullptr;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));

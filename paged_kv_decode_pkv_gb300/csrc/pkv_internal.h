@@ -128,7 +128,7 @@ struct DecodeParams {
   // log, units of the scaled scores; nullable) that join the merge's denominator.
   int window;
   const float* sinks;
-  int early;  // one-launch mode: copy pages before the launch wait (PKV_OPT_EARLY_PAGES)
+  int early;  // one-launch mode: stages per warp copied before the launch wait (PKV_OPT_EARLY_PAGES)
   const unsigned char* pool8;  // int8 cache: blocks [num_pages][2][hkv][16 * d + 64]
 };
 
