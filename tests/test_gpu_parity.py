@@ -159,8 +159,8 @@ def test_device_generator_matches_host():
 
 def _full_size_check(cid, layers_to_check, seqs_fn):
     """The workload at its full size, launched as bench.py launches it (pkv_append_decode_attention
-    per layer, programmatic dependent launch, the planner's automatic split), checked on sampled
-    sequences regenerated on the host."""
+    per layer, programmatic dependent launch with early page copies, the planner's automatic split),
+    checked on sampled sequences regenerated on the host."""
     import torch
 
     import paged_kv_decode_pkv_gb300 as pkv
@@ -173,7 +173,8 @@ def _full_size_check(cid, layers_to_check, seqs_fn):
     sinks_host = [W.sink_logits(step, l) for l in layers] if cfg.sinks else None
     sinks = [torch.from_numpy(x).cuda() for x in sinks_host] if cfg.sinks else None
     cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                      pools=pools, options=pkv.OPT_PDL, windows=[cfg.window] * cfg.layers if cfg.window else None,
+                      pools=pools, options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES,
+                      windows=[cfg.window] * cfg.layers if cfg.window else None,
                       sinks=sinks)
     tp = int(step.page_indptr[-1])
     counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")

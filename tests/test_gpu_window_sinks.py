@@ -39,9 +39,9 @@ def _setup(name, window, with_sinks, seed_extra=0):
     sinks_host = (rng.standard_normal(cfg.hq) * 2).astype(np.float32) if with_sinks else None
     sinks = torch.from_numpy(sinks_host).cuda() if with_sinks else None
 
-    def cache_over(pool_dev):
+    def cache_over(pool_dev, options=0):
         return pkv.Cache(1, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
-                         pools=[pool_dev], windows=[window], sinks=[sinks])
+                         pools=[pool_dev], windows=[window], sinks=[sinks], options=options)
 
     return step, host_pool, sinks_host, sinks, cache_over
 
@@ -114,8 +114,11 @@ def test_windowed_partials_combine_and_merged_agree(name, window, plan):
 
 @pytest.mark.parametrize("name", ["tiny", "ragged_d96", "gqa2_d96", "gqa8_d128"])
 @pytest.mark.parametrize("window", [1, 17, 100])
-def test_windowed_one_launch_step_is_bit_identical(name, window):
+@pytest.mark.parametrize("early", [False, True])
+def test_windowed_one_launch_step_is_bit_identical(name, window, early):
     import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
 
     step, host_pool, sinks_host, sinks, cache_over = _setup(name, window, True, seed_extra=11)
     cfg = step.cfg
@@ -123,7 +126,8 @@ def test_windowed_one_launch_step_is_bit_identical(name, window):
         pytest.skip("one-launch layout needs one new token per sequence")
     pool_a = H.to_dev(host_pool, torch.float16)
     pool_b = H.to_dev(host_pool, torch.float16)
-    cache_a, cache_b = cache_over(pool_a), cache_over(pool_b)
+    cache_a = cache_over(pool_a)
+    cache_b = cache_over(pool_b, (pkv.OPT_PDL | pkv.OPT_EARLY_PAGES) if early else 0)
     tabs = H.device_tables(step)
     q, k, v = H.device_qkv(step, 0)
     tp = int(step.page_indptr[-1])
