@@ -1,8 +1,11 @@
 """Benchmark of the decode-step paged-KV attention path (append -> split-K decode -> combine).
 
-Default workload: the Phi-3-mini-shaped single-stream decode (32 layers, 32 heads of 96, batch 1,
-context 4096, 16-slot pages, identity page table).  One step runs the whole path for every layer;
-the step is captured once as a CUDA graph with programmatic dependent launch and replayed.
+Default workload: the long-context GQA decode (28 layers, 16 query heads / 8 KV heads of 128,
+batch 8 x 32 768 tokens, 16-slot pages, 1 % outlier keys), the largest single-GPU workload and
+one of the two the 70 % HBM-roofline target is set on.  One step runs the whole path for every
+layer; the step is captured once as a CUDA graph with programmatic dependent launch and replayed.
+The same JSON line also carries the other workloads (mixed serving, ragged batch, single stream,
+sliding window), each timed the same way under the same clock sampling (`extra_workloads`).
 
 Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
 Multi-GPU runs (torchrun) are independent replicas: the path has no exchange step.
@@ -29,9 +32,15 @@ if ROOT not in sys.path:
 from pkv_inputs import workloads as W  # noqa: E402
 
 METRIC = "decode-attention KV GB/s & % of GB300 HBM roofline; attention µs/step/layer"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 4
+DEFAULT_EXTRA = "5,3,2,6"  # the other workloads, timed after the headline one
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_phi3_b1_ctx4096.md")
+# ncu summaries of the headline kernel (per workload id): per-launch DRAM bytes and the hash of the
+# kernel sources they were taken from
+PROFILE_SUMMARY = {
+    2: os.path.join(ROOT, "profiles", "decode_kernel_phi3_b1_ctx4096.md"),
+    4: os.path.join(ROOT, "profiles", "decode_kernel_gqa16x8_d128_b8_ctx32768.md"),
+}
 # the decode kernel's sources, in the order their bytes are hashed for the profile summary
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_decode_pkv_gb300", "csrc", f) for f in
                   ("decode_partial.cu", "merge.cuh", "ptx.cuh", "rope.cuh", "pkv_internal.h")]
@@ -57,12 +66,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bound of the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="bound of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # smaller variants of a workload, for profiler captures of the same kernels
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size")
     ap.add_argument("--pool-pages", type=int, default=0, help="override the pool size in pages")
+    ap.add_argument("--extra", default=DEFAULT_EXTRA,
+                    help="comma-separated workload ids timed after the headline one ('' for none)")
     ap.add_argument("--int8", action="store_true",
                     help="int8 KV cache (PKV_OPT_INT8_KV; workloads with Hq / Hkv >= 2): the history is "
                          "appended through the library's quantizing append; bytes are the int8 blocks read")
@@ -92,11 +103,13 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def ncu_traffic(cid: int):
+    """Per-launch DRAM bytes of the decode kernel on workload `cid` from the committed ncu summary,
+    or None when there is none or the kernel source changed since the counters were taken."""
+    if cid not in PROFILE_SUMMARY:
+        return None
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY[cid]).read()
         src = decode_sources_sha256()
         m_hash = re.search(r"kernel sources sha256:\s*([0-9a-f]{64})", text)
         m_val = re.search(r"dram bytes per launch:\s*([0-9]+)", text)
@@ -193,9 +206,10 @@ def oracle_sample(step: W.Step, seconds: float, max_layers: int):
 
     from tests import harness as H
 
-    # bound the sample to one sequence when a layer is large, so a few layers fit in the budget
+    # bound the sample to one sequence when a layer is larger than the long-context GQA layer
+    # (1.07 GB, timed whole)
     seqs = list(range(step.batch))
-    if step.kv_bytes() > 256e6:
+    if step.kv_bytes() > 1.2e9:
         seqs = [int(np.argmax(step.seq_len))]
     sub = W.substep(step, seqs) if len(seqs) < step.batch else step
     done_bytes, done_time, layers = 0, 0.0, 0
@@ -406,8 +420,9 @@ def kv_bytes_layer(step: W.Step, int8: bool) -> int:
 
 
 def int8_pools(step: W.Step, cfg, layers, dev):
-    """int8 pools whose history (every position but the step's new tokens) went through the
-    library's quantizing append: seeded raw k and v rows appended sequence by sequence."""
+    """int8 pools, one per entry of `layers` (workload layer ids), whose history (every position
+    but the step's new tokens) went through the library's quantizing append: seeded raw k and v
+    rows of that layer appended sequence by sequence."""
     import torch
 
     import paged_kv_decode_pkv_gb300 as pkv
@@ -417,12 +432,12 @@ def int8_pools(step: W.Step, cfg, layers, dev):
         raise SystemExit("--int8 needs a workload with Hq / Hkv >= 2")
     blk = 16 * cfg.head_dim + 64
     pools = [torch.zeros((step.num_pages, 2, cfg.hkv, blk), dtype=torch.uint8, device=dev) for _ in layers]
-    builder = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+    builder = pkv.Cache(len(layers), step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
                         pools=pools, options=pkv.OPT_INT8_KV)
     pi = torch.from_numpy(step.page_indptr.astype(np.int32)).to(dev)
     px = torch.from_numpy(step.page_indices.astype(np.int32)).to(dev)
     cached = (step.seq_len - step.new_tokens).astype(np.int64)
-    for l in layers:
+    for slot, l in enumerate(layers):
         for s in range(step.batch):
             n = int(cached[s])
             if n <= 0:
@@ -439,8 +454,8 @@ def int8_pools(step: W.Step, cfg, layers, dev):
             seq_px = px[int(step.page_indptr[s]):int(step.page_indptr[s + 1])].contiguous()
             pos = torch.arange(n, dtype=torch.int32, device=dev)
             ai = torch.tensor([0, n], dtype=torch.int32, device=dev)
-            builder.append_rope(l, q, k.view(n, cfg.hkv, cfg.head_dim), v.view(n, cfg.hkv, cfg.head_dim), pos, ai,
-                                seq_pi, seq_px)
+            builder.append_rope(slot, q, k.view(n, cfg.hkv, cfg.head_dim), v.view(n, cfg.hkv, cfg.head_dim), pos,
+                                ai, seq_pi, seq_px)
     torch.cuda.synchronize()
     code, flags = builder.check_status()
     if code != 0:
@@ -473,8 +488,6 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    import paged_kv_decode_pkv_gb300 as pkv
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -484,6 +497,126 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     cfg = workload(args)
+    line = measure_headline(args, cfg, world, rank, local, dev)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # the headline workload's pools are released before the next ones
+    extra = [] if args.int8 else [int(x) for x in args.extra.split(",") if x.strip()]
+    if extra:
+        line["extra_workloads"] = {}
+        for cid in extra:
+            res = measure_extra(args, W.CONFIGS[cid], world, rank, local, dev)
+            line["extra_workloads"][res["workload"]] = res
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        step = W.make_step(cfg, rank_seed(cfg, rank))
+        gbs, threads, what = oracle_sample(step, args.cpu_seconds, cfg.layers)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": what}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_extra(args, cfg, world, rank, local, dev):
+    """Another workload timed like the headline one: its whole step (every layer, the headline
+    layer step per layer) captured as one CUDA graph with programmatic dependent launch and early
+    page copies, replayed K times after W warm-up replays, with the clocks sampled meanwhile.
+    Inputs resident in HBM; every step reads more KV than the L2 holds."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    step = W.make_step(cfg, rank_seed(cfg, rank))
+    layers = list(range(cfg.layers))
+    pools = [W.device_pool(step, l) for l in layers]
+    windows = [cfg.window] * cfg.layers if cfg.window else None
+    sinks = [torch.from_numpy(W.sink_logits(step, l)).to(dev) for l in layers] if cfg.sinks else None
+    cache = pkv.Cache(cfg.layers, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+                      pools=pools, options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES, windows=windows, sinks=sinks)
+    B, T = step.batch, step.num_tokens
+    total_pages = int(step.page_indptr[-1])
+    S, chunk = cache.plan_decode(B, step.max_pages_per_seq, total_pages)
+    tabs = {k: torch.from_numpy(np.ascontiguousarray(getattr(step, k), dtype=np.int32)).to(dev) for k in
+            ("pos_map", "append_indptr", "page_indptr", "page_indices", "last_page_len")}
+    qkv = []
+    for l in layers:
+        q, k, v = W.new_qkv(step, l)
+        qkv.append(tuple(torch.from_numpy(x).view(torch.float16).to(dev) for x in (q, k, v)))
+    q_out = [torch.empty((T, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
+    po = torch.empty((B, cfg.hq, S, cfg.head_dim), dtype=torch.float32, device=dev)
+    pl = torch.empty((B, cfg.hq, S), dtype=torch.float32, device=dev)
+    outs = [torch.empty((B, cfg.hq, cfg.head_dim), dtype=torch.float16, device=dev) for _ in layers]
+    lses = [torch.empty((B, cfg.hq), dtype=torch.float32, device=dev) for _ in layers]
+    counters = torch.zeros(B * cfg.hkv, dtype=torch.int32, device=dev)
+
+    def step_fn():
+        for l in layers:
+            q, k, v = qkv[l]
+            cache.append_decode_attention(l, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                                          tabs["page_indices"], tabs["last_page_len"], step.max_pages_per_seq,
+                                          counters, total_pages=total_pages, q_out=q_out[l], partial_o=po,
+                                          partial_lse=pl, out=outs[l], lse=lses[l])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step_fn()
+    torch.cuda.synchronize()
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"{cfg.name}: device status {pkv.status_string(code)} flags {flags:#x}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_fn()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def time_graph(g):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            ev0.record()
+            for _ in range(args.steps):
+                g.replay()
+            ev1.record()
+        torch.cuda.synchronize()
+        return reduce_max(ev0.elapsed_time(ev1) / args.steps, world, dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms = time_graph(graph)
+    code, flags = cache.check_status(stream)
+    if code != 0:
+        raise RuntimeError(f"{cfg.name}: device status after the timed region {pkv.status_string(code)} "
+                           f"flags {flags:#x}")
+    peak, _ = measured_peaks()
+    kv_step = step.kv_bytes() * cfg.layers
+    value = world * kv_step / (step_ms * 1e-3) / 1e9
+    one_launch = T == B
+    res = {"workload": cfg.name, "value": value, "unit": "GB/s", "frac": value / world / peak,
+           "ms_per_step": step_ms, "us_per_layer": step_ms * 1e3 / cfg.layers, "layers": cfg.layers, "batch": B,
+           "kv_bytes_per_step": kv_step, "splits": S,
+           "step": "per layer: pkv_append_decode_attention (" +
+                   ("1 launch)" if one_launch else "2 launches for chunked appends: append, merged decode)"),
+           **({"window": cfg.window} if cfg.window else {}),
+           "clocks": clocks.summary()}
+    pf = prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, dev)
+    if pf is not None:
+        res["prefill"] = pf
+    return res
+
+
+def measure_headline(args, cfg, world, rank, local, dev):
+    """The headline workload: the JSON line's value, roofline, e2e, launch layouts, and the fused
+    QKV projection and chunked prefill where the workload has them."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
     step = W.make_step(cfg, rank_seed(cfg, rank))
     layers = list(range(cfg.layers))
     pools = int8_pools(step, cfg, layers, dev) if args.int8 else [W.device_pool(step, l) for l in layers]
@@ -675,7 +808,8 @@ def run_ours(args):
     launch_ms = step_ms / cfg.layers if one_launch else dec_ms
     achieved = kv_layer / (launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = ncu_traffic()
+    overridden = bool(args.batch or args.pool_pages or args.int8)
+    traffic = None if overridden else ncu_traffic(cfg.cid)
 
     # ---- end to end through the API with host buffers ------------------------------------------
     h2d = sum(a.nbytes for a in in_arrays)
@@ -764,13 +898,7 @@ def run_ours(args):
         **({"prefill": prefill} if prefill is not None else {}),
         "clocks": clocks.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        gbs, threads, what = oracle_sample(step, args.cpu_seconds, cfg.layers)
-        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": what}
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def main():

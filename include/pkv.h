@@ -64,12 +64,19 @@ typedef enum {
 
 /* Cache option bits (pkv_cache_desc.options). */
 #define PKV_OPT_PDL 0x1 /* launch with programmatic dependent launch: each kernel may start while
-                           the previous kernel in the stream finishes.  Kernels wait for it before
-                           reading q, k, v, the pool and the partials, but read their int32 page
-                           tables (page_indptr, append_indptr, last_page_len, q_indptr) earlier:
-                           do not produce those arrays in the kernel launched right before. */
-#define PKV_OPT_INT8_KV 0x4 /* int8 KV pages (SURVEY's NEXT-2 reading; the Zero TVM page exposes int8
-                               KV behind a flag): each layer's pool is uint8 blocks
+                           the previous kernel in the stream finishes.  Kernels wait for it (the
+                           launch wait) before reading q, k, v, x, the pool, the partials and the
+                           counters, but read their int32 index arrays (page_indptr, page_indices,
+                           last_page_len, append_indptr, q_indptr, pos_map) and, for the QKV entry
+                           points, the weights and scales before it.  Those arrays must be complete
+                           when the kernel starts: written by the host, by a copy, or by a kernel
+                           that does not let its dependents start early (a kernel launched without
+                           programmatic dependent launch signals the next one only when it has
+                           finished).  Do not produce them in a kernel that starts its dependents
+                           early, such as this library's own kernels under this option. */
+#define PKV_OPT_INT8_KV 0x4 /* int8 KV pages (Zero TVM Documentation, "The memory-bandwidth ceiling":
+                               int8 KV behind a flag; the format is this library's reading): each
+                               layer's pool is uint8 blocks
                                [num_pages][2][Hkv][16 * head_dim + 64] holding the 16 slots' int8
                                codes [16][head_dim] then their fp32 scales [16].  The append
                                quantizes each new K row (after RoPE and its fp16 rounding) and V row:
@@ -81,11 +88,20 @@ typedef enum {
                                PKV_ERR_UNSUPPORTED. */
 #define PKV_OPT_EARLY_PAGES 0x2 /* with PKV_OPT_PDL, the one-launch step (pkv_append_decode_attention
                                    with one token per sequence) starts copying the layer's cached
-                                   pages before that wait, so the copies overlap the end of the
-                                   previous kernel; the new tokens' q, k, v are read after it.  The
-                                   kernel launched right before must not write this layer's pool.
-                                   The whole ring goes early when Hq / Hkv >= 2 (tensor-core path),
-                                   two stages per warp otherwise (the depths that measured fastest). */
+                                   pages before the launch wait, so the copies overlap the end of the
+                                   previous kernels; the new tokens' q, k, v are read after it.  The
+                                   last two pages of every sequence, which hold the 16 positions
+                                   before its new token (written by the preceding decode steps of
+                                   the layer, which may still be running), are always copied after
+                                   the wait.  A layer whose pool was written by another call since
+                                   its last one-launch step (pkv_append_rope, pkv_qkv_append_rope, a
+                                   chunked pkv_append_decode_attention) runs its next one-launch step
+                                   without early copies; the choice is made when the call is made
+                                   (also while a stream is being captured).  The caller's own writes
+                                   to a pool must come from kernels that do not start their
+                                   dependents early (see PKV_OPT_PDL).  The whole ring goes early
+                                   when Hq / Hkv >= 2 (tensor-core path), two stages per warp
+                                   otherwise (the depths that measured fastest). */
 
 typedef struct pkv_cache pkv_cache; /* opaque, host-only */
 
@@ -363,8 +379,10 @@ pkv_status pkv_append_decode_attention(pkv_cache* cache, int layer, const void* 
  * A request whose partials (batch * Hq * splits * (head_dim + 1) * 4 bytes) and counters
  * (batch * Hkv * 4 bytes) exceed 32 MiB returns PKV_ERR_UNSUPPORTED (see pkv_last_error).
  * The first call on a device, with that device current, looks up the array's device address
- * once; make that first call before any stream capture.  Each call clears the counters on its
- * stream before launching.  All calls share the one array: calls that overlap on the GPU race.
+ * once; make that first call before any stream capture.  Call it with the cache's device current
+ * (otherwise PKV_ERR_INVALID_ARG).  A device reset gives the device a new context, and the next
+ * call looks the address up again.  Each call clears the counters on its stream before launching.
+ * All calls share the one array: calls that overlap on the GPU race.
  */
 pkv_status pkv_decode_attention_noalloc(const pkv_cache* cache, int layer, const void* q_rope,
                                         const int32_t* q_indptr, const int32_t* page_indptr,
@@ -394,6 +412,18 @@ pkv_status pkv_combine(const pkv_cache* cache, const float* partial_o, const flo
  * PKV_ERR_CUDA if a CUDA call failed.  flags (nullable) receives the raw bits.
  */
 pkv_status pkv_check_status(pkv_cache* cache, pkv_stream_t stream, int* flags);
+
+/*
+ * Limit of the kernels' waits for their staged copies, in nanoseconds of the GPU's global timer
+ * (default 2 s; 0 restores it).  A decode or prefill warp whose wait runs out sets
+ * PKV_FLAG_TIMEOUT, waits up to 125 ms (a fixed limit) for its own copies still in flight, and
+ * returns without writing its results; pkv_check_status then reports PKV_ERR_TIMEOUT.  Used to
+ * test that failure path: a limit shorter than a copy's latency (say 1 ns) makes waits run out on
+ * a healthy GPU.  After a timeout, outputs are undefined and chunk_counters must be re-zeroed.
+ * Applies to the launches that follow the call.  Host only; returns PKV_ERR_INVALID_ARG for NULL.
+ * (Everything WebGPU AI.md, "Fail Fast": failures surface as typed errors, not hangs.)
+ */
+pkv_status pkv_set_wait_limit(pkv_cache* cache, unsigned long long limit_ns);
 
 /* Static description of a status code. */
 const char* pkv_status_string(pkv_status status);

@@ -215,8 +215,8 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
 }
 
 /* ------------------------------------------------------------------------------------------ */
-/* int8 KV pages (SURVEY's NEXT-2; Zero TVM Documentation, "The memory-bandwidth ceiling": int8
- * KV is exposed behind a flag; the format is this build's reading).
+/* int8 KV pages (Zero TVM Documentation, "The memory-bandwidth ceiling": int8 KV is exposed
+ * behind a flag; the format is this library's reading).
  * Layout per layer: uint8 pool8[num_pages][2][Hkv][16 * d + 64]: a block holds the 16 slots'
  * int8 codes [16][d] and then their fp32 scales [16].
  * Row quantizer (one row = one token, one KV head, K or V, of d fp16 values x_i; K after RoPE and
@@ -457,8 +457,8 @@ int orc_attention(const orc_geom* g, const uint16_t* pool, const uint16_t* q_rop
   return rc;
 }
 
-/* Chunked-prefill attention (the step after the append when a sequence appends several tokens:
- * SURVEY's NEXT-1; Zero TVM Documentation, "Decode loop": a token attends to itself and to every
+/* Chunked-prefill attention (the step after the append when a sequence appends several tokens;
+ * Zero TVM Documentation, "How it works": prefill in chunks; "Decode loop": a token attends to itself and to every
  * earlier position of its sequence).  Token t of sequence s (append_indptr) at position
  * p = pos_map[t] attends to the positions [window_start(p + 1, W), p] of s, the cache after the
  * append holding them; sinks as in orc_attention.  q_rope: [T][Hq][d] fp16 bits; out: [T][Hq][d];

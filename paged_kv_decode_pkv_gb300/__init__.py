@@ -95,6 +95,8 @@ def lib():
         L.pkv_combine.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
         L.pkv_check_status.restype = i
         L.pkv_check_status.argtypes = [P, P, ctypes.POINTER(i)]
+        L.pkv_set_wait_limit.restype = i
+        L.pkv_set_wait_limit.argtypes = [P, ctypes.c_ulonglong]
         _lib = L
     return _lib
 
@@ -391,6 +393,10 @@ class Cache:
                                          _ptr(append_indptr), T, B, _ptr(page_indptr), _ptr(page_indices),
                                          _ptr(q_out), _stream(stream)), "pkv_qkv_append_rope")
         return q_out
+
+    def set_wait_limit(self, limit_ns: int = 0):
+        """pkv_set_wait_limit: limit of the kernels' waits for staged copies (0 = the 2 s default)."""
+        _check(lib().pkv_set_wait_limit(self.handle, int(limit_ns)), "pkv_set_wait_limit")
 
     def check_status(self, stream=None):
         """pkv_check_status; returns (status code, flag bits) without raising."""

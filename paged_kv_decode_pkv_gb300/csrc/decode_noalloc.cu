@@ -9,9 +9,12 @@
 //
 // The array's device address is looked up once per device, on the first call made with that
 // device current (cudaGetSymbolAddress; its return code is checked), and passed to the kernel as
-// ordinary pointers.  That first call on a device should come before any stream capture.  Every
-// call shares the one array and it keeps the last call's contents: each call clears the chunk
-// counters on its stream before the kernel runs, and calls that overlap on the GPU race on the array.
+// ordinary pointers.  That first call on a device should come before any stream capture.  The
+// address belongs to the device's context: after a device reset (cudaDeviceReset) the next call
+// finds a new context and looks the address up again (a cache created before the reset is itself
+// no longer usable: its pools and tables were freed with the old context).  Every call shares the
+// one array and it keeps the last call's contents: each call clears the chunk counters on its
+// stream before the kernel runs, and calls that overlap on the GPU race on the array.
 #include <mutex>
 
 #include "../../include/pkv.h"
@@ -26,31 +29,62 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_setup_mutex;
 void* g_scratch_address[kMaxDevices] = {};
+unsigned long long g_scratch_context[kMaxDevices] = {};  // context id the address belongs to
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Device address of the scratch array on the current device, looked up on first use.
-pkv_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    pkv::set_last_error("pkv_decode_attention_noalloc: cudaGetDevice failed");
-    return PKV_ERR_CUDA;
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (0 if the driver cannot tell): a device reset creates a new one.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked_up = true;
   }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device, looked up on first use (and again
+// when the device's context changed).
+pkv_status scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) {
     pkv::set_last_error("pkv_decode_attention_noalloc: device ordinal above 63");
     return PKV_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_address[dev] == nullptr) {
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr) {
-      pkv::set_last_error("pkv_decode_attention_noalloc: cudaGetSymbolAddress of the scratch array failed");
-      return PKV_ERR_CUDA;
-    }
-    g_scratch_address[dev] = ptr;
+  // the runtime makes the device's primary context current on its first call; the symbol lookup
+  // below is such a call, so the context id is taken after it
+  if (g_scratch_address[dev] != nullptr && g_scratch_context[dev] != 0 &&
+      g_scratch_context[dev] == current_context_id()) {
+    *out = g_scratch_address[dev];
+    return PKV_OK;
   }
-  *out = g_scratch_address[dev];
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || ptr == nullptr) {
+    pkv::set_last_error("pkv_decode_attention_noalloc: cudaGetSymbolAddress of the scratch array failed");
+    return PKV_ERR_CUDA;
+  }
+  g_scratch_address[dev] = ptr;
+  g_scratch_context[dev] = current_context_id();
+  *out = ptr;
   return PKV_OK;
 }
 
@@ -86,8 +120,17 @@ extern "C" pkv_status pkv_decode_attention_noalloc(const pkv_cache* cache, int l
     if (splits_used) *splits_used = S;
     return PKV_OK;
   }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    pkv::set_last_error("pkv_decode_attention_noalloc: cudaGetDevice failed");
+    return PKV_ERR_CUDA;
+  }
+  if (dev != pkv::cache_device(cache)) {
+    pkv::set_last_error("pkv_decode_attention_noalloc: the current device is not the cache's device");
+    return PKV_ERR_INVALID_ARG;
+  }
   void* base = nullptr;
-  const pkv_status as = scratch_address(&base);
+  const pkv_status as = scratch_address(dev, &base);
   if (as != PKV_OK) return as;
   unsigned char* scratch = static_cast<unsigned char*>(base);
   int32_t* counters = reinterpret_cast<int32_t*>(scratch);

@@ -34,8 +34,9 @@
 // rotates q and k there, and the staged copy of the page that holds the token is patched (and the
 // pool written) before it is used.
 //
-// Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
-// bounded time for its own copies in flight and returns.
+// Every wait is bounded (2 s of global time unless pkv_set_wait_limit sets another limit), with
+// one answer per warp; on expiry the warp flags PKV_FLAG_TIMEOUT, waits a fixed bounded time for
+// its own copies in flight (so none lands in the shared memory of a finished block) and returns.
 #include <algorithm>
 
 #include "merge.cuh"
@@ -1019,7 +1020,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
   };
 
-  auto produce = [&]() -> bool {
+  // early: called before the launch wait.  Then the last two pages of a sequence, which hold the
+  // 16 positions before its new token (written by the decode steps just before this one, which
+  // may still be running under programmatic dependent launch), are not copied: the early fill
+  // stops there and the copy is issued after the wait.
+  auto produce = [&](bool early) -> bool {
     while (!cur.active) {
       if (!nxt.active) return false;
       cur = nxt;
@@ -1030,6 +1035,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
     if (cur.p1 != cur.p0 && cur.pnext == cur.p0 && items_issued - items_begun >= kItemSlots)
       return false;  // both item slots are taken: wait until the consumer begins an item
+    if (early && cur.p1 != cur.p0 && cur.pnext >= cur.n - 2) return false;
     const int k = ik;
     StageMeta mt;
     mt.s = cur.s;
@@ -1134,7 +1140,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   }
 
   if (!waited) {
-    while (issued < min(nst, p.early) && produce()) {
+    while (issued < min(nst, p.early) && produce(true)) {
     }
     pdl_wait();  // the new token's q, k, v come from the preceding kernel
     waited = true;
@@ -1172,12 +1178,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
   }
 
-  // Bounded wait for stage number c (ring slot k, phase parity ph); on expiry flag a timeout and
-  // drain (bounded) the copies in flight.
+  // Bounded wait for stage number c (ring slot k, phase parity ph), with one answer for the warp;
+  // on expiry flag a timeout and drain (bounded) the copies in flight, stage c's included (stage c
+  // may be the merge's copy, numbered `issued` before it is counted).
   auto wait_stage = [&](int c, int k, uint32_t ph) -> bool {
-    if (mbar_wait_bounded(&bar[k], ph, kWaitLimitNs)) return true;
+    if (warp_wait_bounded(&bar[k], ph, p.wait_ns)) return true;
     if (lane == 0) atomicOr(p.status, kFlagTimeout);
-    for (int d = c + 1; d < issued; ++d) mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kWaitLimitNs / 16);
+    for (int d = c; d < max(issued, c + 1); ++d)
+      mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kDrainLimitNs);
+    __syncwarp();
     return false;
   };
 
@@ -1292,7 +1301,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   // The ring is filled (and refilled after every step) at the top of the loop, the one place that
   // issues copies, so the producer code exists once.
   while (true) {
-    while (issued - consumed < nst && produce()) {
+    while (issued - consumed < nst && produce(false)) {
     }
     if (consumed == issued) break;
     const int k = ck;

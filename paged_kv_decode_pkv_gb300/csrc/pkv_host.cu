@@ -23,6 +23,11 @@ struct pkv_cache {
   int group = 1;
   bool pdl = false;
   bool int8 = false;  // PKV_OPT_INT8_KV: int8 blocks with per-slot scales
+  unsigned long long wait_ns = pkv::kWaitLimitNs;  // limit of the kernels' waits for staged copies
+  // Per layer: the pool was written by a call other than the one-launch step (an append or a QKV
+  // append) since the last one-launch step of that layer.  The next one-launch step of the layer
+  // then copies no page before its launch wait, since the writing kernel may still be running.
+  std::vector<char> pool_dirty;
 };
 
 namespace {
@@ -195,6 +200,8 @@ void cache_geometry(const pkv_cache* c, int* hq, int* hkv, int* d) {
   *d = c->desc.head_dim;
 }
 
+int cache_device(const pkv_cache* c) { return c->device; }
+
 void set_last_error(const char* what) { ::set_error(what, nullptr); }
 
 }  // namespace pkv
@@ -268,6 +275,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   c->desc.layer_pools = nullptr;
   c->windows.assign(d->num_layers, 0);
   c->sinks.assign(d->num_layers, nullptr);
+  c->pool_dirty.assign(d->num_layers, 0);
   for (int l = 0; l < d->num_layers; ++l) {
     if (d->layer_window != nullptr) c->windows[l] = d->layer_window[l];
     if (d->layer_sinks != nullptr) c->sinks[l] = d->layer_sinks[l];
@@ -388,10 +396,14 @@ pkv_status pkv_append_rope(pkv_cache* c, int layer, const void* q, const void* k
   if (c->int8) {
     p.pool = nullptr;
     p.pool8 = static_cast<unsigned char*>(c->pools[layer]);
-    return launch_status("append_rope launch", pkv::launch_append_q8(p, stream, c->pdl));
+    const pkv_status st = launch_status("append_rope launch", pkv::launch_append_q8(p, stream, c->pdl));
+    if (st == PKV_OK) c->pool_dirty[layer] = 1;
+    return st;
   }
   p.pool8 = nullptr;
-  return launch_status("append_rope launch", pkv::launch_append(p, stream, c->pdl));
+  const pkv_status st = launch_status("append_rope launch", pkv::launch_append(p, stream, c->pdl));
+  if (st == PKV_OK) c->pool_dirty[layer] = 1;
+  return st;
 }
 
 namespace {
@@ -444,7 +456,9 @@ pkv_status pkv_qkv_append_rope(pkv_cache* c, int layer, const void* x, const uin
   p.batch = batch;
   p.q_out = static_cast<__half*>(q_out);
   p.pool = static_cast<__half*>(c->pools[layer]);
-  return launch_status("qkv launch", pkv::launch_qkv(p, stream, c->pdl));
+  const pkv_status ls = launch_status("qkv launch", pkv::launch_qkv(p, stream, c->pdl));
+  if (ls == PKV_OK) c->pool_dirty[layer] = 1;
+  return ls;
 }
 
 pkv_status pkv_qkv_project(const pkv_cache* c, const void* x, const uint32_t* w, const void* scales, int hidden,
@@ -497,6 +511,7 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
   p.nstage = cfg.nstage;
   const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.wait_ns = c->wait_ns;
   const int grid = c->num_sms;
   return launch_status("prefill launch", pkv::launch_prefill(p, c->maps[layer], cfg, D, grid, stream, c->pdl));
 }
@@ -527,6 +542,7 @@ struct FusedArgs {
   const void* v;
   const int32_t* pos_map;
   void* q_out;
+  bool early_ok;  // no other call wrote the layer's pool since its last one-launch step
 };
 
 // Shared body of pkv_decode_attention, pkv_decode_attention_merged and pkv_append_decode_attention.
@@ -615,8 +631,9 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   // 3 510 GB/s; one stage 3 390, three 3 435, the whole ring 3 125, where the early copies slow the
   // previous launch's merge tail).
   p.early = 0;
-  if (fused != nullptr && (c->desc.options & PKV_OPT_EARLY_PAGES))
+  if (fused != nullptr && fused->early_ok && (c->desc.options & PKV_OPT_EARLY_PAGES))
     p.early = c->group >= 2 ? kEarlyStagesGroup : kEarlyStagesOneHead;
+  p.wait_ns = c->wait_ns;
   p.pool8 = c->int8 ? static_cast<const unsigned char*>(c->pools[layer]) : nullptr;
   if (c->int8) p.pool = nullptr;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
@@ -643,6 +660,7 @@ pkv_status pkv_append_decode_attention(pkv_cache* c, int layer, const void* q, c
                                        int num_splits, int chunk_pages, int max_splits, float sm_scale, void* q_out,
                                        float* partial_o, float* partial_lse, int32_t* chunk_counters, void* out,
                                        float* lse_out, int* splits_used, pkv_stream_t stream) {
+  if (c == nullptr || layer < 0 || layer >= c->desc.num_layers) return fail(PKV_ERR_INVALID_ARG, "cache or layer");
   if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative num_tokens");
   if (num_tokens != batch || c->int8) {
     // several new tokens per sequence (a chunked append), or an int8 cache: the append launch, then
@@ -654,10 +672,12 @@ pkv_status pkv_append_decode_attention(pkv_cache* c, int layer, const void* q, c
                          max_pages, total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o,
                          partial_lse, chunk_counters, out, lse_out, true, splits_used, stream);
   }
-  const FusedArgs fa{k, v, pos_map, q_out};
-  return decode_common(c, layer, q, append_indptr, page_indptr, page_indices, last_page_len, batch, max_pages,
-                       total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o, partial_lse,
-                       chunk_counters, out, lse_out, true, splits_used, stream, &fa);
+  const FusedArgs fa{k, v, pos_map, q_out, c->pool_dirty[layer] == 0};
+  const pkv_status st = decode_common(c, layer, q, append_indptr, page_indptr, page_indices, last_page_len, batch,
+                                      max_pages, total_pages, num_splits, chunk_pages, max_splits, sm_scale, partial_o,
+                                      partial_lse, chunk_counters, out, lse_out, true, splits_used, stream, &fa);
+  if (st == PKV_OK) c->pool_dirty[layer] = 0;
+  return st;
 }
 
 pkv_status pkv_decode_attention_merged(const pkv_cache* c, int layer, const void* q_rope, const int32_t* q_indptr,
@@ -690,6 +710,12 @@ pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* 
   p.splits = num_splits;
   p.head_dim = head_dim;
   return launch_status("combine launch", pkv::launch_combine(p, stream, c != nullptr && c->pdl));
+}
+
+pkv_status pkv_set_wait_limit(pkv_cache* c, unsigned long long limit_ns) {
+  if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "null cache");
+  c->wait_ns = limit_ns == 0 ? pkv::kWaitLimitNs : limit_ns;
+  return PKV_OK;
 }
 
 pkv_status pkv_check_status(pkv_cache* c, pkv_stream_t stream, int* flags) {

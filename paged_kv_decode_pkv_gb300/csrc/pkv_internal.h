@@ -13,7 +13,10 @@ constexpr int kPageSize = 16;
 constexpr int kMaxGroup = 8;        // Hq / Hkv handled by the kernels
 constexpr int kMaxDecodeBatch = 4096;  // sequences per decode call (per-CTA shared-memory prefix)
 constexpr int kMaxDecodeWarps = 8;     // warps per decode CTA, at most
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s (default)
+// A warp that gave up waits this long for its own copies still in flight before it returns, so
+// that no copy lands in the shared memory of a finished block.  Not affected by the settable limit.
+constexpr unsigned long long kDrainLimitNs = kWaitLimitNs / 16;
 
 // Device status word bits (mirrors PKV_FLAG_* of include/pkv.h).
 constexpr int kFlagBadPage = 0x1;
@@ -73,6 +76,7 @@ struct PrefillParams {
   int window;       // 0 = full attention
   int nstage;
   float scale_log2;
+  unsigned long long wait_ns;  // limit of a wait for a staged copy (kWaitLimitNs unless set)
 };
 constexpr int kPrefillWarps = 8;  // consumer warps per CTA (plus one producer warp)
 struct PrefillConfig {
@@ -130,6 +134,7 @@ struct DecodeParams {
   const float* sinks;
   int early;  // one-launch mode: stages per warp copied before the launch wait (PKV_OPT_EARLY_PAGES)
   const unsigned char* pool8;  // int8 cache: blocks [num_pages][2][hkv][16 * d + 64]
+  unsigned long long wait_ns;  // limit of a wait for a staged copy (kWaitLimitNs unless set)
 };
 
 struct CombineParams {
@@ -176,6 +181,7 @@ namespace pkv {
 
 // Host-side helpers for entry points defined outside pkv_host.cu.
 void cache_geometry(const pkv_cache* cache, int* num_qo_heads, int* num_kv_heads, int* head_dim);
+int cache_device(const pkv_cache* cache);  // the device that was current when the cache was created
 void set_last_error(const char* what);
 
 }  // namespace pkv

@@ -15,8 +15,9 @@
 // re-used as the A operand) and P V accumulated in fp32.  V rows past the sequence end are zeroed
 // in shared memory.  No split: a tile's result is final (sinks fold into its denominator).
 //
-// Every wait is bounded (2 s of global time); on expiry the warp flags PKV_FLAG_TIMEOUT, waits a
-// bounded time for its own copies in flight and returns.
+// Every wait is bounded (2 s of global time unless pkv_set_wait_limit sets another limit), with
+// one answer per warp; on expiry the warp flags PKV_FLAG_TIMEOUT, waits a fixed bounded time for
+// its own copies in flight (so none lands in the shared memory of a finished block) and returns.
 #include "pkv_internal.h"
 #include "ptx.cuh"
 
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const
   const int G = p.group;
   const int c2 = 2 * (lane & 3);
   int seq = 0;  // pages the CTA has streamed so far (ring slot and phases)
+  int fills = 0;  // producer: stages filled so far (those it must drain before leaving)
 
   pdl_wait();  // q and the pool (the append) come from the preceding kernel
 
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const
         }
         const int pid = __shfl_sync(kAll, window_ids, i - win_base);
         const int f = seq + i, slot = f % nst;
-        if (f >= nst && !mbar_wait_bounded(&empty[slot], (uint32_t)(((f / nst) - 1) & 1), kWaitLimitNs)) {
+        if (f >= nst && !warp_wait_bounded(&empty[slot], (uint32_t)(((f / nst) - 1) & 1), p.wait_ns)) {
           if (lane == 0) {
             atomicOr(p.status, kFlagTimeout);
             abort_flag = 1;
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const
           break;
         }
         const bool ok = pid >= 0 && pid < p.num_pages;
+        fills = f + 1;
         if (!ok && lane == 0) atomicOr(p.status, kFlagBadPage);
         mbar_arrive_expect_tx_if(lane == 0 && ok, &full[slot], (uint32_t)Gm::STAGE);
         mbar_arrive_if(lane == 0 && !ok, &full[slot]);
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const
     bool stop = false;
     for (int i = 0; i < np; ++i) {
       const int f = seq + i, slot = f % nst;
-      if (!mbar_wait_bounded(&full[slot], (uint32_t)((f / nst) & 1), kWaitLimitNs)) {
+      if (!warp_wait_bounded(&full[slot], (uint32_t)((f / nst) & 1), p.wait_ns)) {
         if (lane == 0) {
           atomicOr(p.status, kFlagTimeout);
           abort_flag = 1;
@@ -383,8 +386,8 @@ __global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const
   }
   // the producer leaves only when its copies have landed: wait (bounded) for the last fills
   if (producer && *reinterpret_cast<volatile int*>(&abort_flag)) {
-    for (int f = max(0, seq - nst); f < seq; ++f)
-      mbar_wait_bounded(&full[f % nst], (uint32_t)((f / nst) & 1), kWaitLimitNs / 16);
+    for (int f = max(0, fills - nst); f < fills; ++f)
+      mbar_wait_bounded(&full[f % nst], (uint32_t)((f / nst) & 1), kDrainLimitNs);
   }
 }
 

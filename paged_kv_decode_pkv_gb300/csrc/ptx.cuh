@@ -61,14 +61,52 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Limits below this are polled without suspending the thread (try_wait may suspend for a
+// system-dependent time, longer than such a limit).
+constexpr uint64_t kShortWaitNs = 1000000;
+
 // Wait for the phase with the given parity to complete, giving up after `limit_ns` of global
 // time.  Returns false on timeout.  Every lane of the calling warp may call it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// The wait for a whole warp, with one answer for every lane.  Lanes poll together: the warp goes
+// on when every lane has seen the phase complete (a completed phase stays complete until the
+// barrier is re-armed, so once one lane sees it the others do at their next poll), and gives up
+// only when no lane has seen it and the limit has passed.  Every lane of the warp must call it.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    const bool ok = limit_ns < kShortWaitNs ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (!__any_sync(0xffffffffu, ok) && __any_sync(0xffffffffu, global_timer_ns() - t0 > limit_ns)) return false;
   }
 }
 
