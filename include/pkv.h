@@ -418,8 +418,9 @@ pkv_status pkv_check_status(pkv_cache* cache, pkv_stream_t stream, int* flags);
  * (default 2 s; 0 restores it).  A decode or prefill warp whose wait runs out sets
  * PKV_FLAG_TIMEOUT, waits up to 125 ms (a fixed limit) for its own copies still in flight, and
  * returns without writing its results; pkv_check_status then reports PKV_ERR_TIMEOUT.  Used to
- * test that failure path: a limit shorter than a copy's latency (say 1 ns) makes waits run out on
- * a healthy GPU.  After a timeout, outputs are undefined and chunk_counters must be re-zeroed.
+ * test that failure path: a limit shorter than a copy's latency (say 1) makes waits run out on a
+ * healthy GPU.  Limits below 1 ms are such a test setting: they are counted in SM clock cycles
+ * (about half a nanosecond each) and the waits poll without suspending.  After a timeout, outputs are undefined and chunk_counters must be re-zeroed.
  * Applies to the launches that follow the call.  Host only; returns PKV_ERR_INVALID_ARG for NULL.
  * (Everything WebGPU AI.md, "Fail Fast": failures surface as typed errors, not hangs.)
  */

@@ -74,25 +74,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Limits below this are polled without suspending the thread (try_wait may suspend for a
-// system-dependent time, longer than such a limit).
+// Limits below this (1 ms) are a test setting: they are counted in SM clock cycles, which resolve
+// a few nanoseconds where the global timer may tick only every microsecond, and polled without
+// suspending the thread (try_wait may suspend for a system-dependent time longer than the limit).
 constexpr uint64_t kShortWaitNs = 1000000;
+
+__device__ __forceinline__ uint64_t wait_clock(bool short_limit) {
+  return short_limit ? (uint64_t)clock64() : global_timer_ns();
+}
 
 // Wait for the phase with the given parity to complete, giving up after `limit_ns` of global
 // time.  Returns false on timeout.  Every lane of the calling warp may call it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (limit_ns < kShortWaitNs) {
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if (global_timer_ns() - t0 > limit_ns) return false;
-    }
-  }
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const bool short_limit = limit_ns < kShortWaitNs;
+  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = wait_clock(short_limit);
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
+    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (wait_clock(short_limit) - t0 > limit_ns) return false;
   }
 }
 
@@ -101,12 +100,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // barrier is re-armed, so once one lane sees it the others do at their next poll), and gives up
 // only when no lane has seen it and the limit has passed.  Every lane of the warp must call it.
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  const uint64_t t0 = global_timer_ns();
+  const bool short_limit = limit_ns < kShortWaitNs;
+  if (__all_sync(0xffffffffu, short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = wait_clock(short_limit);
   while (true) {
-    const bool ok = limit_ns < kShortWaitNs ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+    const bool ok = short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
-    if (!__any_sync(0xffffffffu, ok) && __any_sync(0xffffffffu, global_timer_ns() - t0 > limit_ns)) return false;
+    if (!__any_sync(0xffffffffu, ok) && __any_sync(0xffffffffu, wait_clock(short_limit) - t0 > limit_ns))
+      return false;
   }
 }
 

@@ -214,7 +214,7 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct(name, entry):
     if entry == "one_launch":
         cfg = W.scaled(cfg, chunk_seqs=0, chunk_tokens=0)
     if entry == "prefill" and not cfg.chunk_seqs:
-        cfg = W.scaled(cfg, batch=2, chunk_seqs=1, chunk_tokens=40)
+        cfg = W.scaled(cfg, batch=2, chunk_seqs=1, chunk_tokens=40, pool_pages=100)
     step = W.make_step(cfg)
     host_pool = W.host_pool(step, 0)
     tabs = H.device_tables(step)
