@@ -17,7 +17,8 @@ struct pkv_cache {
   std::vector<void*> pools;
   std::vector<int> windows;         // per layer, 0 = full attention
   std::vector<const float*> sinks;  // per layer, device fp32 [Hq] or null
-  std::vector<CUtensorMap> maps;  // one per layer pool
+  std::vector<CUtensorMap> maps;     // one per layer pool: boxes of one page's K and V (decode)
+  std::vector<CUtensorMap> maps_pf;  // one per layer pool: boxes of one page's K or V (prefill)
   int device = 0;
   int num_sms = 0;
   int group = 1;
@@ -325,7 +326,11 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
     return cuda_fail("setting kernel attributes", e);
   }
   c->maps.resize(d->num_layers);
-  if (c->int8) memset(c->maps.data(), 0, sizeof(CUtensorMap) * c->maps.size());  // int8 pages use plain copies
+  c->maps_pf.resize(d->num_layers);
+  if (c->int8) {  // int8 pages use plain copies
+    memset(c->maps.data(), 0, sizeof(CUtensorMap) * c->maps.size());
+    memset(c->maps_pf.data(), 0, sizeof(CUtensorMap) * c->maps_pf.size());
+  }
   for (int l = 0; l < d->num_layers && !c->int8; ++l) {
     const cuuint64_t gdim[4] = {(cuuint64_t)D, (cuuint64_t)PKV_PAGE_SIZE, (cuuint64_t)d->num_kv_heads,
                                 (cuuint64_t)d->num_pages * 2};
@@ -336,9 +341,15 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
     const CUtensorMapSwizzle swz = cfg.swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : cfg.swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                              : CU_TENSOR_MAP_SWIZZLE_NONE;
-    const CUresult r = encode(&c->maps[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box,
-                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode(&c->maps[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // the prefill kernel copies a page's K and its V as separate boxes (16 slots x one swizzle row)
+    const cuuint32_t box1[4] = {(cuuint32_t)cfg.box_inner, (cuuint32_t)PKV_PAGE_SIZE, 1, 1};
+    if (r == CUDA_SUCCESS)
+      r = encode(&c->maps_pf[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box1, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       delete c;
       char msg[64];
@@ -513,7 +524,7 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.wait_ns = c->wait_ns;
   const int grid = c->num_sms;
-  return launch_status("prefill launch", pkv::launch_prefill(p, c->maps[layer], cfg, D, grid, stream, c->pdl));
+  return launch_status("prefill launch", pkv::launch_prefill(p, c->maps_pf[layer], cfg, D, grid, stream, c->pdl));
 }
 
 pkv_status pkv_plan_decode(const pkv_cache* c, int batch, int max_pages, int total_pages, int num_splits,

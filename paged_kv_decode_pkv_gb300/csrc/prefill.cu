@@ -1,25 +1,44 @@
-// Chunked-prefill attention over the paged KV cache: every appended token of a sequence attends
-// causally to the positions up to its own (Zero TVM Documentation, "Decode loop": a token attends
-// to itself and to the earlier positions of its sequence; "KV cache": 16-slot pages behind a page
-// table; "Port to Phi-4-mini or Qwen3": query head h reads KV head h / (Hq / Hkv)).  With several
-// tokens per sequence this is a dense contraction, and it runs on tensor cores.
+// Chunked-prefill attention over the paged KV cache on the 5th-generation tensor cores: every
+// appended token of a sequence attends causally to the positions up to its own (Zero TVM
+// Documentation, "How it works": prefill in chunks; "Decode loop": a token attends to itself and
+// to the earlier positions of its sequence; "KV cache": 16-slot pages behind a page table; "Port
+// to Phi-4-mini or Qwen3": query head h reads KV head h / (Hq / Hkv)).  With many tokens per
+// sequence this is a dense contraction, S = Q K^T and O = P V, run with tcgen05.mma.
 //
-// Work decomposition.  A tile is (sequence s, KV head g, a block of 16 / G of the sequence's
-// appended tokens): 16 rows of mma.sync m16n8k16, row r = token r / G of the block, query head
-// g * G + r % G.  One warp owns a tile at a time (tiles gw, gw + W, ... over a persistent grid)
-// and walks the pages from the first one any row attends to (its window start) to the last one
-// (its position), each copied once for the 16 rows by swizzled TMA boxes into the warp's own ring
-// of shared-memory stages.  Per page: S = Q K^T for the 16 rows and 16 slots, a per-row mask
-// (slot position within [start_r, pos_r]), an online softmax per row in the log2 domain with the
-// running max raised only when a score exceeds it by 2^8, P rounded to fp16 (the score fragments
-// re-used as the A operand) and P V accumulated in fp32.  V rows past the sequence end are zeroed
-// in shared memory.  No split: a tile's result is final (sinks fold into its denominator).
+// Work decomposition.  A tile is (sequence s, KV head g, 128 / G consecutive appended tokens of s):
+// 128 query rows, row r = token r / G of the tile and query head g * G + r % G, so a page of KV
+// head g is read once for all G heads that use it.  A key block is 8 pages (128 keys).  Tiles are
+// ordered longest sequence first (tiles of one sequence last tile first) and dealt to the CTAs of
+// a persistent grid (one per SM) in turn.
+//
+// One CTA, six warps:
+//   warp 0  producer: the tile's key blocks, each page's K and V boxes of KV head g copied by the
+//           tensor-memory-access unit into a two-stage ring (128-byte swizzle, 64-byte for
+//           head_dim 96); K and V of a stage have barriers of their own, so the K half is refilled
+//           as soon as its S MMA has completed while the V half waits for its P V MMA;
+//   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two tensor-memory buffers (128
+//           fp32 columns each), then O += P_j V_j into a third (head_dim columns), V read
+//           MN-major straight from the staged pages; every MMA group commits to a barrier;
+//   warps 2-5  softmax (thread = query row = tensor-memory lane): stage the tile's queries in
+//           shared memory, then per block read the row of S, mask it (the row's causal range
+//           [window start, position], pages not loaded), an online softmax in the log2 domain
+//           whose running max is raised only when a score exceeds it by 2^8 (then the row of O is
+//           rescaled in tensor memory), P rounded to fp16 into shared memory for the P V MMA (the
+//           row sum adds the same rounded values); the score loops run as eight independent chains,
+//           since one warp per scheduler has little else to hide latencies with;
+//           finally the row of O divided by the row sum (sinks join the denominator), written in
+//           fp16 with its LSE.
+// S is double-buffered, so the softmax of block j overlaps the MMA of block j + 1.  V rows of keys
+// past the sequence end or in pages not loaded are zeroed in shared memory before P V (P = 0 times
+// a NaN would be NaN).
 //
 // Every wait is bounded (2 s of global time unless pkv_set_wait_limit sets another limit), with
-// one answer per warp; on expiry the warp flags PKV_FLAG_TIMEOUT, waits a fixed bounded time for
-// its own copies in flight (so none lands in the shared memory of a finished block) and returns.
+// one answer per warp; on expiry the warp flags PKV_FLAG_TIMEOUT and the CTA winds down: the
+// producer drains its copies in flight, the MMA thread waits for its MMAs, the tensor memory is
+// freed and the CTA returns.
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
@@ -29,25 +48,52 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;
 
-template <int D>
-struct PfGeom {
-  static constexpr int E = (D == 96) ? 32 : 64;  // TMA box extent along head_dim
-  static constexpr int REGION = 64 * E;          // bytes of one box: [2][16][E] fp16
-  static constexpr int SWZ = (E == 64) ? 7 : 3;  // 128-byte or 64-byte swizzle
-  static constexpr int KS = D / 16;
-  static constexpr int NB = D / 8;
-  static constexpr int STAGE = 64 * D;
+constexpr int kRows = 128;           // query rows of a tile (M)
+constexpr int kKeys = 128;           // keys of a block (N of S, K of P V)
+constexpr int kBlockPages = kKeys / kPageSize;
+constexpr int kStages = 2;           // key blocks in flight
+constexpr int kThreads = 192;        // producer warp, MMA warp, four softmax warps
+constexpr int kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
+constexpr int kMaxSortedBatch = 512; // longest-first order of sequences up to this batch
 
-  // Shared-memory address of the 16-byte chunk holding (kv, slot t, dims dim..dim+7).
-  __device__ static uint32_t chunk_addr(uint32_t stage, int kv, int t, int dim) {
-    const int u = dim / E;
-    const uint32_t off = (uint32_t)((kv * kPageSize + t) * (E * 2) + (dim % E) * 2);
-    return stage + u * REGION + (off ^ (((off >> 7) & SWZ) << 4));
-  }
+template <int D>
+struct Geo {
+  static constexpr int E = (D == 96) ? 32 : 64;  // elements per swizzle row (TMA box extent)
+  static constexpr int SW = 2 * E;               // bytes per swizzle row
+  static constexpr int NA = D / E;               // atoms along head_dim
+  static constexpr int KV_BYTES = kKeys * D * 2; // K (or V) of one block
+  static constexpr int STAGE = 2 * KV_BYTES;     // K then V
+  static constexpr int Q_OFF = kStages * STAGE;
+  static constexpr int P_OFF = Q_OFF + kRows * D * 2;
+  static constexpr int BAR_OFF = P_OFF + kRows * kKeys * 2;
+  static constexpr int PAGE_BOX = kPageSize * SW;  // bytes of one page's box (16 rows of one atom)
+  static constexpr uint32_t IDESC_S = tc::idesc_f16(kRows, kKeys, false);
+  static constexpr uint32_t IDESC_O = tc::idesc_f16(kRows, D, true);
 };
 
-__device__ __forceinline__ int find_seq(const int* prefix, int batch, int w) {
-  int lo = 0, hi = batch;  // prefix[lo] <= w < prefix[hi]
+// Barriers and small shared state after the operand regions.
+struct Shared {
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full, o_done, q_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  // pages loaded of block i (bit l = page 8b + l), slot i % 4: written when the block's K copy is
+  // issued (after the S MMA of block i - 2 completed), read before the softmax frees block i's S
+  // buffer, which block i + 4's copy waits for
+  int stage_mask[4];
+  int warp_sums[8];
+};
+
+// 2^x with the special-function unit's approximation (relative error about 2^-22; subnormal results
+// flush to zero, 2^-inf = 0); the probabilities it gives are rounded to fp16.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ int find_pos(const int* prefix, int n, int w) {
+  int lo = 0, hi = n;  // prefix[lo] <= w < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (prefix[mid] <= w) lo = mid; else hi = mid;
@@ -55,359 +101,479 @@ __device__ __forceinline__ int find_seq(const int* prefix, int batch, int w) {
   return lo;
 }
 
+// The tile of work item w: sequence, KV head, first token and token count.
+struct Tile {
+  int s, g, t0, nt, first, n, last, len;
+  bool seq_ok;
+};
+
+__device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const int* prefix, const int* order, int nseq,
+                                        int tb) {
+  Tile t;
+  const int i = find_pos(prefix, nseq, w);
+  t.s = order != nullptr ? order[i] : i;
+  const int a0 = p.append_indptr[t.s], a1 = p.append_indptr[t.s + 1];
+  const int ntiles = (a1 - a0 + tb - 1) / tb;
+  const int r = w - prefix[i];
+  const int rank = r / p.hkv;
+  t.g = r - rank * p.hkv;
+  const int tile = ntiles - 1 - rank;  // a sequence's later tokens see more keys: last tile first
+  t.t0 = a0 + tile * tb;
+  t.nt = min(tb, a1 - t.t0);
+  t.first = p.page_indptr[t.s];
+  t.n = p.page_indptr[t.s + 1] - t.first;
+  t.last = t.n > 0 ? p.last_page_len[t.s] : 0;
+  t.seq_ok = t.n > 0 && t.last >= 1 && t.last <= kPageSize;
+  t.len = t.seq_ok ? (t.n - 1) * kPageSize + t.last : 0;
+  return t;
+}
+
+// Page range [pmin, pmax] the tile's valid tokens attend to (every lane of the calling warp gets it).
+__device__ __forceinline__ void tile_pages(const Tile& t, const PrefillParams& p, int lane, int& pmin, int& pmax) {
+  pmin = 0x7fffffff;
+  pmax = -1;
+  for (int i = lane; i < t.nt; i += 32) {
+    const int pos = t.seq_ok ? p.pos_map[t.t0 + i] : -1;
+    if (pos >= 0 && pos < t.len) {
+      const int st = (p.window > 0 && pos + 1 > p.window) ? pos + 1 - p.window : 0;
+      pmin = min(pmin, st >> 4);
+      pmax = max(pmax, pos >> 4);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    pmin = min(pmin, __shfl_xor_sync(kAll, pmin, off));
+    pmax = max(pmax, __shfl_xor_sync(kAll, pmax, off));
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__((kPrefillWarps + 1) * 32) prefill_kernel(const __grid_constant__ CUtensorMap map,
-                                                                           PrefillParams p) {
-  using Gm = PfGeom<D>;
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap map, PrefillParams p) {
+  using G = Geo<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int nst = p.nstage;
-  unsigned char* stages = base;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)nst * Gm::STAGE);
-  uint64_t* empty = full + nst;
-  int* prefix = reinterpret_cast<int*>(empty + nst);
-  __shared__ int warp_sums[kPrefillWarps + 1];
-  __shared__ int abort_flag;
+  Shared& sh = *reinterpret_cast<Shared*>(base + G::BAR_OFF);
+  int* prefix = reinterpret_cast<int*>(base + G::BAR_OFF + sizeof(Shared));  // [batch + 1]
+  int* order = prefix + p.batch + 1;                                          // [batch] (sorted batches)
+  int* lens = order + p.batch;                                                // [batch] (sorted batches)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tb = kRows / p.group;  // tokens per tile
+  volatile int* abort_flag = &sh.abort_flag;
 
   pdl_launch_dependents();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool producer = warp == kPrefillWarps;
   if (tid == 0) {
     prefetch_tensormap(&map);
-    abort_flag = 0;
-  }
-  for (int i = tid; i < nst; i += blockDim.x) {
-    mbar_init(&full[i], 1);
-    mbar_init(&empty[i], kPrefillWarps);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_free[i], kRows);
+    }
+    mbar_init(&sh.p_full, kRows);
+    mbar_init(&sh.o_done, 1);
+    mbar_init(&sh.q_full, kRows);
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
   }
   fence_mbarrier_init();
+  if (warp == 1) tc::alloc(&sh.tmem_base, kTmemCols);
 
-  // tasks of each sequence (Hkv x blocks of kPrefillWarps tiles of tpt tokens) and their prefix
-  const int block_tokens = kPrefillWarps * p.tpt;
+  // Sequences longest first (when the batch is small enough to sort here), then the work prefix
+  // (tiles x KV heads per sequence, in that order).
+  const bool sorted = p.batch <= kMaxSortedBatch;
+  auto seq_len = [&](int s) {
+    const int n = p.page_indptr[s + 1] - p.page_indptr[s];
+    return n > 0 ? (n - 1) * kPageSize + p.last_page_len[s] : 0;
+  };
+  if (sorted) {
+    for (int s = tid; s < p.batch; s += kThreads) lens[s] = seq_len(s);
+    __syncthreads();
+    for (int s = tid; s < p.batch; s += kThreads) {
+      const int ls = lens[s];
+      int rank = 0;
+      for (int u = 0; u < p.batch; ++u) {
+        const int lu = lens[u];
+        rank += (lu > ls || (lu == ls && u < s)) ? 1 : 0;
+      }
+      order[rank] = s;
+    }
+  }
+  __syncthreads();
   {
-    const int per = (p.batch + blockDim.x - 1) / blockDim.x;
-    const int s0 = min(p.batch, tid * per), s1 = min(p.batch, s0 + per);
-    auto tasks_of = [&](int s) {
+    const int per = (p.batch + kThreads - 1) / kThreads;
+    const int i0 = min(p.batch, tid * per), i1 = min(p.batch, i0 + per);
+    auto items_of = [&](int i) {
+      const int s = sorted ? order[i] : i;
       const int c = p.append_indptr[s + 1] - p.append_indptr[s];
-      return c > 0 ? p.hkv * ((c + block_tokens - 1) / block_tokens) : 0;
+      return c > 0 ? p.hkv * ((c + tb - 1) / tb) : 0;
     };
     int local = 0;
-    for (int s = s0; s < s1; ++s) local += tasks_of(s);
+    for (int i = i0; i < i1; ++i) local += items_of(i);
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int v = __shfl_up_sync(kAll, incl, off);
       if (lane >= off) incl += v;
     }
-    if (lane == 31) warp_sums[warp] = incl;
+    if (lane == 31) sh.warp_sums[warp] = incl;
     __syncthreads();
     int run = incl - local;
-    for (int w = 0; w < warp; ++w) run += warp_sums[w];
-    for (int s = s0; s < s1; ++s) {
-      prefix[s] = run;
-      run += tasks_of(s);
+    for (int w = 0; w < warp; ++w) run += sh.warp_sums[w];
+    for (int i = i0; i < i1; ++i) {
+      prefix[i] = run;
+      run += items_of(i);
     }
-    if (tid == blockDim.x - 1) prefix[p.batch] = run;
+    if (tid == kThreads - 1) prefix[p.batch] = run;
   }
+  tc::fence_before_sync();
   __syncthreads();
+  tc::fence_after_sync();
   const int total = prefix[p.batch];
-
-  // the tiles of one (sequence, KV head) run side by side and read the same pages: keep them in L2
-  const uint64_t policy = l2_policy_evict_last();
-  const int G = p.group;
-  const int c2 = 2 * (lane & 3);
-  int seq = 0;  // pages the CTA has streamed so far (ring slot and phases)
-  int fills = 0;  // producer: stages filled so far (those it must drain before leaving)
+  const int* ord = sorted ? order : nullptr;
+  const uint32_t tmem = sh.tmem_base;
+  const uint32_t sbase = smem_u32(base);
 
   pdl_wait();  // q and the pool (the append) come from the preceding kernel
 
-  for (int task = blockIdx.x; task < total; task += gridDim.x) {
-    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-    const int s = find_seq(prefix, p.batch, task);
-    const int a0 = p.append_indptr[s], cnt = p.append_indptr[s + 1] - a0;
-    const int per_head = (cnt + block_tokens - 1) / block_tokens;
-    const int r = task - prefix[s];
-    const int g = r / per_head;
-    const int tb0 = a0 + (r - g * per_head) * block_tokens;  // first token of the block
-    const int nb_tok = min(block_tokens, a0 + cnt - tb0);
-    const int first = p.page_indptr[s];
-    const int n = p.page_indptr[s + 1] - first;
-    const int last = n > 0 ? p.last_page_len[s] : 0;
-    const bool seq_ok = n > 0 && last >= 1 && last <= kPageSize;
-    const int len = seq_ok ? (n - 1) * kPageSize + last : 0;
-    if (!seq_ok && tid == 0 && r == 0) atomicOr(p.status, kFlagBadSequence);
-
-    // the block's page range (every warp computes it from the block's positions)
-    int pmin = 0x7fffffff, pmax = -1;
-    for (int t = lane; t < nb_tok; t += 32) {
-      const int pos = seq_ok ? p.pos_map[tb0 + t] : -1;
-      if (pos >= 0 && pos < len) {
-        const int st = (p.window > 0 && pos + 1 > p.window) ? pos + 1 - p.window : 0;
-        pmin = min(pmin, st >> 4);
-        pmax = max(pmax, pos >> 4);
-      }
+  // A bounded warp-wide wait; on expiry the CTA winds down.
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (warp_wait_bounded(bar, parity, p.wait_ns)) return true;
+    if (lane == 0) {
+      atomicOr(p.status, kFlagTimeout);
+      *abort_flag = 1;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      pmin = min(pmin, __shfl_xor_sync(kAll, pmin, off));
-      pmax = max(pmax, __shfl_xor_sync(kAll, pmax, off));
-    }
-    if (pmax < 0) continue;  // no valid token (reported below by the rows)
-    const int np = pmax - pmin + 1;
+    __syncwarp();
+    return false;
+  };
 
-    if (producer) {
-      // ---- the CTA's producer: page copies into the shared ring ----
-      int win_base = 0;
-      int window_ids = lane < np ? p.page_indices[first + pmin + lane] : 0;
-      for (int i = 0; i < np; ++i) {
-        if (i - win_base >= 32) {
-          win_base = i & ~31;
-          window_ids = win_base + lane < np ? p.page_indices[first + pmin + win_base + lane] : 0;
-        }
-        const int pid = __shfl_sync(kAll, window_ids, i - win_base);
-        const int f = seq + i, slot = f % nst;
-        if (f >= nst && !warp_wait_bounded(&empty[slot], (uint32_t)(((f / nst) - 1) & 1), p.wait_ns)) {
-          if (lane == 0) {
-            atomicOr(p.status, kFlagTimeout);
-            abort_flag = 1;
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    const uint64_t policy = l2_policy_evict_last();  // a block's pages serve the tiles of its heads
+    int kv_it = 0;
+    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
+      int pmin, pmax;
+      tile_pages(t, p, lane, pmin, pmax);
+      if (pmax < 0) continue;
+      bool ok = true;
+      for (int b = pmin / kBlockPages; b <= pmax / kBlockPages && ok; ++b, ++kv_it) {
+        const int st = kv_it % kStages;
+        const uint32_t par = (uint32_t)(((kv_it / kStages) - 1) & 1);
+        // K of the stage is free once the S MMA that read it has completed, V once the P V MMA has
+        if (kv_it >= kStages && !(ok = wait(&sh.k_empty[st], par))) break;
+        // lane l < 8 owns page 8b + l of the block
+        const int ord_pg = b * kBlockPages + lane;
+        int pid = -1;
+        if (lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax) pid = p.page_indices[t.first + ord_pg];
+        const bool in_range = pid >= 0 && pid < p.num_pages;
+        if (lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax && !in_range) atomicOr(p.status, kFlagBadPage);
+        const unsigned loaded = __ballot_sync(kAll, in_range) & 0xffu;
+        const uint32_t bytes = (uint32_t)__popc(loaded) * kPageSize * D * 2u;  // K (or V) of the loaded pages
+        unsigned char* kdst = base + st * G::STAGE + lane * G::PAGE_BOX;
+        if (lane == 0) {
+          sh.stage_mask[kv_it & 3] = (int)loaded;
+          if (bytes != 0u) {
+            mbar_arrive_expect_tx(&sh.k_full[st], bytes);
+          } else {
+            mbar_arrive(&sh.k_full[st]);
           }
+        }
+        __syncwarp();
+        if (in_range) {
+#pragma unroll
+          for (int u = 0; u < G::NA; ++u)
+            tma_load_4d(kdst + u * kKeys * G::SW, &map, &sh.k_full[st], u * G::E, 0, t.g, 2 * pid, policy);
+        }
+        if (kv_it >= kStages && !(ok = wait(&sh.v_empty[st], par))) {
+          ++kv_it;  // this stage's K copies are in flight: drained below
           break;
         }
-        const bool ok = pid >= 0 && pid < p.num_pages;
-        fills = f + 1;
-        if (!ok && lane == 0) atomicOr(p.status, kFlagBadPage);
-        mbar_arrive_expect_tx_if(lane == 0 && ok, &full[slot], (uint32_t)Gm::STAGE);
-        mbar_arrive_if(lane == 0 && !ok, &full[slot]);
-        unsigned char* dst = stages + (size_t)slot * Gm::STAGE;
-#pragma unroll
-        for (int u = 0; u < D / Gm::E; ++u)
-          tma_load_4d_if(lane == 0 && ok, dst + u * Gm::REGION, &map, &full[slot], u * Gm::E, 0, g, 2 * pid, policy);
-      }
-      seq += np;
-      continue;
-    }
-
-    // ---- consumer warp: 16 rows = tokens tok0 .. tok0 + tpt - 1 of the block x the group's heads ----
-    const int tok0 = tb0 + warp * p.tpt;
-    int tok[2], head[2], pos[2], start[2];
-    bool valid[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int rho = (lane >> 2) + 8 * i;
-      const int tk = rho / G;
-      tok[i] = tok0 + tk;
-      head[i] = g * G + rho % G;
-      valid[i] = seq_ok && tk < p.tpt && tok[i] < a0 + cnt;
-      pos[i] = valid[i] ? p.pos_map[tok[i]] : 0;
-      if (valid[i] && (pos[i] < 0 || pos[i] >= len)) {
-        atomicOr(p.status, kFlagBadPosition);
-        valid[i] = false;
-      }
-      start[i] = (p.window > 0 && pos[i] + 1 > p.window) ? pos[i] + 1 - p.window : 0;
-    }
-    // the warp's own last page (nothing to compute after it), and the positions every valid row
-    // attends to (pages inside [full_lo, full_hi] need no mask)
-    int wmax = -1, full_lo = 0, full_hi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (valid[i]) {
-        wmax = max(wmax, pos[i] >> 4);
-        full_lo = max(full_lo, start[i]);
-        full_hi = min(full_hi, pos[i]);
-      }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      wmax = max(wmax, __shfl_xor_sync(kAll, wmax, off));
-      full_lo = max(full_lo, __shfl_xor_sync(kAll, full_lo, off));
-      full_hi = min(full_hi, __shfl_xor_sync(kAll, full_hi, off));
-    }
-
-    uint32_t qa[Gm::KS][4];
-#pragma unroll
-    for (int ks = 0; ks < Gm::KS; ++ks) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const __half* qr = p.q + ((long long)tok[i] * p.hq + head[i]) * D + ks * 16 + c2;
-        qa[ks][i] = valid[i] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-        qa[ks][2 + i] = valid[i] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
-      }
-    }
-    float acc[Gm::NB][4];
-#pragma unroll
-    for (int nb = 0; nb < Gm::NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-    bool stop = false;
-    for (int i = 0; i < np; ++i) {
-      const int f = seq + i, slot = f % nst;
-      if (!warp_wait_bounded(&full[slot], (uint32_t)((f / nst) & 1), p.wait_ns)) {
         if (lane == 0) {
-          atomicOr(p.status, kFlagTimeout);
-          abort_flag = 1;
-        }
-        stop = true;
-        break;
-      }
-      const int ord = pmin + i;
-      const uint32_t stage = smem_u32(stages + (size_t)slot * Gm::STAGE);
-      if (ord <= wmax) {
-        const int nvalid = ord == n - 1 ? last : kPageSize;
-        // S = Q K^T: two n-blocks of 8 slots (V rows past the end are masked through P below,
-        // and their values are zeroed so that P = 0 times anything stays 0)
-        // (even and odd k-steps accumulate apart: four independent mma chains instead of two)
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          float sc_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          const int mi = lane >> 3, rr = lane & 7;
-          const int t = (mi >> 1) * 8 + rr;
-          const int dsub = (mi & 1) * 8;
-#pragma unroll
-          for (int ks = 0; ks < Gm::KS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(Gm::chunk_addr(stage, 0, t, ks * 16 + dsub), b0, b1, b2, b3);
-            float (&c0)[4] = (ks & 1) ? sc_odd[0] : sc[0];
-            float (&c1)[4] = (ks & 1) ? sc_odd[1] : sc[1];
-            mma_16816(c0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_16816(c1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[0][e] += sc_odd[0][e];
-            sc[1][e] += sc_odd[1][e];
-          }
-        }
-        // a page every valid row sees whole needs no mask (rows without a token are never written)
-        const bool whole = ord * kPageSize >= full_lo && ord * kPageSize + kPageSize - 1 <= full_hi &&
-                           nvalid == kPageSize;
-        float pr[2][4];
-#pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          float v[4];
-          if (whole) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = sc[e >> 1][2 * i2 + (e & 1)] * p.scale_log2;
+          if (bytes != 0u) {
+            mbar_arrive_expect_tx(&sh.v_full[st], bytes);
           } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = (e >> 1) * 8 + c2 + (e & 1);
-              const int tpos = ord * kPageSize + col;
-              const float x = sc[e >> 1][2 * i2 + (e & 1)] * p.scale_log2;
-              v[e] = (valid[i2] && tpos >= start[i2] && tpos <= pos[i2]) ? x : -INFINITY;
-            }
-          }
-          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
-          if (mx > m[i2] + kLazy) {
-            const float alpha = exp2f(m[i2] - mx);
-            l[i2] *= alpha;
-#pragma unroll
-            for (int nb = 0; nb < Gm::NB; ++nb) {
-              acc[nb][2 * i2] *= alpha;
-              acc[nb][2 * i2 + 1] *= alpha;
-            }
-            m[i2] = mx;
-          }
-          // a row may see no position yet (its window starts further on): its P is 0, not NaN
-#pragma unroll
-          for (int e = 0; e < 4; ++e) pr[i2][e] = v[e] == -INFINITY ? 0.f : exp2f(v[e] - m[i2]);
-        }
-        uint32_t pa[4];
-#pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          const __half2 lo = __floats2half2_rn(pr[i2][0], pr[i2][1]);
-          const __half2 hi = __floats2half2_rn(pr[i2][2], pr[i2][3]);
-          const float2 flo = __half22float2(lo), fhi = __half22float2(hi);
-          l[i2] += (flo.x + flo.y) + (fhi.x + fhi.y);
-          pa[i2] = *reinterpret_cast<const uint32_t*>(&lo);
-          pa[2 + i2] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
-        if (nvalid < kPageSize) {
-          // the ring is shared: instead of zeroing V rows past the end, zero their P (already 0
-          // through the mask) and read those V rows as zero via a guarded copy of the fragment
-          // inputs below
-        }
-        {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int t = (mi & 1) * 8 + rr;
-          const int dsub = (mi >> 1) * 8;
-#pragma unroll
-          for (int mm = 0; mm < D / 16; ++mm) {
-            uint32_t v0, v1, v2, v3;
-            ldmatrix_x4_trans(Gm::chunk_addr(stage, 1, t, mm * 16 + dsub), v0, v1, v2, v3);
-            if (nvalid < kPageSize) {
-              // V fragments of slots past the sequence end may hold anything (NaN): zero them
-              // (ldmatrix.trans gives this lane slots tr and tr + 8 of its two 8x8 matrices)
-              const int tr = 2 * (lane & 3);
-              if (tr >= nvalid) v0 = 0u;
-              if (tr + 1 >= nvalid) v0 &= 0x0000FFFFu;
-              if (tr + 8 >= nvalid) v1 = 0u;
-              if (tr + 9 >= nvalid) v1 &= 0x0000FFFFu;
-              if (tr >= nvalid) v2 = 0u;
-              if (tr + 1 >= nvalid) v2 &= 0x0000FFFFu;
-              if (tr + 8 >= nvalid) v3 = 0u;
-              if (tr + 9 >= nvalid) v3 &= 0x0000FFFFu;
-            }
-            mma_16816(acc[2 * mm], pa[0], pa[1], pa[2], pa[3], v0, v1);
-            mma_16816(acc[2 * mm + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
+            mbar_arrive(&sh.v_full[st]);
           }
         }
+        __syncwarp();
+        if (in_range) {
+#pragma unroll
+          for (int u = 0; u < G::NA; ++u)
+            tma_load_4d(kdst + G::KV_BYTES + u * kKeys * G::SW, &map, &sh.v_full[st], u * G::E, 0, t.g, 2 * pid + 1,
+                        policy);
+        }
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag) {
+      // wait (bounded) for the copies in flight of the last stages before leaving
+      for (int i = max(0, kv_it - kStages); i < kv_it; ++i) {
+        mbar_wait_bounded(&sh.k_full[i % kStages], (uint32_t)((i / kStages) & 1), kDrainLimitNs);
+        mbar_wait_bounded(&sh.v_full[i % kStages], (uint32_t)((i / kStages) & 1), kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    int kvc = 0, sc = 0, pc = 0, qi = 0;
+    const bool leader = lane == 0;
+    // O += P_j V_j for the block in stage `st`; `first` starts the accumulator
+    auto issue_pv = [&](int st, int vit, bool first) -> bool {
+      if (!wait(&sh.p_full, (uint32_t)(pc & 1))) return false;
+      if (!wait(&sh.v_full[st], (uint32_t)((vit / kStages) & 1))) return false;
+      ++pc;
+      tc::fence_after_sync();
+      if (leader) {
+        const uint32_t vbase = sbase + st * G::STAGE + G::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint32_t pa = sbase + G::P_OFF + (uint32_t)((16 * kk) / 64) * kRows * 128 + (uint32_t)((32 * kk) % 128);
+          const uint64_t ad = tc::smem_desc(pa, 16, 1024, tc::kLayoutSwizzle128);
+          const uint64_t bd = tc::smem_desc(vbase + (uint32_t)(16 * kk * G::SW), kKeys * G::SW, 8 * G::SW,
+                                            tc::layout_for(G::E));
+          tc::mma_f16(tmem + 256, ad, bd, G::IDESC_O, !(first && kk == 0));
+        }
+        tc::commit(&sh.v_empty[st]);
+        tc::commit(&sh.o_done);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage
-    }
-    seq += np;
-    if (stop) break;
-
-    // finish the two rows: out = acc / l (with the sink in the denominator), lse
+      return true;
+    };
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok && !*abort_flag; w += gridDim.x) {
+      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
+      int pmin, pmax;
+      tile_pages(t, p, lane, pmin, pmax);
+      if (pmax < 0) continue;
+      if (!(ok = wait(&sh.q_full, (uint32_t)(qi & 1)))) break;
+      ++qi;
+      const int nb = pmax / kBlockPages - pmin / kBlockPages + 1;
+      int prev_st = 0;
+      for (int j = 0; j < nb; ++j, ++kvc, ++sc) {
+        const int st = kvc % kStages, sb = sc & 1;
+        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvc / kStages) & 1)))) break;
+        if (sc >= 2 && !(ok = wait(&sh.s_free[sb], (uint32_t)(((sc >> 1) - 1) & 1)))) break;
+        tc::fence_after_sync();
+        if (leader) {
+          const uint32_t kbase = sbase + st * G::STAGE;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      float lt = l[i];
-      lt += __shfl_xor_sync(kAll, lt, 1);
-      lt += __shfl_xor_sync(kAll, lt, 2);
-      float mm = m[i], scale = 1.f;
-      if (p.sinks != nullptr && valid[i]) {
-        const float sl = p.sinks[head[i]] * kLog2e;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)((16 * kk) / G::E) * kRows * G::SW + (uint32_t)((32 * kk) % G::SW);
+            const uint64_t ad = tc::smem_desc(sbase + G::Q_OFF + off, 16, 8 * G::SW, tc::layout_for(G::E));
+            const uint64_t bd = tc::smem_desc(kbase + off, 16, 8 * G::SW, tc::layout_for(G::E));
+            tc::mma_f16(tmem + 128 * sb, ad, bd, G::IDESC_S, kk > 0);
+          }
+          tc::commit(&sh.s_full[sb]);
+          tc::commit(&sh.k_empty[st]);
+        }
+        __syncwarp();
+        if (j > 0 && !(ok = issue_pv(prev_st, kvc - 1, j == 1))) break;
+        prev_st = st;
+      }
+      if (ok) ok = issue_pv(prev_st, kvc - 1, nb == 1);
+    }
+    // before the tensor memory is freed: every MMA this thread issued has completed
+    if (leader) tc::commit(&sh.drain);
+    __syncwarp();
+    mbar_wait_bounded(&sh.drain, 0, kDrainLimitNs);
+  } else {
+    // ---------------------------------------------------------------- softmax warps
+    const int quarter = warp & 3;              // the tensor-memory lanes this warp may access
+    const int r = 32 * quarter + lane;         // query row = tensor-memory lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    int kvs = 0, ss = 0, pw = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok && !*abort_flag; w += gridDim.x) {
+      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
+      // this row's token and query head, its position and the first position it attends to
+      const int tk = r / p.group;
+      const int tok = t.t0 + tk;
+      const int head = t.g * p.group + r % p.group;
+      bool valid = t.seq_ok && tk < t.nt;
+      int pos = valid ? p.pos_map[tok] : 0;
+      if (valid && (pos < 0 || pos >= t.len)) {
+        atomicOr(p.status, kFlagBadPosition);  // the row is left unwritten
+        valid = false;
+      }
+      if (!t.seq_ok && r == 0 && t.g == 0 && t.nt > 0) atomicOr(p.status, kFlagBadSequence);
+      int pmin, pmax;
+      tile_pages(t, p, lane, pmin, pmax);
+      if (pmax < 0) continue;
+      const int start = (valid && p.window > 0 && pos + 1 > p.window) ? pos + 1 - p.window : 0;
+      if (!valid) pos = -1;  // attends to nothing
+
+      // the tile's queries, row r, into the K-major swizzled Q region
+      {
+        const __half* src = p.q + ((long long)tok * p.hq + head) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = valid ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(base + G::Q_OFF + tc::kmajor_offset(kRows, G::E, r, 8 * c)) = v;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.q_full);
+      }
+
+      float m = -INFINITY, l = 0.f;
+      const int b0 = pmin / kBlockPages, nb = pmax / kBlockPages - b0 + 1;
+      for (int j = 0; j < nb; ++j, ++kvs, ++ss) {
+        const int b = b0 + j, st = kvs % kStages, sb = ss & 1;
+        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvs / kStages) & 1)))) break;
+        if (!(ok = wait(&sh.s_full[sb], (uint32_t)((ss >> 1) & 1)))) break;
+        tc::fence_after_sync();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_addr + 128 * sb + 32 * q4, sv[q4]);
+        const int loaded = sh.stage_mask[kvs & 3];
+        tc::wait_ld();
+        tc::fence_before_sync();
+        mbar_arrive(&sh.s_free[sb]);
+        const int k0 = b * kKeys;  // position of the block's first key
+        float x[kKeys];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[32 * q4 + e] = __uint_as_float(sv[q4][e]);
+        // keys outside the row's range [start, pos] or in pages not loaded take no part (the warp
+        // skips the test when every row of it sees the whole block)
+        const bool whole = loaded == 0xff && k0 >= start && k0 + kKeys - 1 <= pos;
+        if (!__all_sync(kAll, whole)) {
+          const int lo = start - k0, hi = pos - k0;
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c)
+            x[c] = (((loaded >> (c >> 4)) & 1) && c >= lo && c <= hi) ? x[c] : -INFINITY;
+        }
+        // row max of the raw scores (eight independent chains), then scaled: sm_scale > 0
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mb = mraw * p.scale_log2;  // -inf stays -inf
+        // raise the running max only when a score exceeds it by more than 2^8
+        const bool raise = mb > m + kLazy;
+        const float m_new = raise ? mb : m;
+        const float alpha = raise ? ex2(m - m_new) : 1.f;  // 0 on the first raise (m = -inf)
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;  // a row that sees no key yet: every P is 0
+        float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[kKeys / 2];
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 2) {
+          const float p0 = ex2(fmaf(x[c], p.scale_log2, -m_use));  // exp2(-inf) = 0 for masked keys
+          const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, -m_use));
+          const __half2 h = __floats2half2_rn(p0, p1);
+          const float2 f = __half22float2(h);  // the denominator adds the rounded values P V uses
+          sums[(c >> 1) & 7] += f.x + f.y;
+          pk[c / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
+        l = l * alpha + sum;
+        m = m_new;
+        // the P buffer and O are free once the previous block's P V has completed
+        if (j > 0) {
+          if (!(ok = wait(&sh.o_done, (uint32_t)(pw & 1)))) break;
+          ++pw;
+          tc::fence_after_sync();
+          if (__any_sync(kAll, raise)) {  // tensor-memory loads and stores are warp-wide (alpha = 1 elsewhere)
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tc::ld32(lane_addr + 256 + c, ov);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tc::st32(lane_addr + 256 + c, ov);
+            }
+            tc::wait_st();
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < kKeys / 8; ++c)
+          *reinterpret_cast<uint4*>(base + G::P_OFF + tc::kmajor_offset(kRows, 64, r, 8 * c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        // key row r of the block's V: zero it when its key lies past the sequence end or in a
+        // page that was not loaded (its contents are stale or a NaN sentinel)
+        const bool zero_v = !(((loaded >> (r >> 4)) & 1) && k0 + r < t.len);
+        if (__any_sync(kAll, zero_v) && !(ok = wait(&sh.v_full[st], (uint32_t)((kvs / kStages) & 1)))) break;
+        if (zero_v) {
+          unsigned char* vrow = base + st * G::STAGE + G::KV_BYTES + r * G::SW;
+#pragma unroll
+          for (int u = 0; u < G::NA; ++u)
+#pragma unroll
+            for (int c = 0; c < G::SW / 16; ++c)
+              *reinterpret_cast<uint4*>(vrow + u * kKeys * G::SW + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        mbar_arrive(&sh.p_full);
+      }
+      if (!ok) break;
+      // the last block's P V, then the row of O
+      if (!(ok = wait(&sh.o_done, (uint32_t)(pw & 1)))) break;
+      ++pw;
+      tc::fence_after_sync();
+      float mm = m, scale = 1.f, lt = l;
+      if (p.sinks != nullptr && valid) {
+        const float sl = p.sinks[head] * kLog2e;
         const float M2 = fmaxf(mm, sl);
         scale = exp2f(mm - M2);
         lt = lt * scale + exp2f(sl - M2);
         mm = M2;
       }
-      if (!valid[i]) continue;
       const bool any = lt > 0.f;
       const float inv = any ? scale / lt : 0.f;
-      __half* dst = p.out + ((long long)tok[i] * p.hq + head[i]) * D + c2;
+      __half* dst = p.out + ((long long)tok * p.hq + head) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tc::ld32(lane_addr + 256 + c, ov);
+        tc::wait_ld();
+        if (valid) {
 #pragma unroll
-      for (int nb = 0; nb < Gm::NB; ++nb)
-        *reinterpret_cast<__half2*>(dst + nb * 8) = __floats2half2_rn(acc[nb][2 * i] * inv, acc[nb][2 * i + 1] * inv);
-      if (p.lse != nullptr && (lane & 3) == 0)
-        p.lse[(long long)tok[i] * p.hq + head[i]] = any ? (mm + log2f(lt)) * kLn2 : -INFINITY;
+          for (int e = 0; e < 32; e += 8) {
+            uint4 o;
+            o.x = pack_half2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+            o.y = pack_half2(__uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+            o.z = pack_half2(__uint_as_float(ov[e + 4]) * inv, __uint_as_float(ov[e + 5]) * inv);
+            o.w = pack_half2(__uint_as_float(ov[e + 6]) * inv, __uint_as_float(ov[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c + e) = o;
+          }
+        }
+      }
+      if (valid && p.lse != nullptr) p.lse[(long long)tok * p.hq + head] = any ? (mm + log2f(lt)) * kLn2 : -INFINITY;
+      tc::fence_before_sync();  // the O reads above come before the next tile's first P V
     }
   }
-  // the producer leaves only when its copies have landed: wait (bounded) for the last fills
-  if (producer && *reinterpret_cast<volatile int*>(&abort_flag)) {
-    for (int f = max(0, fills - nst); f < fills; ++f)
-      mbar_wait_bounded(&full[f % nst], (uint32_t)((f / nst) & 1), kDrainLimitNs);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::dealloc(tmem, kTmemCols);
   }
 }
 
 template <int D>
-size_t prefill_smem(int nstage, int batch) {
-  return 1024 + (size_t)nstage * PfGeom<D>::STAGE + (size_t)nstage * 16 + (size_t)(batch + 1) * 4;
+size_t prefill_smem(int batch) {
+  // operand regions, the barriers, the work prefix and the sort order, and the alignment slack;
+  // at least 120 KB, so that two CTAs (each holding all tensor-memory columns) never share an SM
+  const size_t need = 1024 + Geo<D>::BAR_OFF + sizeof(Shared) + (size_t)(batch + 1) * 4 +
+                      (batch <= kMaxSortedBatch ? (size_t)(2 * batch) * 4 : 0);
+  return need < 122880 ? 122880 : need;
 }
 
 }  // namespace
 
 PrefillConfig prefill_config(int head_dim, int batch) {
   PrefillConfig c;
-  const int budget = 232448 - 256;  // one CTA (nine warps) per SM
-  c.nstage = 8;
-  auto smem = [&](int n) {
-    return head_dim == 64 ? prefill_smem<64>(n, batch) : head_dim == 96 ? prefill_smem<96>(n, batch)
-                                                                         : prefill_smem<128>(n, batch);
-  };
-  while (c.nstage >= 2 && smem(c.nstage) > (size_t)budget) --c.nstage;
-  c.smem_bytes = c.nstage >= 2 ? smem(c.nstage) : 0;
+  const size_t budget = 232448 - 1024;
+  c.smem_bytes = head_dim == 64 ? prefill_smem<64>(batch) : head_dim == 96 ? prefill_smem<96>(batch)
+                                                                            : prefill_smem<128>(batch);
+  c.nstage = c.smem_bytes <= budget ? kStages : 0;
+  if (c.nstage == 0) c.smem_bytes = 0;
   return c;
 }
 
@@ -415,7 +581,7 @@ cudaError_t prefill_prepare() {
   const void* k[] = {(const void*)&prefill_kernel<64>, (const void*)&prefill_kernel<96>,
                      (const void*)&prefill_kernel<128>};
   for (const void* f : k) {
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 256);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
@@ -427,7 +593,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& map, const
                            int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);
-  lc.blockDim = dim3((kPrefillWarps + 1) * 32);  // consumers and one producer warp
+  lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
