@@ -11,19 +11,21 @@
 // ordered longest sequence first (tiles of one sequence last tile first) and dealt to the CTAs of
 // a persistent grid (one per SM) in turn.
 //
-// One CTA, six warps:
-//   warp 0  producer: the tile's key blocks, each page's K and V boxes of KV head g copied by the
-//           tensor-memory-access unit into a two-stage ring (128-byte swizzle, 64-byte for
-//           head_dim 96); K and V of a stage have barriers of their own, so the K half is refilled
-//           as soon as its S MMA has completed while the V half waits for its P V MMA;
+// One CTA, seven warps:
+//   warps 0 and 6  producers: the tile's key blocks, each page's K (warp 0) and V (warp 6) boxes of
+//           KV head g copied by the tensor-memory-access unit into rings of three K and two V
+//           stages (128-byte swizzle, 64-byte for head_dim 96), each with its own barriers, so a K
+//           stage is refilled as soon as its S MMA has completed while a V stage waits for its
+//           P V MMA;
 //   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two tensor-memory buffers (128
-//           fp32 columns each), then O += P_j V_j into a third (head_dim columns), V read
-//           MN-major straight from the staged pages; every MMA group commits to a barrier;
+//           fp32 columns each), then O += P_j V_j into a third (head_dim columns), P read from
+//           tensor memory where the softmax left it (in S_j's buffer) and V MN-major straight from
+//           the staged pages; every MMA group commits to a barrier;
 //   warps 2-5  softmax (thread = query row = tensor-memory lane): stage the tile's queries in
 //           shared memory, then per block read the row of S, mask it (the row's causal range
 //           [window start, position], pages not loaded), an online softmax in the log2 domain
 //           whose running max is raised only when a score exceeds it by 2^8 (then the row of O is
-//           rescaled in tensor memory), P rounded to fp16 into shared memory for the P V MMA (the
+//           rescaled in tensor memory), P rounded to fp16 over the scores in tensor memory (the
 //           row sum adds the same rounded values); the score loops run as eight independent chains,
 //           since one warp per scheduler has little else to hide latencies with;
 //           finally the row of O divided by the row sum (sinks join the denominator), written in
@@ -51,8 +53,10 @@ constexpr float kLazy = 8.f;
 constexpr int kRows = 128;           // query rows of a tile (M)
 constexpr int kKeys = 128;           // keys of a block (N of S, K of P V)
 constexpr int kBlockPages = kKeys / kPageSize;
-constexpr int kStages = 2;           // key blocks in flight
-constexpr int kThreads = 192;        // producer warp, MMA warp, four softmax warps
+constexpr int kKStages = 3;          // key blocks whose K is in flight
+constexpr int kVStages = 2;          // and whose V is
+constexpr int kThreads = 224;        // K producer, MMA issuer, four softmax warps, V producer
+constexpr int kSoftmaxWarps = 4;
 constexpr int kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
 constexpr int kMaxSortedBatch = 512; // longest-first order of sequences up to this batch
 
@@ -62,10 +66,10 @@ struct Geo {
   static constexpr int SW = 2 * E;               // bytes per swizzle row
   static constexpr int NA = D / E;               // atoms along head_dim
   static constexpr int KV_BYTES = kKeys * D * 2; // K (or V) of one block
-  static constexpr int STAGE = 2 * KV_BYTES;     // K then V
-  static constexpr int Q_OFF = kStages * STAGE;
-  static constexpr int P_OFF = Q_OFF + kRows * D * 2;
-  static constexpr int BAR_OFF = P_OFF + kRows * kKeys * 2;
+  static constexpr int K_OFF = 0;                // K stages, then V stages, then the queries
+  static constexpr int V_OFF = kKStages * KV_BYTES;
+  static constexpr int Q_OFF = V_OFF + kVStages * KV_BYTES;
+  static constexpr int BAR_OFF = Q_OFF + kRows * D * 2;
   static constexpr int PAGE_BOX = kPageSize * SW;  // bytes of one page's box (16 rows of one atom)
   static constexpr uint32_t IDESC_S = tc::idesc_f16(kRows, kKeys, false);
   static constexpr uint32_t IDESC_O = tc::idesc_f16(kRows, D, true);
@@ -73,14 +77,14 @@ struct Geo {
 
 // Barriers and small shared state after the operand regions.
 struct Shared {
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full, o_done, q_full, drain;
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full, o_done, q_full, drain;
   uint32_t tmem_base;
   int abort_flag;
-  // pages loaded of block i (bit l = page 8b + l), slot i % 4: written when the block's K copy is
-  // issued (after the S MMA of block i - 2 completed), read before the softmax frees block i's S
-  // buffer, which block i + 4's copy waits for
-  int stage_mask[4];
+  // pages loaded of block i (bit l = page 8b + l), slot i % 8: written when the block's K copy is
+  // issued, read by the softmax warps before they release the block's K stage, which the copy of
+  // block i + 3 waits for
+  int stage_mask[8];
   int warp_sums[8];
 };
 
@@ -163,16 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   pdl_launch_dependents();
   if (tid == 0) {
     prefetch_tensormap(&map);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&sh.k_full[i], 1);
-      mbar_init(&sh.k_empty[i], 1);
+      // K of a stage is free when its S MMA has completed and every softmax warp has passed the
+      // block's K barrier (it reads the block's page mask there): a later K copy can then never
+      // complete a phase of that barrier before a softmax warp has waited for the earlier one
+      mbar_init(&sh.k_empty[i], 1 + kSoftmaxWarps);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sh.v_full[i], 1);
       mbar_init(&sh.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.s_free[i], kRows);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&sh.s_full[i], 1);
     mbar_init(&sh.p_full, kRows);
     mbar_init(&sh.o_done, 1);
     mbar_init(&sh.q_full, kRows);
@@ -250,9 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return false;
   };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+  if (warp == 0 || warp == 6) {
+    // ---------------------------------------------------------------- producers (K: warp 0, V: warp 6)
+    const bool is_k = warp == 0;
     const uint64_t policy = l2_policy_evict_last();  // a block's pages serve the tiles of its heads
+    uint64_t* full = is_k ? sh.k_full : sh.v_full;
+    uint64_t* empty = is_k ? sh.k_empty : sh.v_empty;
+    const int kv = is_k ? 0 : 1;
+    const int nst = is_k ? kKStages : kVStages;
+    const int region = is_k ? G::K_OFF : G::V_OFF;
     int kv_it = 0;
     for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
       const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
@@ -261,80 +273,63 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (pmax < 0) continue;
       bool ok = true;
       for (int b = pmin / kBlockPages; b <= pmax / kBlockPages && ok; ++b, ++kv_it) {
-        const int st = kv_it % kStages;
-        const uint32_t par = (uint32_t)(((kv_it / kStages) - 1) & 1);
-        // K of the stage is free once the S MMA that read it has completed, V once the P V MMA has
-        if (kv_it >= kStages && !(ok = wait(&sh.k_empty[st], par))) break;
+        const int st = kv_it % nst;
+        // K of a stage is free once the S MMA that read it has completed, V once the P V MMA has
+        if (kv_it >= nst && !(ok = wait(&empty[st], (uint32_t)(((kv_it / nst) - 1) & 1)))) break;
         // lane l < 8 owns page 8b + l of the block
         const int ord_pg = b * kBlockPages + lane;
         int pid = -1;
         if (lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax) pid = p.page_indices[t.first + ord_pg];
         const bool in_range = pid >= 0 && pid < p.num_pages;
-        if (lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax && !in_range) atomicOr(p.status, kFlagBadPage);
+        if (is_k && lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax && !in_range)
+          atomicOr(p.status, kFlagBadPage);
         const unsigned loaded = __ballot_sync(kAll, in_range) & 0xffu;
         const uint32_t bytes = (uint32_t)__popc(loaded) * kPageSize * D * 2u;  // K (or V) of the loaded pages
-        unsigned char* kdst = base + st * G::STAGE + lane * G::PAGE_BOX;
         if (lane == 0) {
-          sh.stage_mask[kv_it & 3] = (int)loaded;
+          if (is_k) sh.stage_mask[kv_it & 7] = (int)loaded;
           if (bytes != 0u) {
-            mbar_arrive_expect_tx(&sh.k_full[st], bytes);
+            mbar_arrive_expect_tx(&full[st], bytes);
           } else {
-            mbar_arrive(&sh.k_full[st]);
+            mbar_arrive(&full[st]);
           }
         }
         __syncwarp();
         if (in_range) {
+          unsigned char* dst = base + region + st * G::KV_BYTES + lane * G::PAGE_BOX;
 #pragma unroll
           for (int u = 0; u < G::NA; ++u)
-            tma_load_4d(kdst + u * kKeys * G::SW, &map, &sh.k_full[st], u * G::E, 0, t.g, 2 * pid, policy);
-        }
-        if (kv_it >= kStages && !(ok = wait(&sh.v_empty[st], par))) {
-          ++kv_it;  // this stage's K copies are in flight: drained below
-          break;
-        }
-        if (lane == 0) {
-          if (bytes != 0u) {
-            mbar_arrive_expect_tx(&sh.v_full[st], bytes);
-          } else {
-            mbar_arrive(&sh.v_full[st]);
-          }
-        }
-        __syncwarp();
-        if (in_range) {
-#pragma unroll
-          for (int u = 0; u < G::NA; ++u)
-            tma_load_4d(kdst + G::KV_BYTES + u * kKeys * G::SW, &map, &sh.v_full[st], u * G::E, 0, t.g, 2 * pid + 1,
-                        policy);
+            tma_load_4d(dst + u * kKeys * G::SW, &map, &full[st], u * G::E, 0, t.g, 2 * pid + kv, policy);
         }
       }
       if (!ok) break;
     }
     if (*abort_flag) {
       // wait (bounded) for the copies in flight of the last stages before leaving
-      for (int i = max(0, kv_it - kStages); i < kv_it; ++i) {
-        mbar_wait_bounded(&sh.k_full[i % kStages], (uint32_t)((i / kStages) & 1), kDrainLimitNs);
-        mbar_wait_bounded(&sh.v_full[i % kStages], (uint32_t)((i / kStages) & 1), kDrainLimitNs);
-      }
+      for (int i = max(0, kv_it - nst); i < kv_it; ++i)
+        mbar_wait_bounded(&full[i % nst], (uint32_t)((i / nst) & 1), kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    int kvc = 0, sc = 0, pc = 0, qi = 0;
+    int kvc = 0, sc = 0, pc = 0, qi = 0;  // blocks, S MMAs, P V MMAs, tiles
     const bool leader = lane == 0;
     // O += P_j V_j for the block in stage `st`; `first` starts the accumulator
-    auto issue_pv = [&](int st, int vit, bool first) -> bool {
+    // O += P V for block number vit: P in the block's S buffer of tensor memory (two fp16 per
+    // column, written by the softmax over the scores it read), V from its stage.  MMAs execute in
+    // issue order, so this one reads P before the S MMA two blocks on overwrites the buffer.
+    auto issue_pv = [&](int vit, bool first) -> bool {
+      const int st = vit % kVStages;
       if (!wait(&sh.p_full, (uint32_t)(pc & 1))) return false;
-      if (!wait(&sh.v_full[st], (uint32_t)((vit / kStages) & 1))) return false;
+      if (!wait(&sh.v_full[st], (uint32_t)((vit / kVStages) & 1))) return false;
       ++pc;
       tc::fence_after_sync();
       if (leader) {
-        const uint32_t vbase = sbase + st * G::STAGE + G::KV_BYTES;
+        const uint32_t vbase = sbase + G::V_OFF + st * G::KV_BYTES;
+        const uint32_t pbase = tmem + 128 * (vit & 1);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint32_t pa = sbase + G::P_OFF + (uint32_t)((16 * kk) / 64) * kRows * 128 + (uint32_t)((32 * kk) % 128);
-          const uint64_t ad = tc::smem_desc(pa, 16, 1024, tc::kLayoutSwizzle128);
           const uint64_t bd = tc::smem_desc(vbase + (uint32_t)(16 * kk * G::SW), kKeys * G::SW, 8 * G::SW,
                                             tc::layout_for(G::E));
-          tc::mma_f16(tmem + 256, ad, bd, G::IDESC_O, !(first && kk == 0));
+          tc::mma_f16_ts(tmem + 256, pbase + 8 * kk, bd, G::IDESC_O, !(first && kk == 0));
         }
         tc::commit(&sh.v_empty[st]);
         tc::commit(&sh.o_done);
@@ -351,14 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (!(ok = wait(&sh.q_full, (uint32_t)(qi & 1)))) break;
       ++qi;
       const int nb = pmax / kBlockPages - pmin / kBlockPages + 1;
-      int prev_st = 0;
       for (int j = 0; j < nb; ++j, ++kvc, ++sc) {
-        const int st = kvc % kStages, sb = sc & 1;
-        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvc / kStages) & 1)))) break;
-        if (sc >= 2 && !(ok = wait(&sh.s_free[sb], (uint32_t)(((sc >> 1) - 1) & 1)))) break;
+        // S buffer sb held P of block kvc - 2, whose P V MMA was issued in the previous iteration
+        const int st = kvc % kKStages, sb = sc & 1;
+        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvc / kKStages) & 1)))) break;
         tc::fence_after_sync();
         if (leader) {
-          const uint32_t kbase = sbase + st * G::STAGE;
+          const uint32_t kbase = sbase + G::K_OFF + st * G::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((16 * kk) / G::E) * kRows * G::SW + (uint32_t)((32 * kk) % G::SW);
@@ -370,10 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tc::commit(&sh.k_empty[st]);
         }
         __syncwarp();
-        if (j > 0 && !(ok = issue_pv(prev_st, kvc - 1, j == 1))) break;
-        prev_st = st;
+        if (j > 0 && !(ok = issue_pv(kvc - 1, j == 1))) break;
       }
-      if (ok) ok = issue_pv(prev_st, kvc - 1, nb == 1);
+      if (ok) ok = issue_pv(kvc - 1, nb == 1);
     }
     // before the tensor memory is freed: every MMA this thread issued has completed
     if (leader) tc::commit(&sh.drain);
@@ -420,17 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float m = -INFINITY, l = 0.f;
       const int b0 = pmin / kBlockPages, nb = pmax / kBlockPages - b0 + 1;
       for (int j = 0; j < nb; ++j, ++kvs, ++ss) {
-        const int b = b0 + j, st = kvs % kStages, sb = ss & 1;
-        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvs / kStages) & 1)))) break;
+        const int b = b0 + j, st = kvs % kKStages, vst = kvs % kVStages, sb = ss & 1;
+        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvs / kKStages) & 1)))) break;
         if (!(ok = wait(&sh.s_full[sb], (uint32_t)((ss >> 1) & 1)))) break;
         tc::fence_after_sync();
         uint32_t sv[4][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_addr + 128 * sb + 32 * q4, sv[q4]);
-        const int loaded = sh.stage_mask[kvs & 3];
+        const int loaded = sh.stage_mask[kvs & 7];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.k_empty[st]);
         tc::wait_ld();
-        tc::fence_before_sync();
-        mbar_arrive(&sh.s_free[sb]);
         const int k0 = b * kKeys;  // position of the block's first key
         float x[kKeys];
 #pragma unroll
@@ -473,7 +466,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
         l = l * alpha + sum;
         m = m_new;
-        // the P buffer and O are free once the previous block's P V has completed
+        // P into the block's S buffer (the scores were read above), two fp16 per column
+        tc::st32(lane_addr + 128 * sb, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tc::st32(lane_addr + 128 * sb + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        // key row r of the block's V: zero it when its key lies past the sequence end or in a
+        // page that was not loaded (its contents are stale or a NaN sentinel)
+        const bool zero_v = !(((loaded >> (r >> 4)) & 1) && k0 + r < t.len);
+        if (__any_sync(kAll, zero_v)) {
+          if (!(ok = wait(&sh.v_full[vst], (uint32_t)((kvs / kVStages) & 1)))) break;
+          if (zero_v) {
+            unsigned char* vrow = base + G::V_OFF + vst * G::KV_BYTES + r * G::SW;
+#pragma unroll
+            for (int u = 0; u < G::NA; ++u)
+#pragma unroll
+              for (int c = 0; c < G::SW / 16; ++c)
+                *reinterpret_cast<uint4*>(vrow + u * kKeys * G::SW + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        // O is quiescent once the previous block's P V has completed: rescale it then, if the
+        // running max was raised
         if (j > 0) {
           if (!(ok = wait(&sh.o_done, (uint32_t)(pw & 1)))) break;
           ++pw;
@@ -488,26 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
               tc::st32(lane_addr + 256 + c, ov);
             }
-            tc::wait_st();
           }
         }
-#pragma unroll
-        for (int c = 0; c < kKeys / 8; ++c)
-          *reinterpret_cast<uint4*>(base + G::P_OFF + tc::kmajor_offset(kRows, 64, r, 8 * c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        // key row r of the block's V: zero it when its key lies past the sequence end or in a
-        // page that was not loaded (its contents are stale or a NaN sentinel)
-        const bool zero_v = !(((loaded >> (r >> 4)) & 1) && k0 + r < t.len);
-        if (__any_sync(kAll, zero_v) && !(ok = wait(&sh.v_full[st], (uint32_t)((kvs / kStages) & 1)))) break;
-        if (zero_v) {
-          unsigned char* vrow = base + st * G::STAGE + G::KV_BYTES + r * G::SW;
-#pragma unroll
-          for (int u = 0; u < G::NA; ++u)
-#pragma unroll
-            for (int c = 0; c < G::SW / 16; ++c)
-              *reinterpret_cast<uint4*>(vrow + u * kKeys * G::SW + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
+        tc::wait_st();
         tc::fence_before_sync();
         mbar_arrive(&sh.p_full);
       }
@@ -572,7 +567,7 @@ PrefillConfig prefill_config(int head_dim, int batch) {
   const size_t budget = 232448 - 1024;
   c.smem_bytes = head_dim == 64 ? prefill_smem<64>(batch) : head_dim == 96 ? prefill_smem<96>(batch)
                                                                             : prefill_smem<128>(batch);
-  c.nstage = c.smem_bytes <= budget ? kStages : 0;
+  c.nstage = c.smem_bytes <= budget ? kKStages : 0;
   if (c.nstage == 0) c.smem_bytes = 0;
   return c;
 }
