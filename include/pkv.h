@@ -78,13 +78,14 @@ typedef enum {
                                int8 KV behind a flag; the format is this library's reading): each
                                layer's pool is uint8 blocks
                                [num_pages][2][Hkv][16 * head_dim + 64] holding the 16 slots' int8
-                               codes [16][head_dim] then their fp32 scales [16].  The append
+                               codes, then their fp32 scales [16]: K codes slot-major
+                               [16][head_dim], V codes dim-major [head_dim][16].  The append
                                quantizes each new K row (after RoPE and its fp16 rounding) and V row:
                                s = max|x| / 127 (fp32), code = clamp(rint(x / s), -127, 127) (fp32);
-                               attention runs on the exact codes and applies the scales in fp32 to
-                               the scores (K) and the probabilities (V).  Needs
-                               Hq / Hkv >= 2 (tensor-core path); pkv_append_decode_attention runs as
-                               two launches; pkv_prefill_attention and pkv_qkv_append_rope return
+                               attention runs on the exact codes (tensor cores, for any Hq / Hkv)
+                               and applies the scales in fp32 to the scores (K) and the
+                               probabilities (V).  pkv_append_decode_attention runs as two
+                               launches; pkv_prefill_attention and pkv_qkv_append_rope return
                                PKV_ERR_UNSUPPORTED. */
 #define PKV_OPT_EARLY_PAGES 0x2 /* with PKV_OPT_PDL, the one-launch step (pkv_append_decode_attention
                                    with one token per sequence) starts copying the layer's cached

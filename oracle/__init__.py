@@ -164,7 +164,8 @@ def append(geom: Geometry, q, k, v, pos_map, append_indptr, page_indptr, page_in
 
 
 def int8_block_bytes(head_dim: int) -> int:
-    """Bytes of one int8 block: the 16 slots' codes [16][d] and fp32 scales [16]."""
+    """Bytes of one int8 block: the 16 slots' codes (K blocks [16][d], V blocks [d][16]) and fp32
+    scales [16]."""
     return 16 * head_dim + 64
 
 

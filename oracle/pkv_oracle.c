@@ -218,7 +218,8 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
 /* int8 KV pages (Zero TVM Documentation, "The memory-bandwidth ceiling": int8 KV is exposed
  * behind a flag; the format is this library's reading).
  * Layout per layer: uint8 pool8[num_pages][2][Hkv][16 * d + 64]: a block holds the 16 slots'
- * int8 codes [16][d] and then their fp32 scales [16].
+ * int8 codes and then their fp32 scales [16]; the codes of a K block are slot-major [16][d], those
+ * of a V block dim-major [d][16] (the 16 slots of one dimension together).
  * Row quantizer (one row = one token, one KV head, K or V, of d fp16 values x_i; K after RoPE and
  * its fp16 rounding, as the fp16 cache stores it): amax = max |x_i|; s = fp32(amax / 127) (fp32
  * division, nearest); code_i = clamp(rint_even(fp32(x_i / s)), -127, 127); amax = 0 gives s = 0 and
@@ -226,6 +227,20 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
  * code * s. */
 static int64_t block8(const orc_geom* g, int64_t page, int kv, int head) {
   return ((page * 2 + kv) * g->num_kv_heads + head) * (int64_t)(16 * g->head_dim + 64);
+}
+
+/* Index of the code of (slot, dimension i) inside a K (kv = 0) or V (kv = 1) block. */
+static int64_t code8(int d, int kv, int slot, int i) { return kv == 0 ? (int64_t)slot * d + i : (int64_t)i * 16 + slot; }
+
+void orc_quantize_row(const uint16_t* x, int d, int8_t* codes, float* scale);
+
+/* Quantize one row into its block: codes at code8(), the scale after the 16 x d codes. */
+static void store_row8(uint8_t* blk, int d, int kv, int slot, const uint16_t* row) {
+  int8_t codes[256];
+  float sc;
+  orc_quantize_row(row, d, codes, &sc);
+  for (int i = 0; i < d; ++i) ((int8_t*)blk)[code8(d, kv, slot, i)] = codes[i];
+  memcpy(blk + 16 * d + 4 * slot, &sc, 4);
 }
 
 void orc_quantize_row(const uint16_t* x, int d, int8_t* codes, float* scale) {
@@ -265,14 +280,9 @@ int orc_append_int8(const orc_geom* g, const uint16_t* q, const uint16_t* k, con
         const int p = pos_map[t];
         const int64_t page = page_indices[page_indptr[s] + p / ORC_PAGE];
         const int slot = p % ORC_PAGE;
-        for (int h = 0; h < Hkv; ++h) {
-          for (int kv = 0; kv < 2; ++kv) {
-            uint8_t* blk = pool8 + block8(g, page, kv, h);
-            float sc;
-            orc_quantize_row(scratch + pool_row(g, page, kv, h, slot), d, (int8_t*)(blk + slot * d), &sc);
-            memcpy(blk + 16 * d + 4 * slot, &sc, 4);
-          }
-        }
+        for (int h = 0; h < Hkv; ++h)
+          for (int kv = 0; kv < 2; ++kv)
+            store_row8(pool8 + block8(g, page, kv, h), d, kv, slot, scratch + pool_row(g, page, kv, h, slot));
       }
     }
   }
@@ -287,14 +297,9 @@ void orc_quantize_pool(const orc_geom* g, const uint16_t* pool, uint8_t* pool8) 
 #pragma omp parallel for schedule(static)
   for (int64_t page = 0; page < g->num_pages; ++page)
     for (int kv = 0; kv < 2; ++kv)
-      for (int h = 0; h < Hkv; ++h) {
-        uint8_t* blk = pool8 + block8(g, page, kv, h);
-        for (int slot = 0; slot < ORC_PAGE; ++slot) {
-          float sc;
-          orc_quantize_row(pool + pool_row(g, page, kv, h, slot), d, (int8_t*)(blk + slot * d), &sc);
-          memcpy(blk + 16 * d + 4 * slot, &sc, 4);
-        }
-      }
+      for (int h = 0; h < Hkv; ++h)
+        for (int slot = 0; slot < ORC_PAGE; ++slot)
+          store_row8(pool8 + block8(g, page, kv, h), d, kv, slot, pool + pool_row(g, page, kv, h, slot));
 }
 
 /* Dequantize an int8 pool into fp64 rows laid out like the fp16 pool: out[page][kv][head][slot][d]. */
@@ -308,7 +313,7 @@ void orc_dequantize_pool(const orc_geom* g, const uint8_t* pool8, double* out) {
           float sc;
           memcpy(&sc, blk + 16 * d + 4 * slot, 4);
           for (int i = 0; i < d; ++i)
-            out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i] * (double)sc;
+            out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)] * (double)sc;
         }
       }
 }

@@ -157,8 +157,9 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) 
 
 // ------------------------------------------------------------------------------------------------
 // The append into an int8 cache (PKV_OPT_INT8_KV).  Layout per layer: uint8 blocks
-// [num_pages][2][Hkv][16 * d + 64], a block holding the 16 slots' int8 codes [16][d] and then their
-// fp32 scales [16].  Row quantizer: amax = max |x_i| of the row's fp16 values (K after RoPE and its
+// [num_pages][2][Hkv][16 * d + 64], a block holding the 16 slots' int8 codes and then their fp32
+// scales [16]; K codes are slot-major [16][d], V codes dim-major [d][16] (the layouts the decode's
+// tensor-core fragments read four codes at a time from).  Row quantizer: amax = max |x_i| of the row's fp16 values (K after RoPE and its
 // fp16 rounding, as the fp16 cache stores it; V as given), s = amax / 127 (fp32 division),
 // code_i = clamp(rint_even(x_i / s), -127, 127) (fp32 division), amax = 0 giving s = 0 and codes 0.
 // One warp per (token, row): Hq query rows (rotated to q_out, fp16), Hkv K rows, Hkv V rows.
@@ -262,8 +263,13 @@ __global__ void __launch_bounds__(kQ8Warps * 32) append_rope_q8_kernel(AppendPar
   for (int u = 0; u < kPairs; ++u) {
     const int j = lane + 32 * u;
     if (j < D / 2) {
-      blk[slot * D + j] = (unsigned char)code(lo_v[u]);
-      blk[slot * D + j + D / 2] = (unsigned char)code(hi_v[u]);
+      if (is_k) {
+        blk[slot * D + j] = (unsigned char)code(lo_v[u]);
+        blk[slot * D + j + D / 2] = (unsigned char)code(hi_v[u]);
+      } else {
+        blk[j * 16 + slot] = (unsigned char)code(lo_v[u]);
+        blk[(j + D / 2) * 16 + slot] = (unsigned char)code(hi_v[u]);
+      }
     }
   }
   if (lane == 0) *reinterpret_cast<float*>(blk + 16 * D + 4 * slot) = s;

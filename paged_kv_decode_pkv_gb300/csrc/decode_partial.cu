@@ -77,9 +77,11 @@ constexpr int kSmemBudget = 232448 - 256;
 constexpr int kSmemPerSm = 233472;
 constexpr int kCtasPerSm = 2;
 
-// Alignment of the shared-memory base: 1024 bytes for the swizzled boxes of the tensor-core path,
-// 128 bytes for the plain boxes of the CUDA-core path.
-__host__ __device__ constexpr int smem_align(int group) { return group >= 2 ? 1024 : 128; }
+// Alignment of the shared-memory base: 1024 bytes on the tensor-core path (its swizzled boxes; the
+// int8 cache always takes that path), 128 bytes on the CUDA-core path.  The kernel aligns its base
+// by the same rule and the layout reserves that much slack.
+__host__ __device__ constexpr bool uses_mma(int group, bool q8) { return group >= 2 || q8; }
+__host__ __device__ constexpr int smem_align(bool mma) { return mma ? 1024 : 128; }
 
 struct Layout {
   int stage_bytes, ring_off, qslot_bytes, q_off, patch_off, bar_off, meta_off, pid_off, defer_off, prefix_off,
@@ -99,10 +101,9 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
                                               bool fused, bool windowed = false, bool q8 = false) {
   Layout L;
   const int n = warps * nstage;
-  // K and V of one page for one KV head (int8 cache: the two int8 blocks as stored, expanded per
-  // page into the warp's fp16 tile, which then comes first)
+  // K and V of one page for one KV head (int8 cache: the two int8 blocks as stored)
   L.stage_bytes = q8 ? 2 * int8_block_bytes(head_dim) : 64 * head_dim;
-  L.ring_off = q8 ? warps * 64 * head_dim : 0;
+  L.ring_off = 0;
   L.qslot_bytes = (group * head_dim * 2 + (fused ? 8 * head_dim : 0) + 15) & ~15;
   L.q_off = L.ring_off + n * L.stage_bytes;
   L.patch_off = L.q_off + warps * kItemSlots * L.qslot_bytes;
@@ -115,7 +116,7 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
   L.indptr_off = L.prefix_off + (batch + 1) * 4;
   L.aptr_off = L.indptr_off + (batch + 1) * 4;
   L.wstart_off = L.aptr_off + (fused ? (batch + 1) * 4 : 0);
-  L.total = L.wstart_off + (windowed ? batch * 4 : 0) + smem_align(group);  // + slack to align the base
+  L.total = L.wstart_off + (windowed ? batch * 4 : 0) + smem_align(uses_mma(group, q8));  // + slack to align the base
   return L;
 }
 
@@ -498,10 +499,7 @@ struct GroupMma {
     vref = 0.f;
   }
 
-  // ks, vs (int8 cache): the 16 slots' K and V scales; the staged tile then holds the exact codes,
-  // K scales multiply the scores, V scales the probabilities (relative to vref, raised lazily).
-  __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2, const float* ks = nullptr,
-                       const float* vs = nullptr) {
+  __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2) {
     const uint32_t stage = smem_u32(stage_ptr);
     if (nvalid < kPageSize) {
       // Slots past the sequence end may hold anything (even NaN): zero their V rows so that
@@ -532,12 +530,6 @@ struct GroupMma {
     }
     const int c = 2 * (lane & 3);
     float s[4] = {sc[0][0] * scale_log2, sc[0][1] * scale_log2, sc[1][0] * scale_log2, sc[1][1] * scale_log2};
-    if (ks != nullptr) {
-      s[0] = sc[0][0] * ks[c] * scale_log2;
-      s[1] = sc[0][1] * ks[c + 1] * scale_log2;
-      s[2] = sc[1][0] * ks[c + 8] * scale_log2;
-      s[3] = sc[1][1] * ks[c + 9] * scale_log2;
-    }
     s[0] = (c >= lo && c < nvalid) ? s[0] : -INFINITY;
     s[1] = (c + 1 >= lo && c + 1 < nvalid) ? s[1] : -INFINITY;
     s[2] = (c + 8 >= lo && c + 8 < nvalid) ? s[2] : -INFINITY;
@@ -563,32 +555,8 @@ struct GroupMma {
     const __half2 p23 = __floats2half2_rn(e2, e3);
     const float2 f01 = __half22float2(p01), f23 = __half22float2(p23);
     l += (f01.x + f01.y) + (f23.x + f23.y);
-    uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
-    uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
-    if (vs != nullptr) {
-      // P times each slot's V scale over vref (raised, with a rescale of acc, only when a scale
-      // exceeds it by 2^7, so P * scale / vref stays below 2^15, inside fp16)
-      const float v0 = (c >= lo && c < nvalid) ? vs[c] : 0.f, v1 = (c + 1 >= lo && c + 1 < nvalid) ? vs[c + 1] : 0.f;
-      const float v2 = (c + 8 >= lo && c + 8 < nvalid) ? vs[c + 8] : 0.f;
-      const float v3 = (c + 9 >= lo && c + 9 < nvalid) ? vs[c + 9] : 0.f;
-      float vm = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
-      vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 1));
-      vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 2));
-      if (vm > vref * 128.f) {
-        const float alpha = vref / vm;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          acc[nb][0] *= alpha;
-          acc[nb][1] *= alpha;
-        }
-        vref = vm;
-      }
-      const float inv = vref > 0.f ? 1.f / vref : 0.f;
-      const __half2 q01 = __floats2half2_rn(e0 * (v0 * inv), e1 * (v1 * inv));
-      const __half2 q23 = __floats2half2_rn(e2 * (v2 * inv), e3 * (v3 * inv));
-      pa0 = *reinterpret_cast<const uint32_t*>(&q01);
-      pa2 = *reinterpret_cast<const uint32_t*>(&q23);
-    }
+    const uint32_t pa0 = *reinterpret_cast<const uint32_t*>(&p01);
+    const uint32_t pa2 = *reinterpret_cast<const uint32_t*>(&p23);
     {
       const int mi = lane >> 3, r = lane & 7;
       const int t = (mi & 1) * 8 + r;
@@ -600,6 +568,139 @@ struct GroupMma {
         mma_16816(acc[2 * mm], pa0, 0u, pa2, 0u, v0, v1);
         mma_16816(acc[2 * mm + 1], pa0, 0u, pa2, 0u, v2, v3);
       }
+    }
+  }
+
+  // ---- int8 cache: the page computed from its codes, with no fp16 copy ----
+  // The dot products run over the head dimensions in a permuted order (the sums are the same): at
+  // k-step ks, lane (g, c) takes dimensions D/4 * c + 4 ks + {0, 1, 2, 3} for q and for the K codes,
+  // contiguous across the k-steps, so a lane reads its D/4 codes of a key row at once.  The 16
+  // slots are permuted too: the S columns of lane c are slots 4c .. 4c + 3, which is also the order
+  // of the P V contraction, so the V fragment of a dimension is four consecutive codes of the
+  // dim-major V block.  Codes become exact fp16 values ((code ^ 0x80) + 1024 - 1152).
+  __device__ static void codes_to_half(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x5342);
+    const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&x);
+    hi = *reinterpret_cast<const uint32_t*>(&y);
+  }
+
+  __device__ void begin8(const unsigned char* qslot) {
+    const int c = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (h < group) {
+        const uint2 w = *reinterpret_cast<const uint2*>(qslot + (h * D + (D / 4) * c + 4 * ks) * 2);
+        qa[ks][0] = w.x;
+        qa[ks][1] = w.y;
+      } else {
+        qa[ks][0] = 0u;
+        qa[ks][1] = 0u;
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+    vref = 0.f;
+  }
+
+  // stage: the page's K block (codes [16][D] slot-major, then 16 fp32 scales) and V block (codes
+  // [D][16] dim-major, then 16 fp32 scales) as stored.  K scales multiply the scores, V scales the
+  // probabilities (relative to vref, raised lazily), in fp32.  Codes of slots past the sequence end
+  // are finite and meet P = 0; their scales are masked.
+  __device__ void page8(const unsigned char* stage, int lo, int nvalid, float scale_log2) {
+    constexpr int kBlk = int8_block_bytes(D);
+    const unsigned char* kb = stage;
+    const unsigned char* vb = stage + kBlk;
+    const float* ksc = reinterpret_cast<const float*>(kb + 16 * D);
+    const float* vsc = reinterpret_cast<const float*>(vb + 16 * D);
+    const int g = lane >> 2, c = lane & 3;
+    // even and odd k-steps accumulate apart: four independent MMA chains instead of two
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      const int slot = 4 * (g >> 1) + (g & 1) + 2 * nb;  // the key row of S column g of this n-block
+      const unsigned char* row = kb + slot * D + (D / 4) * c;
+      uint32_t w[KS];
+      if constexpr (D == 96) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          const uint2 v = *reinterpret_cast<const uint2*>(row + 8 * i);
+          w[2 * i] = v.x;
+          w[2 * i + 1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < KS / 4; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * i);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t b0, b1;
+        codes_to_half(w[ks], b0, b1);
+        mma_16816((ks & 1) ? so[nb] : sc[nb], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nb][e] += so[nb][e];
+    }
+    const int s0 = 4 * c;  // this lane's slots s0 .. s0 + 3
+    float s[4] = {sc[0][0] * ksc[s0] * scale_log2, sc[0][1] * ksc[s0 + 1] * scale_log2,
+                  sc[1][0] * ksc[s0 + 2] * scale_log2, sc[1][1] * ksc[s0 + 3] * scale_log2};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = (s0 + i >= lo && s0 + i < nvalid) ? s[i] : -INFINITY;
+    float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    if (mx > m + kLazyRescale) {
+      const float alpha = exp2f(m - mx);
+      l *= alpha;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        acc[nb][0] *= alpha;
+        acc[nb][1] *= alpha;
+      }
+      m = mx;
+    }
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = exp2f(s[i] - m);
+    const float2 f01 = __half22float2(__floats2half2_rn(e[0], e[1]));
+    const float2 f23 = __half22float2(__floats2half2_rn(e[2], e[3]));
+    l += (f01.x + f01.y) + (f23.x + f23.y);
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (s0 + i >= lo && s0 + i < nvalid) ? vsc[s0 + i] : 0.f;
+    float vm = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 1));
+    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 2));
+    if (vm > vref * 128.f) {
+      const float alpha = vref / vm;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        acc[nb][0] *= alpha;
+        acc[nb][1] *= alpha;
+      }
+      vref = vm;
+    }
+    const float inv = vref > 0.f ? 1.f / vref : 0.f;
+    const uint32_t pa0 = pack_half2(e[0] * (v[0] * inv), e[1] * (v[1] * inv));
+    const uint32_t pa2 = pack_half2(e[2] * (v[2] * inv), e[3] * (v[3] * inv));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(vb + (8 * nb + g) * 16 + 4 * c);
+      uint32_t b0, b1;
+      codes_to_half(w, b0, b1);
+      mma_16816(acc[nb], pa0, 0u, pa2, 0u, b0, b1);
     }
   }
 
@@ -815,37 +916,6 @@ __device__ __forceinline__ void apply_patch(unsigned char* stage, const unsigned
   __syncwarp();
 }
 
-// int8 cache: expand a staged page's codes (the K and V blocks as stored: codes [16][d], then fp32
-// scales [16]) into the fp16 tile layout the tensor-core path reads; the codes are exact in fp16
-// ((code ^ 0x80) + 1024 - 1152) and the scales are applied to the scores and probabilities.
-template <int D>
-__device__ __forceinline__ void expand_q8(const unsigned char* landing, unsigned char* tile, int lane) {
-  constexpr int kBlk = int8_block_bytes(D);
-  constexpr int kChunks = D / 8;  // 16-byte fp16 chunks of a row
-  const uint32_t tb = smem_u32(tile);
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-  for (int c = lane; c < 2 * kPageSize * kChunks; c += 32) {
-    const int kv = c / (kPageSize * kChunks);
-    const int rem = c - kv * kPageSize * kChunks;
-    const int t = rem / kChunks, cc = rem - t * kChunks;
-    const unsigned char* blk = landing + kv * kBlk;
-    const uint2 w = *reinterpret_cast<const uint2*>(blk + t * D + 8 * cc);
-    const uint32_t u0 = w.x ^ 0x80808080u, u1 = w.y ^ 0x80808080u;
-    const uint32_t b[4] = {__byte_perm(u0, 0x64646464u, 0x5140), __byte_perm(u0, 0x64646464u, 0x5342),
-                           __byte_perm(u1, 0x64646464u, 0x5140), __byte_perm(u1, 0x64646464u, 0x5342)};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&b[j]), bias);  // exact codes
-      o[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    const uint32_t a = GroupMma<D>::chunk_addr(tb, kv, t, 8 * cc);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                 : "memory");
-  }
-  __syncwarp();
-}
-
 // Validate an item whose loads have been issued; an invalid or empty sequence becomes one empty
 // item per KV head (its chunks are reported as -inf).
 __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, int lane) {
@@ -873,7 +943,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   extern __shared__ unsigned char smem_raw[];
   // aligned (smem_align) by an offset from the shared array itself, so that every access below is
   // compiled as a shared-memory access
-  constexpr uint32_t kAlign = smem_align(MMA ? 2 : 1);
+  constexpr uint32_t kAlign = smem_align(MMA);
   unsigned char* base = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
   const Layout L = make_layout(p.warps, p.nstage, D, p.group, p.batch, FUSED, p.window > 0, Q8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bar_off);
@@ -965,7 +1035,6 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   int* meta_pid = reinterpret_cast<int*>(base + L.pid_off) + warp * p.nstage;
   constexpr int kBlk = int8_block_bytes(D);
   const uint32_t page_bytes = Q8 ? (uint32_t)(2 * kBlk) : (uint32_t)(64 * D);
-  unsigned char* tile = base + (size_t)warp * 64 * D;  // int8 cache: the page expanded to fp16
   const uint64_t policy = l2_policy_evict_first();
 
   // Producer state: the item being issued (cur) and the next one, whose loads are in flight.
@@ -1325,6 +1394,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
             cmp.store_query(p.q_out + ((long long)qrow * p.hq + (long long)mt.g() * p.group) * D);
           }
           if (mt.flags & kMetaNew) make_patch<D>(qs + q_bytes, qs + q_bytes + cs_bytes, patch, lane);
+        } else if constexpr (Q8) {
+          cmp.begin8(qs);
         } else if constexpr (MMA) {
           cmp.begin(qs);
         } else {
@@ -1366,12 +1437,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
             apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
         if constexpr (Q8) {
-          if (nvalid > 0) {
-            expand_q8<D>(s1, tile, lane);
-            const float* ksc = reinterpret_cast<const float*>(s1 + 16 * D);
-            const float* vsc = reinterpret_cast<const float*>(s1 + kBlk + 16 * D);
-            cmp.page(tile, mt.lo(), nvalid, p.scale_log2, ksc, vsc);
-          }
+          if (nvalid > 0) cmp.page8(s1, mt.lo(), nvalid, p.scale_log2);
         } else {
           if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
         }
@@ -1430,7 +1496,7 @@ int cta_budget(int ctas) { return std::min(kSmemBudget, (kSmemPerSm - ctas * 102
 DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool windowed, bool q8) {
   DecodeConfig c;
   c.q8 = q8;
-  c.mma = group >= 2;
+  c.mma = uses_mma(group, q8);  // the int8 page computation is the tensor-core one (rows padded to 16)
   c.fused = fused;
   // Warps per SM: the most stages in flight per SM (warps x ring depth) that fit the plain layout
   // in one CTA, on a tie the deeper ring (the CUDA-core path always runs 8 warps, the tensor-core
@@ -1445,6 +1511,9 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
       sm_warps = w;
     }
   }
+  // The int8 cache's stages are half as large and its page computation is latency-bound: it runs
+  // the most warps the registers allow (8 per SM).
+  if (q8) sm_warps = kMaxDecodeWarps;
   c.warps = sm_warps;
   c.ctas_per_sm = 1;
   c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget, q8);

@@ -258,8 +258,6 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   for (int l = 0; l < d->num_layers; ++l)
     if (d->layer_pools[l] == nullptr || !aligned(d->layer_pools[l], 256)) return PKV_ERR_INVALID_ARG;
   if (d->options & ~(PKV_OPT_PDL | PKV_OPT_EARLY_PAGES | PKV_OPT_INT8_KV)) return PKV_ERR_INVALID_ARG;
-  if ((d->options & PKV_OPT_INT8_KV) && d->num_qo_heads / d->num_kv_heads < 2)
-    return fail(PKV_ERR_UNSUPPORTED, "int8 KV cache: the tensor-core path (Hq / Hkv >= 2) only");
   for (int l = 0; l < d->num_layers; ++l) {
     if (d->layer_window != nullptr && d->layer_window[l] < 0) return PKV_ERR_INVALID_ARG;
     if (d->layer_sinks != nullptr && d->layer_sinks[l] != nullptr && !aligned(d->layer_sinks[l], 4))

@@ -7,7 +7,8 @@
   sequences is compared with the oracle's causal attention over the GPU's own cache and rotated
   queries.
 * The int8 KV cache on the long-context GQA workload (8 x 32 768 tokens; two of its 28 layers,
-  the per-layer work is the same for every layer) and on the mixed-serving workload at full size,
+  the per-layer work is the same for every layer), on the ragged Phi-3 batch (one query head per
+  KV head) and on the mixed-serving workload at full size,
   run through the one-launch entry point as `bench.py --int8` runs it, compared on sampled
   sequences with the oracle's int8 attention over the GPU's own int8 pool.
 
@@ -131,6 +132,11 @@ def _int8_full_size(cid, layers_of_workload, seqs_fn):
 
 def test_full_size_int8_gqa_long_context():
     _int8_full_size(4, [0, 27], lambda st: [0, 7])
+
+
+def test_full_size_int8_ragged_batch64():
+    """One query head per KV head (the Phi-3 ragged batch)."""
+    _int8_full_size(3, [0], lambda st: [0, int(np.argmax(st.seq_len)), int(np.argmin(st.seq_len)), 63])
 
 
 def test_full_size_int8_mixed_serving():

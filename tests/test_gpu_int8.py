@@ -13,7 +13,9 @@ from tests.test_gpu_parity import SMALL
 
 pytestmark = pytest.mark.gpu
 
-CASES = ["gqa2_d128_outliers", "gqa4_mixed_chunks", "gqa2_d96", "gqa4_d64", "gqa8_d128"]
+# group sizes 1 (one query head per KV head), 2, 4 and 8; head dims 64, 96 and 128
+CASES = ["gqa2_d128_outliers", "gqa4_mixed_chunks", "gqa2_d96", "gqa4_d64", "gqa8_d128", "tiny", "ragged_d96",
+         "phi3_b1_ctx300"]
 
 
 def _bits(t):

@@ -37,8 +37,11 @@ MUTANTS = [
     ("prefill not causal", "window_start(p + 1, window), p + 1, page_indptr,", "window_start(p + 1, window), p + 2, page_indptr,"),
     ("int8 rounding truncates", "float q = nearbyintf((float)dec(x[i]) / s);", "float q = truncf((float)dec(x[i]) / s);"),
     ("int8 scale divisor", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
-    ("int8 scale offset", "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i] * (double)sc;",
-     "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[slot * d + i];"),
+    ("int8 scale offset", "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)] * (double)sc;",
+     "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)];"),
+    ("int8 V block read slot-major",
+     "static int64_t code8(int d, int kv, int slot, int i) { return kv == 0 ? (int64_t)slot * d + i : (int64_t)i * 16 + slot; }",
+     "static int64_t code8(int d, int kv, int slot, int i) { return (int64_t)slot * d + i; }"),
     ("last page length ignored", "*len = (n - 1) * ORC_PAGE + last;", "*len = n * ORC_PAGE;"),
     ("slot index", "const int64_t krow = pool_row(g, page, 0, kv_head, t % ORC_PAGE);",
      "const int64_t krow = pool_row(g, page, 0, kv_head, (t + 1) % ORC_PAGE);"),
