@@ -402,11 +402,38 @@ def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, o
     peak, _ = measured_peaks()
     per_layer_us = proj_ms * 1e3 / cfg.layers
     gbs = wbytes * cfg.layers / (proj_ms * 1e-3) / 1e9
+    # the projection alone (pkv_qkv_project) for several token counts over every layer's weights: one
+    # token on CUDA cores, several on tensor cores (mma.sync)
+    sweep = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(step.seed)
+    for T in (1, 8, 16, 32):
+        xs = [(torch.randn((T, hidden), generator=gen, device=dev) * 0.5).to(torch.float16) for _ in layers]
+        ys = [torch.empty((T, n_rows), dtype=torch.float16, device=dev) for _ in layers]
+
+        def proj_only():
+            for l in layers:
+                cache.qkv_project(xs[l], ws[l][1], ws[l][2], y=ys[l])
+
+        with torch.cuda.stream(stream):
+            proj_only()
+        torch.cuda.synchronize()
+        g3 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g3, stream=stream):
+            proj_only()
+        torch.cuda.synchronize()
+        ms_t = time_graph(g3)
+        tb = n_rows * hidden // 2 + n_rows * (hidden // 32) * 2 + T * hidden * 2
+        sweep[str(T)] = {"us_per_layer": ms_t * 1e3 / cfg.layers,
+                         "gbs": tb * cfg.layers / (ms_t * 1e-3) / 1e9,
+                         "tflops": 2.0 * T * n_rows * hidden * cfg.layers / (ms_t * 1e-3) / 1e12}
     return {"value": gbs, "unit": "GB/s", "bytes_per_layer": wbytes, "us_per_layer": per_layer_us,
             "roofline_frac": gbs / peak, "hidden": hidden, "rows": n_rows,
             "step": "per layer: pkv_qkv_append_rope (Q4F16_1 projection + RoPE + append, one launch)",
             "with_decode_us_per_layer": both_ms * 1e3 / cfg.layers,
-            "with_decode": "per layer: pkv_qkv_append_rope + pkv_decode_attention_merged"}
+            "with_decode": "per layer: pkv_qkv_append_rope + pkv_decode_attention_merged",
+            "project_tokens": sweep,
+            "project_tokens_step": "per layer: pkv_qkv_project of T tokens (one token: CUDA cores; several: mma.sync)"}
 
 
 def kv_bytes_layer(step: W.Step, int8: bool) -> int:

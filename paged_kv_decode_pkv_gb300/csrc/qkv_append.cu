@@ -19,6 +19,8 @@
 // rows to q_out, k and v rows into the pool.  Tokens are processed two at a time (one: a kernel
 // specialised for a single token).  The token slots are looked up before the programmatic
 // dependent launch wait (page tables and positions are not produced by the preceding kernel).
+#include <algorithm>
+
 #include "pkv_internal.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -75,6 +77,205 @@ __device__ __forceinline__ float reduce8(const float (&acc)[8][kTok], int t, int
   float v1 = (b2 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? v2[0] : v2[1], 4);
   v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
   return v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Several tokens: the projection on tensor cores (mma.sync m16n8k16, fp16 weights and inputs, fp32
+// accumulation).  A CTA owns the same 16 rows (M: row g = element 8b + g of the head, row g + 8 its
+// RoPE partner D/2 + 8b + g) and takes the tokens 8, 16 or 32 at a time (one to four n-tiles of N =
+// 8).  Its weight rows are copied once into shared memory (rows padded by 16 bytes) before the launch
+// wait.  The inputs are split over the warps in blocks of 64 (8 words of a row); within a block the
+// sum runs over the inputs in a permuted order that leaves it unchanged: at k-step s, lane (g, c)
+// takes word 2c + s/2 of the block and its nibble pairs {2(s%2), +4} and {2(s%2) + 1, +4}, which one
+// mask-and-or per pair dequantizes, for rows g and g + 8 (the A fragment), and the same input pairs
+// of token g, read from the 16 bytes of that word's inputs (the B fragment).  Each weight is
+// dequantized once per pass, the format's fp16 product as in the CUDA-core kernel.  The warps'
+// fragments are summed in a fixed order, rounded to fp16, rotated and written like the CUDA-core
+// kernel's.
+constexpr int kMmaWarps = 8;
+
+template <int NT>
+struct QkvMmaSmem {
+  // bytes of the shared layout for `hidden` inputs: barrier, weight rows, scales, warp fragments
+  static size_t bytes(int hidden) {
+    const size_t w = (size_t)16 * (hidden / 2 + 16);
+    const size_t sc = ((size_t)16 * (hidden / 32) * 2 + 15) & ~(size_t)15;
+    const size_t red = (size_t)kMmaWarps * NT * 16 * 8 * 4;
+    return 16 + w + sc + red;
+  }
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kMmaWarps * 32) qkv_mma_kernel(QkvParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int words = p.hidden / 8, groups = p.hidden / 32;
+  const int wstride = p.hidden / 2 + 16;  // bytes per staged weight row
+  const int tok_cap = min(8 * NT, p.num_tokens);
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);
+  unsigned char* ws = smem + 16;
+  __half* scs = reinterpret_cast<__half*>(ws + 16 * wstride);
+  float* red = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(scs) + ((16 * groups * 2 + 15) & ~15));
+  // [warp][NT][16][8]
+  __shared__ QkvSlot slots[8 * NT];
+  __shared__ float2 cs[8 * NT][8];
+  pdl_launch_dependents();
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int blocks_per_head = D / 16;
+  const int hh = blockIdx.x / blocks_per_head;
+  const int b = blockIdx.x - hh * blocks_per_head;
+  const int N = (p.hq + 2 * p.hkv) * D;
+  auto row_of = [&](int r) -> long long { return (long long)hh * D + (r < 8 ? 8 * b + r : D / 2 + 8 * b + r - 8); };
+
+  // the CTA's 16 weight rows and their scales: inputs of the weights, copied before the wait
+  if (tid == 0) {
+    mbar_init(wbar, 1);
+    fence_mbarrier_init();
+    mbar_arrive_expect_tx(wbar, (uint32_t)(16 * (p.hidden / 2)));
+  }
+  __syncthreads();
+  if (tid < 16)
+    bulk_load(ws + tid * wstride, reinterpret_cast<const unsigned char*>(p.w) + row_of(tid) * (p.hidden / 2),
+              (uint32_t)(p.hidden / 2), wbar);
+  for (int i = tid; i < 16 * groups; i += blockDim.x) {
+    const int r = i / groups, k = i - r * groups;
+    scs[i] = p.scales[row_of(r) * groups + k];
+  }
+  auto lookup_slot = [&](int t, int i) {
+    QkvSlot ts{-1, 0};
+    if (t < p.num_tokens && p.pool != nullptr) {
+      int lo = 0, hi = p.batch;
+      if (p.append_indptr[0] <= t && t < p.append_indptr[p.batch]) {
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.append_indptr[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int pos = p.pos_map[t];
+        const int first = p.page_indptr[lo];
+        const int n_pages = p.page_indptr[lo + 1] - first;
+        if (pos < 0 || pos >= p.max_position || (pos >> 4) >= n_pages) {
+          atomicOr(p.status, kFlagBadPosition);
+        } else {
+          const int page = p.page_indices[first + (pos >> 4)];
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.status, kFlagBadPage);
+          } else {
+            ts.k_off = ((long long)page * 2 * p.hkv * kPageSize + (pos & 15)) * D;
+            ts.pos = pos;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cs[i][e] = p.rope[(long long)pos * (D / 2) + 8 * b + e];
+          }
+        }
+      } else {
+        atomicOr(p.status, kFlagBadSequence);
+      }
+    }
+    slots[i] = ts;
+  };
+  if (tid < tok_cap) lookup_slot(tid, tid);  // the first tokens, before the wait
+  pdl_wait();  // the input rows and the pool may come from the preceding kernel
+  const bool weights_ok = mbar_wait_bounded(wbar, 0, kWaitLimitNs);
+  if (!weights_ok) {
+    if (tid == 0) atomicOr(p.status, kFlagTimeout);
+    mbar_wait_bounded(wbar, 0, kDrainLimitNs);  // the copies may still land: wait (bounded) before leaving
+    return;
+  }
+
+  const int nblk = p.hidden / 64;          // whole blocks of 64 inputs
+  const bool tail = (p.hidden & 63) != 0;  // a last half block of 32 inputs
+  for (int t0 = 0; t0 < p.num_tokens; t0 += 8 * NT) {
+    const int nt = min(8 * NT, p.num_tokens - t0);
+    if (t0 > 0 && tid < nt) lookup_slot(t0 + tid, tid);
+    __syncthreads();
+
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    // A of one k-step: the word's nibble pairs {j0, +4} and {j0 + 1, +4} of rows g and g + 8
+    auto afrag = [&](int wglob, int j0, uint32_t (&a)[4]) {
+      const uint32_t wg = *reinterpret_cast<const uint32_t*>(ws + g * wstride + 4 * wglob);
+      const uint32_t wg8 = *reinterpret_cast<const uint32_t*>(ws + (g + 8) * wstride + 4 * wglob);
+      const int grp = wglob >> 2;
+      const uint32_t s0 = __half_as_ushort(scs[g * groups + grp]), s1 = __half_as_ushort(scs[(g + 8) * groups + grp]);
+      const uint32_t sh[4] = {wg >> (4 * j0), wg8 >> (4 * j0), wg >> (4 * j0 + 4), wg8 >> (4 * j0 + 4)};
+      const uint32_t sc2[4] = {s0 | (s0 << 16), s1 | (s1 << 16), s0 | (s0 << 16), s1 | (s1 << 16)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b32 t;\n\t"
+            "lop3.b32 t, %1, 0x000F000F, 0x64006400, 0xEA;\n\tsub.rn.f16x2 t, t, %3;\n\tmul.rn.f16x2 %0, t, %2;\n\t}"
+            : "=r"(a[i]) : "r"(sh[i]), "r"(sc2[i]), "r"(0x64076407u));
+    };
+    // one word of the block: its two k-steps (pairs {0, 1}, then {2, 3}) for every n-tile; B is the
+    // word's eight inputs of token 8n + g, rearranged into the pairs {x_j, x_j+4}
+    auto word_steps = [&](int wglob, int nsteps) {
+      uint4 xv[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int t = 8 * n + g;
+        xv[n] = t < nt ? *reinterpret_cast<const uint4*>(p.x + (long long)(t0 + t) * p.hidden + 8 * wglob)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (s2 >= nsteps) break;
+        uint32_t a[4];
+        afrag(wglob, 2 * s2, a);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const uint32_t lo = s2 == 0 ? xv[n].x : xv[n].y, hi = s2 == 0 ? xv[n].z : xv[n].w;
+          mma_16816(acc[n], a[0], a[1], a[2], a[3], __byte_perm(lo, hi, 0x5410), __byte_perm(lo, hi, 0x7632));
+        }
+      }
+    };
+    for (int blk = warp; blk < nblk; blk += kMmaWarps) {
+      word_steps(8 * blk + 2 * c, 2);
+      word_steps(8 * blk + 2 * c + 1, 2);
+    }
+    if (tail && warp == nblk % kMmaWarps) word_steps(8 * nblk + c, 2);  // the last 32 inputs: word c
+    // the warps' fragments, then their sum in a fixed order
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      float* rw = red + ((size_t)(warp * NT + n) * 16) * 8;
+      rw[g * 8 + 2 * c] = acc[n][0];
+      rw[g * 8 + 2 * c + 1] = acc[n][1];
+      rw[(g + 8) * 8 + 2 * c] = acc[n][2];
+      rw[(g + 8) * 8 + 2 * c + 1] = acc[n][3];
+    }
+    __syncthreads();
+    for (int i = tid; i < nt * 8; i += blockDim.x) {
+      const int t = i >> 3, r = i & 7;
+      const int n = t >> 3, tc = t & 7;
+      float ylo = 0.f, yhi = 0.f;
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float* rw = red + ((size_t)(w * NT + n) * 16) * 8;
+        ylo += rw[r * 8 + tc];
+        yhi += rw[(r + 8) * 8 + tc];
+      }
+      const __half hlo = __float2half_rn(ylo), hhi = __float2half_rn(yhi);
+      const int e = 8 * b + r;
+      const long long tok = t0 + t;
+      if (p.y_out != nullptr) {
+        p.y_out[tok * N + hh * D + e] = hlo;
+        p.y_out[tok * N + hh * D + D / 2 + e] = hhi;
+        continue;
+      }
+      const QkvSlot ts = slots[t];
+      if (ts.k_off < 0) continue;
+      __half olo = hlo, ohi = hhi;
+      if (hh < p.hq + p.hkv) {
+        float ra, rb;
+        rope_pair(__half2float(hlo), __half2float(hhi), cs[t][r], ra, rb);
+        olo = __float2half_rn(ra);
+        ohi = __float2half_rn(rb);
+      }
+      __half* dst = hh < p.hq ? p.q_out + (tok * p.hq + hh) * D
+                              : p.pool + ts.k_off + (long long)(hh - p.hq) * kPageSize * D;  // K or V block
+      dst[e] = olo;
+      dst[D / 2 + e] = ohi;
+    }
+    __syncthreads();
+  }
 }
 
 template <int D, int kTok>
@@ -257,10 +458,21 @@ __global__ void __launch_bounds__(256, kTok == 1 ? 3 : 2) qkv_append_kernel(QkvP
 
 cudaError_t qkv_prepare() {
   const void* k[] = {(const void*)&qkv_append_kernel<64, 1>, (const void*)&qkv_append_kernel<96, 1>,
-                     (const void*)&qkv_append_kernel<128, 1>, (const void*)&qkv_append_kernel<64, kTokMax>,
-                     (const void*)&qkv_append_kernel<96, kTokMax>, (const void*)&qkv_append_kernel<128, kTokMax>};
+                     (const void*)&qkv_append_kernel<128, 1>};
   for (const void* f : k) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvMaxSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  const void* km[] = {(const void*)&qkv_mma_kernel<64, 1>, (const void*)&qkv_mma_kernel<96, 1>,
+                      (const void*)&qkv_mma_kernel<128, 1>, (const void*)&qkv_mma_kernel<64, 2>,
+                      (const void*)&qkv_mma_kernel<96, 2>, (const void*)&qkv_mma_kernel<128, 2>,
+                      (const void*)&qkv_mma_kernel<64, 4>, (const void*)&qkv_mma_kernel<96, 4>,
+                      (const void*)&qkv_mma_kernel<128, 4>};
+  for (const void* f : km) {
+    // at most QkvMmaSmem<4>::bytes(4096) (~53 KB); the kernel's static shared memory comes on top
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
@@ -274,25 +486,39 @@ size_t qkv_smem_bytes(int hidden, int parts, int tok) {
 
 cudaError_t launch_qkv(const QkvParams& p, cudaStream_t stream, bool pdl) {
   if (p.num_tokens <= 0) return cudaSuccess;
-  const int parts = (p.hidden + kPartIn - 1) / kPartIn;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.hq + 2 * p.hkv) * (p.head_dim / 16)));
-  cfg.blockDim = dim3(64 * parts);
-  const bool one = p.num_tokens == 1;
-  cfg.dynamicSmemBytes = qkv_smem_bytes(p.hidden, parts, one ? 1 : kTokMax);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (p.num_tokens == 1) {
+    // one token: the CUDA-core kernel (every weight is used once; nothing to share across tokens)
+    const int parts = (p.hidden + kPartIn - 1) / kPartIn;
+    cfg.blockDim = dim3(64 * parts);
+    cfg.dynamicSmemBytes = qkv_smem_bytes(p.hidden, parts, 1);
+    switch (p.head_dim) {
+      case 64: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<64, 1>, p);
+      case 96: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<96, 1>, p);
+      case 128: return cudaLaunchKernelEx(&cfg, qkv_append_kernel<128, 1>, p);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  // several tokens: tensor cores, 8, 16 or 32 tokens per pass
+  cfg.blockDim = dim3(kMmaWarps * 32);
+  const int nt = p.num_tokens <= 8 ? 1 : p.num_tokens <= 16 ? 2 : 4;
+  cfg.dynamicSmemBytes = nt == 1 ? QkvMmaSmem<1>::bytes(p.hidden) : nt == 2 ? QkvMmaSmem<2>::bytes(p.hidden)
+                                                                            : QkvMmaSmem<4>::bytes(p.hidden);
+  auto pick = [&](auto k1, auto k2, auto k4) {
+    return nt == 1 ? cudaLaunchKernelEx(&cfg, k1, p) : nt == 2 ? cudaLaunchKernelEx(&cfg, k2, p)
+                                                               : cudaLaunchKernelEx(&cfg, k4, p);
+  };
   switch (p.head_dim) {
-    case 64: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<64, 1>, p)
-                        : cudaLaunchKernelEx(&cfg, qkv_append_kernel<64, kTokMax>, p);
-    case 96: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<96, 1>, p)
-                        : cudaLaunchKernelEx(&cfg, qkv_append_kernel<96, kTokMax>, p);
-    case 128: return one ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<128, 1>, p)
-                         : cudaLaunchKernelEx(&cfg, qkv_append_kernel<128, kTokMax>, p);
+    case 64: return pick(qkv_mma_kernel<64, 1>, qkv_mma_kernel<64, 2>, qkv_mma_kernel<64, 4>);
+    case 96: return pick(qkv_mma_kernel<96, 1>, qkv_mma_kernel<96, 2>, qkv_mma_kernel<96, 4>);
+    case 128: return pick(qkv_mma_kernel<128, 1>, qkv_mma_kernel<128, 2>, qkv_mma_kernel<128, 4>);
     default: return cudaErrorInvalidValue;
   }
 }
