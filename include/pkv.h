@@ -415,17 +415,30 @@ pkv_status pkv_combine(const pkv_cache* cache, const float* partial_o, const flo
 pkv_status pkv_check_status(pkv_cache* cache, pkv_stream_t stream, int* flags);
 
 /*
- * Limit of the kernels' waits for their staged copies, in nanoseconds of the GPU's global timer
- * (default 2 s; 0 restores it).  A decode or prefill warp whose wait runs out sets
- * PKV_FLAG_TIMEOUT, waits up to 125 ms (a fixed limit) for its own copies still in flight, and
- * returns without writing its results; pkv_check_status then reports PKV_ERR_TIMEOUT.  Used to
- * test that failure path: a limit shorter than a copy's latency (say 1) makes waits run out on a
- * healthy GPU.  Limits below 1 ms are such a test setting: they are counted in SM clock cycles
- * (about half a nanosecond each) and the waits poll without suspending.  After a timeout, outputs are undefined and chunk_counters must be re-zeroed.
+ * Limit of the kernels' waits for their staged copies, in nanoseconds (default 2 s; 0 restores
+ * it).  A decode or prefill warp whose wait runs out sets PKV_FLAG_TIMEOUT, waits up to 125 ms (a
+ * fixed limit) for its own copies still in flight, and returns without writing its results;
+ * pkv_check_status then reports PKV_ERR_TIMEOUT.  After a timeout, outputs are undefined and
+ * chunk_counters must be re-zeroed.  The decode kernels count the limit on the GPU's global timer
+ * and poll with suspending waits; the prefill kernel does the same from 1 ms up, and counts limits
+ * below 1 ms (a test setting) in SM clock cycles (about half a nanosecond each), polling without
+ * suspending, so that a limit shorter than a copy's latency (say 1) makes its waits run out on a
+ * healthy GPU.  The decode kernels' failure path is tested with pkv_set_stage_stall.
  * Applies to the launches that follow the call.  Host only; returns PKV_ERR_INVALID_ARG for NULL.
  * (Everything WebGPU AI.md, "Fail Fast": failures surface as typed errors, not hangs.)
  */
 pkv_status pkv_set_wait_limit(pkv_cache* cache, unsigned long long limit_ns);
+
+/*
+ * Test setting of the decode kernels (pkv_decode_attention, pkv_decode_attention_merged,
+ * pkv_append_decode_attention and the no-alloc entry point): with `on` nonzero, each stage
+ * barrier of the decode kernel is initialised for two arrivals where the producer makes one, so
+ * that no stage's phase completes and every stage wait runs out at the wait limit (a wait for
+ * something nothing provides), on every lane of every warp alike.  The copies themselves land as
+ * usual.  With `on` zero (the default) one arrival completes a stage.  Applies to the launches that
+ * follow the call.  Host only; returns PKV_ERR_INVALID_ARG for NULL.
+ */
+pkv_status pkv_set_stage_stall(pkv_cache* cache, int on);
 
 /* Static description of a status code. */
 const char* pkv_status_string(pkv_status status);

@@ -97,6 +97,8 @@ def lib():
         L.pkv_check_status.argtypes = [P, P, ctypes.POINTER(i)]
         L.pkv_set_wait_limit.restype = i
         L.pkv_set_wait_limit.argtypes = [P, ctypes.c_ulonglong]
+        L.pkv_set_stage_stall.restype = i
+        L.pkv_set_stage_stall.argtypes = [P, i]
         _lib = L
     return _lib
 
@@ -397,6 +399,11 @@ class Cache:
     def set_wait_limit(self, limit_ns: int = 0):
         """pkv_set_wait_limit: limit of the kernels' waits for staged copies (0 = the 2 s default)."""
         _check(lib().pkv_set_wait_limit(self.handle, int(limit_ns)), "pkv_set_wait_limit")
+
+    def set_stage_stall(self, on: bool = True):
+        """pkv_set_stage_stall (test setting): the decode kernel's stage barriers wait for an
+        arrival that nothing makes, so that every stage wait runs out at the wait limit."""
+        _check(lib().pkv_set_stage_stall(self.handle, 1 if on else 0), "pkv_set_stage_stall")
 
     def check_status(self, stream=None):
         """pkv_check_status; returns (status code, flag bits) without raising."""

@@ -34,9 +34,11 @@
 // rotates q and k there, and the staged copy of the page that holds the token is patched (and the
 // pool written) before it is used.
 //
-// Every wait is bounded (2 s of global time unless pkv_set_wait_limit sets another limit), with
-// one answer per warp; on expiry the warp flags PKV_FLAG_TIMEOUT, waits a fixed bounded time for
-// its own copies in flight (so none lands in the shared memory of a finished block) and returns.
+// Every wait is bounded (2 s of global time unless pkv_set_wait_limit sets another limit); on
+// expiry the warp flags PKV_FLAG_TIMEOUT, waits a fixed bounded time for its own copies in flight
+// (so none lands in the shared memory of a finished block) and returns.  The test setting
+// pkv_set_stage_stall makes every stage's phase wait for an arrival that nothing makes, so that
+// the waits run out on a healthy GPU.
 #include <algorithm>
 
 #include "merge.cuh"
@@ -959,7 +961,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) prefetch_tensormap(&map);
-  for (int i = tid; i < p.warps * p.nstage; i += blockDim.x) mbar_init(&bars[i], 1);
+  // one arrival (the producer's) completes a stage's phase; the test setting pkv_set_stage_stall
+  // asks for a second one, which nothing makes
+  for (int i = tid; i < p.warps * p.nstage; i += blockDim.x) mbar_init(&bars[i], p.stall ? 2 : 1);
   fence_mbarrier_init();
 
   // Page ranges of every sequence, then items per sequence and their exclusive prefix sum (chunk
@@ -1247,11 +1251,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     }
   }
 
-  // Bounded wait for stage number c (ring slot k, phase parity ph), with one answer for the warp;
-  // on expiry flag a timeout and drain (bounded) the copies in flight, stage c's included (stage c
-  // may be the merge's copy, numbered `issued` before it is counted).
+  // Bounded wait for stage number c (ring slot k, phase parity ph), called by the whole warp in
+  // step; on expiry flag a timeout and drain (bounded) the copies in flight, stage c's included
+  // (stage c may be the merge's copy, numbered `issued` before it is counted).
   auto wait_stage = [&](int c, int k, uint32_t ph) -> bool {
-    if (warp_wait_bounded(&bar[k], ph, p.wait_ns)) return true;
+    if (mbar_wait_bounded(&bar[k], ph, p.wait_ns)) return true;
     if (lane == 0) atomicOr(p.status, kFlagTimeout);
     for (int d = c; d < max(issued, c + 1); ++d)
       mbar_wait_bounded(&bar[d % nst], (uint32_t)((d / nst) & 1), kDrainLimitNs);

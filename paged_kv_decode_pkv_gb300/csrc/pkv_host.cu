@@ -25,6 +25,7 @@ struct pkv_cache {
   bool pdl = false;
   bool int8 = false;  // PKV_OPT_INT8_KV: int8 blocks with per-slot scales
   unsigned long long wait_ns = pkv::kWaitLimitNs;  // limit of the kernels' waits for staged copies
+  bool stall = false;  // test setting (pkv_set_stage_stall): decode stages never complete
   // Per layer: the pool was written by a call other than the one-launch step (an append or a QKV
   // append) since the last one-launch step of that layer.  The next one-launch step of the layer
   // then copies no page before its launch wait, since the writing kernel may still be running.
@@ -643,6 +644,7 @@ pkv_status decode_common(const pkv_cache* c, int layer, const void* q_rope, cons
   if (fused != nullptr && fused->early_ok && (c->desc.options & PKV_OPT_EARLY_PAGES))
     p.early = c->group >= 2 ? kEarlyStagesGroup : kEarlyStagesOneHead;
   p.wait_ns = c->wait_ns;
+  p.stall = c->stall ? 1 : 0;
   p.pool8 = c->int8 ? static_cast<const unsigned char*>(c->pools[layer]) : nullptr;
   if (c->int8) p.pool = nullptr;
   return launch_status("decode launch", pkv::launch_decode(p, c->maps[layer], cfg, D, (int)grid, stream, c->pdl));
@@ -724,6 +726,12 @@ pkv_status pkv_combine(const pkv_cache* c, const float* partial_o, const float* 
 pkv_status pkv_set_wait_limit(pkv_cache* c, unsigned long long limit_ns) {
   if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "null cache");
   c->wait_ns = limit_ns == 0 ? pkv::kWaitLimitNs : limit_ns;
+  return PKV_OK;
+}
+
+pkv_status pkv_set_stage_stall(pkv_cache* c, int on) {
+  if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "null cache");
+  c->stall = on != 0;
   return PKV_OK;
 }
 

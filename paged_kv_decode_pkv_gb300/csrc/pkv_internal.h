@@ -135,6 +135,7 @@ struct DecodeParams {
   int early;  // one-launch mode: stages per warp copied before the launch wait (PKV_OPT_EARLY_PAGES)
   const unsigned char* pool8;  // int8 cache: blocks [num_pages][2][hkv][16 * d + 64]
   unsigned long long wait_ns;  // limit of a wait for a staged copy (kWaitLimitNs unless set)
+  int stall;  // test setting (pkv_set_stage_stall): stage barriers wait for a second arrival
 };
 
 struct CombineParams {

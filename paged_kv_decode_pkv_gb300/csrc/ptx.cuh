@@ -74,25 +74,28 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Limits below this (1 ms) are a test setting: they are counted in SM clock cycles, which resolve
-// a few nanoseconds where the global timer may tick only every microsecond, and polled without
-// suspending the thread (try_wait may suspend for a system-dependent time longer than the limit).
+// Wait for the phase with the given parity to complete, giving up after `limit_ns` of global
+// time; returns false on timeout.  Each lane waits for itself, with no warp-collective operation
+// (the decode kernel's stage wait sits in its hot loop, where a vote, or any longer loop body,
+// measurably slows it).  The lanes of a converged warp poll the same barrier word and read the
+// same timer in each step, so they leave the loop in the same step with the same answer.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Limits below this (1 ms) are a test setting of warp_wait_bounded: they are counted in SM clock
+// cycles, which resolve a few nanoseconds where the global timer may tick only every microsecond,
+// and polled without suspending the thread (try_wait may suspend for a system-dependent time
+// longer than the limit).
 constexpr uint64_t kShortWaitNs = 1000000;
 
 __device__ __forceinline__ uint64_t wait_clock(bool short_limit) {
   return short_limit ? (uint64_t)clock64() : global_timer_ns();
-}
-
-// Wait for the phase with the given parity to complete, giving up after `limit_ns` of global
-// time.  Returns false on timeout.  Every lane of the calling warp may call it.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const bool short_limit = limit_ns < kShortWaitNs;
-  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = wait_clock(short_limit);
-  while (true) {
-    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (wait_clock(short_limit) - t0 > limit_ns) return false;
-  }
 }
 
 // The wait for a whole warp, with one answer for every lane.  Lanes poll together: the warp goes

@@ -108,7 +108,7 @@ struct QkvMmaSmem {
 template <int D, int NT>
 __global__ void __launch_bounds__(kMmaWarps * 32) qkv_mma_kernel(QkvParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int words = p.hidden / 8, groups = p.hidden / 32;
+  const int groups = p.hidden / 32;
   const int wstride = p.hidden / 2 + 16;  // bytes per staged weight row
   const int tok_cap = min(8 * NT, p.num_tokens);
   uint64_t* wbar = reinterpret_cast<uint64_t*>(smem);

@@ -70,6 +70,7 @@ def test_argument_errors_return_before_any_device_work(lib):
     assert lib.pkv_combine(None, None, None, None, 0, 4, 2, 128, None, None, None) == pkv.OK
     assert lib.pkv_check_status(None, None, None) == pkv.ERR_INVALID_ARG
     assert lib.pkv_set_wait_limit(None, 1) == pkv.ERR_INVALID_ARG
+    assert lib.pkv_set_stage_stall(None, 1) == pkv.ERR_INVALID_ARG
     s, c = ctypes.c_int(), ctypes.c_int()
     assert lib.pkv_plan_decode(None, 1, 1, 0, 0, 0, 4, ctypes.byref(s), ctypes.byref(c)) == pkv.ERR_INVALID_ARG
     lib.pkv_destroy(None)

@@ -9,9 +9,10 @@ of the same layer, and page tables written by an ordinary kernel right before th
 is compared with the oracle's two appends and attention, and bit for bit with the same steps on a
 cache without programmatic dependent launch.
 
-The bounded waits are tested the accepted way: a wait limit shorter than a copy makes healthy
-waits run out, the kernels report PKV_ERR_TIMEOUT, and the next call with the default limit is
-checked against the oracle.
+The bounded waits are tested on a healthy GPU: the decode kernels' page stages are armed for more
+bytes than they receive (a wait for something nothing provides), the prefill kernel's waits get a
+limit shorter than a copy; the kernels report PKV_ERR_TIMEOUT, and the next call with the default
+settings is checked against the oracle.
 """
 import numpy as np
 import pytest
@@ -240,12 +241,15 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct(name, entry):
 
     pool = H.to_dev(host_pool, torch.float16)
     cache = H.make_cache(step, [0], [pool], options=pkv.OPT_PDL | pkv.OPT_EARLY_PAGES)
-    cache.set_wait_limit(1)  # 1 ns: every wait for a copy runs out
+    cache.set_wait_limit(1)  # 1 ns: the prefill kernel's waits for its copies run out
+    if entry != "prefill":
+        cache.set_stage_stall(True)  # the decode stages never complete: every stage wait runs out
     run(cache, pool)
     code, flags = cache.check_status()
     assert code == pkv.ERR_TIMEOUT and flags & pkv.FLAG_TIMEOUT, (code, flags)
-    # the default limit again, on a fresh pool (the timed-out launch left its work unfinished)
+    # the default settings again, on a fresh pool (the timed-out launch left its work unfinished)
     cache.set_wait_limit(0)
+    cache.set_stage_stall(False)
     pool.copy_(H.to_dev(host_pool, torch.float16))
     out, lse = run(cache, pool)
     torch.cuda.synchronize()
