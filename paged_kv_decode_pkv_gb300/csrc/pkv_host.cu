@@ -18,7 +18,7 @@ struct pkv_cache {
   std::vector<int> windows;         // per layer, 0 = full attention
   std::vector<const float*> sinks;  // per layer, device fp32 [Hq] or null
   std::vector<CUtensorMap> maps;     // one per layer pool: boxes of one page's K and V (decode)
-  std::vector<CUtensorMap> maps_pf;  // one per layer pool: boxes of one page's K or V (prefill)
+  std::vector<CUtensorMap> maps_pf;  // one per layer pool: one page's K or V of one KV head (prefill)
   int device = 0;
   int num_sms = 0;
   int group = 1;
@@ -343,10 +343,19 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
     CUresult r = encode(&c->maps[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    // the prefill kernel copies a page's K and its V as separate boxes (16 slots x one swizzle row)
-    const cuuint32_t box1[4] = {(cuuint32_t)cfg.box_inner, (cuuint32_t)PKV_PAGE_SIZE, 1, 1};
+    // The prefill kernel copies a page's K (or V) of one KV head in one box, landing as
+    // [half page][swizzle atom][8 slots][one swizzle row]: the dimensions, innermost first, are the
+    // elements of an atom, the slot within a half page, the atom, the half page, and (page, K or V,
+    // KV head) together.
+    const int E = cfg.box_inner, NA = D / E;
+    const cuuint64_t gdim5[5] = {(cuuint64_t)E, 8, (cuuint64_t)NA, 2,
+                                 (cuuint64_t)d->num_pages * 2 * (cuuint64_t)d->num_kv_heads};
+    const cuuint64_t gstride5[4] = {(cuuint64_t)D * 2, (cuuint64_t)E * 2, (cuuint64_t)8 * D * 2,
+                                    (cuuint64_t)PKV_PAGE_SIZE * D * 2};
+    const cuuint32_t box5[5] = {(cuuint32_t)E, 8, (cuuint32_t)NA, 2, 1};
+    const cuuint32_t estride5[5] = {1, 1, 1, 1, 1};
     if (r == CUDA_SUCCESS)
-      r = encode(&c->maps_pf[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, c->pools[l], gdim, gstride, box1, estride,
+      r = encode(&c->maps_pf[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, c->pools[l], gdim5, gstride5, box5, estride5,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {

@@ -12,9 +12,9 @@
 // a persistent grid (one per SM) in turn.
 //
 // One CTA, seven warps:
-//   warps 0 and 6  producers: the tile's key blocks, each page's K (warp 0) and V (warp 6) boxes of
-//           KV head g copied by the tensor-memory-access unit into rings of three K and two V
-//           stages (128-byte swizzle, 64-byte for head_dim 96), each with its own barriers, so a K
+//   warps 0 and 6  producers: the tile's key blocks, each page's K (warp 0) and V (warp 6) of KV
+//           head g copied as one box by the tensor-memory-access unit into rings of three K and two
+//           V stages (128-byte swizzle, 64-byte for head_dim 96), each with its own barriers, so a K
 //           stage is refilled as soon as its S MMA has completed while a V stage waits for its
 //           P V MMA;
 //   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two tensor-memory buffers (128
@@ -56,7 +56,6 @@ constexpr int kBlockPages = kKeys / kPageSize;
 constexpr int kKStages = 3;          // key blocks whose K is in flight
 constexpr int kVStages = 2;          // and whose V is
 constexpr int kThreads = 224;        // K producer, MMA issuer, four softmax warps, V producer
-constexpr int kSoftmaxWarps = 4;
 constexpr int kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
 constexpr int kMaxSortedBatch = 512; // longest-first order of sequences up to this batch
 
@@ -70,7 +69,12 @@ struct Geo {
   static constexpr int V_OFF = kKStages * KV_BYTES;
   static constexpr int Q_OFF = V_OFF + kVStages * KV_BYTES;
   static constexpr int BAR_OFF = Q_OFF + kRows * D * 2;
-  static constexpr int PAGE_BOX = kPageSize * SW;  // bytes of one page's box (16 rows of one atom)
+  // K and V stages hold a block as [8-key group][atom][8 keys][one swizzle row], a page (two
+  // groups) as one copy lands: a swizzle atom of 8 rows, GROUP bytes, then the atoms of the
+  // group's head dimensions, ROWGRP bytes per 8 keys
+  static constexpr int GROUP = 8 * SW;
+  static constexpr int ROWGRP = NA * GROUP;
+  static constexpr int PAGE_BYTES = 2 * ROWGRP;
   static constexpr uint32_t IDESC_S = tc::idesc_f16(kRows, kKeys, false);
   static constexpr uint32_t IDESC_O = tc::idesc_f16(kRows, D, true);
 };
@@ -81,10 +85,6 @@ struct Shared {
   uint64_t s_full[2], p_full, o_done, q_full, drain;
   uint32_t tmem_base;
   int abort_flag;
-  // pages loaded of block i (bit l = page 8b + l), slot i % 8: written when the block's K copy is
-  // issued, read by the softmax warps before they release the block's K stage, which the copy of
-  // block i + 3 waits for
-  int stage_mask[8];
   int warp_sums[8];
 };
 
@@ -151,6 +151,39 @@ __device__ __forceinline__ void tile_pages(const Tile& t, const PrefillParams& p
   }
 }
 
+// The page ids of a tile's key blocks, read ahead in groups of four blocks (one coalesced load per
+// group, four blocks before its first use, so no wait for a page id sits in a warp's per-block
+// loop): lane 8 i + l of `cur` holds page l of block bq + i (of `nxt`, of block bq + 4 + i), or -1
+// outside the tile's page range [pmin, pmax].  Every lane of the warp calls it.
+struct BlockIds {
+  int cur, nxt, bq;
+  const int* ids;
+  int pmin, pmax;
+  __device__ __forceinline__ int load(int b, int lane) const {
+    const int ord = b * kBlockPages + lane;
+    return (ord >= pmin && ord <= pmax) ? ids[ord] : -1;
+  }
+  __device__ __forceinline__ void start(const int* tile_ids, int b0, int lo, int hi, int lane) {
+    ids = tile_ids;
+    pmin = lo;
+    pmax = hi;
+    bq = b0;
+    cur = load(b0, lane);
+    nxt = load(b0 + 4, lane);
+  }
+  // Called once per block, b increasing from the start block: page l of block b on lane l < 8, -1
+  // on the other lanes.
+  __device__ __forceinline__ int page(int b, int lane) {
+    if (b >= bq + 4) {
+      bq += 4;
+      cur = nxt;
+      nxt = load(bq + 4, lane);
+    }
+    const int v = __shfl_sync(kAll, cur, 8 * (b - bq) + (lane & 7));
+    return lane < kBlockPages ? v : -1;
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap map, PrefillParams p) {
   using G = Geo<D>;
@@ -169,10 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     prefetch_tensormap(&map);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&sh.k_full[i], 1);
-      // K of a stage is free when its S MMA has completed and every softmax warp has passed the
-      // block's K barrier (it reads the block's page mask there): a later K copy can then never
-      // complete a phase of that barrier before a softmax warp has waited for the earlier one
-      mbar_init(&sh.k_empty[i], 1 + kSoftmaxWarps);
+      // K of a stage is free when its S MMA has completed (only the MMA thread waits for K)
+      mbar_init(&sh.k_empty[i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sh.v_full[i], 1);
@@ -272,21 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tile_pages(t, p, lane, pmin, pmax);
       if (pmax < 0) continue;
       bool ok = true;
+      BlockIds bid;
+      bid.start(p.page_indices + t.first, pmin / kBlockPages, pmin, pmax, lane);
       for (int b = pmin / kBlockPages; b <= pmax / kBlockPages && ok; ++b, ++kv_it) {
         const int st = kv_it % nst;
+        const int pid = bid.page(b, lane);  // lane l < 8: page 8b + l of the block
         // K of a stage is free once the S MMA that read it has completed, V once the P V MMA has
         if (kv_it >= nst && !(ok = wait(&empty[st], (uint32_t)(((kv_it / nst) - 1) & 1)))) break;
-        // lane l < 8 owns page 8b + l of the block
         const int ord_pg = b * kBlockPages + lane;
-        int pid = -1;
-        if (lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax) pid = p.page_indices[t.first + ord_pg];
         const bool in_range = pid >= 0 && pid < p.num_pages;
         if (is_k && lane < kBlockPages && ord_pg >= pmin && ord_pg <= pmax && !in_range)
           atomicOr(p.status, kFlagBadPage);
         const unsigned loaded = __ballot_sync(kAll, in_range) & 0xffu;
         const uint32_t bytes = (uint32_t)__popc(loaded) * kPageSize * D * 2u;  // K (or V) of the loaded pages
         if (lane == 0) {
-          if (is_k) sh.stage_mask[kv_it & 7] = (int)loaded;
           if (bytes != 0u) {
             mbar_arrive_expect_tx(&full[st], bytes);
           } else {
@@ -295,10 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
         if (in_range) {
-          unsigned char* dst = base + region + st * G::KV_BYTES + lane * G::PAGE_BOX;
-#pragma unroll
-          for (int u = 0; u < G::NA; ++u)
-            tma_load_4d(dst + u * kKeys * G::SW, &map, &full[st], u * G::E, 0, t.g, 2 * pid + kv, policy);
+          unsigned char* dst = base + region + st * G::KV_BYTES + lane * G::PAGE_BYTES;
+          tma_load_5d(dst, &map, &full[st], 0, 0, 0, 0, (2 * pid + kv) * p.hkv + t.g, policy);
         }
       }
       if (!ok) break;
@@ -327,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t pbase = tmem + 128 * (vit & 1);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t bd = tc::smem_desc(vbase + (uint32_t)(16 * kk * G::SW), kKeys * G::SW, 8 * G::SW,
+          const uint64_t bd = tc::smem_desc(vbase + (uint32_t)(2 * kk * G::ROWGRP), G::GROUP, G::ROWGRP,
                                             tc::layout_for(G::E));
           tc::mma_f16_ts(tmem + 256, pbase + 8 * kk, bd, G::IDESC_O, !(first && kk == 0));
         }
@@ -355,9 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const uint32_t kbase = sbase + G::K_OFF + st * G::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((16 * kk) / G::E) * kRows * G::SW + (uint32_t)((32 * kk) % G::SW);
-            const uint64_t ad = tc::smem_desc(sbase + G::Q_OFF + off, 16, 8 * G::SW, tc::layout_for(G::E));
-            const uint64_t bd = tc::smem_desc(kbase + off, 16, 8 * G::SW, tc::layout_for(G::E));
+            const uint32_t u = (uint32_t)((16 * kk) / G::E), col = (uint32_t)((32 * kk) % G::SW);
+            const uint64_t ad = tc::smem_desc(sbase + G::Q_OFF + u * kRows * G::SW + col, 16, 8 * G::SW,
+                                              tc::layout_for(G::E));
+            const uint64_t bd = tc::smem_desc(kbase + u * G::GROUP + col, 16, G::ROWGRP, tc::layout_for(G::E));
             tc::mma_f16(tmem + 128 * sb, ad, bd, G::IDESC_S, kk > 0);
           }
           tc::commit(&sh.s_full[sb]);
@@ -412,17 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
       float m = -INFINITY, l = 0.f;
       const int b0 = pmin / kBlockPages, nb = pmax / kBlockPages - b0 + 1;
+      BlockIds bid;
+      bid.start(p.page_indices + t.first, b0, pmin, pmax, lane);
       for (int j = 0; j < nb; ++j, ++kvs, ++ss) {
-        const int b = b0 + j, st = kvs % kKStages, vst = kvs % kVStages, sb = ss & 1;
-        if (!(ok = wait(&sh.k_full[st], (uint32_t)((kvs / kKStages) & 1)))) break;
+        const int b = b0 + j, vst = kvs % kVStages, sb = ss & 1;
+        // the block's pages the producers load (bit l = page 8b + l), decided as they decide it
+        const int bpid = bid.page(b, lane);
+        const int loaded = (int)(__ballot_sync(kAll, bpid >= 0 && bpid < p.num_pages) & 0xffu);
         if (!(ok = wait(&sh.s_full[sb], (uint32_t)((ss >> 1) & 1)))) break;
         tc::fence_after_sync();
         uint32_t sv[4][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_addr + 128 * sb + 32 * q4, sv[q4]);
-        const int loaded = sh.stage_mask[kvs & 7];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.k_empty[st]);
         tc::wait_ld();
         const int k0 = b * kKeys;  // position of the block's first key
         float x[kKeys];
@@ -475,12 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (__any_sync(kAll, zero_v)) {
           if (!(ok = wait(&sh.v_full[vst], (uint32_t)((kvs / kVStages) & 1)))) break;
           if (zero_v) {
-            unsigned char* vrow = base + G::V_OFF + vst * G::KV_BYTES + r * G::SW;
+            unsigned char* vrow = base + G::V_OFF + vst * G::KV_BYTES + (r >> 3) * G::ROWGRP + (r & 7) * G::SW;
 #pragma unroll
             for (int u = 0; u < G::NA; ++u)
 #pragma unroll
               for (int c = 0; c < G::SW / 16; ++c)
-                *reinterpret_cast<uint4*>(vrow + u * kKeys * G::SW + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(vrow + u * G::GROUP + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
         }
