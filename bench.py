@@ -342,7 +342,7 @@ def prefill_measure(cfg, step, cache, layers, tabs, q_out, stream, time_graph, d
             "peak_source": kind + "; fp16 mma runs at the bf16 rate", "us_per_layer": ms * 1e3 / cfg.layers,
             "flops_per_layer": flops, "tokens": T, "sequences": int(seqs.size),
             "step": "per layer: pkv_prefill_attention over the sequences that appended a chunk (every chunk "
-                    "token, causal; mma.sync m16n8k16)"}
+                    "token, causal; tcgen05.mma with tensor-memory accumulators)"}
 
 
 def qkv_measure(args, cfg, step, cache, layers, tabs, q_out, counters, po, pl, outs, lses, total_pages, stream,

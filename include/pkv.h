@@ -18,7 +18,8 @@
  * Conventions that hold for every entry point:
  *  - Ownership: the caller allocates and frees every device buffer (pools, the
  *    RoPE table, the status word, q/k/v, page tables, partials, outputs).  A
- *    pkv_cache handle owns host memory only; pkv_destroy frees nothing else.
+ *    pkv_cache handle owns its host memory and one 8-byte device counter (the
+ *    prefill kernel's work counter); pkv_destroy frees both and nothing else.
  *  - Device: a cache is bound to the CUDA device that was current when it was
  *    created; call the other entry points with that device current.
  *  - Asynchrony: calls enqueue kernels on the given stream and return; results
@@ -161,14 +162,15 @@ size_t pkv_rope_table_bytes(int max_position, int head_dim);
 /*
  * Create a cache handle over caller-owned storage (the create_kv_cache role of the MLC model
  * artifact manifest page: the constructor takes sizes only; here also the storage).
- * Blocks: fills desc->rope_table and zeroes desc->status_word with synchronous copies, and
- * builds one TMA descriptor per layer pool.  The pools' contents are not touched.
+ * Blocks: fills desc->rope_table and zeroes desc->status_word with synchronous copies,
+ * allocates and zeroes the handle's 8-byte device work counter, and builds the TMA descriptors
+ * of each layer pool.  The pools' contents are not touched.
  * Returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED for bad descriptors, PKV_ERR_CUDA if a
  * CUDA call fails; *out is set only on PKV_OK.
  */
 pkv_status pkv_create_cache(const pkv_cache_desc* desc, pkv_cache** out);
 
-/* Free the handle (host memory only).  NULL is ignored. */
+/* Free the handle and its device work counter (on the cache's device).  NULL is ignored. */
 void pkv_destroy(pkv_cache* cache);
 
 /*
@@ -213,10 +215,12 @@ pkv_status pkv_append_rope(pkv_cache* cache, int layer, const void* q, const voi
  *   lse_out[t][h] = ln(sum_u e^{s_u} + e^{sink_h}),   s_u = sm_scale * q_t,h . K_u.
  *   q_rope   fp16 [num_tokens][Hq][head_dim] (e.g. q_out of pkv_append_rope), 16-byte aligned
  *   out      fp16 [num_tokens][Hq][head_dim], 16-byte aligned;  lse_out fp32 [num_tokens][Hq] or NULL
- * Tiles of (sequence, KV head, 16 / G tokens) run mma.sync over the pages the tile attends to.
- * Device-detected errors: page ids out of range, positions outside [0, len_s), bad
- * last_page_len (the token's rows are left unwritten).  With one token per sequence at its last
- * position this equals the merged decode up to rounding.
+ * Tiles of (sequence, KV head, 128 / G tokens x G heads) run tcgen05.mma over 128-key blocks of
+ * the pages the tile attends to, taken longest first by the CTAs through the cache's device work
+ * counter: prefill calls on one cache must not overlap on the GPU (call them on one stream, or
+ * order their streams).  Device-detected errors: page ids out of range, positions outside
+ * [0, len_s), bad last_page_len (the token's rows are left unwritten).  With one token per
+ * sequence at its last position this equals the merged decode up to rounding.
  */
 pkv_status pkv_prefill_attention(const pkv_cache* cache, int layer, const void* q_rope,
                                  const int32_t* append_indptr, const int32_t* pos_map, int num_tokens,

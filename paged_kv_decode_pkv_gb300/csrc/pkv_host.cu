@@ -30,6 +30,7 @@ struct pkv_cache {
   // append) since the last one-launch step of that layer.  The next one-launch step of the layer
   // then copies no page before its launch wait, since the writing kernel may still be running.
   std::vector<char> pool_dirty;
+  int* prefill_work = nullptr;  // device int[2], owned: the prefill kernel's work counter
 };
 
 namespace {
@@ -306,8 +307,10 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   }
   e = cudaMemcpy(d->rope_table, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(d->status_word, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&c->prefill_work, 2 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->prefill_work, 0, 2 * sizeof(int));
   if (e != cudaSuccess) {
-    delete c;
+    pkv_destroy(c);
     return cuda_fail("writing the RoPE table / status word", e);
   }
 
@@ -321,7 +324,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   if (e == cudaSuccess) e = pkv::append_prepare();
   if (e == cudaSuccess) e = pkv::combine_prepare();
   if (e != cudaSuccess) {
-    delete c;
+    pkv_destroy(c);
     return cuda_fail("setting kernel attributes", e);
   }
   c->maps.resize(d->num_layers);
@@ -359,7 +362,7 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
-      delete c;
+      pkv_destroy(c);
       char msg[64];
       snprintf(msg, sizeof(msg), "CUresult %d for layer %d", (int)r, l);
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled", msg);
@@ -369,7 +372,17 @@ pkv_status pkv_create_cache(const pkv_cache_desc* d, pkv_cache** out) {
   return PKV_OK;
 }
 
-void pkv_destroy(pkv_cache* c) { delete c; }
+void pkv_destroy(pkv_cache* c) {
+  if (c == nullptr) return;
+  if (c->prefill_work != nullptr) {
+    int cur = 0;
+    const bool restore = cudaGetDevice(&cur) == cudaSuccess && cur != c->device;
+    if (restore) cudaSetDevice(c->device);
+    cudaFree(c->prefill_work);
+    if (restore) cudaSetDevice(cur);
+  }
+  delete c;
+}
 
 pkv_status pkv_device_info(const pkv_cache* c, int* num_sms, int* decode_warps_per_sm) {
   if (c == nullptr) return PKV_ERR_INVALID_ARG;
@@ -530,6 +543,7 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
   p.nstage = cfg.nstage;
   const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.work = c->prefill_work;
   p.wait_ns = c->wait_ns;
   const int grid = c->num_sms;
   return launch_status("prefill launch", pkv::launch_prefill(p, c->maps_pf[layer], cfg, D, grid, stream, c->pdl));

@@ -77,6 +77,7 @@ struct PrefillParams {
   int nstage;
   float scale_log2;
   unsigned long long wait_ns;  // limit of a wait for a staged copy (kWaitLimitNs unless set)
+  int* work;  // device [2]: next work item, CTAs finished (the last CTA resets both to 0)
 };
 constexpr int kPrefillWarps = 8;  // consumer warps per CTA (plus one producer warp)
 struct PrefillConfig {

@@ -8,8 +8,10 @@
 // Work decomposition.  A tile is (sequence s, KV head g, 128 / G consecutive appended tokens of s):
 // 128 query rows, row r = token r / G of the tile and query head g * G + r % G, so a page of KV
 // head g is read once for all G heads that use it.  A key block is 8 pages (128 keys).  Tiles are
-// ordered longest sequence first (tiles of one sequence last tile first) and dealt to the CTAs of
-// a persistent grid (one per SM) in turn.
+// ordered longest sequence first (tiles of one sequence last tile first) and taken in that order by
+// the CTAs of a persistent grid (one per SM) from a shared counter whenever a CTA is free (the
+// longest-first greedy schedule: a fixed deal left the CTAs of long histories working while
+// others idled).
 //
 // One CTA, seven warps:
 //   warps 0 and 6  producers: the tile's key blocks, each page's K (warp 0) and V (warp 6) of KV
@@ -58,6 +60,8 @@ constexpr int kVStages = 2;          // and whose V is
 constexpr int kThreads = 224;        // K producer, MMA issuer, four softmax warps, V producer
 constexpr int kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
 constexpr int kMaxSortedBatch = 512; // longest-first order of sequences up to this batch
+constexpr int kItemSlots = 8;        // work items taken ahead by the K producer, published to the other warps
+constexpr int kItemReaders = 6;      // V producer, MMA issuer, four softmax warps
 
 template <int D>
 struct Geo {
@@ -83,9 +87,11 @@ struct Geo {
 struct Shared {
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full, o_done, q_full, drain;
+  uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   uint32_t tmem_base;
   int abort_flag;
   int warp_sums[8];
+  int item_ring[kItemSlots];  // the CTA's i-th work item in slot i % kItemSlots (-1: no more)
 };
 
 // 2^x with the special-function unit's approximation (relative error about 2^-22; subnormal results
@@ -214,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&sh.o_done, 1);
     mbar_init(&sh.q_full, kRows);
     mbar_init(&sh.drain, 1);
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&sh.item_full[i], 1);
+      mbar_init(&sh.item_empty[i], kItemReaders);
+    }
     sh.abort_flag = 0;
   }
   fence_mbarrier_init();
@@ -287,6 +297,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return false;
   };
 
+  // Work items are taken in order from the launch's shared counter, so each CTA starts the longest
+  // remaining item whenever it is free (the longest-first greedy schedule).  The K producer takes
+  // them (a counter value past the last item means none is left) and publishes each in the item
+  // ring; the other warps read them from there in the same order.  Returns the item, or -1.
+  int item_i = 0;  // items this warp has taken or read
+  auto take_item = [&]() -> int {
+    const int slot = item_i % kItemSlots;
+    if (item_i >= kItemSlots && !wait(&sh.item_empty[slot], (uint32_t)(((item_i / kItemSlots) - 1) & 1))) return -1;
+    int w = 0;
+    if (lane == 0) {
+      w = atomicAdd(p.work, 1);
+      if (w >= total) w = -1;
+      sh.item_ring[slot] = w;
+      mbar_arrive(&sh.item_full[slot]);
+    }
+    ++item_i;
+    return __shfl_sync(kAll, w, 0);
+  };
+  auto read_item = [&]() -> int {
+    const int slot = item_i % kItemSlots;
+    if (!wait(&sh.item_full[slot], (uint32_t)((item_i / kItemSlots) & 1))) return -1;
+    const int w = *reinterpret_cast<volatile int*>(&sh.item_ring[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.item_empty[slot]);
+    ++item_i;
+    return w;
+  };
+
   if (warp == 0 || warp == 6) {
     // ---------------------------------------------------------------- producers (K: warp 0, V: warp 6)
     const bool is_k = warp == 0;
@@ -297,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int nst = is_k ? kKStages : kVStages;
     const int region = is_k ? G::K_OFF : G::V_OFF;
     int kv_it = 0;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+    while (!*abort_flag) {
+      const int w = is_k ? take_item() : read_item();
+      if (w < 0) break;
       const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
       int pmin, pmax;
       tile_pages(t, p, lane, pmin, pmax);
@@ -366,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       return true;
     };
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok && !*abort_flag; w += gridDim.x) {
+    while (ok && !*abort_flag) {
+      const int w = read_item();
+      if (w < 0) break;
       const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
       int pmin, pmax;
       tile_pages(t, p, lane, pmin, pmax);
@@ -408,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     int kvs = 0, ss = 0, pw = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok && !*abort_flag; w += gridDim.x) {
+    while (ok && !*abort_flag) {
+      const int w = read_item();
+      if (w < 0) break;
       const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
       // this row's token and query head, its position and the first position it attends to
       const int tk = r / p.group;
@@ -575,6 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
   tc::fence_before_sync();
   __syncthreads();
+  // the last CTA to finish (every CTA has taken its last item) resets the work counter for the
+  // next launch, which reads it only after its launch wait
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.work + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.work, 0);
+      atomicExch(p.work + 1, 0);
+    }
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::dealloc(tmem, kTmemCols);
