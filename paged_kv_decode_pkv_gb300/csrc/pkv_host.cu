@@ -538,7 +538,6 @@ pkv_status pkv_prefill_attention(const pkv_cache* c, int layer, const void* q_ro
   p.hkv = c->desc.num_kv_heads;
   p.group = c->group;
   p.num_pages = c->desc.num_pages;
-  p.tpt = 16 / c->group;
   p.window = c->windows[layer];
   p.nstage = cfg.nstage;
   const float scale = sm_scale > 0.f ? sm_scale : (float)(1.0 / std::sqrt((double)D));

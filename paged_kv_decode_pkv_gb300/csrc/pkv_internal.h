@@ -72,14 +72,12 @@ struct PrefillParams {
   int* status;
   const float* sinks;  // nullable, per query head
   int batch, num_tokens, hq, hkv, group, num_pages;
-  int tpt;          // tokens per tile: 16 / group
   int window;       // 0 = full attention
-  int nstage;
+  int nstage;       // K stages
   float scale_log2;
   unsigned long long wait_ns;  // limit of a wait for a staged copy (kWaitLimitNs unless set)
   int* work;  // device [2]: next work item, CTAs finished (the last CTA resets both to 0)
 };
-constexpr int kPrefillWarps = 8;  // consumer warps per CTA (plus one producer warp)
 struct PrefillConfig {
   int nstage;
   size_t smem_bytes;

@@ -94,3 +94,40 @@ def test_one_token_prefill_agrees_with_the_merged_decode(name):
     b = _bits(d_out).view(np.uint16).view(np.float16).astype(np.float64)
     assert np.abs(a - b).max() <= 2e-3
     assert np.abs(lse.cpu().numpy() - d_lse.cpu().numpy()).max() <= 5e-4
+
+
+@pytest.mark.parametrize("name", ["mixed_chunks_g4_d128", "chunks_g1_d96"])
+def test_back_to_back_prefill_launches_share_the_work_counter(name):
+    """Three prefill launches on one stream with no host synchronisation between them, under
+    programmatic dependent launch: the CTAs of each take their work items from the cache's device
+    counter, which the previous launch's last CTA resets.  Every launch computes every row: the
+    three outputs are bit-identical and match the oracle."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    cfg = CASES[name]
+    step = W.make_step(cfg)
+    pool = H.to_dev(W.host_pool(step, 0), torch.float16)
+    cache = pkv.Cache(1, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta, pools=[pool],
+                      options=pkv.OPT_PDL)
+    tabs = H.device_tables(step)
+    q, k, v = H.device_qkv(step, 0)
+    q_out = cache.append_rope(0, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                              tabs["page_indices"])
+    T = step.num_tokens
+    outs = []
+    for _ in range(3):  # NaN-filled outputs: a row no launch wrote stays NaN
+        o = torch.full((T, cfg.hq, cfg.head_dim), float("nan"), dtype=torch.float16, device="cuda")
+        l = torch.full((T, cfg.hq), float("nan"), dtype=torch.float32, device="cuda")
+        outs.append(cache.prefill_attention(0, q_out, tabs["append_indptr"], tabs["pos_map"], tabs["page_indptr"],
+                                            tabs["page_indices"], tabs["last_page_len"], out=o, lse=l))
+    torch.cuda.synchronize()
+    assert cache.check_status() == (0, 0)
+    for o, l in outs[1:]:
+        assert np.array_equal(_bits(o), _bits(outs[0][0])) and np.array_equal(_bits(l), _bits(outs[0][1]))
+    ref_out, ref_lse = oracle.prefill_attention(H.geometry(step), _bits(pool).view(np.uint16),
+                                                _bits(q_out).view(np.uint16), step.append_indptr, step.pos_map,
+                                                step.page_indptr, step.page_indices, step.last_page_len)
+    H.assert_close_out(_bits(outs[2][0]).view(np.uint16), ref_out)
+    H.assert_close_lse(outs[2][1].cpu().numpy(), ref_lse)
