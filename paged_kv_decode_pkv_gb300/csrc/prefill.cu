@@ -83,6 +83,19 @@ struct Geo {
   static constexpr uint32_t IDESC_O = tc::idesc_f16(kRows, D, true);
 };
 
+// The tile of work item w: sequence, KV head, first token and token count.
+struct Tile {
+  int s, g, t0, nt, first, n, last, len;
+  bool seq_ok;
+};
+
+// A work item as the K producer takes it: the item number (-1: none left), its tile and the
+// tile's page range (pmax < 0: nothing to attend).
+struct ItemInfo {
+  int w, pmin, pmax;
+  Tile t;
+};
+
 // Barriers and small shared state after the operand regions.
 struct Shared {
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
@@ -91,7 +104,7 @@ struct Shared {
   uint32_t tmem_base;
   int abort_flag;
   int warp_sums[8];
-  int item_ring[kItemSlots];  // the CTA's i-th work item in slot i % kItemSlots (-1: no more)
+  ItemInfo item_ring[kItemSlots];  // the CTA's i-th work item in slot i % kItemSlots
 };
 
 // 2^x with the special-function unit's approximation (relative error about 2^-22; subnormal results
@@ -110,12 +123,6 @@ __device__ __forceinline__ int find_pos(const int* prefix, int n, int w) {
   }
   return lo;
 }
-
-// The tile of work item w: sequence, KV head, first token and token count.
-struct Tile {
-  int s, g, t0, nt, first, n, last, len;
-  bool seq_ok;
-};
 
 __device__ __forceinline__ Tile tile_of(int w, const PrefillParams& p, const int* prefix, const int* order, int nseq,
                                         int tb) {
@@ -300,29 +307,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // Work items are taken in order from the launch's shared counter, so each CTA starts the longest
   // remaining item whenever it is free (the longest-first greedy schedule).  The K producer takes
   // them (a counter value past the last item means none is left) and publishes each in the item
-  // ring; the other warps read them from there in the same order.  Returns the item, or -1.
+  // ring with its tile and page range, so that the other warps, which read them from there in the
+  // same order, do no global load to learn them.
   int item_i = 0;  // items this warp has taken or read
-  auto take_item = [&]() -> int {
+  auto no_item = []() {
+    ItemInfo it;
+    it.w = -1;
+    it.pmin = 0;
+    it.pmax = -1;
+    return it;
+  };
+  auto take_item = [&]() -> ItemInfo {
     const int slot = item_i % kItemSlots;
-    if (item_i >= kItemSlots && !wait(&sh.item_empty[slot], (uint32_t)(((item_i / kItemSlots) - 1) & 1))) return -1;
+    ItemInfo it = no_item();
+    if (item_i >= kItemSlots && !wait(&sh.item_empty[slot], (uint32_t)(((item_i / kItemSlots) - 1) & 1))) return it;
     int w = 0;
+    if (lane == 0) w = atomicAdd(p.work, 1);
+    w = __shfl_sync(kAll, w, 0);
+    if (w < total) {
+      it.w = w;
+      it.t = tile_of(w, p, prefix, ord, p.batch, tb);
+      tile_pages(it.t, p, lane, it.pmin, it.pmax);
+    }
     if (lane == 0) {
-      w = atomicAdd(p.work, 1);
-      if (w >= total) w = -1;
-      sh.item_ring[slot] = w;
+      sh.item_ring[slot] = it;
       mbar_arrive(&sh.item_full[slot]);
     }
     ++item_i;
-    return __shfl_sync(kAll, w, 0);
+    return it;
   };
-  auto read_item = [&]() -> int {
+  auto read_item = [&]() -> ItemInfo {
     const int slot = item_i % kItemSlots;
-    if (!wait(&sh.item_full[slot], (uint32_t)((item_i / kItemSlots) & 1))) return -1;
-    const int w = *reinterpret_cast<volatile int*>(&sh.item_ring[slot]);
+    if (!wait(&sh.item_full[slot], (uint32_t)((item_i / kItemSlots) & 1))) return no_item();
+    const ItemInfo it = sh.item_ring[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.item_empty[slot]);
     ++item_i;
-    return w;
+    return it;
   };
 
   if (warp == 0 || warp == 6) {
@@ -336,11 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int region = is_k ? G::K_OFF : G::V_OFF;
     int kv_it = 0;
     while (!*abort_flag) {
-      const int w = is_k ? take_item() : read_item();
-      if (w < 0) break;
-      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
-      int pmin, pmax;
-      tile_pages(t, p, lane, pmin, pmax);
+      const ItemInfo it = is_k ? take_item() : read_item();
+      if (it.w < 0) break;
+      const Tile& t = it.t;
+      const int pmin = it.pmin, pmax = it.pmax;
       if (pmax < 0) continue;
       bool ok = true;
       BlockIds bid;
@@ -407,11 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     };
     bool ok = true;
     while (ok && !*abort_flag) {
-      const int w = read_item();
-      if (w < 0) break;
-      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
-      int pmin, pmax;
-      tile_pages(t, p, lane, pmin, pmax);
+      const ItemInfo it = read_item();
+      if (it.w < 0) break;
+      const int pmin = it.pmin, pmax = it.pmax;
       if (pmax < 0) continue;
       if (!(ok = wait(&sh.q_full, (uint32_t)(qi & 1)))) break;
       ++qi;
@@ -450,10 +468,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     int kvs = 0, ss = 0, pw = 0;
     bool ok = true;
-    while (ok && !*abort_flag) {
-      const int w = read_item();
-      if (w < 0) break;
-      const Tile t = tile_of(w, p, prefix, ord, p.batch, tb);
+    // the tile's queries, row r, into the K-major swizzled Q region: asynchronously (rows outside
+    // the tile are zero-filled); the caller waits for the copies and publishes them (q_full)
+    auto copy_queries = [&](const Tile& t) {
+      const int tk = r / p.group;
+      const bool row_ok = t.seq_ok && tk < t.nt;
+      const __half* src = p.q + ((long long)(row_ok ? t.t0 + tk : 0) * p.hq + t.g * p.group + r % p.group) * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        cp_async16(base + G::Q_OFF + tc::kmajor_offset(kRows, G::E, r, 8 * c), src + 8 * c, row_ok ? 16u : 0u);
+    };
+    // the next item that has pages (all warps skip the others), or none
+    auto next_item = [&]() -> ItemInfo {
+      while (true) {
+        const ItemInfo in = read_item();
+        if (in.w < 0 || in.pmax >= 0) return in;
+      }
+    };
+    ItemInfo it = read_item();
+    bool q_ready = false;  // the item's queries were copied during the previous item and published
+    while (ok && !*abort_flag && it.w >= 0) {
+      const Tile t = it.t;
       // this row's token and query head, its position and the first position it attends to
       const int tk = r / p.group;
       const int tok = t.t0 + tk;
@@ -465,23 +500,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         valid = false;
       }
       if (!t.seq_ok && r == 0 && t.g == 0 && t.nt > 0) atomicOr(p.status, kFlagBadSequence);
-      int pmin, pmax;
-      tile_pages(t, p, lane, pmin, pmax);
-      if (pmax < 0) continue;
+      const int pmin = it.pmin, pmax = it.pmax;
+      if (pmax < 0) {
+        it = read_item();
+        continue;
+      }
       const int start = (valid && p.window > 0 && pos + 1 > p.window) ? pos + 1 - p.window : 0;
       if (!valid) pos = -1;  // attends to nothing
 
-      // the tile's queries, row r, into the K-major swizzled Q region
-      {
-        const __half* src = p.q + ((long long)tok * p.hq + head) * D;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 v = valid ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(base + G::Q_OFF + tc::kmajor_offset(kRows, G::E, r, 8 * c)) = v;
-        }
+      if (!q_ready) {  // the first item (later ones are copied during the item before)
+        copy_queries(t);
+        cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&sh.q_full);
       }
+      ItemInfo in = no_item();  // the next item, taken during this one's last block
 
       float m = -INFINITY, l = 0.f;
       const int b0 = pmin / kBlockPages, nb = pmax / kBlockPages - b0 + 1;
@@ -494,6 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int loaded = (int)(__ballot_sync(kAll, bpid >= 0 && bpid < p.num_pages) & 0xffu);
         if (!(ok = wait(&sh.s_full[sb], (uint32_t)((ss >> 1) & 1)))) break;
         tc::fence_after_sync();
+        if (j == nb - 1) {
+          // the item's last S MMA has completed, so the Q region is free: start copying the next
+          // item's queries, which land while this block's softmax runs
+          in = next_item();
+          if (in.w >= 0) copy_queries(in.t);
+        }
         uint32_t sv[4][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_addr + 128 * sb + 32 * q4, sv[q4]);
@@ -581,6 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_arrive(&sh.p_full);
       }
       if (!ok) break;
+      // publish the next item's queries, so that its first S MMA can run during this epilogue
+      if (in.w >= 0) {
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.q_full);
+      }
       // the last block's P V, then the row of O
       if (!(ok = wait(&sh.o_done, (uint32_t)(pw & 1)))) break;
       ++pw;
@@ -615,7 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       if (valid && p.lse != nullptr) p.lse[(long long)tok * p.hq + head] = any ? (mm + log2f(lt)) * kLn2 : -INFINITY;
       tc::fence_before_sync();  // the O reads above come before the next tile's first P V
+      it = in;
+      q_ready = in.w >= 0;
     }
+    cp_async_wait_all();  // (after a timeout) no query copy may land in a finished CTA's memory
   }
   tc::fence_before_sync();
   __syncthreads();
