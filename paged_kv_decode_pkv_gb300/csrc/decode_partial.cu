@@ -61,6 +61,7 @@ constexpr int kMetaEmpty = 1 << 8;
 constexpr int kMetaNew = 1 << 9;     // one-launch mode: the stage also carries the new token's k and v
 constexpr int kMetaPatch = 1 << 10;  // one-launch mode: the page holds the new token (slot in bits 11..14)
 constexpr int kMetaSlotShift = 11;
+constexpr int kMetaValid2Shift = 9;  // int8 cache (never one-launch): valid slots of the stage's second page
 constexpr int kMetaChunkShift = 16;  // bits 16..31: chunks of the item's sequence
 
 // Stage metadata: sequence, chunk, KV head and (low half of gl's high bits) the first attended slot
@@ -103,8 +104,8 @@ __host__ __device__ inline Layout make_layout(int warps, int nstage, int head_di
                                               bool fused, bool windowed = false, bool q8 = false) {
   Layout L;
   const int n = warps * nstage;
-  // K and V of one page for one KV head (int8 cache: the two int8 blocks as stored)
-  L.stage_bytes = q8 ? 2 * int8_block_bytes(head_dim) : 64 * head_dim;
+  // K and V of one page for one KV head (int8 cache: the two int8 blocks as stored, of two pages)
+  L.stage_bytes = q8 ? 4 * int8_block_bytes(head_dim) : 64 * head_dim;
   L.ring_off = 0;
   L.qslot_bytes = (group * head_dim * 2 + (fused ? 8 * head_dim : 0) + 15) & ~15;
   L.q_off = L.ring_off + n * L.stage_bytes;
@@ -425,7 +426,6 @@ struct GroupMma {
   uint32_t qa[KS][2];
   float acc[NB][4];
   float m, l;
-  float vref;  // int8 cache: acc holds sum p * scale * code / vref (vref = the largest V scale so far)
   int lane, h, group;
 
   __device__ void init(int lane_, int group_) {
@@ -465,7 +465,6 @@ struct GroupMma {
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     m = -INFINITY;
     l = 0.f;
-    vref = 0.f;
   }
 
   // Store the rotated query rows (fused mode): q_out_rows points at head g*G of the query token.
@@ -498,7 +497,6 @@ struct GroupMma {
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
     m = -INFINITY;
     l = 0.f;
-    vref = 0.f;
   }
 
   __device__ void page(unsigned char* stage_ptr, int lo, int nvalid, float scale_log2) {
@@ -573,139 +571,6 @@ struct GroupMma {
     }
   }
 
-  // ---- int8 cache: the page computed from its codes, with no fp16 copy ----
-  // The dot products run over the head dimensions in a permuted order (the sums are the same): at
-  // k-step ks, lane (g, c) takes dimensions D/4 * c + 4 ks + {0, 1, 2, 3} for q and for the K codes,
-  // contiguous across the k-steps, so a lane reads its D/4 codes of a key row at once.  The 16
-  // slots are permuted too: the S columns of lane c are slots 4c .. 4c + 3, which is also the order
-  // of the P V contraction, so the V fragment of a dimension is four consecutive codes of the
-  // dim-major V block.  Codes become exact fp16 values ((code ^ 0x80) + 1024 - 1152).
-  __device__ static void codes_to_half(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x5342);
-    const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-    const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-    lo = *reinterpret_cast<const uint32_t*>(&x);
-    hi = *reinterpret_cast<const uint32_t*>(&y);
-  }
-
-  __device__ void begin8(const unsigned char* qslot) {
-    const int c = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      if (h < group) {
-        const uint2 w = *reinterpret_cast<const uint2*>(qslot + (h * D + (D / 4) * c + 4 * ks) * 2);
-        qa[ks][0] = w.x;
-        qa[ks][1] = w.y;
-      } else {
-        qa[ks][0] = 0u;
-        qa[ks][1] = 0u;
-      }
-    }
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-    m = -INFINITY;
-    l = 0.f;
-    vref = 0.f;
-  }
-
-  // stage: the page's K block (codes [16][D] slot-major, then 16 fp32 scales) and V block (codes
-  // [D][16] dim-major, then 16 fp32 scales) as stored.  K scales multiply the scores, V scales the
-  // probabilities (relative to vref, raised lazily), in fp32.  Codes of slots past the sequence end
-  // are finite and meet P = 0; their scales are masked.
-  __device__ void page8(const unsigned char* stage, int lo, int nvalid, float scale_log2) {
-    constexpr int kBlk = int8_block_bytes(D);
-    const unsigned char* kb = stage;
-    const unsigned char* vb = stage + kBlk;
-    const float* ksc = reinterpret_cast<const float*>(kb + 16 * D);
-    const float* vsc = reinterpret_cast<const float*>(vb + 16 * D);
-    const int g = lane >> 2, c = lane & 3;
-    // even and odd k-steps accumulate apart: four independent MMA chains instead of two
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      const int slot = 4 * (g >> 1) + (g & 1) + 2 * nb;  // the key row of S column g of this n-block
-      const unsigned char* row = kb + slot * D + (D / 4) * c;
-      uint32_t w[KS];
-      if constexpr (D == 96) {
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const uint2 v = *reinterpret_cast<const uint2*>(row + 8 * i);
-          w[2 * i] = v.x;
-          w[2 * i + 1] = v.y;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < KS / 4; ++i) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * i);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-      }
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t b0, b1;
-        codes_to_half(w[ks], b0, b1);
-        mma_16816((ks & 1) ? so[nb] : sc[nb], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nb][e] += so[nb][e];
-    }
-    const int s0 = 4 * c;  // this lane's slots s0 .. s0 + 3
-    float s[4] = {sc[0][0] * ksc[s0] * scale_log2, sc[0][1] * ksc[s0 + 1] * scale_log2,
-                  sc[1][0] * ksc[s0 + 2] * scale_log2, sc[1][1] * ksc[s0 + 3] * scale_log2};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = (s0 + i >= lo && s0 + i < nvalid) ? s[i] : -INFINITY;
-    float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    if (mx > m + kLazyRescale) {
-      const float alpha = exp2f(m - mx);
-      l *= alpha;
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        acc[nb][0] *= alpha;
-        acc[nb][1] *= alpha;
-      }
-      m = mx;
-    }
-    float e[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = exp2f(s[i] - m);
-    const float2 f01 = __half22float2(__floats2half2_rn(e[0], e[1]));
-    const float2 f23 = __half22float2(__floats2half2_rn(e[2], e[3]));
-    l += (f01.x + f01.y) + (f23.x + f23.y);
-    float v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (s0 + i >= lo && s0 + i < nvalid) ? vsc[s0 + i] : 0.f;
-    float vm = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 1));
-    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 2));
-    if (vm > vref * 128.f) {
-      const float alpha = vref / vm;
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        acc[nb][0] *= alpha;
-        acc[nb][1] *= alpha;
-      }
-      vref = vm;
-    }
-    const float inv = vref > 0.f ? 1.f / vref : 0.f;
-    const uint32_t pa0 = pack_half2(e[0] * (v[0] * inv), e[1] * (v[1] * inv));
-    const uint32_t pa2 = pack_half2(e[2] * (v[2] * inv), e[3] * (v[3] * inv));
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(vb + (8 * nb + g) * 16 + 4 * c);
-      uint32_t b0, b1;
-      codes_to_half(w, b0, b1);
-      mma_16816(acc[nb], pa0, 0u, pa2, 0u, b0, b1);
-    }
-  }
-
   __device__ bool finish(float* po, float* pl, long long head_row0, int S, int j) {
     float lt = l;
     lt += __shfl_xor_sync(kFull, lt, 1);
@@ -713,7 +578,7 @@ struct GroupMma {
     const bool any = __shfl_sync(kFull, lt, 0) > 0.f;  // every head row saw the same tokens
     if (!any) return false;
     if (h < group) {
-      const float inv = (vref > 0.f ? vref : 1.f) / lt;
+      const float inv = 1.f / lt;
       const long long row = head_row0 + h;
       float* dst = po + (row * S + j) * D + 2 * (lane & 3);
 #pragma unroll
@@ -730,7 +595,7 @@ struct GroupMma {
     lt += __shfl_xor_sync(kFull, lt, 2);
     if (h < group) {
       const bool any = lt > 0.f;
-      const float inv = any ? (vref > 0.f ? vref : 1.f) / lt : 0.f;
+      const float inv = any ? 1.f / lt : 0.f;
       const long long row = head_row0 + h;
       __half* dst = out + row * D + 2 * (lane & 3);
 #pragma unroll
@@ -738,6 +603,285 @@ struct GroupMma {
         *reinterpret_cast<__half2*>(dst + nb * 8) =
             __floats2half2_rn(any ? acc[nb][0] * inv : 0.f, any ? acc[nb][1] * inv : 0.f);
       if (lse_out != nullptr && (lane & 3) == 0) lse_out[row] = any ? (m + log2f(lt)) * kLn2 : -INFINITY;
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// int8 cache, every group size (G <= 8 query heads of one KV head): the page is computed from its
+// codes on the tensor cores with the slots, not the heads, as the 16 rows of each product, so no
+// row is padding:
+//   S^T = K q^T      rows = the page's 16 slots, columns = the G heads (8 wide), k = head dims
+//   O^T += V^T P^T   rows = 16 head dims per product, columns = the heads, k = the 16 slots
+// The head dimensions are taken in a permuted order (the sums are the same): at k-step ks, lane
+// (g, c) takes dimensions D/4 c + 4 ks + {0, 1, 2, 3} of q and of the K codes, so the four codes of
+// one 32-bit word are its A fragment pair.  The 16 slots are permuted too: row r of S^T is slot
+// sigma(r), r = 2c + e -> 4c + e and r = 8 + 2c + e -> 4c + 2 + e, which makes the P V fragment of a
+// dimension the word c (slots 4c .. 4c + 3) of the dim-major V block, and the transpose of S^T's
+// 8x8 halves (movmatrix) exactly the B fragments of P^T.  Codes become exact fp16 values
+// ((code ^ 0x80) + 1024 - 1152).  K scales multiply the scores and V scales the probabilities,
+// relative to a reference vref raised lazily (by 2^7) so that the scaled probabilities stay inside
+// fp16; the output is acc * vref / l.  A stage holds one or two pages of the item.
+template <int D>
+struct GroupQ8 {
+  static constexpr int KS = D / 16;  // k-steps of S^T (head dims)
+  static constexpr int MB = D / 16;  // 16-dim row blocks of O^T
+  static constexpr int kBlk = int8_block_bytes(D);
+  uint32_t qb[KS][2];  // B fragments of q^T: head g, dims D/4 c + 4 ks + {0, 1} and {2, 3}
+  float acc[MB][4];    // O^T: dims 16 i + g and 16 i + g + 8, heads 2c and 2c + 1
+  float m0, m1;        // running max (log2 domain) of heads 2c and 2c + 1
+  float l0, l1;        // this lane's share (its two slots of every page) of the row sums of those heads
+  float vref, vinv;
+  int lane, g, c, group;
+
+  __device__ void init(int lane_, int group_) {
+    lane = lane_;
+    g = lane >> 2;
+    c = lane & 3;
+    group = group_;
+  }
+
+  __device__ static void codes_to_half(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x5342);
+    const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&x);
+    hi = *reinterpret_cast<const uint32_t*>(&y);
+  }
+
+  __device__ void begin8(const unsigned char* qslot) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (g < group) {
+        const uint2 w = *reinterpret_cast<const uint2*>(qslot + (g * D + (D / 4) * c + 4 * ks) * 2);
+        qb[ks][0] = w.x;
+        qb[ks][1] = w.y;
+      } else {
+        qb[ks][0] = 0u;
+        qb[ks][1] = 0u;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < MB; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    // a finite floor: a fully masked page before the first attended slot gives exp2(-inf) = 0
+    m0 = m1 = -1e30f;
+    l0 = l1 = 0.f;
+    vref = 0.f;
+    vinv = 0.f;
+  }
+
+  // The D/4 codes of key row `row` this lane contracts: words w[ks] = dims D/4 c + 4 ks .. + 3.
+  __device__ void key_words(const unsigned char* kb, int row, uint32_t (&w)[KS]) const {
+    const unsigned char* src = kb + row * D + (D / 4) * c;
+    if constexpr (D == 96) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src + 8 * i);
+        w[2 * i] = v.x;
+        w[2 * i + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < KS / 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+    }
+  }
+
+  // NP pages of one stage: page 0 with valid slots [lo, nv0), page 1 (NP == 2) with [0, nv1).  Each
+  // page is the K block (codes [16][D] slot-major, then 16 fp32 scales) and the V block (codes
+  // [D][16] dim-major, then 16 fp32 scales) as stored.  Codes of masked slots are finite and meet
+  // P = 0; their scales are never used.
+  template <int NP>
+  __device__ void page8(const unsigned char* stage, int lo, int nv0, int nv1, float scale_log2) {
+    const int rA = 4 * (g >> 1) + (g & 1), rB = rA + 2;  // slots of S^T rows g and g + 8
+    float x[NP][4];   // scores (log2 domain): slot rA heads 2c, 2c+1; slot rB heads 2c, 2c+1
+    bool va[NP], vb[NP];
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const unsigned char* kb = stage + pg * 2 * kBlk;
+      uint32_t wa[KS], wb[KS];
+      key_words(kb, rA, wa);
+      key_words(kb, rB, wb);
+      // even and odd k-steps accumulate apart: two independent MMA chains
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        codes_to_half(wa[ks], a0, a2);
+        codes_to_half(wb[ks], a1, a3);
+        mma_16816_nv((ks & 1) ? s1 : s0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+      const int first = pg == 0 ? lo : 0, nv = pg == 0 ? nv0 : nv1;
+      va[pg] = rA >= first && rA < nv;
+      vb[pg] = rB >= first && rB < nv;
+      const float* ksc = reinterpret_cast<const float*>(kb + 16 * D);
+      const float fa = ksc[rA] * scale_log2, fb = ksc[rB] * scale_log2;
+      x[pg][0] = va[pg] ? (s0[0] + s1[0]) * fa : -INFINITY;
+      x[pg][1] = va[pg] ? (s0[1] + s1[1]) * fa : -INFINITY;
+      x[pg][2] = vb[pg] ? (s0[2] + s1[2]) * fb : -INFINITY;
+      x[pg][3] = vb[pg] ? (s0[3] + s1[3]) * fb : -INFINITY;
+    }
+    // Raise a head's running max (and rescale) only when one of its scores exceeds it by more than
+    // 2^8; the common case costs one vote.
+    bool need = false;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg)
+      need |= fmaxf(x[pg][0], x[pg][2]) > m0 + kLazyRescale || fmaxf(x[pg][1], x[pg][3]) > m1 + kLazyRescale;
+    if (__any_sync(kFull, need)) {
+      float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+      for (int pg = 1; pg < NP; ++pg) {
+        mx0 = fmaxf(mx0, fmaxf(x[pg][0], x[pg][2]));
+        mx1 = fmaxf(mx1, fmaxf(x[pg][1], x[pg][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {  // over the slots (g); lanes of one c hold the same heads
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+      }
+      float a0 = 1.f, a1 = 1.f;
+      if (mx0 > m0 + kLazyRescale) {
+        a0 = exp2f(m0 - mx0);
+        m0 = mx0;
+      }
+      if (mx1 > m1 + kLazyRescale) {
+        a1 = exp2f(m1 - mx1);
+        m1 = mx1;
+      }
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int i = 0; i < MB; ++i) {
+        acc[i][0] *= a0;
+        acc[i][2] *= a0;
+        acc[i][1] *= a1;
+        acc[i][3] *= a1;
+      }
+    }
+    float e[NP][4];
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      e[pg][0] = exp2f(x[pg][0] - m0);
+      e[pg][1] = exp2f(x[pg][1] - m1);
+      e[pg][2] = exp2f(x[pg][2] - m0);
+      e[pg][3] = exp2f(x[pg][3] - m1);
+      // the row sums add the fp16-rounded probabilities
+      const float2 fa = __half22float2(__floats2half2_rn(e[pg][0], e[pg][1]));
+      const float2 fb = __half22float2(__floats2half2_rn(e[pg][2], e[pg][3]));
+      l0 += fa.x + fb.x;
+      l1 += fa.y + fb.y;
+    }
+    // V scales of this lane's slots (0 where masked); the reference rises when one exceeds 2^7 vref
+    float v[NP][2];
+    bool vneed = false;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const float* vsc = reinterpret_cast<const float*>(stage + pg * 2 * kBlk + kBlk + 16 * D);
+      v[pg][0] = va[pg] ? vsc[rA] : 0.f;
+      v[pg][1] = vb[pg] ? vsc[rB] : 0.f;
+      vneed |= fmaxf(v[pg][0], v[pg][1]) > vref * 128.f;
+    }
+    if (__any_sync(kFull, vneed)) {
+      float vm = fmaxf(v[0][0], v[0][1]);
+#pragma unroll
+      for (int pg = 1; pg < NP; ++pg) vm = fmaxf(vm, fmaxf(v[pg][0], v[pg][1]));
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, o));
+      if (vm > vref * 128.f) {  // the same answer on every lane (slots depend on g only)
+        const float alpha = vref / vm;
+#pragma unroll
+        for (int i = 0; i < MB; ++i) {
+          acc[i][0] *= alpha;
+          acc[i][1] *= alpha;
+          acc[i][2] *= alpha;
+          acc[i][3] *= alpha;
+        }
+        vref = vm;
+        vinv = 1.f / vm;
+      }
+    }
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const float wa = v[pg][0] * vinv, wb = v[pg][1] * vinv;
+      // P^T fragments: the 8x8 halves of P (slot rows, head columns) transposed
+      const uint32_t b0 = movmatrix_trans(pack_half2(e[pg][0] * wa, e[pg][1] * wa));
+      const uint32_t b1 = movmatrix_trans(pack_half2(e[pg][2] * wb, e[pg][3] * wb));
+      const unsigned char* vblk = stage + pg * 2 * kBlk + kBlk;
+#pragma unroll
+      for (int i = 0; i < MB; ++i) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vblk + (16 * i + g) * 16 + 4 * c);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vblk + (16 * i + g + 8) * 16 + 4 * c);
+        uint32_t a0, a1, a2, a3;
+        codes_to_half(w0, a0, a2);
+        codes_to_half(w1, a1, a3);
+        mma_16816_nv(acc[i], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+
+  // Row sums of heads 2c and 2c + 1 over the warp's slots (every lane of a c holds the totals).
+  __device__ void row_sums(float& t0, float& t1) const {
+    t0 = l0;
+    t1 = l1;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      t0 += __shfl_xor_sync(kFull, t0, o);
+      t1 += __shfl_xor_sync(kFull, t1, o);
+    }
+  }
+
+  __device__ bool finish(float* po, float* pl, long long head_row0, int S, int j) {
+    float t0, t1;
+    row_sums(t0, t1);
+    const bool any = __shfl_sync(kFull, t0, 0) > 0.f;  // every head saw the same slots
+    if (!any) return false;
+    const float sc = vref > 0.f ? vref : 1.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * c + e;
+      if (h < group) {
+        const float lt = e ? t1 : t0;
+        const float inv = sc / lt;
+        const long long row = head_row0 + h;
+        float* dst = po + (row * S + j) * D + g;
+#pragma unroll
+        for (int i = 0; i < MB; ++i) {
+          dst[16 * i] = acc[i][e] * inv;
+          dst[16 * i + 8] = acc[i][2 + e] * inv;
+        }
+        if (g == 0) pl[row * S + j] = ((e ? m1 : m0) + log2f(lt)) * kLn2;
+      }
+    }
+    return true;
+  }
+
+  __device__ void finish_out(__half* out, float* lse_out, long long head_row0) {
+    float t0, t1;
+    row_sums(t0, t1);
+    const float sc = vref > 0.f ? vref : 1.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * c + e;
+      if (h < group) {
+        const float lt = e ? t1 : t0;
+        const bool any = lt > 0.f;
+        const float inv = any ? sc / lt : 0.f;
+        const long long row = head_row0 + h;
+        __half* dst = out + row * D + g;
+#pragma unroll
+        for (int i = 0; i < MB; ++i) {
+          dst[16 * i] = __float2half_rn(any ? acc[i][e] * inv : 0.f);
+          dst[16 * i + 8] = __float2half_rn(any ? acc[i][2 + e] * inv : 0.f);
+        }
+        if (lse_out != nullptr && g == 0) lse_out[row] = any ? ((e ? m1 : m0) + log2f(lt)) * kLn2 : -INFINITY;
+      }
     }
   }
 };
@@ -1122,8 +1266,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       mbar_arrive_if(lane == 0, &bar[k]);
       cur.active = false;
     } else {
-      const bool first = cur.pnext == cur.p0, lastp = cur.pnext + 1 == cur.p1;
-      if (cur.pnext - cur.win_base >= 32) {
+      // int8 cache: a stage takes two consecutive pages of the item when it has them
+      const bool pair = Q8 && cur.pnext + 1 < cur.p1;
+      const bool first = cur.pnext == cur.p0, lastp = cur.pnext + (pair ? 2 : 1) >= cur.p1;
+      if (cur.pnext - cur.win_base >= (Q8 ? 31 : 32)) {
         cur.win_base = cur.pnext;
         const int idx = cur.pnext + lane;
         cur.window = idx < cur.p1 ? p.page_indices[cur.first + idx] : 0;
@@ -1134,6 +1280,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       const bool lastchunk = cur.j == cur.nch - 1;
       mt.flags = nvalid | (first ? kMetaFirst : 0) | (lastp ? kMetaLast : 0) | (lastchunk ? kMetaLastChunk : 0) |
                  (cur.nch << kMetaChunkShift);
+      int pid2 = 0;
+      bool page2_ok = false;
+      if constexpr (Q8) {
+        pid2 = __shfl_sync(kFull, cur.window, (cur.pnext + 1 - cur.win_base) & 31);
+        page2_ok = pair && pid2 >= 0 && pid2 < p.num_pages;
+        const int nvalid2 = page2_ok ? ((cur.pnext + 1 == cur.n - 1) ? cur.last : kPageSize) : 0;
+        mt.flags |= nvalid2 << kMetaValid2Shift;
+        if (pair && !page2_ok && lane == 0) atomicOr(p.status, kFlagBadPage);
+      }
       if constexpr (FUSED) {
         // The first stage also brings the new token's raw k and v; the consumer patches the page
         // that holds the token in shared memory (the copy of that slot from the pool is stale).
@@ -1149,8 +1304,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       const bool l0 = lane == 0;
       if (cur.pnext == 0) mt.gl |= cur.lo << 16;  // a window's first attended slot
       st_shared_v4_if(l0, &meta[k], mt.s, mt.j, mt.gl, mt.flags);
-      const uint32_t bytes = (page_ok ? page_bytes : 0u) + (first ? q_bytes + cs_bytes : 0u) +
-                             ((mt.flags & kMetaNew) ? kv_bytes : 0u);
+      const uint32_t bytes = (page_ok ? page_bytes : 0u) + (page2_ok ? page_bytes : 0u) +
+                             (first ? q_bytes + cs_bytes : 0u) + ((mt.flags & kMetaNew) ? kv_bytes : 0u);
       mbar_arrive_expect_tx_if(l0 && bytes != 0u, &bar[k], bytes);
       mbar_arrive_if(l0 && bytes == 0u, &bar[k]);
       if (first) {
@@ -1183,6 +1338,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         const unsigned char* kb = p.pool8 + (((long long)pid * 2) * p.hkv + cur.g) * kBlk;
         bulk_load_hint_if(l0 && page_ok, dst, kb, kBlk, &bar[k], policy);
         bulk_load_hint_if(l0 && page_ok, dst + kBlk, kb + (long long)p.hkv * kBlk, kBlk, &bar[k], policy);
+        const unsigned char* kb2 = p.pool8 + (((long long)pid2 * 2) * p.hkv + cur.g) * kBlk;
+        bulk_load_hint_if(l0 && page2_ok, dst + 2 * kBlk, kb2, kBlk, &bar[k], policy);
+        bulk_load_hint_if(l0 && page2_ok, dst + 3 * kBlk, kb2 + (long long)p.hkv * kBlk, kBlk, &bar[k], policy);
       } else if constexpr (MMA) {
         constexpr int E = GroupMma<D>::E;
 #pragma unroll
@@ -1196,7 +1354,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         bulk_load_hint_if(l0 && page_ok, dst + page_bytes / 2, kb + (long long)p.hkv * kPageSize * D, page_bytes / 2,
                           &bar[k], policy);
       }
-      ++cur.pnext;
+      cur.pnext += pair ? 2 : 1;
       if (lastp) cur.active = false;
     }
     ++issued;
@@ -1204,7 +1362,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     return true;
   };
 
-  using Compute = typename std::conditional<MMA, GroupMma<D>, GroupOne<D>>::type;
+  using Compute = typename std::conditional<Q8, GroupQ8<D>,
+                                            typename std::conditional<MMA, GroupMma<D>, GroupOne<D>>::type>::type;
   Compute cmp;
   if constexpr (MMA) {
     cmp.init(lane, p.group);
@@ -1441,7 +1600,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
             apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
         if constexpr (Q8) {
-          if (nvalid > 0) cmp.page8(s1, mt.lo(), nvalid, p.scale_log2);
+          const int nvalid2 = (mt.flags >> kMetaValid2Shift) & kMetaValid;
+          if (nvalid2 > 0) {
+            cmp.template page8<2>(s1, mt.lo(), nvalid, nvalid2, p.scale_log2);
+          } else if (nvalid > 0) {
+            cmp.template page8<1>(s1, mt.lo(), nvalid, 0, p.scale_log2);
+          }
         } else {
           if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
         }
