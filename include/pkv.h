@@ -79,7 +79,8 @@ typedef enum {
                                int8 KV behind a flag; the format is this library's reading): each
                                layer's pool is uint8 blocks
                                [num_pages][2][Hkv][16 * head_dim + 64] holding the 16 slots' int8
-                               codes, then their fp32 scales [16]: K codes slot-major
+                               codes, each stored as the byte code + 128, then their fp32 scales
+                               [16]: K codes slot-major
                                [16][head_dim], V codes dim-major [head_dim][16].  The append
                                quantizes each new K row (after RoPE and its fp16 rounding) and V row:
                                s = max|x| / 127 (fp32), code = clamp(rint(x / s), -127, 127) (fp32);

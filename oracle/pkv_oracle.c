@@ -218,8 +218,9 @@ int orc_append(const orc_geom* g, const uint16_t* q, const uint16_t* k, const ui
 /* int8 KV pages (Zero TVM Documentation, "The memory-bandwidth ceiling": int8 KV is exposed
  * behind a flag; the format is this library's reading).
  * Layout per layer: uint8 pool8[num_pages][2][Hkv][16 * d + 64]: a block holds the 16 slots'
- * int8 codes and then their fp32 scales [16]; the codes of a K block are slot-major [16][d], those
- * of a V block dim-major [d][16] (the 16 slots of one dimension together).
+ * int8 codes, each stored as the unsigned byte code + 128 (offset binary), and then their fp32
+ * scales [16]; the codes of a K block are slot-major [16][d], those of a V block dim-major [d][16]
+ * (the 16 slots of one dimension together).
  * Row quantizer (one row = one token, one KV head, K or V, of d fp16 values x_i; K after RoPE and
  * its fp16 rounding, as the fp16 cache stores it): amax = max |x_i|; s = fp32(amax / 127) (fp32
  * division, nearest); code_i = clamp(rint_even(fp32(x_i / s)), -127, 127); amax = 0 gives s = 0 and
@@ -239,7 +240,7 @@ static void store_row8(uint8_t* blk, int d, int kv, int slot, const uint16_t* ro
   int8_t codes[256];
   float sc;
   orc_quantize_row(row, d, codes, &sc);
-  for (int i = 0; i < d; ++i) ((int8_t*)blk)[code8(d, kv, slot, i)] = codes[i];
+  for (int i = 0; i < d; ++i) blk[code8(d, kv, slot, i)] = (uint8_t)(codes[i] + 128);
   memcpy(blk + 16 * d + 4 * slot, &sc, 4);
 }
 
@@ -313,7 +314,7 @@ void orc_dequantize_pool(const orc_geom* g, const uint8_t* pool8, double* out) {
           float sc;
           memcpy(&sc, blk + 16 * d + 4 * slot, 4);
           for (int i = 0; i < d; ++i)
-            out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)] * (double)sc;
+            out[pool_row(g, page, kv, h, slot) + i] = (double)((int)blk[code8(d, kv, slot, i)] - 128) * (double)sc;
         }
       }
 }

@@ -157,10 +157,11 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream, bool pdl) 
 
 // ------------------------------------------------------------------------------------------------
 // The append into an int8 cache (PKV_OPT_INT8_KV).  Layout per layer: uint8 blocks
-// [num_pages][2][Hkv][16 * d + 64], a block holding the 16 slots' int8 codes and then their fp32
-// scales [16]; K codes are slot-major [16][d], V codes dim-major [d][16] (the layouts the decode's
-// tensor-core fragments read four codes at a time from).  Row quantizer: amax = max |x_i| of the row's fp16 values (K after RoPE and its
-// fp16 rounding, as the fp16 cache stores it; V as given), s = amax / 127 (fp32 division),
+// [num_pages][2][Hkv][16 * d + 64], a block holding the 16 slots' int8 codes, each stored as the
+// byte code + 128, and then their fp32 scales [16]; K codes are slot-major [16][d], V codes
+// dim-major [d][16] (the layouts the decode's tensor-core fragments read four codes at a time
+// from).  Row quantizer: amax = max |x_i| of the row's fp16 values (K after RoPE and its fp16
+// rounding, as the fp16 cache stores it; V as given), s = amax / 127 (fp32 division),
 // code_i = clamp(rint_even(x_i / s), -127, 127) (fp32 division), amax = 0 giving s = 0 and codes 0.
 // One warp per (token, row): Hq query rows (rotated to q_out, fp16), Hkv K rows, Hkv V rows.
 
@@ -254,21 +255,21 @@ __global__ void __launch_bounds__(kQ8Warps * 32) append_rope_q8_kernel(AppendPar
   const int kv = is_k ? 0 : 1;
   unsigned char* blk = p.pool8 + ((blk_page * 2 + kv) * p.hkv + head) * (long long)(16 * D + 64);
   const int slot = pos & 15;
-  auto code = [&](__half h) -> signed char {
-    if (s == 0.f) return 0;
+  auto code = [&](__half h) -> unsigned char {  // the stored byte: code + 128
+    if (s == 0.f) return 128;
     const float q = rintf(__half2float(h) / s);
-    return (signed char)fminf(127.f, fmaxf(-127.f, q));
+    return (unsigned char)(128 + (int)fminf(127.f, fmaxf(-127.f, q)));
   };
 #pragma unroll
   for (int u = 0; u < kPairs; ++u) {
     const int j = lane + 32 * u;
     if (j < D / 2) {
       if (is_k) {
-        blk[slot * D + j] = (unsigned char)code(lo_v[u]);
-        blk[slot * D + j + D / 2] = (unsigned char)code(hi_v[u]);
+        blk[slot * D + j] = code(lo_v[u]);
+        blk[slot * D + j + D / 2] = code(hi_v[u]);
       } else {
-        blk[j * 16 + slot] = (unsigned char)code(lo_v[u]);
-        blk[(j + D / 2) * 16 + slot] = (unsigned char)code(hi_v[u]);
+        blk[j * 16 + slot] = code(lo_v[u]);
+        blk[(j + D / 2) * 16 + slot] = code(hi_v[u]);
       }
     }
   }

@@ -618,8 +618,8 @@ struct GroupMma {
 // one 32-bit word are its A fragment pair.  The 16 slots are permuted too: row r of S^T is slot
 // sigma(r), r = 2c + e -> 4c + e and r = 8 + 2c + e -> 4c + 2 + e, which makes the P V fragment of a
 // dimension the word c (slots 4c .. 4c + 3) of the dim-major V block, and the transpose of S^T's
-// 8x8 halves (movmatrix) exactly the B fragments of P^T.  Codes become exact fp16 values
-// ((code ^ 0x80) + 1024 - 1152).  K scales multiply the scores and V scales the probabilities,
+// 8x8 halves (movmatrix) exactly the B fragments of P^T.  A stored byte (code + 128) placed in the
+// mantissa of 1024 is the exact fp16 value 1152 + code, from which 1152 is subtracted.  K scales multiply the scores and V scales the probabilities,
 // relative to a reference vref raised lazily (by 2^7) so that the scaled probabilities stay inside
 // fp16; the output is acc * vref / l.  A stage holds one or two pages of the item.
 template <int D>
@@ -641,10 +641,10 @@ struct GroupQ8 {
     group = group_;
   }
 
+  // Four stored bytes (codes + 128) -> their codes as fp16 pairs: bytes 0, 1 in lo, bytes 2, 3 in hi.
   __device__ static void codes_to_half(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
     const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140), b = __byte_perm(u, 0x64646464u, 0x5342);
+    const uint32_t a = __byte_perm(w, 0x64646464u, 0x5140), b = __byte_perm(w, 0x64646464u, 0x5342);
     const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
     const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
     lo = *reinterpret_cast<const uint32_t*>(&x);
@@ -1679,8 +1679,8 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
       sm_warps = w;
     }
   }
-  // The int8 cache's stages are half as large and its page computation is latency-bound: it runs
-  // the most warps the registers allow (8 per SM).
+  // The int8 cache's stages (two pages) are as large as the fp16 ones, and its page computation
+  // decides its speed: it runs the most warps the registers allow (8 per SM).
   if (q8) sm_warps = kMaxDecodeWarps;
   c.warps = sm_warps;
   c.ctas_per_sm = 1;

@@ -61,8 +61,8 @@ def test_int8_append_matches_oracle(name):
     assert int(H.ulp_distance(_bits(q_out).view(np.uint16), ref_q).max()) <= 1
     # V blocks bit for bit; K codes within one step and scales within the fp16 rounding of K
     assert np.array_equal(got8[:, 1], ref8[:, 1]), "V blocks"
-    kc_got = got8[:, 0, :, :16 * d].view(np.int8).astype(np.int32)
-    kc_ref = ref8[:, 0, :, :16 * d].view(np.int8).astype(np.int32)
+    kc_got = got8[:, 0, :, :16 * d].astype(np.int32)  # stored code + 128: differences are code differences
+    kc_ref = ref8[:, 0, :, :16 * d].astype(np.int32)
     assert int(np.abs(kc_got - kc_ref).max()) <= 1
     ks_got = got8[:, 0, :, 16 * d:].copy().view(np.float32)
     ks_ref = ref8[:, 0, :, 16 * d:].copy().view(np.float32)

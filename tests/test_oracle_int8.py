@@ -59,24 +59,35 @@ def _pool8_case(rng, lengths, hq, hkv, d):
             for kv in range(2):
                 for h in range(hkv):
                     codes, sc = oracle.quantize_row(pool[page, kv, h, t % 16])
+                    stored = _stored(codes)
                     if kv == 0:  # K codes slot-major [16][d]
-                        pool8[page, kv, h, (t % 16) * d:(t % 16 + 1) * d] = codes.view(np.uint8)
+                        pool8[page, kv, h, (t % 16) * d:(t % 16 + 1) * d] = stored
                     else:        # V codes dim-major [d][16]
-                        pool8[page, kv, h, t % 16:16 * d:16] = codes.view(np.uint8)
+                        pool8[page, kv, h, t % 16:16 * d:16] = stored
                     pool8[page, kv, h, 16 * d + 4 * (t % 16):16 * d + 4 * (t % 16) + 4] = \
                         np.array([sc], np.float32).view(np.uint8)
     return g, pool, pool8, q, pi, px, last
 
 
-def _row_codes(blk, kv, slot, d):
-    """The codes of one slot row in a block: K rows are contiguous, V rows a stride-16 column."""
+def _stored(codes):
+    """The bytes a block stores for int8 codes: code + 128 (offset binary)."""
+    return (codes.astype(np.int16) + 128).astype(np.uint8)
+
+
+def _row_bytes(blk, kv, slot, d):
+    """The stored bytes of one slot row in a block: K rows are contiguous, V rows a stride-16 column."""
     return blk[slot * d:(slot + 1) * d] if kv == 0 else blk[slot:16 * d:16]
 
 
+def _row_codes(blk, kv, slot, d):
+    """The codes of one slot row in a block, read back from their offset-binary bytes."""
+    return (_row_bytes(blk, kv, slot, d).astype(np.int16) - 128).astype(np.int8)
+
+
 def _dequant(pool8, d):
-    """Independent read of the block format: int8 codes (K blocks [16][d], V blocks [d][16]), then
-    fp32 scales [16]."""
-    raw = pool8[..., :16 * d].view(np.int8)
+    """Independent read of the block format: int8 codes stored as code + 128 (K blocks [16][d], V
+    blocks [d][16]), then fp32 scales [16]."""
+    raw = pool8[..., :16 * d].astype(np.int16) - 128
     k = raw[:, 0].reshape(raw.shape[0], raw.shape[2], 16, d)
     v = raw[:, 1].reshape(raw.shape[0], raw.shape[2], d, 16).transpose(0, 1, 3, 2)
     codes = np.stack([k, v], axis=1).astype(np.float64)
@@ -117,7 +128,7 @@ def test_append_int8_writes_the_quantized_rotated_rows():
             for h in range(hkv):
                 codes, sc = oracle.quantize_row(pool16[page, kv, h, slot])
                 blk = pool8[page, kv, h]
-                assert np.array_equal(_row_codes(blk, kv, slot, d).view(np.int8), codes)
+                assert np.array_equal(_row_codes(blk, kv, slot, d), codes)
                 assert blk[16 * d + 4 * slot:16 * d + 4 * slot + 4].view(np.float32)[0] == sc
     # nothing else was written
     touched = np.zeros(pool8.shape[:-1] + (16,), dtype=bool)
@@ -128,7 +139,7 @@ def test_append_int8_writes_the_quantized_rotated_rows():
             for h in range(hkv):
                 for slot in range(16):
                     if not touched[page, kv, h, slot]:
-                        assert np.all(_row_codes(pool8[page, kv, h], kv, slot, d) == 0x55)
+                        assert np.all(_row_bytes(pool8[page, kv, h], kv, slot, d) == 0x55)
 
 
 @pytest.mark.parametrize("window", [0, 20])
@@ -176,5 +187,5 @@ def test_quantize_pool_matches_the_row_quantizer():
                 for slot in range(16):
                     codes, sc = oracle.quantize_row(pool[page, kv, h, slot])
                     blk = pool8[page, kv, h]
-                    assert np.array_equal(_row_codes(blk, kv, slot, 16).view(np.int8), codes)
+                    assert np.array_equal(_row_codes(blk, kv, slot, 16), codes)
                     assert blk[256 + 4 * slot:256 + 4 * slot + 4].view(np.float32)[0] == sc or (np.isnan(sc))

@@ -37,8 +37,12 @@ MUTANTS = [
     ("prefill not causal", "window_start(p + 1, window), p + 1, page_indptr,", "window_start(p + 1, window), p + 2, page_indptr,"),
     ("int8 rounding truncates", "float q = nearbyintf((float)dec(x[i]) / s);", "float q = truncf((float)dec(x[i]) / s);"),
     ("int8 scale divisor", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
-    ("int8 scale offset", "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)] * (double)sc;",
-     "out[pool_row(g, page, kv, h, slot) + i] = (double)((const int8_t*)blk)[code8(d, kv, slot, i)];"),
+    ("int8 scale offset", "out[pool_row(g, page, kv, h, slot) + i] = (double)((int)blk[code8(d, kv, slot, i)] - 128) * (double)sc;",
+     "out[pool_row(g, page, kv, h, slot) + i] = (double)((int)blk[code8(d, kv, slot, i)] - 128);"),
+    ("int8 byte bias on read", "out[pool_row(g, page, kv, h, slot) + i] = (double)((int)blk[code8(d, kv, slot, i)] - 128) * (double)sc;",
+     "out[pool_row(g, page, kv, h, slot) + i] = (double)((int)blk[code8(d, kv, slot, i)] - 127) * (double)sc;"),
+    ("int8 byte stored without its bias", "blk[code8(d, kv, slot, i)] = (uint8_t)(codes[i] + 128);",
+     "blk[code8(d, kv, slot, i)] = (uint8_t)codes[i];"),
     ("int8 V block read slot-major",
      "static int64_t code8(int d, int kv, int slot, int i) { return kv == 0 ? (int64_t)slot * d + i : (int64_t)i * 16 + slot; }",
      "static int64_t code8(int d, int kv, int slot, int i) { return (int64_t)slot * d + i; }"),
