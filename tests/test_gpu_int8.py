@@ -132,3 +132,76 @@ def test_int8_step_entry_point_runs_append_then_merged_decode(name):
     torch.cuda.synchronize()
     assert np.array_equal(pool_a.cpu().numpy(), pool_b.cpu().numpy())
     assert np.array_equal(_bits(out_a), _bits(out_b)) and np.array_equal(_bits(lse_a), _bits(lse_b))
+
+
+@pytest.mark.parametrize("name", ["gqa2_d128_outliers", "ragged_d96", "gqa4_d64", "gqa8_d128", "tiny"])
+@pytest.mark.parametrize("window", [1, 17, 100])
+@pytest.mark.parametrize("with_sinks", [False, True])
+def test_int8_window_and_sinks_match_oracle(name, window, with_sinks):
+    """A windowed int8 layer (the first visible page may start inside a two-page stage's first page)
+    with and without sink logits: merged decode against the oracle over the GPU's own int8 pool."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    cfg = SMALL[name]
+    step = W.make_step(cfg)
+    g = H.geometry(step)
+    pool8 = torch.from_numpy(oracle.quantize_pool(g, W.host_pool(step, 0))).cuda()
+    rng = np.random.default_rng(300 + window)
+    sinks_host = (rng.standard_normal(cfg.hq) * 2).astype(np.float32) if with_sinks else None
+    sinks = torch.from_numpy(sinks_host).cuda() if with_sinks else None
+    cache = pkv.Cache(1, step.num_pages, cfg.hq, cfg.hkv, cfg.head_dim, step.max_position, cfg.theta,
+                      pools=[pool8], options=pkv.OPT_INT8_KV, windows=[window], sinks=[sinks])
+    tabs = H.device_tables(step)
+    q, k, v = H.device_qkv(step, 0)
+    q_out = cache.append_rope(0, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                              tabs["page_indices"])
+    counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")
+    out, lse = cache.decode_attention_merged(0, q_out, tabs["page_indptr"], tabs["page_indices"],
+                                             tabs["last_page_len"], step.max_pages_per_seq, counters,
+                                             q_indptr=tabs["q_indptr"], total_pages=int(step.page_indptr[-1]))
+    torch.cuda.synchronize()
+    assert cache.check_status() == (0, 0)
+    gq = _bits(q_out).view(np.uint16)[H.query_rows(step)]
+    ref_out, ref_lse = oracle.attention_int8(g, pool8.cpu().numpy(), gq, step.page_indptr, step.page_indices,
+                                             step.last_page_len, window=window,
+                                             sinks=None if sinks_host is None else sinks_host.astype(np.float64))
+    H.assert_close_out(_bits(out).view(np.uint16), ref_out)
+    H.assert_close_lse(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_int8_bad_page_in_a_stage_sets_status_and_masks_it(which):
+    """A page id out of range as the first (which = 0) or second (which = 1) page of a two-page
+    stage: the status word reports it, the page is masked out, the other sequences are unchanged."""
+    import torch
+
+    import paged_kv_decode_pkv_gb300 as pkv
+
+    step, g, host16, host8, pool8, cache = _setup("ragged_d96")
+    cfg = step.cfg
+    tabs = H.device_tables(step)
+    q, k, v = H.device_qkv(step, 0)
+    q_out = cache.append_rope(0, q, k, v, tabs["pos_map"], tabs["append_indptr"], tabs["page_indptr"],
+                              tabs["page_indices"])
+
+    def run(pages):
+        counters = torch.zeros(step.batch * cfg.hkv, dtype=torch.int32, device="cuda")
+        out, lse = cache.decode_attention_merged(0, q_out, tabs["page_indptr"], pages, tabs["last_page_len"],
+                                                 step.max_pages_per_seq, counters, q_indptr=tabs["q_indptr"],
+                                                 num_splits=1)
+        torch.cuda.synchronize()
+        return out, lse, cache.check_status()
+
+    good_out, good_lse, st = run(tabs["page_indices"])
+    assert st == (0, 0)
+    s = int(np.argmax(np.diff(step.page_indptr)))  # the longest sequence: one chunk, pages in pairs
+    assert int(step.page_indptr[s + 1] - step.page_indptr[s]) >= 4
+    bad = tabs["page_indices"].clone()
+    bad[int(step.page_indptr[s]) + 2 + which] = step.num_pages + 5
+    out, lse, (code, flags) = run(bad)
+    assert code == pkv.ERR_OUT_OF_RANGE and flags & pkv.FLAG_BAD_PAGE
+    others = [i for i in range(step.batch) if i != s]
+    assert np.array_equal(_bits(out)[others], _bits(good_out)[others])
+    assert np.all(np.isfinite(out.float().cpu().numpy()[s]))
