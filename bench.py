@@ -905,6 +905,8 @@ def measure_headline(args, cfg, world, rank, local, dev):
         "step_us_per_layer": step_ms * 1e3 / cfg.layers,
         "step": "per layer: pkv_append_decode_attention (" +
                 ("1 launch: append, split-K decode and merge)" if one_launch else
+                 "2 launches on an int8 cache: the quantizing append, then split-K decode with the merge)"
+                 if args.int8 else
                  "2 launches for chunked appends: append, then split-K decode with the merge)"),
         "two_kernels": {"value": world * kv_step / (step_two_ms * 1e-3) / 1e9, "ms_per_step": step_two_ms,
                         "step": "per layer: pkv_append_rope + pkv_decode_attention_merged"},
