@@ -84,8 +84,9 @@ typedef enum {
                                [16][head_dim], V codes dim-major [head_dim][16].  The append
                                quantizes each new K row (after RoPE and its fp16 rounding) and V row:
                                s = max|x| / 127 (fp32), code = clamp(rint(x / s), -127, 127) (fp32);
-                               attention runs on the exact codes (tensor cores, for any Hq / Hkv)
-                               and applies the scales in fp32 to the scores (K) and the
+                               attention runs on the exact codes (tensor cores when Hq / Hkv >= 2,
+                               CUDA cores for one query head per KV head, as for fp16 pages) and
+                               applies the scales in fp32 to the scores (K) and the
                                probabilities (V).  pkv_append_decode_attention runs as two
                                launches; pkv_prefill_attention and pkv_qkv_append_rope return
                                PKV_ERR_UNSUPPORTED. */

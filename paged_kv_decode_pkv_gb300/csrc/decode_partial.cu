@@ -80,10 +80,13 @@ constexpr int kSmemBudget = 232448 - 256;
 constexpr int kSmemPerSm = 233472;
 constexpr int kCtasPerSm = 2;
 
-// Alignment of the shared-memory base: 1024 bytes on the tensor-core path (its swizzled boxes; the
-// int8 cache always takes that path), 128 bytes on the CUDA-core path.  The kernel aligns its base
-// by the same rule and the layout reserves that much slack.
-__host__ __device__ constexpr bool uses_mma(int group, bool q8) { return group >= 2 || q8; }
+// Alignment of the shared-memory base: 1024 bytes on the tensor-core path (its swizzled boxes), 128
+// bytes on the CUDA-core path.  The kernel aligns its base by the same rule and the layout reserves
+// that much slack.
+__host__ __device__ constexpr bool uses_mma(int group, bool q8) {
+  (void)q8;  // an int8 cache takes the same path as an fp16 one: tensor cores for G >= 2
+  return group >= 2;
+}
 __host__ __device__ constexpr int smem_align(bool mma) { return mma ? 1024 : 128; }
 
 struct Layout {
@@ -410,6 +413,194 @@ struct GroupOne {
       for (int e = 0; e < DPL; ++e) dst[e] = __float2half_rn(any ? o[e] * inv : 0.f);
     }
     if (lse_out != nullptr && lane == 0) lse_out[row] = any ? (m + log2f(lt)) * kLn2 : -INFINITY;
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// int8 cache, one query head per KV head, on CUDA cores: GroupOne's arrangement over the codes.
+// q.k: a half-warp covers one key row, each lane D/16 dimensions; the lane's codes of the row (the
+// stored bytes, code + 128) become exact fp16 values (byte in the mantissa of 1024, minus 1152) and
+// meet the query in fp16 x fp16 -> fp32 fused multiply-adds; the transposing butterfly leaves each
+// lane one row's sum, which takes the row's K scale.  P V: each half-warp takes eight of the
+// page's slots, each lane D/16 dimensions, whose eight codes are one 8-byte run of the dim-major V
+// block; the probabilities carry the V scales relative to a lazily raised reference (as in the
+// tensor-core int8 form), and the two halves' sums are added at the end.  A stage holds one or two
+// pages of the item.
+template <int D>
+struct GroupOneQ8 : GroupOne<D> {
+  using Base = GroupOne<D>;
+  using Base::DPL;
+  using Base::HPL;
+  static constexpr int kBlk = int8_block_bytes(D);
+  float vref, vinv;
+
+  // Four stored bytes -> their codes as fp16 pairs: bytes 0, 1 in lo, bytes 2, 3 in hi.
+  __device__ static void codes_to_half(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const uint32_t a = __byte_perm(w, 0x64646464u, 0x5140), b = __byte_perm(w, 0x64646464u, 0x5342);
+    const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&x);
+    hi = *reinterpret_cast<const uint32_t*>(&y);
+  }
+
+  __device__ void begin8(const unsigned char* qslot) {
+    Base::load_row(qslot, this->li, this->q2);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) this->o[e] = 0.f;
+    this->m = -1e30f;  // a finite floor: a fully masked page gives exp2(-inf) = 0
+    this->l = 0.f;
+    vref = 0.f;
+    vinv = 0.f;
+  }
+
+  // The lane's D/16 codes of a key row as fp16 pairs.
+  __device__ void row_codes(const unsigned char* row, uint32_t (&x)[HPL]) const {
+    const unsigned char* src = row + this->li * DPL;
+    if constexpr (D == 128) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      codes_to_half(w.x, x[0], x[1]);
+      codes_to_half(w.y, x[2], x[3]);
+    } else if constexpr (D == 96) {
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(src);
+      const uint32_t w0 = (uint32_t)h[0] | ((uint32_t)h[1] << 16), w1 = (uint32_t)h[2];
+      uint32_t unused;
+      codes_to_half(w0, x[0], x[1]);
+      codes_to_half(w1, x[2], unused);
+    } else {
+      codes_to_half(*reinterpret_cast<const uint32_t*>(src), x[0], x[1]);
+    }
+  }
+
+  template <int NP>
+  __device__ void page8(const unsigned char* stage, int lo, int nv0, int nv1, float scale_log2) {
+    const int half = this->half, li = this->li;
+    this->scale_log2 = scale_log2;  // the butterfly's scaling of the row sums
+    // q.k partials of the lane's 8 rows of each page, then the rows' sums (log2 domain)
+    float acc[8 * NP];
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const unsigned char* kb = stage + pg * 2 * kBlk;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t x[HPL];
+        row_codes(kb + (2 * i + half) * D, x);
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < HPL; ++e) a = Base::fma2(this->q2[e], x[e], a);
+        acc[8 * pg + i] = a;
+      }
+    }
+    float sc[NP];
+    this->template reduce_rows<NP>(acc, sc);
+    const int row = 2 * ((li >> 1) & 7) + half;  // the row this lane holds
+    bool valid[NP];
+    float v[NP];
+    bool need = false, vneed = false;
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const unsigned char* kb = stage + pg * 2 * kBlk;
+      const float* ksc = reinterpret_cast<const float*>(kb + 16 * D);
+      const float* vsc = reinterpret_cast<const float*>(kb + kBlk + 16 * D);
+      valid[pg] = row >= (pg == 0 ? lo : 0) && row < (pg == 0 ? nv0 : nv1);
+      sc[pg] = valid[pg] ? sc[pg] * ksc[row] : -INFINITY;
+      v[pg] = valid[pg] ? vsc[row] : 0.f;
+      need |= sc[pg] > this->m + kLazyRescale;
+      vneed |= v[pg] > vref * 128.f;
+    }
+    // the running max, raised (with a rescale) only when a score exceeds it by more than 2^8
+    if (__any_sync(kFull, need)) {
+      float mx = sc[0];
+#pragma unroll
+      for (int pg = 1; pg < NP; ++pg) mx = fmaxf(mx, sc[pg]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      if (mx > this->m + kLazyRescale) {
+        const float alpha = exp2f(this->m - mx);
+        this->l *= alpha;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) this->o[e] *= alpha;
+        this->m = mx;
+      }
+    }
+    // the V-scale reference, raised only when a scale exceeds it by more than 2^7
+    if (__any_sync(kFull, vneed)) {
+      float vm = v[0];
+#pragma unroll
+      for (int pg = 1; pg < NP; ++pg) vm = fmaxf(vm, v[pg]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, off));
+      if (vm > vref * 128.f) {
+        const float alpha = vref / vm;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) this->o[e] *= alpha;
+        vref = vm;
+        vinv = 1.f / vm;
+      }
+    }
+#pragma unroll
+    for (int pg = 0; pg < NP; ++pg) {
+      const float ex = exp2f(sc[pg] - this->m);
+      // the row sum adds the fp16-rounded probability (each row sits in two lanes)
+      this->l += (li & 1) ? 0.f : __half2float(__float2half_rn(ex));
+      const uint32_t pbits = (uint32_t)__half_as_ushort(__float2half_rn(ex * (v[pg] * vinv)));
+      // this half-warp's slots 8 half + k come from the lanes holding those rows
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int s0 = 8 * half + 2 * k;  // slots s0 (even) and s0 + 1 (odd)
+        const uint32_t a = __shfl_sync(kFull, pbits, 2 * (s0 >> 1));
+        const uint32_t b = __shfl_sync(kFull, pbits, 16 + 2 * (s0 >> 1));
+        pk[k] = a | (b << 16);
+      }
+      const unsigned char* vb = stage + pg * 2 * kBlk + kBlk;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        const uint2 w = *reinterpret_cast<const uint2*>(vb + (li * DPL + e) * 16 + 8 * half);
+        uint32_t c01, c23, c45, c67;
+        codes_to_half(w.x, c01, c23);
+        codes_to_half(w.y, c45, c67);
+        float a = this->o[e];
+        a = Base::fma2(pk[0], c01, a);
+        a = Base::fma2(pk[1], c23, a);
+        a = Base::fma2(pk[2], c45, a);
+        a = Base::fma2(pk[3], c67, a);
+        this->o[e] = a;
+      }
+    }
+  }
+
+  __device__ bool finish(float* po, float* pl, long long row_base, int S, int j) {
+    float lt = this->l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFull, lt, off);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) this->o[e] += __shfl_xor_sync(kFull, this->o[e], 16);
+    if (!(lt > 0.f)) return false;
+    const float inv = (vref > 0.f ? vref : 1.f) / lt;
+    if (this->half == 0) {
+      float* dst = po + (row_base * S + j) * D + this->li * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) dst[e] = this->o[e] * inv;
+    }
+    if (this->lane == 0) pl[row_base * S + j] = (this->m + log2f(lt)) * kLn2;
+    return true;
+  }
+
+  __device__ void finish_out(__half* out, float* lse_out, long long row) {
+    float lt = this->l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFull, lt, off);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) this->o[e] += __shfl_xor_sync(kFull, this->o[e], 16);
+    const bool any = lt > 0.f;
+    const float inv = any ? (vref > 0.f ? vref : 1.f) / lt : 0.f;
+    if (this->half == 0) {
+      __half* dst = out + row * D + this->li * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) dst[e] = __float2half_rn(any ? this->o[e] * inv : 0.f);
+    }
+    if (lse_out != nullptr && this->lane == 0) lse_out[row] = any ? (this->m + log2f(lt)) * kLn2 : -INFINITY;
   }
 };
 
@@ -1362,8 +1553,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     return true;
   };
 
-  using Compute = typename std::conditional<Q8, GroupQ8<D>,
-                                            typename std::conditional<MMA, GroupMma<D>, GroupOne<D>>::type>::type;
+  using Compute = typename std::conditional<
+      Q8, typename std::conditional<MMA, GroupQ8<D>, GroupOneQ8<D>>::type,
+      typename std::conditional<MMA, GroupMma<D>, GroupOne<D>>::type>::type;
   Compute cmp;
   if constexpr (MMA) {
     cmp.init(lane, p.group);
@@ -1567,7 +1759,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       }
       const int nvalid = mt.flags & kMetaValid;
       unsigned char* s1 = stages + (size_t)k * L.stage_bytes;
-      if constexpr (!MMA) {
+      if constexpr (Q8) {
+        // an int8 stage holds one or two pages of the item (never the one-launch layout)
+        const int nvalid2 = (mt.flags >> kMetaValid2Shift) & kMetaValid;
+        if (nvalid2 > 0) {
+          cmp.template page8<2>(s1, mt.lo(), nvalid, nvalid2, p.scale_log2);
+        } else if (nvalid > 0) {
+          cmp.template page8<1>(s1, mt.lo(), nvalid, 0, p.scale_log2);
+        }
+      } else if constexpr (!MMA) {
         // two pages of the same item at once when the next one is already in flight
         int n2 = 0;
         unsigned char* s2 = s1;
@@ -1599,16 +1799,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           if (mt.flags & kMetaPatch)
             apply_patch<D, Compute>(s1, patch, (mt.flags >> kMetaSlotShift) & 15, meta_pid[k], mt.g(), p, lane);
         }
-        if constexpr (Q8) {
-          const int nvalid2 = (mt.flags >> kMetaValid2Shift) & kMetaValid;
-          if (nvalid2 > 0) {
-            cmp.template page8<2>(s1, mt.lo(), nvalid, nvalid2, p.scale_log2);
-          } else if (nvalid > 0) {
-            cmp.template page8<1>(s1, mt.lo(), nvalid, 0, p.scale_log2);
-          }
-        } else {
-          if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
-        }
+        if (nvalid > 0) cmp.page(s1, mt.lo(), nvalid, p.scale_log2);
       }
     }
     if (fin.flags & kMetaLast) finish_item(fin);
@@ -1636,12 +1827,12 @@ void* select_kernel_t(int head_dim, bool mma) {
 }
 
 void* select_kernel(int head_dim, bool mma, bool fused, bool q8) {
-  if (q8) {  // int8 cache: tensor-core path, separate launches only
-    if (!mma || fused) return nullptr;
+  if (q8) {  // int8 cache: separate launches only
+    if (fused) return nullptr;
     switch (head_dim) {
-      case 64: return kernel_ptr<64, true, false, true>();
-      case 96: return kernel_ptr<96, true, false, true>();
-      case 128: return kernel_ptr<128, true, false, true>();
+      case 64: return mma ? kernel_ptr<64, true, false, true>() : kernel_ptr<64, false, false, true>();
+      case 96: return mma ? kernel_ptr<96, true, false, true>() : kernel_ptr<96, false, false, true>();
+      case 128: return mma ? kernel_ptr<128, true, false, true>() : kernel_ptr<128, false, false, true>();
       default: return nullptr;
     }
   }
@@ -1664,7 +1855,7 @@ int cta_budget(int ctas) { return std::min(kSmemBudget, (kSmemPerSm - ctas * 102
 DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool windowed, bool q8) {
   DecodeConfig c;
   c.q8 = q8;
-  c.mma = uses_mma(group, q8);  // the int8 page computation is the tensor-core one (rows padded to 16)
+  c.mma = uses_mma(group, q8);
   c.fused = fused;
   // Warps per SM: the most stages in flight per SM (warps x ring depth) that fit the plain layout
   // in one CTA, on a tie the more warps (the CUDA-core path always runs 8 warps, the tensor-core
