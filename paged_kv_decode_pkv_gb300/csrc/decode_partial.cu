@@ -1276,7 +1276,7 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
 }
 
 template <int D, bool MMA, bool FUSED, bool Q8>
-__global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
+__global__ void __launch_bounds__((Q8 && !MMA) ? 384 : 256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
   // aligned (smem_align) by an offset from the shared array itself, so that every access below is
   // compiled as a shared-memory access
@@ -1874,18 +1874,25 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
     }
   }
   // The int8 cache's stages (two pages) are as large as the fp16 ones, and its page computation
-  // decides its speed: it runs the most warps the registers allow (8 per SM).
+  // decides its speed: it runs the most warps the registers allow, 8 per SM on the tensor-core path
+  // and 12 (at most 168 registers) on the CUDA-core path, when there are enough sequences; with
+  // few, more warps only cut the segments into more pieces, whose merge ends the launch (measured
+  // on the CUDA-core path: ragged batch of 64, 232 -> 191 us per layer with 12 warps; single
+  // stream, 15.4 -> 18.9 us).
   if (q8) sm_warps = kMaxDecodeWarps;
+  const bool q8_wide = q8 && !c.mma && batch >= kQ8WideBatch;
+  if (q8_wide) sm_warps = kQ8WideWarps;
   c.warps = sm_warps;
   c.ctas_per_sm = 1;
   c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget, q8);
   // The SM's warps split over kCtasPerSm CTAs when the ring stays as deep: a CTA that is still
   // merging at the end of a launch then holds only its share of the SM, and the next launch's CTAs
-  // start (and run their prologue) in the rest.
+  // start (and run their prologue) in the rest.  The wide int8 layout always splits (two stages of
+  // two pages per warp still keep 150 KB per SM in flight).
   if (kCtasPerSm > 1 && sm_warps % kCtasPerSm == 0) {
     const int w = sm_warps / kCtasPerSm;
     const int n = ring_depth(w, head_dim, group, batch, fused, windowed, cta_budget(kCtasPerSm), q8);
-    if (n >= c.nstage && n >= 2) {
+    if ((n >= c.nstage || q8_wide) && n >= 2) {
       c.warps = w;
       c.ctas_per_sm = kCtasPerSm;
       c.nstage = n;

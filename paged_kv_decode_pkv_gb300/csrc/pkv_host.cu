@@ -108,10 +108,12 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
   // equal run of (sequence, KV head, page) units; a segment of n pages meets at most
   // ceil(n * W / U) + 1 runs.
   // The bound takes the most warps any decode launch runs (the one-launch layout may run more warps
-  // per CTA than the plain one), so one plan serves every entry point.
+  // per CTA than the plain one; an int8 cache may run 12 per SM), so one plan serves every entry
+  // point.
   if (total_pages > 0) {
     const long long U = (long long)total_pages * c->desc.num_kv_heads;
-    const long long W = std::min((long long)c->num_sms * pkv::kMaxDecodeWarps, U);
+    const int sm_warps = c->int8 ? std::max(pkv::kMaxDecodeWarps, pkv::kQ8WideWarps) : pkv::kMaxDecodeWarps;
+    const long long W = std::min((long long)c->num_sms * sm_warps, U);
     const long long s_bal = ((long long)max_pages * W + U - 1) / U + 1;
     if (U < 0x7fffffffLL && s_bal <= max_splits) {
       *splits = (int)s_bal;
