@@ -454,8 +454,10 @@ const char* pkv_status_string(pkv_status status);
 const char* pkv_last_error(void);
 
 /* Number of streaming multiprocessors of the cache's device and the resident warps the decode
- * kernel uses per SM (what the planner fills). */
-pkv_status pkv_device_info(const pkv_cache* cache, int* num_sms, int* decode_warps_per_sm);
+ * kernel uses per SM for a batch of `batch` sequences (the page-balanced partition cuts the work
+ * into num_sms * decode_warps_per_sm runs; the CUDA-core path runs more warps for large batches).
+ * PKV_ERR_INVALID_ARG for a null cache or batch < 1. */
+pkv_status pkv_device_info(const pkv_cache* cache, int batch, int* num_sms, int* decode_warps_per_sm);
 
 #ifdef __cplusplus
 }

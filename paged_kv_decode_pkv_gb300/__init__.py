@@ -68,7 +68,7 @@ def lib():
         L.pkv_destroy.restype = None
         L.pkv_destroy.argtypes = [P]
         L.pkv_device_info.restype = i
-        L.pkv_device_info.argtypes = [P, ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.pkv_device_info.argtypes = [P, i, ctypes.POINTER(i), ctypes.POINTER(i)]
         L.pkv_append_rope.restype = i
         L.pkv_append_rope.argtypes = [P, i, P, P, P, P, P, i, i, P, P, P, P]
         L.pkv_plan_decode.restype = i
@@ -210,9 +210,10 @@ class Cache:
 
     # -- entry points ---------------------------------------------------------------------------
 
-    def device_info(self):
+    def device_info(self, batch=1):
+        """pkv_device_info: (SMs, decode warps per SM for a batch of ``batch`` sequences)."""
         n, w = ctypes.c_int(), ctypes.c_int()
-        _check(lib().pkv_device_info(self.handle, ctypes.byref(n), ctypes.byref(w)), "pkv_device_info")
+        _check(lib().pkv_device_info(self.handle, int(batch), ctypes.byref(n), ctypes.byref(w)), "pkv_device_info")
         return n.value, w.value
 
     def append_rope(self, layer, q, k, v, pos_map, append_indptr, page_indptr, page_indices, q_out=None,

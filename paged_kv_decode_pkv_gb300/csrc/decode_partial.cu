@@ -1275,8 +1275,8 @@ __device__ __forceinline__ void activate_item(Item& it, const DecodeParams& p, i
   }
 }
 
-template <int D, bool MMA, bool FUSED, bool Q8>
-__global__ void __launch_bounds__((Q8 && !MMA) ? 384 : 256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
+template <int D, bool MMA, bool FUSED, bool Q8, bool WIDE>
+__global__ void __launch_bounds__(WIDE ? 384 : 256, 1) decode_kernel(const __grid_constant__ CUtensorMap map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
   // aligned (smem_align) by an offset from the shared array itself, so that every access below is
   // compiled as a shared-memory access
@@ -1811,32 +1811,32 @@ __global__ void __launch_bounds__((Q8 && !MMA) ? 384 : 256, 1) decode_kernel(con
   }
 }
 
-template <int D, bool MMA, bool FUSED, bool Q8 = false>
+template <int D, bool MMA, bool FUSED, bool Q8, bool WIDE = false>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&decode_kernel<D, MMA, FUSED, Q8>);
+  return reinterpret_cast<void*>(&decode_kernel<D, MMA, FUSED, Q8, WIDE>);
 }
 
-template <bool FUSED>
-void* select_kernel_t(int head_dim, bool mma) {
+// The kernel of a head dim and layout: the tensor-core path, or the CUDA-core path in its 8-warp
+// or its wide (12-warp, at most 168 registers) form; int8 caches run separate launches only.
+template <int D, bool FUSED, bool Q8>
+void* select_kernel_d(bool mma, bool wide) {
+  if (mma) return kernel_ptr<D, true, FUSED, Q8>();
+  return wide ? kernel_ptr<D, false, FUSED, Q8, true>() : kernel_ptr<D, false, FUSED, Q8>();
+}
+
+template <bool FUSED, bool Q8>
+void* select_kernel_t(int head_dim, bool mma, bool wide) {
   switch (head_dim) {
-    case 64: return mma ? kernel_ptr<64, true, FUSED>() : kernel_ptr<64, false, FUSED>();
-    case 96: return mma ? kernel_ptr<96, true, FUSED>() : kernel_ptr<96, false, FUSED>();
-    case 128: return mma ? kernel_ptr<128, true, FUSED>() : kernel_ptr<128, false, FUSED>();
+    case 64: return select_kernel_d<64, FUSED, Q8>(mma, wide);
+    case 96: return select_kernel_d<96, FUSED, Q8>(mma, wide);
+    case 128: return select_kernel_d<128, FUSED, Q8>(mma, wide);
     default: return nullptr;
   }
 }
 
-void* select_kernel(int head_dim, bool mma, bool fused, bool q8) {
-  if (q8) {  // int8 cache: separate launches only
-    if (fused) return nullptr;
-    switch (head_dim) {
-      case 64: return mma ? kernel_ptr<64, true, false, true>() : kernel_ptr<64, false, false, true>();
-      case 96: return mma ? kernel_ptr<96, true, false, true>() : kernel_ptr<96, false, false, true>();
-      case 128: return mma ? kernel_ptr<128, true, false, true>() : kernel_ptr<128, false, false, true>();
-      default: return nullptr;
-    }
-  }
-  return fused ? select_kernel_t<true>(head_dim, mma) : select_kernel_t<false>(head_dim, mma);
+void* select_kernel(int head_dim, bool mma, bool fused, bool q8, bool wide) {
+  if (q8) return fused ? nullptr : select_kernel_t<false, true>(head_dim, mma, wide);
+  return fused ? select_kernel_t<true, false>(head_dim, mma, wide) : select_kernel_t<false, false>(head_dim, mma, wide);
 }
 
 }  // namespace
@@ -1874,25 +1874,26 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
     }
   }
   // The int8 cache's stages (two pages) are as large as the fp16 ones, and its page computation
-  // decides its speed: it runs the most warps the registers allow, 8 per SM on the tensor-core path
-  // and 12 (at most 168 registers) on the CUDA-core path, when there are enough sequences; with
-  // few, more warps only cut the segments into more pieces, whose merge ends the launch (measured
-  // on the CUDA-core path: ragged batch of 64, 232 -> 191 us per layer with 12 warps; single
-  // stream, 15.4 -> 18.9 us).
+  // decides its speed: it runs the most warps the registers allow (8 per SM on the tensor-core
+  // path).  The CUDA-core path (one query head per KV head, fp16 or int8 pages) runs 12 warps (at
+  // most 168 registers) when there are enough sequences; with few, more warps only cut the segments
+  // into more pieces, whose merge ends the launch.  Measured: ragged batch of 64, int8 232 -> 191
+  // and fp16 263.7 -> 255.4 us per layer with 12 warps; single stream (int8), 15.4 -> 18.9 us.
   if (q8) sm_warps = kMaxDecodeWarps;
-  const bool q8_wide = q8 && !c.mma && batch >= kQ8WideBatch;
-  if (q8_wide) sm_warps = kQ8WideWarps;
+  const bool wide = !c.mma && batch >= kWideBatch;
+  if (wide) sm_warps = kWideWarps;
+  c.wide = wide;
   c.warps = sm_warps;
   c.ctas_per_sm = 1;
   c.nstage = ring_depth(sm_warps, head_dim, group, batch, fused, windowed, kSmemBudget, q8);
   // The SM's warps split over kCtasPerSm CTAs when the ring stays as deep: a CTA that is still
   // merging at the end of a launch then holds only its share of the SM, and the next launch's CTAs
-  // start (and run their prologue) in the rest.  The wide int8 layout always splits (two stages of
-  // two pages per warp still keep 150 KB per SM in flight).
+  // start (and run their prologue) in the rest.  The wide layout always splits (two stages per warp
+  // still keep ~150 KB per SM in flight).
   if (kCtasPerSm > 1 && sm_warps % kCtasPerSm == 0) {
     const int w = sm_warps / kCtasPerSm;
     const int n = ring_depth(w, head_dim, group, batch, fused, windowed, cta_budget(kCtasPerSm), q8);
-    if ((n >= c.nstage || q8_wide) && n >= 2) {
+    if ((n >= c.nstage || wide) && n >= 2) {
       c.warps = w;
       c.ctas_per_sm = kCtasPerSm;
       c.nstage = n;
@@ -1909,16 +1910,21 @@ DecodeConfig decode_config(int group, int head_dim, int batch, bool fused, bool 
 }
 
 cudaError_t decode_prepare(const DecodeConfig& cfg, int head_dim) {
-  void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8);
-  if (k == nullptr) return cudaErrorInvalidValue;
-  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  // both forms of the CUDA-core kernel: the batch of a launch chooses between them
+  for (int w = 0; w < (cfg.mma ? 1 : 2); ++w) {
+    void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8, w == 1);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& map, const DecodeConfig& cfg, int head_dim,
                           int grid, cudaStream_t stream, bool pdl) {
-  void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8);
+  void* k = select_kernel(head_dim, cfg.mma, cfg.fused, cfg.q8, cfg.wide);
   if (k == nullptr || cfg.smem_bytes == 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);

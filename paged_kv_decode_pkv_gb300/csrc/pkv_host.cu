@@ -108,11 +108,11 @@ pkv_status plan(const pkv_cache* c, int batch, int max_pages, int total_pages, i
   // equal run of (sequence, KV head, page) units; a segment of n pages meets at most
   // ceil(n * W / U) + 1 runs.
   // The bound takes the most warps any decode launch runs (the one-launch layout may run more warps
-  // per CTA than the plain one; an int8 cache may run 12 per SM), so one plan serves every entry
-  // point.
+  // per CTA than the plain one; the CUDA-core layout runs 12 per SM for large batches), so one plan
+  // serves every entry point.
   if (total_pages > 0) {
     const long long U = (long long)total_pages * c->desc.num_kv_heads;
-    const int sm_warps = c->int8 ? std::max(pkv::kMaxDecodeWarps, pkv::kQ8WideWarps) : pkv::kMaxDecodeWarps;
+    const int sm_warps = std::max(pkv::kMaxDecodeWarps, pkv::kWideWarps);
     const long long W = std::min((long long)c->num_sms * sm_warps, U);
     const long long s_bal = ((long long)max_pages * W + U - 1) / U + 1;
     if (U < 0x7fffffffLL && s_bal <= max_splits) {
@@ -386,11 +386,11 @@ void pkv_destroy(pkv_cache* c) {
   delete c;
 }
 
-pkv_status pkv_device_info(const pkv_cache* c, int* num_sms, int* decode_warps_per_sm) {
-  if (c == nullptr) return PKV_ERR_INVALID_ARG;
+pkv_status pkv_device_info(const pkv_cache* c, int batch, int* num_sms, int* decode_warps_per_sm) {
+  if (c == nullptr || batch < 1) return PKV_ERR_INVALID_ARG;
   if (num_sms) *num_sms = c->num_sms;
   if (decode_warps_per_sm) {
-    const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, 1);
+    const DecodeConfig cfg = pkv::decode_config(c->group, c->desc.head_dim, batch, false, false, c->int8);
     *decode_warps_per_sm = cfg.warps * cfg.ctas_per_sm;
   }
   return PKV_OK;

@@ -13,10 +13,10 @@ constexpr int kPageSize = 16;
 constexpr int kMaxGroup = 8;        // Hq / Hkv handled by the kernels
 constexpr int kMaxDecodeBatch = 4096;  // sequences per decode call (per-CTA shared-memory prefix)
 constexpr int kMaxDecodeWarps = 8;     // warps per decode CTA, at most
-// int8 pages with one query head per KV head, from this many sequences on: 12 warps per SM (two
-// CTAs of six), the most of any decode layout
-constexpr int kQ8WideBatch = 8;
-constexpr int kQ8WideWarps = 12;
+// The CUDA-core decode (one query head per KV head), from this many sequences on: 12 warps per SM
+// (two CTAs of six), the most of any decode layout
+constexpr int kWideBatch = 8;
+constexpr int kWideWarps = 12;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s (default)
 // A warp that gave up waits this long for its own copies still in flight before it returns, so
 // that no copy lands in the shared memory of a finished block.  Not affected by the settable limit.
@@ -158,6 +158,7 @@ struct DecodeConfig {
   int warps;            // warps per CTA
   int ctas_per_sm;      // resident CTAs per SM (the grid of a full launch is SMs x this)
   int nstage;           // per-warp ring depth
+  bool wide;            // CUDA-core layout of 12 warps per SM (its kernel holds at most 168 registers)
   size_t smem_bytes;    // dynamic shared memory
   int box_inner;        // TMA box extent along head_dim (elements)
   int swizzle_bytes;    // 0 (none), 64 or 128

@@ -107,7 +107,7 @@ def test_partials_parity_balanced_partition(name):
     step, host_pool, cache, tabs, g = _gpu_pool_after(SMALL[name], plan={})
     S, chunk = cache.plan_decode(step.batch, step.max_pages_per_seq, int(step.page_indptr[-1]))
     assert chunk == -1 and g["pl"].shape[2] == S
-    sms, warps = cache.device_info()
+    sms, warps = cache.device_info(step.batch)
     W = min(sms * warps, step.cfg.hkv * int(step.page_indptr[-1]))
     gq = g["q_out"][H.query_rows(step)]
     po, pl = oracle.split_attention_balanced(H.geometry(step), g["pool"], gq, step.page_indptr, step.page_indices,

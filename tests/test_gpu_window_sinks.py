@@ -168,7 +168,7 @@ def test_windowed_balanced_partials_match_oracle(name, window):
     out_c, lse_c = cache.combine(po, pl, sinks=sinks)
     torch.cuda.synchronize()
     assert cache.check_status() == (0, 0)
-    sms, warps = cache.device_info()
+    sms, warps = cache.device_info(step.batch)
     L = step.seq_len
     visible = int(sum(-(-int(x) // 16) - max(0, int(x) - window) // 16 for x in L)) * step.cfg.hkv
     gpool = _bits(pool).view(np.uint16)
