@@ -73,6 +73,7 @@ def test_argument_errors_return_before_any_device_work(lib):
     assert lib.pkv_set_stage_stall(None, 1) == pkv.ERR_INVALID_ARG
     s, c = ctypes.c_int(), ctypes.c_int()
     assert lib.pkv_plan_decode(None, 1, 1, 0, 0, 0, 4, ctypes.byref(s), ctypes.byref(c)) == pkv.ERR_INVALID_ARG
+    assert lib.pkv_device_info(None, 8, ctypes.byref(s), ctypes.byref(c)) == pkv.ERR_INVALID_ARG
     lib.pkv_destroy(None)
 
 
