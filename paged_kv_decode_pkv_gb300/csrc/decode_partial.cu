@@ -27,7 +27,10 @@
 // accumulate): the G query heads are rows of A (padded to 16), the 16 slots of a page are two
 // n-blocks, and the score accumulators are re-used directly as the A operand of P.V.  K/V boxes
 // use the 128-byte (64-byte for head_dim 96) TMA swizzle so the ldmatrix row reads are free of
-// bank conflicts.
+// bank conflicts.  An int8 cache (template flag Q8) stages two pages of an item per stage and
+// computes from the codes: on CUDA cores with the fp16 arrangement for G = 1 (GroupOneQ8), on
+// tensor cores with the page's slots as the MMA rows for G >= 2 (GroupQ8).  The CUDA-core path
+// has a wide form (template flag WIDE: 12 warps per SM, at most 168 registers) for large batches.
 //
 // One-launch mode (template flag FUSED) also performs the append of a decode step: the first
 // stage of an item brings the new token's raw k and v and its (cos, sin) row, the consumer
